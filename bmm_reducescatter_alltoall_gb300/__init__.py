@@ -1,0 +1,291 @@
+"""GB300-native fused MoE BMM -> TP ReduceScatter -> bias Add -> EP AllToAll
+and all_to_all_v over virtual ranks on one GPU.
+
+Thin Python binding over libbmmrsa2a.so (the C ABI in include/bmm_rs_a2a.h):
+it checks tensors (device, dtype, contiguity), passes their data pointers and
+the current CUDA stream, and raises on a non-zero status.  Every step of the
+computation runs in the library's CUDA kernels; there is no other code path.
+The library is built in-tree by `bmm_reducescatter_alltoall_gb300._build`;
+calling into a missing library raises `RuntimeError`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+__all__ = [
+    "BraError", "FP16", "BF16", "FP32", "INT8", "VARIANT_TC", "VARIANT_SIMT",
+    "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
+    "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked",
+    "cal_all_to_all_v_blocks", "l2_flush", "fault_status", "status_str", "version",
+]
+
+FP16, BF16, FP32, INT8 = 0, 1, 2, 3
+VARIANT_TC, VARIANT_SIMT = 1, 2
+OK, ERR_NULLPTR, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = (
+    0, 161001, 161002, 161003, 161100, 161101)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "lib", "libbmmrsa2a.so")
+_lib = None
+
+
+class BraError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_str(code) if _lib else code} ({code})")
+        self.code = code
+
+
+def library() -> ctypes.CDLL:
+    """The loaded native library (loaded on first use)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise RuntimeError(
+            f"native library {library_path} is not built; run "
+            "`python -m bmm_reducescatter_alltoall_gb300._build` (needs nvcc)")
+    lib = ctypes.CDLL(library_path)
+    vp, i64, i32, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    lib.bmm_rs_a2a.argtypes = [pp, pp, pp, i64, i64, i64, i64, i64, i64, i64, c_int, pp, vp]
+    lib.bmm_rs_a2a.restype = c_int
+    lib.bmm_rs_a2a_variant.argtypes = [pp, pp, pp, i64, i64, i64, i64, i64, i64, i64, c_int, pp]
+    lib.bmm_rs_a2a_variant.restype = c_int
+    lib.bmm_rs_a2a_infer_shape.argtypes = [i64] * 7 + [i64p] * 4
+    lib.bmm_rs_a2a_infer_shape.restype = c_int
+    lib.cal_all_to_all_v_blocks.argtypes = [i64, i64]
+    lib.cal_all_to_all_v_blocks.restype = i64
+    lib.all_to_all_v.argtypes = [pp, vp, vp, vp, vp, pp, i64, i64, c_int, vp]
+    lib.all_to_all_v.restype = c_int
+    lib.all_to_all_v_checked.argtypes = [pp, vp, vp, vp, vp, pp, i64, i64, c_int, i64p, vp, vp]
+    lib.all_to_all_v_checked.restype = c_int
+    lib.bra_status_str.argtypes = [c_int]
+    lib.bra_status_str.restype = ctypes.c_char_p
+    lib.bra_l2_flush.argtypes = [vp, ctypes.c_size_t, vp]
+    lib.bra_l2_flush.restype = c_int
+    lib.bra_fault_status.argtypes = [ctypes.POINTER(i32), c_int]
+    lib.bra_fault_status.restype = c_int
+    lib.bra_version.argtypes = []
+    lib.bra_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_str(code: int) -> str:
+    return library().bra_status_str(int(code)).decode()
+
+
+def version() -> str:
+    return library().bra_version().decode()
+
+
+def _check(code: int, what: str) -> None:
+    if code != OK:
+        raise BraError(code, what)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr_array(ptrs: Sequence[Optional[int]]):
+    arr = (ctypes.c_void_p * max(1, len(ptrs)))()
+    for k, p in enumerate(ptrs):
+        arr[k] = p if p else None
+    return arr
+
+
+def _stream_handle(stream) -> Optional[int]:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev_tensor(t, what: str, dtype=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{what} must be a CUDA tensor (got {t.device})")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype} (got {t.dtype})")
+    return t
+
+
+def _fused_dtype(dt) -> int:
+    torch = _torch()
+    if dt == torch.float16:
+        return FP16
+    if dt == torch.bfloat16:
+        return BF16
+    raise TypeError(f"fused op takes float16 or bfloat16, got {dt}")
+
+
+def bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type) -> dict:
+    """Per-rank shapes: {'x','w','bias','y'} as tuples (bias in 3-D form)."""
+    arrs = [(ctypes.c_int64 * 3)() for _ in range(4)]
+    _check(library().bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type, *arrs),
+           "bmm_rs_a2a_infer_shape")
+    return {k: tuple(a) for k, a in zip(("x", "w", "bias", "y"), arrs)}
+
+
+def _shape_check(t, want, what):
+    if tuple(t.shape) != tuple(want):
+        raise ValueError(f"{what} has shape {tuple(t.shape)}, expected {tuple(want)}")
+
+
+def _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out):
+    P = ep * tp
+    if len(x) != P or len(weight) != P:
+        raise ValueError(f"x and weight need ep*tp = {P} entries")
+    shapes = bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type)
+    dt = x[0].dtype
+    for r in range(P):
+        _shape_check(_dev_tensor(x[r], f"x[{r}]", dt), shapes["x"], f"x[{r}]")
+        _shape_check(_dev_tensor(weight[r], f"weight[{r}]", dt), shapes["w"], f"weight[{r}]")
+    bptr = None
+    if bias is not None:
+        if len(bias) != P:
+            raise ValueError(f"bias needs ep*tp = {P} entries")
+        torch = _torch()
+        bdt = torch.float16 if dt == torch.float16 else torch.float32
+        b3 = shapes["bias"]
+        ptrs = []
+        for r, b in enumerate(bias):
+            if b is None:
+                ptrs.append(0)
+                continue
+            _dev_tensor(b, f"bias[{r}]", bdt)
+            if tuple(b.shape) not in (tuple(b3), (b3[0], b3[2])):
+                raise ValueError(f"bias[{r}] has shape {tuple(b.shape)}, expected {b3} "
+                                 f"or {(b3[0], b3[2])}")
+            ptrs.append(b.data_ptr())
+        bptr = _ptr_array(ptrs)
+    if len(out) != P:
+        raise ValueError(f"out needs ep*tp = {P} entries")
+    for r in range(P):
+        _shape_check(_dev_tensor(out[r], f"out[{r}]", dt), shapes["y"], f"out[{r}]")
+    return (_ptr_array([t.data_ptr() for t in x]), _ptr_array([t.data_ptr() for t in weight]),
+            bptr, _ptr_array([t.data_ptr() for t in out]), _fused_dtype(dt))
+
+
+def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int, tp: int,
+               E: int, C: int, M: int, H: int, y_shard_type: int,
+               out: Optional[Sequence] = None, stream=None) -> List:
+    """Fused BMM -> ReduceScatter -> Add -> AllToAll over P = ep*tp ranks.
+
+    x[r], weight[r], bias[r] (or bias None) and out[r] are CUDA tensors of
+    the shapes `bmm_rs_a2a_infer_shape` gives; out is allocated when None.
+    Returns out.  Asynchronous on `stream` (default: current stream).
+    """
+    torch = _torch()
+    if out is None:
+        ys = bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type)["y"]
+        out = [torch.empty(ys, dtype=x[0].dtype, device=x[0].device) for _ in range(ep * tp)]
+    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out)
+    _check(library().bmm_rs_a2a(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp,
+                                _stream_handle(stream)), "bmm_rs_a2a")
+    return out
+
+
+def bmm_rs_a2a_variant(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out) -> int:
+    """VARIANT_TC or VARIANT_SIMT; raises BraError if the call would be rejected."""
+    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out)
+    v = library().bmm_rs_a2a_variant(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp)
+    if v < 0:
+        raise BraError(-v, "bmm_rs_a2a_variant")
+    return v
+
+
+def cal_all_to_all_v_blocks(P: int, L: int) -> int:
+    return int(library().cal_all_to_all_v_blocks(int(P), int(L)))
+
+
+def _a2av_args(inputs, send_counts, out, send_displs, recv_counts, recv_displs):
+    torch = _torch()
+    P = len(inputs)
+    if len(out) != P:
+        raise ValueError("inputs and out need the same number of ranks")
+    dt = inputs[0].dtype
+    if dt == torch.float32:
+        code = FP32
+    elif dt == torch.int8:
+        code = INT8
+    else:
+        raise TypeError(f"all_to_all_v takes float32 or int8, got {dt}")
+    for r in range(P):
+        _dev_tensor(inputs[r], f"inputs[{r}]", dt)
+        _dev_tensor(out[r], f"out[{r}]", dt)
+    _dev_tensor(send_counts, "send_counts", torch.int64)
+    if tuple(send_counts.shape) != (P, P):
+        raise ValueError(f"send_counts must be ({P}, {P})")
+    dev = send_counts.device
+    mk = lambda t, n: t if t is not None else torch.empty((P, P), dtype=torch.int64, device=dev)
+    sd, rc, rd = mk(send_displs, "sd"), mk(recv_counts, "rc"), mk(recv_displs, "rd")
+    for t, n in ((sd, "send_displs"), (rc, "recv_counts"), (rd, "recv_displs")):
+        _dev_tensor(t, n, torch.int64)
+        if tuple(t.shape) != (P, P):
+            raise ValueError(f"{n} must be ({P}, {P})")
+    return P, code, sd, rc, rd
+
+
+def all_to_all_v(inputs: Sequence, send_counts, out: Sequence, core_num: int,
+                 send_displs=None, recv_counts=None, recv_displs=None, stream=None) -> dict:
+    """Variable-count exchange among P = len(inputs) ranks (see the C header).
+
+    send_counts: CUDA int64 (P, P).  out[j] must hold what rank j receives.
+    Returns {'out', 'send_displs', 'recv_counts', 'recv_displs'}.
+    """
+    P, code, sd, rc, rd = _a2av_args(inputs, send_counts, out, send_displs, recv_counts,
+                                     recv_displs)
+    _check(library().all_to_all_v(_ptr_array([t.data_ptr() for t in inputs]),
+                                  send_counts.data_ptr(), sd.data_ptr(), rc.data_ptr(),
+                                  rd.data_ptr(), _ptr_array([t.data_ptr() for t in out]), P,
+                                  int(core_num), code, _stream_handle(stream)), "all_to_all_v")
+    return {"out": out, "send_displs": sd, "recv_counts": rc, "recv_displs": rd}
+
+
+def all_to_all_v_checked(inputs: Sequence, send_counts, out: Sequence, core_num: int,
+                         out_capacity: Optional[Sequence[int]] = None, status=None,
+                         send_displs=None, recv_counts=None, recv_displs=None,
+                         stream=None) -> dict:
+    """all_to_all_v plus device-side checks; the int32 status tensor receives
+    0 or ERR_INVALID (negative count or over capacity).  out_capacity defaults
+    to each out[j]'s length."""
+    torch = _torch()
+    P, code, sd, rc, rd = _a2av_args(inputs, send_counts, out, send_displs, recv_counts,
+                                     recv_displs)
+    if out_capacity is None:
+        out_capacity = [t.numel() for t in out]
+    cap = (ctypes.c_int64 * P)(*[int(c) for c in out_capacity])
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=send_counts.device)
+    _dev_tensor(status, "status", torch.int32)
+    _check(library().all_to_all_v_checked(
+        _ptr_array([t.data_ptr() for t in inputs]), send_counts.data_ptr(), sd.data_ptr(),
+        rc.data_ptr(), rd.data_ptr(), _ptr_array([t.data_ptr() for t in out]), P,
+        int(core_num), code, cap, status.data_ptr(), _stream_handle(stream)),
+        "all_to_all_v_checked")
+    return {"out": out, "send_displs": sd, "recv_counts": rc, "recv_displs": rd,
+            "status": status}
+
+
+def l2_flush(buf, stream=None) -> None:
+    """Zero `buf` (a CUDA tensor larger than L2) to evict earlier data from L2."""
+    _dev_tensor(buf, "buf")
+    _check(library().bra_l2_flush(buf.data_ptr(), buf.numel() * buf.element_size(),
+                                  _stream_handle(stream)), "bra_l2_flush")
+
+
+def fault_status(clear: bool = False) -> int:
+    """The watchdog word (0, or ERR_TIMEOUT if a bounded wait gave up)."""
+    v = ctypes.c_int32(0)
+    _check(library().bra_fault_status(ctypes.byref(v), 1 if clear else 0), "bra_fault_status")
+    return int(v.value)

@@ -1,0 +1,287 @@
+// Host entry points of libbmmrsa2a.so: argument validation, variant choice
+// and launches.  Every rule cited here is stated in include/bmm_rs_a2a.h.
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "bra_internal.h"
+
+namespace {
+
+constexpr int64_t kInt32Max = 2147483647LL;
+
+bool world_size_ok(int64_t v) {
+  return v == 1 || v == 2 || v == 4 || v == 8 || v == 16 || v == 32;
+}
+
+// Range rules of the CANN guide, section 数据关系与取值范围说明, and the
+// attribute checks of section op_api 层 (CheckAttr / CheckShapeRange).
+int check_fused_attrs(int64_t ep, int64_t tp, int64_t E, int64_t C, int64_t M,
+                      int64_t H, int64_t type) {
+  if (!world_size_ok(ep) || !world_size_ok(tp)) return BRA_ERR_INVALID;
+  if (type != 0 && type != 1) return BRA_ERR_INVALID;
+  if (E < 2 || E > 512 || E % ep != 0) return BRA_ERR_INVALID;
+  if (E / ep < 1 || E / ep > 32) return BRA_ERR_INVALID;
+  if (H < 1 || H > 65535) return BRA_ERR_INVALID;
+  if (M % tp != 0 || M / tp < 1 || M / tp > 65535) return BRA_ERR_INVALID;
+  if (C <= 0) return BRA_ERR_INVALID;
+  if (type == 0 && H % tp != 0) return BRA_ERR_INVALID;
+  if (type == 1 && C % tp != 0) return BRA_ERR_INVALID;
+  return BRA_OK;
+}
+
+struct Range {
+  uintptr_t lo, hi;
+  bool out;
+};
+
+// Validation in the order of CheckParams: null pointers, dtype, attributes,
+// shapes; then the aliasing rule.  On success fills `prob`.
+int validate_fused(const void* const x[], const void* const weight[],
+                   const void* const bias[], int64_t ep, int64_t tp, int64_t E,
+                   int64_t C, int64_t M, int64_t H, int64_t type, int dtype,
+                   void* const out[], bra::FusedProblem* prob) {
+  if (!x || !weight || !out) return BRA_ERR_NULLPTR;
+  if (dtype != BRA_FP16 && dtype != BRA_BF16) return BRA_ERR_INVALID;
+  int rc = check_fused_attrs(ep, tp, E, C, M, H, type);
+  if (rc != BRA_OK) return rc;
+  const int64_t P = ep * tp;
+  for (int64_t r = 0; r < P; ++r)
+    if (!x[r] || !weight[r] || !out[r]) return BRA_ERR_NULLPTR;
+  int nb = 0;
+  if (bias)
+    for (int64_t r = 0; r < P; ++r) nb += bias[r] != nullptr;
+  if (nb != 0 && nb != P) return BRA_ERR_INVALID;
+  if (ep * C >= (int64_t(1) << 31)) return BRA_ERR_UNSUPPORTED;
+
+  const int64_t El = E / ep, Kp = M / tp;
+  const int64_t es = 2;
+  const int64_t bes = dtype == BRA_FP16 ? 2 : 4;
+  const int64_t Hb = type == 0 ? H / tp : H;
+  const int64_t xb = El * ep * C * Kp * es, wb = El * Kp * H * es;
+  const int64_t bb = El * Hb * bes;
+  const int64_t yb = (type == 0 ? E * C * (H / tp) : E * (C / tp) * H) * es;
+  std::vector<Range> in, outs;
+  in.reserve(3 * P);
+  outs.reserve(P);
+  for (int64_t r = 0; r < P; ++r) {
+    in.push_back({(uintptr_t)x[r], (uintptr_t)x[r] + (uintptr_t)xb, false});
+    in.push_back({(uintptr_t)weight[r], (uintptr_t)weight[r] + (uintptr_t)wb, false});
+    if (nb) in.push_back({(uintptr_t)bias[r], (uintptr_t)bias[r] + (uintptr_t)bb, false});
+    outs.push_back({(uintptr_t)out[r], (uintptr_t)out[r] + (uintptr_t)yb, true});
+  }
+  // Outputs may overlap nothing.  Sorted by start, a pair (a before b)
+  // overlaps iff b.lo < a.hi; track the largest end of every earlier range
+  // and of every earlier output.
+  std::vector<Range> all(in);
+  all.insert(all.end(), outs.begin(), outs.end());
+  std::sort(all.begin(), all.end(),
+            [](const Range& a, const Range& b) { return a.lo < b.lo; });
+  uintptr_t max_hi_all = 0, max_hi_out = 0;
+  for (const Range& a : all) {
+    if (a.out ? a.lo < max_hi_all : a.lo < max_hi_out) return BRA_ERR_INVALID;
+    max_hi_all = std::max(max_hi_all, a.hi);
+    if (a.out) max_hi_out = std::max(max_hi_out, a.hi);
+  }
+
+  prob->x = x;
+  prob->w = weight;
+  prob->bias = nb ? bias : nullptr;
+  prob->y = out;
+  prob->ep = (int)ep;
+  prob->tp = (int)tp;
+  prob->El = (int)El;
+  prob->C = (int)C;
+  prob->Kp = (int)Kp;
+  prob->H = (int)H;
+  prob->type = (int)type;
+  prob->dtype = dtype;
+  return BRA_OK;
+}
+
+// BRA_FORCE_VARIANT=tc|simt, read at every call.
+int forced_variant() {
+  const char* v = std::getenv("BRA_FORCE_VARIANT");
+  if (!v || !*v) return BRA_VARIANT_AUTO;
+  if (!std::strcmp(v, "tc")) return BRA_VARIANT_TC;
+  if (!std::strcmp(v, "simt")) return BRA_VARIANT_SIMT;
+  return BRA_VARIANT_AUTO;
+}
+
+int choose_variant(const bra::FusedProblem& p) {
+  const int f = forced_variant();
+  const bool tc_ok = bra::fused_tc_eligible(p);
+  if (f == BRA_VARIANT_SIMT) return BRA_VARIANT_SIMT;
+  if (f == BRA_VARIANT_TC) return tc_ok ? BRA_VARIANT_TC : -BRA_ERR_UNSUPPORTED;
+  return tc_ok ? BRA_VARIANT_TC : BRA_VARIANT_SIMT;
+}
+
+bool log_enabled() {
+  const char* v = std::getenv("BRA_LOG");
+  return v && *v && *v != '0';
+}
+
+int a2av_common(const void* const input[], const int64_t* send_counts,
+                int64_t* send_displs, int64_t* recv_counts,
+                int64_t* recv_displs, void* const out[], int64_t P,
+                int64_t core_num, int dtype, const int64_t* out_capacity,
+                int32_t* status_dev, bool checked, cudaStream_t stream) {
+  if (!input || !send_counts || !send_displs || !recv_counts || !recv_displs || !out)
+    return BRA_ERR_NULLPTR;
+  if (checked && (!out_capacity || !status_dev)) return BRA_ERR_NULLPTR;
+  if (P < 1) return BRA_ERR_INVALID;
+  if (core_num < 1 || core_num > kInt32Max) return BRA_ERR_INVALID;
+  if (dtype != BRA_FP32 && dtype != BRA_INT8) return BRA_ERR_INVALID;
+  if (P > bra::kA2avMaxP) return BRA_ERR_UNSUPPORTED;
+  for (int64_t r = 0; r < P; ++r)
+    if (!input[r] || !out[r]) return BRA_ERR_NULLPTR;
+  for (int64_t j = 0; j < P; ++j) {
+    for (int64_t i = 0; i < P; ++i)
+      if (out[j] == input[i]) return BRA_ERR_INVALID;
+    for (int64_t k = 0; k < j; ++k)
+      if (out[j] == out[k]) return BRA_ERR_INVALID;
+  }
+  const int64_t B = cal_all_to_all_v_blocks(P, core_num);
+  if (B < 1 || B * P > kInt32Max) return BRA_ERR_INVALID;
+
+  bra::A2avArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int64_t r = 0; r < P; ++r) {
+    a.in[r] = input[r];
+    a.out[r] = out[r];
+    a.cap[r] = checked ? out_capacity[r] : 0;
+  }
+  a.sc = send_counts;
+  a.sd = send_displs;
+  a.rc = recv_counts;
+  a.rd = recv_displs;
+  a.status = checked ? status_dev : nullptr;
+  a.P = (int)P;
+  a.B = (int)B;
+  a.esize = dtype == BRA_FP32 ? 4 : 1;
+  a.check_cap = checked ? 1 : 0;
+  const int ctas = bra::a2av_ctas_per_rank((int)P, (int)B);
+  if (log_enabled())
+    std::fprintf(stderr, "[bra] all_to_all_v P=%lld L=%lld B=%lld ctas/rank=%d grid=(%d,%lld)\n",
+                 (long long)P, (long long)core_num, (long long)B, ctas, ctas, (long long)P);
+  cudaError_t e = bra::launch_a2av(a, ctas, stream);
+  return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bmm_rs_a2a(const void* const x[], const void* const weight[],
+               const void* const bias[], int64_t ep, int64_t tp, int64_t E,
+               int64_t C, int64_t M, int64_t H, int64_t yShardType, int dtype,
+               void* const out[], bra_stream_t stream) {
+  bra::FusedProblem p;
+  int rc = validate_fused(x, weight, bias, ep, tp, E, C, M, H, yShardType, dtype, out, &p);
+  if (rc != BRA_OK) return rc;
+  const int v = choose_variant(p);
+  if (v < 0) return -v;
+  if (log_enabled())
+    std::fprintf(stderr, "[bra] bmm_rs_a2a ep=%lld tp=%lld E=%lld C=%lld M=%lld H=%lld type=%lld -> %s\n",
+                 (long long)ep, (long long)tp, (long long)E, (long long)C, (long long)M,
+                 (long long)H, (long long)yShardType, v == BRA_VARIANT_TC ? "tc" : "simt");
+  cudaError_t e = v == BRA_VARIANT_TC ? bra::launch_fused_tc(p, (cudaStream_t)stream)
+                                      : bra::launch_fused_simt(p, (cudaStream_t)stream);
+  if (e == cudaErrorInvalidValue && v == BRA_VARIANT_TC) return BRA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
+}
+
+int bmm_rs_a2a_variant(const void* const x[], const void* const weight[],
+                       const void* const bias[], int64_t ep, int64_t tp,
+                       int64_t E, int64_t C, int64_t M, int64_t H,
+                       int64_t yShardType, int dtype, void* const out[]) {
+  bra::FusedProblem p;
+  int rc = validate_fused(x, weight, bias, ep, tp, E, C, M, H, yShardType, dtype, out, &p);
+  if (rc != BRA_OK) return -rc;
+  return choose_variant(p);
+}
+
+int bmm_rs_a2a_infer_shape(int64_t ep, int64_t tp, int64_t E, int64_t C,
+                           int64_t M, int64_t H, int64_t yShardType,
+                           int64_t x_shape[3], int64_t w_shape[3],
+                           int64_t bias_shape[3], int64_t y_shape[3]) {
+  int rc = check_fused_attrs(ep, tp, E, C, M, H, yShardType);
+  if (rc != BRA_OK) return rc;
+  const int64_t El = E / ep, Kp = M / tp;
+  if (x_shape) {
+    x_shape[0] = El;
+    x_shape[1] = ep * C;
+    x_shape[2] = Kp;
+  }
+  if (w_shape) {
+    w_shape[0] = El;
+    w_shape[1] = Kp;
+    w_shape[2] = H;
+  }
+  if (bias_shape) {
+    bias_shape[0] = El;
+    bias_shape[1] = 1;
+    bias_shape[2] = yShardType == 0 ? H / tp : H;
+  }
+  if (y_shape) {
+    y_shape[0] = E;
+    y_shape[1] = yShardType == 0 ? C : C / tp;
+    y_shape[2] = yShardType == 0 ? H / tp : H;
+  }
+  return BRA_OK;
+}
+
+int64_t cal_all_to_all_v_blocks(int64_t P, int64_t L) {
+  if (P < 1 || L < 1 || L > kInt32Max) return -1;
+  if (L < P) return L;
+  return (L / P) * P;
+}
+
+int all_to_all_v(const void* const input[], const int64_t* send_counts,
+                 int64_t* send_displs, int64_t* recv_counts,
+                 int64_t* recv_displs, void* const out[], int64_t P,
+                 int64_t core_num, int dtype, bra_stream_t stream) {
+  return a2av_common(input, send_counts, send_displs, recv_counts, recv_displs,
+                     out, P, core_num, dtype, nullptr, nullptr, false,
+                     (cudaStream_t)stream);
+}
+
+int all_to_all_v_checked(const void* const input[], const int64_t* send_counts,
+                         int64_t* send_displs, int64_t* recv_counts,
+                         int64_t* recv_displs, void* const out[], int64_t P,
+                         int64_t core_num, int dtype,
+                         const int64_t* out_capacity, int32_t* status_dev,
+                         bra_stream_t stream) {
+  return a2av_common(input, send_counts, send_displs, recv_counts, recv_displs,
+                     out, P, core_num, dtype, out_capacity, status_dev, true,
+                     (cudaStream_t)stream);
+}
+
+const char* bra_status_str(int status) {
+  switch (status) {
+    case BRA_OK: return "BRA_OK";
+    case BRA_ERR_NULLPTR: return "BRA_ERR_NULLPTR";
+    case BRA_ERR_INVALID: return "BRA_ERR_INVALID";
+    case BRA_ERR_UNSUPPORTED: return "BRA_ERR_UNSUPPORTED";
+    case BRA_ERR_CUDA: return "BRA_ERR_CUDA";
+    case BRA_ERR_TIMEOUT: return "BRA_ERR_TIMEOUT";
+    default: return "BRA_UNKNOWN_STATUS";
+  }
+}
+
+int bra_l2_flush(void* buf, size_t bytes, bra_stream_t stream) {
+  if (!buf) return BRA_ERR_NULLPTR;
+  cudaError_t e = bra::launch_l2_flush(buf, bytes, (cudaStream_t)stream);
+  return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
+}
+
+int bra_fault_status(int32_t* code, int clear) {
+  if (!code) return BRA_ERR_NULLPTR;
+  return bra::read_fault_word(code, clear) == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
+}
+
+const char* bra_version(void) { return "0.1.0"; }
+
+}  // extern "C"

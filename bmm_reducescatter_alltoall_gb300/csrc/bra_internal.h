@@ -1,0 +1,62 @@
+// Internal declarations shared by the host entry points and the kernels of
+// libbmmrsa2a.so.  Not installed; the public ABI is include/bmm_rs_a2a.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bmm_rs_a2a.h"
+
+namespace bra {
+
+// all_to_all_v keeps the whole P x P count matrix of int64 in shared memory.
+constexpr int kA2avMaxP = 64;
+constexpr int kA2avThreads = 512;
+
+// Fused kernels: one launch covers the TP groups of up to kChunkRanks source
+// ranks (their x / weight / bias), and may write to any of kMaxRanks outputs.
+constexpr int kChunkRanks = 64;
+constexpr int kMaxRanks = 32 * 32;
+
+struct A2avArgs {
+  const void* in[kA2avMaxP];
+  void* out[kA2avMaxP];
+  int64_t cap[kA2avMaxP];   // receive capacity per rank (elements)
+  const int64_t* sc;        // send_counts [P][P]
+  int64_t* sd;              // send_displs [P][P]
+  int64_t* rc;              // recv_counts [P][P]
+  int64_t* rd;              // recv_displs [P][P]
+  int32_t* status;          // optional device status word
+  int P;
+  int B;                    // CalAllToAllVBlocks(P, L)
+  int esize;                // element size in bytes (4 or 1)
+  int check_cap;            // compare received totals against cap[]
+};
+
+// Launch the exchange with `ctas_per_rank` CTAs per source rank.
+cudaError_t launch_a2av(const A2avArgs& a, int ctas_per_rank, cudaStream_t st);
+// CTAs per rank that fill the GPU about once (never more than B).
+int a2av_ctas_per_rank(int P, int B);
+
+// Problem description shared by both fused variants.
+struct FusedProblem {
+  const void* const* x;      // [P]
+  const void* const* w;      // [P]
+  const void* const* bias;   // [P] or nullptr
+  void* const* y;            // [P]
+  int ep, tp, El, C, Kp, H;
+  int type;                  // yShardType
+  int dtype;                 // BRA_FP16 | BRA_BF16
+};
+
+cudaError_t launch_fused_simt(const FusedProblem& f, cudaStream_t st);
+// Returns cudaErrorInvalidValue if a TMA descriptor cannot be encoded.
+cudaError_t launch_fused_tc(const FusedProblem& f, cudaStream_t st);
+// Shape / alignment predicate of the tensor-core variant.
+bool fused_tc_eligible(const FusedProblem& f);
+
+cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t st);
+cudaError_t read_fault_word(int32_t* code, int clear);
+
+}  // namespace bra

@@ -1,0 +1,254 @@
+/*
+ * bmm_rs_a2a.h -- C ABI of libbmmrsa2a.so: the MoE expert-parallel x
+ * tensor-parallel dataflow BatchMatMul -> TP ReduceScatter -> bias Add -> EP
+ * AllToAll, and the variable-count all_to_all_v exchange, with all ep*tp ranks
+ * resident on one GPU as virtual ranks (one buffer partition per rank).
+ *
+ * Pages cited (by title and section):
+ *   [CANN] "CANN ops-transformer 通算融合算子实战 BatchMatMulReduceScatterAllToAll
+ *          原理、shape 约束与 aclnn 两段式调用"
+ *   [PTO]  "LowerL2TensorCollectives Pass" (PyPTO)
+ *   [VCCL] "vccl alltoallv dev log"
+ *
+ * Conventions shared by every entry point
+ *   - Virtual rank r = s*tp + t: s is the rank's EP index, t its TP index
+ *     ([CANN] §完整调用示例 step 2: EP groups {t, t+tp, ...}, TP groups
+ *     {s*tp .. s*tp+tp-1}).
+ *   - Every tensor is dense, row-major (C order), with no padding.
+ *   - Device pointers are CUDA device (or managed) addresses on the current
+ *     device; the caller owns every buffer and the stream.  The library
+ *     allocates no device memory on any call path.
+ *   - Work is enqueued on `stream` (NULL = legacy default stream) and runs
+ *     asynchronously.  The return value reports argument validation and the
+ *     launch itself, not completion; on any error nothing is launched unless
+ *     the code is BRA_ERR_CUDA from the launch.
+ *   - Calls are stateless: calls whose outputs are disjoint may run
+ *     concurrently on different streams.
+ *   - Functions are thread-safe.
+ */
+#ifndef BMM_RS_A2A_H
+#define BMM_RS_A2A_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(BRA_BUILD) && defined(__GNUC__)
+#define BRA_API __attribute__((visibility("default")))
+#else
+#define BRA_API
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* bra_stream_t;   /* same type as cudaStream_t */
+
+/* Status codes.  NULLPTR and INVALID keep the values of the aclnn codes
+ * ACLNN_ERR_PARAM_NULLPTR / ACLNN_ERR_PARAM_INVALID ([CANN] §调用说明). */
+typedef enum {
+  BRA_OK = 0,
+  BRA_ERR_NULLPTR = 161001,     /* a required pointer is NULL                 */
+  BRA_ERR_INVALID = 161002,     /* dtype, attribute, shape or aliasing rule   */
+  BRA_ERR_UNSUPPORTED = 161003, /* valid per the pages but beyond this build  */
+  BRA_ERR_CUDA = 161100,        /* a CUDA call failed (launch or query)       */
+  BRA_ERR_TIMEOUT = 161101      /* a kernel gave up a bounded wait            */
+} bra_status;
+
+typedef enum { BRA_FP16 = 0, BRA_BF16 = 1, BRA_FP32 = 2, BRA_INT8 = 3 } bra_dtype;
+
+/* Kernel variants of bmm_rs_a2a (see bmm_rs_a2a_variant). */
+typedef enum {
+  BRA_VARIANT_AUTO = 0,
+  BRA_VARIANT_TC = 1,    /* tcgen05 / TMEM / TMA tensor-core kernel        */
+  BRA_VARIANT_SIMT = 2   /* generic kernel: any alignment, any size        */
+} bra_variant;
+
+/* ------------------------------------------------------------------------ */
+/* Fused BatchMatMul -> ReduceScatter -> Add -> AllToAll                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * bmm_rs_a2a -- [CANN] §功能说明与计算流程:
+ *     temp1 = BatchMatMul(x, weight); temp2 = ReduceScatter(temp1) over the
+ *     TP group (sum); temp3 = Add(temp2, bias); y = AllToAll(temp3) over the
+ *     EP group,
+ * computed for all P = ep*tp virtual ranks in one launch, writing straight
+ * into every rank's final y; no intermediate reaches memory.
+ *
+ * Arguments (El = E/ep, Kp = M/tp, Hp = H/tp, Cp = C/tp):
+ *   x[P]      device, x[r] of shape (El, ep*C, Kp), dtype `dtype`
+ *             (yShardType 1 writes dim 1 as ep*tp*C/tp: the same length).
+ *   weight[P] device, weight[r] of shape (El, Kp, H), dtype `dtype`.
+ *   bias[P]   NULL, or an array whose entries are all NULL (no bias), or all
+ *             non-NULL: bias[r] of shape (El, 1, Hp) / (El, Hp) for
+ *             yShardType 0 and (El, 1, H) / (El, H) for yShardType 1 (2-D and
+ *             3-D forms share one memory layout); fp16 when dtype is FP16,
+ *             fp32 when dtype is BF16 ([CANN] §参数说明).
+ *   ep, tp    EP and TP group sizes, each in {1, 2, 4, 8, 16, 32}; the pages
+ *             allow {2..32}, 1 is accepted as the degenerate case.
+ *   E, C, M, H  as in [CANN] §约束说明.
+ *   yShardType 0: reduce-scatter along H; 1: along C.
+ *   dtype     BRA_FP16 or BRA_BF16 (x, weight and y).
+ *   out[P]    device, y[r] of shape (E, C, Hp) for yShardType 0 and
+ *             (E, Cp, H) for yShardType 1, dtype `dtype`.
+ *   stream    CUDA stream.
+ * Semantics (receiver d = j*tp + t, stacked block i = s*El + e):
+ *   Z_{s,e} = sum_{t'=0..tp-1} x[s*tp+t'][e] @ weight[s*tp+t'][e], summed in
+ *   fp32 in t' order, shape (ep*C, H);
+ *   yShardType 0: y[d][i, c, h]  = Z_{s,e}[j*C + c, t*Hp + h] + bias[s*tp+t][e, h]
+ *   yShardType 1: y[d][i, c, h]  = Z_{s,e}[j*C + t*Cp + c, h] + bias[s*tp+t][e, h]
+ *   (the bias add is fp32, then one round-to-nearest-even to dtype).
+ * Errors (checked in the order of [CANN] §op_api 层 CheckParams; nothing is
+ * launched on error):
+ *   BRA_ERR_NULLPTR  x, weight or out (the arrays or any entry) is NULL.
+ *   BRA_ERR_INVALID  dtype not FP16/BF16; ep or tp not in the set above;
+ *                    yShardType not 0/1; E outside [2,512] or not a multiple
+ *                    of ep; E/ep outside [1,32]; H outside [1,65535]; M not
+ *                    a multiple of tp or M/tp outside [1,65535]; C <= 0;
+ *                    yShardType 0 with H % tp != 0; yShardType 1 with
+ *                    C % tp != 0 ([CANN] §数据关系与取值范围说明); some but not
+ *                    all bias entries NULL; an output range overlapping any
+ *                    input range or another output range.
+ *   BRA_ERR_UNSUPPORTED  ep*C >= 2^31.
+ *   BRA_ERR_CUDA     the launch failed (cudaGetLastError).
+ * Variant: the tensor-core kernel runs when every row stride and pointer is
+ * 16-byte aligned (Kp % 8 == 0, H % 8 == 0, and Hp % 8 == 0 for yShardType
+ * 0) and P <= 64; otherwise the generic kernel.  The environment variable
+ * BRA_FORCE_VARIANT=tc|simt overrides the choice (tc on an ineligible shape
+ * returns BRA_ERR_UNSUPPORTED).
+ */
+BRA_API int bmm_rs_a2a(const void* const x[], const void* const weight[],
+               const void* const bias[], int64_t ep, int64_t tp, int64_t E,
+               int64_t C, int64_t M, int64_t H, int64_t yShardType, int dtype,
+               void* const out[], bra_stream_t stream);
+
+/*
+ * bmm_rs_a2a_infer_shape -- per-rank shapes from the attributes ([CANN]
+ * §约束说明 and the infershape of §op_api 层): yShardType 0 gives
+ * y (E, C, H/tp), 1 gives y (E, C/tp, H).  Each output array receives three
+ * int64 values (bias in its 3-D form); any output pointer may be NULL.
+ * Pure host function.  Returns BRA_OK or BRA_ERR_INVALID (same range rules
+ * as bmm_rs_a2a).
+ */
+BRA_API int bmm_rs_a2a_infer_shape(int64_t ep, int64_t tp, int64_t E, int64_t C,
+                           int64_t M, int64_t H, int64_t yShardType,
+                           int64_t x_shape[3], int64_t w_shape[3],
+                           int64_t bias_shape[3], int64_t y_shape[3]);
+
+/*
+ * bmm_rs_a2a_variant -- which kernel bmm_rs_a2a would launch for these
+ * arguments (BRA_VARIANT_TC or BRA_VARIANT_SIMT), honouring
+ * BRA_FORCE_VARIANT.  Pointers are only inspected for alignment.  Returns the
+ * variant, or a negative bra_status (e.g. -BRA_ERR_INVALID) when bmm_rs_a2a
+ * would reject the call.  Pure host function.
+ */
+BRA_API int bmm_rs_a2a_variant(const void* const x[], const void* const weight[],
+                       const void* const bias[], int64_t ep, int64_t tp,
+                       int64_t E, int64_t C, int64_t M, int64_t H,
+                       int64_t yShardType, int dtype, void* const out[]);
+
+/* ------------------------------------------------------------------------ */
+/* all_to_all_v                                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * cal_all_to_all_v_blocks -- admitted block count B for P ranks and a
+ * requested core_num L ([PTO] §启动宽度): L when L < P, otherwise the
+ * largest multiple of P not above L (L=10, P=8 gives 8).  Returns -1 when
+ * P < 1 or L is outside [1, INT32_MAX] ([PTO] §约束与诊断).  Pure host.
+ */
+BRA_API int64_t cal_all_to_all_v_blocks(int64_t P, int64_t L);
+
+/*
+ * all_to_all_v -- variable-count exchange among P virtual ranks ([PTO] §行为
+ * and §ABI; addressing as in [VCCL] §5 ref): rank i sends send_counts[i][j]
+ * elements to rank j, for every pair including i == j:
+ *   send_displs[i][j] = sum_{k<j} send_counts[i][k]
+ *   recv_counts[j][i] = send_counts[i][j]
+ *   recv_displs[j][i] = sum_{k<i} send_counts[k][j]
+ *   out[j][recv_displs[j][i] + n] = input[i][send_displs[i][j] + n],
+ *       0 <= n < send_counts[i][j]
+ * so out[j] holds what rank j received ordered by source rank; its elements
+ * past the received total are not written.
+ *
+ * Arguments:
+ *   input[P]     device; input[i] holds at least sum_j send_counts[i][j]
+ *                elements of `dtype`.
+ *   send_counts  device, int64 [P][P] row-major (read only).
+ *   send_displs, recv_counts, recv_displs
+ *                device, int64 [P][P] row-major, written by the kernel.
+ *   out[P]       device; out[j] must hold sum_i send_counts[i][j] elements
+ *                (the caller's obligation here; see all_to_all_v_checked).
+ *   P            number of ranks, 1 <= P <= 64.
+ *   core_num     requested block count L per rank, in [1, INT32_MAX]; the
+ *                exchange splits each rank's send buffer into
+ *                B = cal_all_to_all_v_blocks(P, L) equal ranges.
+ *   dtype        BRA_FP32 or BRA_INT8 ([PTO] §约束与诊断 allowlist).
+ * Errors (nothing launched):
+ *   BRA_ERR_NULLPTR  any pointer argument or array entry is NULL.
+ *   BRA_ERR_INVALID  P < 1; core_num outside [1, INT32_MAX]; dtype not
+ *                    FP32/INT8; an out[j] equal to any input[i] or to another
+ *                    out[k] ([PTO] §当前限制: input != target, windows
+ *                    pairwise distinct); B*P > INT32_MAX.
+ *   BRA_ERR_UNSUPPORTED  P > 64.
+ *   BRA_ERR_CUDA     the launch failed.
+ * Device-side data check: if any send count is negative the kernel writes
+ * nothing at all (no output, no bookkeeping).
+ */
+BRA_API int all_to_all_v(const void* const input[], const int64_t* send_counts,
+                 int64_t* send_displs, int64_t* recv_counts,
+                 int64_t* recv_displs, void* const out[], int64_t P,
+                 int64_t core_num, int dtype, bra_stream_t stream);
+
+/*
+ * all_to_all_v_checked -- all_to_all_v plus device-side checks whose result
+ * is written to *status_dev (device int32): BRA_OK, or BRA_ERR_INVALID when a
+ * send count is negative or some rank j would receive more than
+ * out_capacity[j] elements; in the error case nothing else is written.
+ * out_capacity: host array of P element counts (copied at the call).
+ * status_dev: device pointer, required (BRA_ERR_NULLPTR if NULL).
+ * The "0 / 1 / capacity / over-capacity / negative" count matrices of
+ * [PTO] §测试 map onto this entry point.
+ */
+BRA_API int all_to_all_v_checked(const void* const input[], const int64_t* send_counts,
+                         int64_t* send_displs, int64_t* recv_counts,
+                         int64_t* recv_displs, void* const out[], int64_t P,
+                         int64_t core_num, int dtype,
+                         const int64_t* out_capacity, int32_t* status_dev,
+                         bra_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Utilities                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Human-readable name of a status code (static string, never NULL). */
+BRA_API const char* bra_status_str(int status);
+
+/*
+ * bra_l2_flush -- overwrite `bytes` bytes of the caller's device buffer `buf`
+ * with zeros from a grid-stride kernel on `stream`, so that data written
+ * earlier leaves L2 before a timed call (the L2-eviction workaround of
+ * [VCCL] §7 dev log item D).  Pass a buffer larger than L2.
+ * Returns BRA_ERR_NULLPTR, BRA_ERR_CUDA or BRA_OK.
+ */
+BRA_API int bra_l2_flush(void* buf, size_t bytes, bra_stream_t stream);
+
+/*
+ * bra_fault_status -- the watchdog word of the current device: 0, or the
+ * BRA_ERR_TIMEOUT code a tensor-core kernel recorded when one of its bounded
+ * waits gave up (the kernel then stops early and its output is incomplete).
+ * Synchronous (reads device memory after prior work on the legacy stream).
+ * With clear != 0 the word is reset to 0.  Returns BRA_OK or BRA_ERR_CUDA.
+ */
+BRA_API int bra_fault_status(int32_t* code, int clear);
+
+/* Library version, "major.minor.patch". */
+BRA_API const char* bra_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BMM_RS_A2A_H */

@@ -10,6 +10,9 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    # Build (or confirm up to date) the in-tree native library once per session.
+    from bmm_reducescatter_alltoall_gb300 import _build
+    _build.build()
 
 
 def pytest_collection_modifyitems(config, items):

@@ -1,0 +1,299 @@
+"""Host-side tests of the C ABI (no GPU needed, no kernel launched).
+
+The library is loaded through ctypes; every symbol the public header declares
+must be exported.  Pure host functions (launch width, shape inference) are
+compared bit-exactly with the oracle; argument validation is driven with
+stand-in pointer values on calls that must be rejected before any launch,
+and with `bmm_rs_a2a_variant`, which runs the same validation without
+launching, for calls that would be accepted.
+"""
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+import bmm_reducescatter_alltoall_gb300 as bra
+from oracle import a2av as oa
+from oracle import fused as of
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bmm_rs_a2a.h")
+
+OK, NULLPTR, INVALID, UNSUPPORTED = 0, 161001, 161002, 161003
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return bra.library()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    return re.findall(r"^BRA_API\s+[\w\s\*]+?\b(\w+)\s*\(", src, flags=re.M)
+
+
+def test_header_declares_the_entry_points():
+    names = set(_declared_functions())
+    assert {"bmm_rs_a2a", "all_to_all_v", "all_to_all_v_checked", "cal_all_to_all_v_blocks",
+            "bmm_rs_a2a_infer_shape", "bra_status_str"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert bra.status_str(OK) == "BRA_OK"
+    assert bra.status_str(INVALID) == "BRA_ERR_INVALID"
+    assert bra.status_str(12345) == "BRA_UNKNOWN_STATUS"
+    assert bra.version().count(".") == 2
+
+
+def test_cal_blocks_matches_oracle(lib):
+    for P in list(range(1, 40)) + [64, 1000]:
+        for L in list(range(0, 130)) + [2**31 - 1, 2**31, -5]:
+            assert bra.cal_all_to_all_v_blocks(P, L) == oa.cal_all_to_all_v_blocks(P, L), (P, L)
+    assert bra.cal_all_to_all_v_blocks(0, 4) == -1
+
+
+def test_infer_shape_matches_oracle_and_rules(lib):
+    rng = np.random.default_rng(0)
+    seen_ok = seen_bad = 0
+    for _ in range(3000):
+        # mostly valid draws, each perturbed in one field a third of the time
+        ep = int(rng.choice([1, 2, 4, 8, 16, 32]))
+        tp = int(rng.choice([1, 2, 4, 8, 16, 32]))
+        E = ep * int(rng.integers(1, 34))
+        t = int(rng.integers(0, 2))
+        C = tp * int(rng.integers(1, 20)) + (int(rng.integers(0, tp)) if t == 0 else 0)
+        M = tp * int(rng.integers(1, 3000))
+        H = tp * int(rng.integers(1, 3000)) + (int(rng.integers(0, tp)) if t == 1 else 0)
+        if rng.random() < 0.33:
+            k = int(rng.integers(0, 7))
+            if k == 0:
+                ep = int(rng.choice([0, 3, 64]))
+            elif k == 1:
+                tp = int(rng.choice([0, 5, 64]))
+            elif k == 2:
+                E = int(rng.choice([0, 1, 513, E + 1]))
+            elif k == 3:
+                C = int(rng.choice([0, -1, C + 1]))
+            elif k == 4:
+                M = int(rng.choice([0, M + 1, 65536 * tp]))
+            elif k == 5:
+                H = int(rng.choice([0, 65536, H + 1]))
+            else:
+                t = int(rng.choice([-1, 2]))
+        try:
+            want = of.infer_shapes(ep, tp, E, C, M, H, t)
+        except of.OracleParamError:
+            want = None
+        arrs = [(ctypes.c_int64 * 3)() for _ in range(4)]
+        rc = lib.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t, *arrs)
+        if want is None:
+            assert rc == INVALID, (ep, tp, E, C, M, H, t)
+            seen_bad += 1
+        else:
+            assert rc == OK
+            got = dict(zip(("x", "w", "bias", "y"), (tuple(a) for a in arrs)))
+            assert got == want
+            seen_ok += 1
+    assert seen_ok > 50 and seen_bad > 50
+    for ep, tp, t in itertools.product((1, 2, 4, 8, 16, 32), (1, 2, 4, 8, 16, 32), (0, 1)):
+        E, C, M, H = 2 * ep, 4 * tp, 6 * tp, 8 * tp
+        assert bra.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t) == of.infer_shapes(
+            ep, tp, E, C, M, H, t)
+
+
+# --------------------------------------------------------------------------
+# Fused-op validation
+# --------------------------------------------------------------------------
+
+class Fake:
+    """Stand-in device addresses laid out like real, disjoint buffers."""
+
+    def __init__(self, ep, tp, E, C, M, H, t, bias=True, base=1 << 40):
+        sh = of.infer_shapes(ep, tp, E, C, M, H, t)
+        P = ep * tp
+        nbytes = lambda s, es=2: int(np.prod(s)) * es
+        addr = base
+        self.x, self.w, self.b, self.y = [], [], [], []
+        for _ in range(P):
+            for lst, n in ((self.x, nbytes(sh["x"])), (self.w, nbytes(sh["w"])),
+                           (self.b, nbytes(sh["bias"], 4)), (self.y, nbytes(sh["y"]))):
+                lst.append(addr)
+                addr += (n + 4095) // 4096 * 4096 + 4096
+        if not bias:
+            self.b = None
+        self.args = (ep, tp, E, C, M, H, t)
+
+    def arrays(self):
+        mk = lambda v: None if v is None else bra._ptr_array(v)
+        return mk(self.x), mk(self.w), mk(self.b), mk(self.y)
+
+
+def _variant(lib, f, dtype=bra.FP16, **over):
+    x, w, b, y = f.arrays()
+    ep, tp, E, C, M, H, t = f.args
+    p = dict(ep=ep, tp=tp, E=E, C=C, M=M, H=H, t=t)
+    p.update(over)
+    return lib.bmm_rs_a2a_variant(x, w, b, p["ep"], p["tp"], p["E"], p["C"], p["M"], p["H"],
+                                  p["t"], dtype, y)
+
+
+def _call_rejected(lib, f, dtype=bra.FP16, **over):
+    """Call the real entry point; the arguments must be rejected."""
+    x, w, b, y = f.arrays()
+    ep, tp, E, C, M, H, t = f.args
+    p = dict(ep=ep, tp=tp, E=E, C=C, M=M, H=H, t=t, x=x, w=w, b=b, y=y)
+    p.update(over)
+    assert _variant(lib, f, dtype, **{k: v for k, v in over.items() if k in "ep tp E C M H t"}) < 0 \
+        or any(k in over for k in ("x", "w", "y", "b"))
+    return lib.bmm_rs_a2a(p["x"], p["w"], p["b"], p["ep"], p["tp"], p["E"], p["C"], p["M"],
+                          p["H"], p["t"], dtype, p["y"], None)
+
+
+def test_valid_shapes_choose_a_variant(lib):
+    f = Fake(4, 2, 16, 12, 12, 4, 1)                  # M/tp = 6: not 16-byte rows
+    assert _variant(lib, f) == bra.VARIANT_SIMT
+    g = Fake(8, 4, 64, 512, 8192, 4096, 1)
+    assert _variant(lib, g) == bra.VARIANT_TC
+    assert _variant(lib, Fake(8, 2, 64, 256, 4096, 4096, 0), bra.BF16) == bra.VARIANT_TC
+    assert _variant(lib, Fake(2, 2, 4, 4, 16, 20, 0)) == bra.VARIANT_SIMT   # H/tp = 10
+
+
+def test_forced_variant(lib, monkeypatch):
+    monkeypatch.setenv("BRA_FORCE_VARIANT", "simt")
+    assert _variant(lib, Fake(8, 4, 64, 512, 8192, 4096, 1)) == bra.VARIANT_SIMT
+    monkeypatch.setenv("BRA_FORCE_VARIANT", "tc")
+    assert _variant(lib, Fake(4, 2, 16, 12, 12, 4, 1)) == -UNSUPPORTED
+
+
+@pytest.mark.parametrize("over", [
+    dict(ep=3), dict(tp=64), dict(ep=0), dict(t=2), dict(t=-1), dict(E=1), dict(E=514),
+    dict(E=12, ep=8), dict(E=264, ep=8), dict(H=0), dict(H=65536), dict(M=7, tp=2),
+    dict(M=2 * 65536, tp=1), dict(C=0), dict(C=-3)])
+def test_attribute_rules_invalid(lib, over):
+    f = Fake(2, 2, 8, 4, 8, 8, 0)
+    assert _variant(lib, f, **over) == -INVALID
+    assert _call_rejected(lib, f, **over) == INVALID
+
+
+def test_shape_divisibility_per_shard_type(lib):
+    assert _variant(lib, Fake(2, 2, 8, 4, 8, 8, 0), H=9) == -INVALID       # H % tp, type 0
+    assert _variant(lib, Fake(2, 2, 8, 4, 8, 8, 1), C=5) == -INVALID       # C % tp, type 1
+    assert _variant(lib, Fake(2, 2, 8, 4, 8, 8, 1), H=9) > 0               # fine for type 1
+    assert _variant(lib, Fake(2, 2, 8, 4, 8, 8, 0), C=5) > 0               # fine for type 0
+
+
+def test_dtype_rule(lib):
+    f = Fake(2, 2, 8, 4, 8, 8, 0)
+    for dt in (bra.FP32, bra.INT8, 7, -1):
+        assert _variant(lib, f, dt) == -INVALID
+        assert _call_rejected(lib, f, dt, ep=3) == INVALID
+
+
+def test_null_pointers(lib):
+    f = Fake(2, 2, 8, 4, 8, 8, 0)
+    assert _call_rejected(lib, f, x=None) == NULLPTR
+    assert _call_rejected(lib, f, w=None) == NULLPTR
+    assert _call_rejected(lib, f, y=None) == NULLPTR
+    for field in ("x", "w", "y"):
+        g = Fake(2, 2, 8, 4, 8, 8, 0)
+        getattr(g, field)[3] = 0
+        assert _variant(lib, g) == -NULLPTR
+        x, w, b, y = g.arrays()
+        assert lib.bmm_rs_a2a(x, w, b, 2, 2, 8, 4, 8, 8, 0, bra.FP16, y, None) == NULLPTR
+
+
+def test_bias_all_or_nothing(lib):
+    g = Fake(2, 2, 8, 4, 8, 8, 0)
+    g.b[1] = 0
+    assert _variant(lib, g) == -INVALID
+    x, w, b, y = g.arrays()
+    assert lib.bmm_rs_a2a(x, w, b, 2, 2, 8, 4, 8, 8, 0, bra.FP16, y, None) == INVALID
+    h = Fake(2, 2, 8, 4, 8, 8, 0)
+    h.b = [0, 0, 0, 0]
+    assert _variant(lib, h) > 0                   # all-null bias = no bias
+
+
+def test_aliasing_rules(lib):
+    g = Fake(2, 2, 8, 4, 8, 8, 0)
+    g.y[2] = g.x[1]                               # output == input
+    assert _variant(lib, g) == -INVALID
+    g = Fake(2, 2, 8, 4, 8, 8, 0)
+    g.y[0] = g.y[3]                               # two outputs share memory
+    assert _variant(lib, g) == -INVALID
+    g = Fake(2, 2, 8, 4, 8, 8, 0)
+    g.y[1] = g.w[2] + 64                          # output overlaps the inside of a weight
+    assert _variant(lib, g) == -INVALID
+    g = Fake(2, 2, 8, 4, 8, 8, 0)
+    g.w[1] = g.w[0]                               # shared weights are fine (read only)
+    assert _variant(lib, g) > 0
+    x, w, b, y = Fake(2, 2, 8, 4, 8, 8, 0).arrays()
+    g = Fake(2, 2, 8, 4, 8, 8, 0)
+    g.y[3] = g.b[0]
+    x, w, b, y = g.arrays()
+    assert lib.bmm_rs_a2a(x, w, b, 2, 2, 8, 4, 8, 8, 0, bra.FP16, y, None) == INVALID
+
+
+def test_tc_alignment_predicate(lib):
+    g = Fake(2, 2, 8, 128, 128, 256, 0)
+    assert _variant(lib, g) == bra.VARIANT_TC
+    g.x[1] += 2                                   # 2-byte aligned only
+    assert _variant(lib, g) == bra.VARIANT_SIMT
+
+
+# --------------------------------------------------------------------------
+# all_to_all_v validation
+# --------------------------------------------------------------------------
+
+def _a2av(lib, P=4, L=4, dtype=bra.FP32, ins=None, outs=None, sc=1 << 30, sd=2 << 30,
+          rc=3 << 30, rd=4 << 30, checked=False, cap=None, status=5 << 30):
+    ins = [(10 + k) << 32 for k in range(P)] if ins is None else ins
+    outs = [(100 + k) << 32 for k in range(P)] if outs is None else outs
+    ip = bra._ptr_array(ins) if ins != "null" else None
+    op = bra._ptr_array(outs) if outs != "null" else None
+    if not checked:
+        return lib.all_to_all_v(ip, sc, sd, rc, rd, op, P, L, dtype, None)
+    capp = None if cap == "null" else (ctypes.c_int64 * max(P, 1))(*([1 << 20] * max(P, 1)))
+    return lib.all_to_all_v_checked(ip, sc, sd, rc, rd, op, P, L, dtype, capp, status, None)
+
+
+@pytest.mark.parametrize("checked", [False, True])
+def test_a2av_rejections(lib, checked):
+    kw = dict(checked=checked)
+    assert _a2av(lib, P=0, **kw) == INVALID
+    assert _a2av(lib, P=-1, **kw) == INVALID
+    assert _a2av(lib, L=0, **kw) == INVALID
+    assert _a2av(lib, L=2**31, **kw) == INVALID
+    for dt in (bra.FP16, bra.BF16, 9):
+        assert _a2av(lib, dtype=dt, **kw) == INVALID
+    assert _a2av(lib, ins="null", **kw) == NULLPTR
+    assert _a2av(lib, outs="null", **kw) == NULLPTR
+    for key in ("sc", "sd", "rc", "rd"):
+        assert _a2av(lib, **{key: None}, **kw) == NULLPTR
+    assert _a2av(lib, ins=[1 << 32, 0, 3 << 32, 4 << 32], **kw) == NULLPTR
+    ins = [(10 + k) << 32 for k in range(4)]
+    assert _a2av(lib, ins=ins, outs=[5 << 40, ins[2], 6 << 40, 7 << 40], **kw) == INVALID
+    assert _a2av(lib, outs=[5 << 40, 6 << 40, 5 << 40, 7 << 40], **kw) == INVALID
+    assert _a2av(lib, P=65, L=65, **kw) == UNSUPPORTED
+    # B * P must fit a 32-bit grid: P = 64 with L near INT32_MAX
+    assert _a2av(lib, P=64, L=2**31 - 1, **kw) == INVALID
+    if checked:
+        assert _a2av(lib, cap="null", **kw) == NULLPTR
+        assert _a2av(lib, status=None, **kw) == NULLPTR
+
+
+def test_binding_rejects_host_tensors():
+    import torch
+    x = [torch.zeros(1, 8, 8, dtype=torch.float16) for _ in range(4)]
+    with pytest.raises(ValueError):
+        bra.bmm_rs_a2a(x, x, None, 2, 2, 2, 4, 16, 8, 0, out=x)
+    with pytest.raises(ValueError):
+        bra.all_to_all_v([torch.zeros(4)] * 2, torch.zeros(2, 2, dtype=torch.int64),
+                         [torch.zeros(4)] * 2, 2)

@@ -1,0 +1,190 @@
+"""Fused BMM -> ReduceScatter -> Add -> AllToAll on the GPU against the oracle.
+
+Tolerance: max|gpu - oracle| / max|oracle| <= 2e-3 for fp16 and 1e-2 for
+bf16, over every output element (small shapes) or over sampled elements
+computed one by one by the oracle (the full-size workloads).  Every case is
+also run without bias, so the bias (N(0,1), the largest term at the full
+sizes) cannot hide an error in the contraction.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bmm_reducescatter_alltoall_gb300 as bra
+from oracle import fused as of
+from workloads import FUSED_CONFIGS, FusedConfig, fused_inputs_device, fused_inputs_host
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"fp16": 2e-3, "bf16": 1e-2}
+
+
+def _to_dev(inp):
+    return {k: (None if v is None else [t.cuda() for t in v]) for k, v in inp.items()}
+
+
+def _run(cfg, dinp, variant=None, monkeypatch=None, prefill_nan=True):
+    dt = torch.float16 if cfg.dtype == "fp16" else torch.bfloat16
+    ys = bra.bmm_rs_a2a_infer_shape(cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H,
+                                    cfg.y_shard_type)["y"]
+    out = [torch.full(ys, float("nan") if prefill_nan else 0.0, dtype=dt, device="cuda")
+           for _ in range(cfg.P)]
+    if monkeypatch is not None:
+        if variant:
+            monkeypatch.setenv("BRA_FORCE_VARIANT", variant)
+        else:
+            monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
+    bra.bmm_rs_a2a(dinp["x"], dinp["w"], dinp["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M,
+                   cfg.H, cfg.y_shard_type, out=out)
+    torch.cuda.synchronize()
+    assert bra.fault_status() == 0
+    return out
+
+
+def _rel_err(gpu, ref):
+    g = np.concatenate([a.float().cpu().numpy().astype(np.float64).ravel() for a in gpu])
+    r = np.concatenate([a.ravel() for a in ref])
+    assert np.isfinite(g).all(), "an output element was not written"
+    return float(np.max(np.abs(g - r)) / max(np.max(np.abs(r)), 1e-30))
+
+
+def _oracle(cfg, inp):
+    return of.bmm_rs_a2a(inp["x"], inp["w"], inp["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M,
+                         cfg.H, cfg.y_shard_type, cfg.dtype)
+
+
+def _check_small(cfg, monkeypatch, variant=None, bias_ndim=3):
+    inp = fused_inputs_host(cfg, bias_ndim=bias_ndim)
+    ref = _oracle(cfg, inp)
+    out = _run(cfg, _to_dev(inp), variant, monkeypatch)
+    err = _rel_err(out, ref)
+    assert err <= TOL[cfg.dtype], f"{cfg} variant={variant}: rel err {err:.3e}"
+    return out, ref
+
+
+def test_eight_rank_example(monkeypatch):
+    cfg = FUSED_CONFIGS["ep4tp2_E16_C12_M12_H4_t1_fp16"]
+    _check_small(cfg, monkeypatch)
+    _check_small(cfg.replace(has_bias=False), monkeypatch)
+    _check_small(cfg, monkeypatch, bias_ndim=2)
+    # the same example with the H-sharded layout
+    _check_small(cfg.replace(y_shard_type=0), monkeypatch)
+
+
+# Shapes the tensor-core kernel takes, with ragged row / column / K tails.
+TC_CASES = [
+    # ep, tp, E, C, M, H, type, dtype
+    (2, 2, 4, 96, 256, 512, 0, "fp16"),
+    (4, 2, 8, 40, 208, 328, 1, "bf16"),
+    (1, 1, 2, 130, 72, 264, 0, "fp16"),
+    (2, 1, 4, 64, 64, 256, 1, "bf16"),
+    (8, 4, 16, 64, 256, 256, 1, "fp16"),
+    (4, 4, 8, 128, 512, 512, 0, "bf16"),
+    (8, 8, 8, 16, 128, 128, 0, "fp16"),       # P = 64
+    (16, 8, 16, 8, 64, 128, 0, "bf16"),       # P = 128: two launches
+    (2, 4, 4, 200, 96, 40, 1, "fp16"),        # H = 40 < one column tile
+    (2, 2, 2, 1, 16, 16, 0, "fp16"),          # one token
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES)
+@pytest.mark.parametrize("bias", [True, False])
+def test_tensor_core_kernel(case, bias, monkeypatch):
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("tc", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=sum(case[:6]), has_bias=bias)
+    inp = fused_inputs_host(cfg)
+    dinp = _to_dev(inp)
+    ys = bra.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t)["y"]
+    probe = [torch.empty(ys, dtype=dinp["x"][0].dtype, device="cuda") for _ in range(cfg.P)]
+    assert bra.bmm_rs_a2a_variant(dinp["x"], dinp["w"], dinp["bias"], ep, tp, E, C, M, H, t,
+                                  probe) == bra.VARIANT_TC
+    ref = _oracle(cfg, inp)
+    out = _run(cfg, dinp, "tc", monkeypatch)
+    err = _rel_err(out, ref)
+    assert err <= TOL[dt], f"{case} bias={bias}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("case", TC_CASES[:5])
+def test_generic_kernel_on_the_same_shapes(case, monkeypatch):
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("simt", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=sum(case[:6]) + 1)
+    _check_small(cfg, monkeypatch, variant="simt")
+
+
+@pytest.mark.parametrize("case", [
+    (2, 2, 4, 6, 12, 10, 0, "fp16"),      # H/tp = 5: unaligned rows
+    (4, 2, 8, 12, 14, 4, 1, "bf16"),      # M/tp = 7
+    (2, 1, 2, 3, 5, 7, 1, "fp16"),
+    (4, 4, 8, 8, 20, 36, 0, "bf16"),
+])
+def test_generic_kernel_unaligned_shapes(case, monkeypatch):
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("u", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=sum(case[:6]) + 2)
+    _check_small(cfg, monkeypatch)
+    _check_small(cfg.replace(has_bias=False), monkeypatch)
+
+
+def test_tc_and_generic_agree(monkeypatch):
+    cfg = FusedConfig("x", ep=4, tp=2, E=8, C=128, M=256, H=512, y_shard_type=1,
+                      dtype="bf16", seed=3)
+    dinp = _to_dev(fused_inputs_host(cfg))
+    a = _run(cfg, dinp, "tc", monkeypatch)
+    b = _run(cfg, dinp, "simt", monkeypatch)
+    ref = [t.float().cpu().numpy().astype(np.float64) for t in b]
+    assert _rel_err(a, ref) <= TOL["bf16"]
+
+
+# --------------------------------------------------------------------------
+# Full-size workloads, sampled outputs
+# --------------------------------------------------------------------------
+
+def _sample_points(cfg, rng, per_rank=24):
+    ys = of.infer_shapes(cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H, cfg.y_shard_type)["y"]
+    pts = []
+    for d in range(cfg.P):
+        edge = [(0, 0, 0), (ys[0] - 1, ys[1] - 1, ys[2] - 1),
+                (int(rng.integers(ys[0])), min(127, ys[1] - 1), min(255, ys[2] - 1)),
+                (int(rng.integers(ys[0])), min(128, ys[1] - 1), min(256, ys[2] - 1))]
+        pts += [(d,) + p for p in edge]
+        for _ in range(per_rank - len(edge)):
+            pts.append((d, int(rng.integers(ys[0])), int(rng.integers(ys[1])),
+                        int(rng.integers(ys[2]))))
+    return pts
+
+
+def _sampled_check(cfg, dinp, out, rng, per_rank):
+    El = cfg.E // cfg.ep
+    pts = _sample_points(cfg, rng, per_rank)
+    got, want = [], []
+    for (d, i, c, h) in pts:
+        src = of.y_source(cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.H, cfg.y_shard_type, d, i, c, h)
+        ranks = [src["s"] * cfg.tp + u for u in range(cfg.tp)]
+        rows = torch.stack([dinp["x"][r][src["e"], src["zrow"], :] for r in ranks]).float().cpu()
+        cols = torch.stack([dinp["w"][r][src["e"], :, src["zcol"]] for r in ranks]).float().cpu()
+        b = None
+        if dinp["bias"] is not None:
+            b = float(dinp["bias"][src["bias_rank"]].reshape(El, -1)[src["e"], src["bias_col"]])
+        want.append(of.bmm_rs_a2a_point(rows.numpy(), cols.numpy(), b, cfg.dtype))
+        got.append(float(out[d][i, c, h]))
+    got, want = np.array(got), np.array(want)
+    return float(np.max(np.abs(got - want)) / np.max(np.abs(want)))
+
+
+@pytest.mark.parametrize("name", ["ep8tp2_E64_C256_M4096_H4096_t0_bf16",
+                                  "ep8tp4_E64_C512_M8192_H4096_t1_fp16"])
+def test_full_size_workloads_sampled(name):
+    cfg = FUSED_CONFIGS[name]
+    rng = np.random.default_rng(99)
+    for bias in (True, False):
+        c = cfg.replace(has_bias=bias)
+        dinp = fused_inputs_device(c)
+        out = _run(c, dinp)
+        for y in out:                                  # every element written
+            assert not torch.isnan(y).any().item()
+        err = _sampled_check(c, dinp, out, rng, per_rank=12 if cfg.P > 16 else 24)
+        assert err <= TOL[cfg.dtype], f"{name} bias={bias}: sampled rel err {err:.3e}"
+        del dinp, out
+        torch.cuda.empty_cache()

@@ -55,9 +55,25 @@ def _digest(extra) -> str:
     return h.hexdigest()
 
 
-def source_digest() -> str:
-    """Hash of every kernel source and header (identifies a kernel build)."""
-    return _digest([])
+KERNEL_SOURCES = {
+    "fused_tc_kernel": "fused_tc.cu",
+    "fused_simt_kernel": "fused_simt.cu",
+    "a2av_kernel": "a2av.cu",
+}
+
+
+def source_digest(kernel: str = None) -> str:
+    """Hash identifying a kernel build: the kernel's translation unit plus
+    every header (all sources when `kernel` is None)."""
+    if kernel is None:
+        return _digest([])
+    h = hashlib.sha256()
+    for p in [os.path.join(CSRC, KERNEL_SOURCES[kernel])] + _headers():
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(ARCH + CFLAGS).encode())
+    return h.hexdigest()
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:

@@ -135,9 +135,10 @@ int a2av_common(const void* const input[], const int64_t* send_counts,
   if (core_num < 1 || core_num > kInt32Max) return BRA_ERR_INVALID;
   if (dtype != BRA_FP32 && dtype != BRA_INT8) return BRA_ERR_INVALID;
   if (P > bra::kA2avMaxP) return BRA_ERR_UNSUPPORTED;
-  for (int64_t r = 0; r < P; ++r)
-    if (!input[r] || !out[r]) return BRA_ERR_NULLPTR;
+  // NULL entries are allowed (a rank with nothing to send or receive may
+  // have an empty buffer); the kernel rejects a call that would touch one.
   for (int64_t j = 0; j < P; ++j) {
+    if (!out[j]) continue;
     for (int64_t i = 0; i < P; ++i)
       if (out[j] == input[i]) return BRA_ERR_INVALID;
     for (int64_t k = 0; k < j; ++k)
@@ -273,13 +274,18 @@ const char* bra_status_str(int status) {
 
 int bra_l2_flush(void* buf, size_t bytes, bra_stream_t stream) {
   if (!buf) return BRA_ERR_NULLPTR;
+  if (reinterpret_cast<uintptr_t>(buf) & 15u) return BRA_ERR_INVALID;
   cudaError_t e = bra::launch_l2_flush(buf, bytes, (cudaStream_t)stream);
   return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
 }
 
 int bra_fault_status(int32_t* code, int clear) {
   if (!code) return BRA_ERR_NULLPTR;
-  return bra::read_fault_word(code, clear) == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
+  int32_t a = 0, b = 0;
+  if (bra::read_fault_word(&a, clear) != cudaSuccess) return BRA_ERR_CUDA;
+  if (bra::read_a2av_fault_word(&b, clear) != cudaSuccess) return BRA_ERR_CUDA;
+  *code = a ? a : b;
+  return BRA_OK;
 }
 
 const char* bra_version(void) { return "0.1.0"; }

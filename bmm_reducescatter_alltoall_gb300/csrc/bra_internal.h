@@ -12,7 +12,7 @@ namespace bra {
 
 // all_to_all_v keeps the whole P x P count matrix of int64 in shared memory.
 constexpr int kA2avMaxP = 64;
-constexpr int kA2avThreads = 512;
+constexpr int kA2avThreads = 256;   // one producer warp + seven consumer warps
 
 // Fused kernels: one launch covers the TP groups of up to kChunkRanks source
 // ranks (their x / weight / bias), and may write to any of kMaxRanks outputs.
@@ -57,6 +57,7 @@ cudaError_t launch_fused_tc(const FusedProblem& f, cudaStream_t st);
 bool fused_tc_eligible(const FusedProblem& f);
 
 cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t st);
-cudaError_t read_fault_word(int32_t* code, int clear);
+cudaError_t read_fault_word(int32_t* code, int clear);        // tensor-core kernel
+cudaError_t read_a2av_fault_word(int32_t* code, int clear);   // all_to_all_v kernel
 
 }  // namespace bra

@@ -47,7 +47,10 @@ __device__ int32_t g_bra_fault_word = 0;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+#ifndef BRA_TC_STAGES
+#define BRA_TC_STAGES 4
+#endif
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = BRA_TC_STAGES;
 constexpr int A_BYTES = BM * BK * 2;              // 16 KiB
 constexpr int B_BOX_BYTES = 64 * BK * 2;          // one 64(N) x 64(K) box, 8 KiB
 constexpr int B_BYTES = BN * BK * 2;              // 32 KiB
@@ -198,17 +201,35 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Tile index -> (local group, m tile, n tile); n fastest so CTAs running at
-// the same time share the A rows and the weight columns of one group in L2.
+// Tile index -> (local group, m tile, n tile).  Within a group the tiles
+// are walked in super-rows of kGroupM m tiles: n tile by n tile, and inside
+// each n tile down the super-row's m tiles.  CTAs running at the same time
+// then share a few weight column bands and a few token row bands, and the
+// next wave reuses the super-row's token rows from L2.
+#ifndef BRA_TC_GROUP_M
+#define BRA_TC_GROUP_M 16
+#endif
+constexpr int kGroupM = BRA_TC_GROUP_M;
 struct TileCoord {
   int g, mt, nt;
 };
 __device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int tile) {
   TileCoord c;
-  c.nt = tile % p.n_tiles;
-  const int rest = tile / p.n_tiles;
-  c.mt = rest % p.m_tiles;
-  c.g = rest / p.m_tiles;
+  const int per_group = p.m_tiles * p.n_tiles;
+  c.g = tile / per_group;
+  const int t = tile - c.g * per_group;
+  if (kGroupM <= 0) {
+    c.mt = t / p.n_tiles;
+    c.nt = t - c.mt * p.n_tiles;
+    return c;
+  }
+  const int span = kGroupM * p.n_tiles;          // tiles in one full super-row
+  const int sr = t / span;
+  const int first_m = sr * kGroupM;
+  const int rows = min(kGroupM, p.m_tiles - first_m);
+  const int u = t - sr * span;
+  c.mt = first_m + u % rows;
+  c.nt = u / rows;
   return c;
 }
 

@@ -115,7 +115,7 @@ typedef enum {
  *   BRA_ERR_CUDA     the launch failed (cudaGetLastError).
  * Variant: the tensor-core kernel runs when every row stride and pointer is
  * 16-byte aligned (Kp % 8 == 0, H % 8 == 0, and Hp % 8 == 0 for yShardType
- * 0) and P <= 64; otherwise the generic kernel.  The environment variable
+ * 0); otherwise the generic kernel.  Both launch once per 64 source ranks.  The environment variable
  * BRA_FORCE_VARIANT=tc|simt overrides the choice (tc on an ineligible shape
  * returns BRA_ERR_UNSUPPORTED).
  */
@@ -175,27 +175,29 @@ BRA_API int64_t cal_all_to_all_v_blocks(int64_t P, int64_t L);
  *
  * Arguments:
  *   input[P]     device; input[i] holds at least sum_j send_counts[i][j]
- *                elements of `dtype`.
+ *                elements of `dtype` (may be NULL when that sum is 0).
  *   send_counts  device, int64 [P][P] row-major (read only).
  *   send_displs, recv_counts, recv_displs
  *                device, int64 [P][P] row-major, written by the kernel.
  *   out[P]       device; out[j] must hold sum_i send_counts[i][j] elements
- *                (the caller's obligation here; see all_to_all_v_checked).
+ *                (the caller's obligation here; see all_to_all_v_checked);
+ *                may be NULL when that sum is 0.
  *   P            number of ranks, 1 <= P <= 64.
  *   core_num     requested block count L per rank, in [1, INT32_MAX]; the
  *                exchange splits each rank's send buffer into
  *                B = cal_all_to_all_v_blocks(P, L) equal ranges.
  *   dtype        BRA_FP32 or BRA_INT8 ([PTO] §约束与诊断 allowlist).
  * Errors (nothing launched):
- *   BRA_ERR_NULLPTR  any pointer argument or array entry is NULL.
+ *   BRA_ERR_NULLPTR  input, out, send_counts or a bookkeeping array is NULL.
  *   BRA_ERR_INVALID  P < 1; core_num outside [1, INT32_MAX]; dtype not
  *                    FP32/INT8; an out[j] equal to any input[i] or to another
  *                    out[k] ([PTO] §当前限制: input != target, windows
  *                    pairwise distinct); B*P > INT32_MAX.
  *   BRA_ERR_UNSUPPORTED  P > 64.
  *   BRA_ERR_CUDA     the launch failed.
- * Device-side data check: if any send count is negative the kernel writes
- * nothing at all (no output, no bookkeeping).
+ * Device-side data check: if any send count is negative, or a NULL
+ * input[i] / out[j] would be read / written, the kernel writes nothing at all
+ * (no output, no bookkeeping).
  */
 BRA_API int all_to_all_v(const void* const input[], const int64_t* send_counts,
                  int64_t* send_displs, int64_t* recv_counts,
@@ -205,8 +207,9 @@ BRA_API int all_to_all_v(const void* const input[], const int64_t* send_counts,
 /*
  * all_to_all_v_checked -- all_to_all_v plus device-side checks whose result
  * is written to *status_dev (device int32): BRA_OK, or BRA_ERR_INVALID when a
- * send count is negative or some rank j would receive more than
- * out_capacity[j] elements; in the error case nothing else is written.
+ * send count is negative, a NULL buffer would be touched, or some rank j
+ * would receive more than out_capacity[j] elements; in the error case nothing
+ * else is written.
  * out_capacity: host array of P element counts (copied at the call).
  * status_dev: device pointer, required (BRA_ERR_NULLPTR if NULL).
  * The "0 / 1 / capacity / over-capacity / negative" count matrices of
@@ -227,18 +230,23 @@ BRA_API int all_to_all_v_checked(const void* const input[], const int64_t* send_
 BRA_API const char* bra_status_str(int status);
 
 /*
- * bra_l2_flush -- overwrite `bytes` bytes of the caller's device buffer `buf`
- * with zeros from a grid-stride kernel on `stream`, so that data written
- * earlier leaves L2 before a timed call (the L2-eviction workaround of
- * [VCCL] §7 dev log item D).  Pass a buffer larger than L2.
- * Returns BRA_ERR_NULLPTR, BRA_ERR_CUDA or BRA_OK.
+ * bra_l2_flush -- read the caller's device buffer `buf` (`bytes` bytes, whole
+ * 16-byte words; buf 16-byte aligned) through L2 from a grid-stride kernel on
+ * `stream`, so L2 holds clean lines of buf afterwards: data written earlier
+ * is back in HBM and written-back before the next timed call, whose inputs
+ * then come from HBM (the L2-eviction idea of [VCCL] §7 dev log item D, done
+ * with reads so the sweep itself leaves nothing dirty).  Pass a buffer larger
+ * than L2.  buf is not modified.
+ * Returns BRA_ERR_NULLPTR, BRA_ERR_INVALID (misaligned), BRA_ERR_CUDA or
+ * BRA_OK.
  */
 BRA_API int bra_l2_flush(void* buf, size_t bytes, bra_stream_t stream);
 
 /*
- * bra_fault_status -- the watchdog word of the current device: 0, or the
- * BRA_ERR_TIMEOUT code a tensor-core kernel recorded when one of its bounded
- * waits gave up (the kernel then stops early and its output is incomplete).
+ * bra_fault_status -- the watchdog words of the current device: 0, or the
+ * BRA_ERR_TIMEOUT code a kernel (tensor-core fused or all_to_all_v) recorded
+ * when one of its bounded waits gave up (the kernel then stops early and its
+ * output is incomplete).
  * Synchronous (reads device memory after prior work on the legacy stream).
  * With clear != 0 the word is reset to 0.  Returns BRA_OK or BRA_ERR_CUDA.
  */

@@ -223,8 +223,11 @@ def test_repeat_calls_are_identical():
         np.testing.assert_array_equal(x.view(np.uint32), y.view(np.uint32))
 
 
-def test_l2_flush_zeroes_buffer():
-    buf = torch.full((1 << 20) + 7, 3, dtype=torch.int8, device="cuda")
+def test_l2_flush_reads_without_writing():
+    buf = torch.arange((1 << 22) + 7, dtype=torch.int32, device="cuda").to(torch.int8)
+    before = buf.clone()
     bra.l2_flush(buf)
     torch.cuda.synchronize()
-    assert int(buf.abs().sum().item()) == 0
+    assert torch.equal(buf, before)
+    with pytest.raises(bra.BraError):
+        bra.l2_flush(buf[1:])                         # not 16-byte aligned

@@ -367,21 +367,6 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   }
 }
 
-// Reads every 16-byte word of buf through L2 (ld.global.cg, volatile so the
-// loads stay): L2 ends up holding clean lines of buf, so dirty lines left by
-// earlier kernels are written back here rather than inside the next timed
-// kernel.  buf is not modified.
-__global__ void l2_flush_kernel(const uint4* __restrict__ buf, size_t nvec) {
-  for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < nvec;
-       k += (size_t)gridDim.x * blockDim.x) {
-    uint32_t x, y, z, w;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(x), "=r"(y), "=r"(z), "=r"(w)
-                 : "l"(buf + k)
-                 : "memory");
-  }
-}
-
 int device_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -435,16 +420,6 @@ cudaError_t launch_a2av(const A2avArgs& a, int ctas_per_rank, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   dim3 grid(ctas_per_rank, a.P);
   a2av_kernel<<<grid, kA2avThreads, kRingBytes, st>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t st) {
-  // Whole 16-byte words only: a partial last word is not read.
-  const size_t nvec = bytes / 16;
-  if (nvec) {
-    const int blocks = 4 * device_sm_count();
-    l2_flush_kernel<<<blocks, 512, 0, st>>>(static_cast<const uint4*>(buf), nvec);
-  }
   return cudaGetLastError();
 }
 

@@ -35,7 +35,7 @@ METRIC = "fused BMM-RS-A2A TFLOP/s & all_to_all_v GB/s (1 GB300) vs roofline"
 def _args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=3)
@@ -104,9 +104,10 @@ class ClockSampler:
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
-        self.rows = []
+        self.rows = []           # (monotonic arrival time, fields)
         self.proc = None
         self.thread = None
+        self.window = None       # (t0, t1) of the timed region
 
     def start(self):
         try:
@@ -122,7 +123,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.rows.append([x.strip() for x in line.split(",")])
+            self.rows.append((time.monotonic(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -136,7 +140,13 @@ class ClockSampler:
             self.thread.join(timeout=5)
         sm, smax, reasons, power = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in self.rows:
+        rows = self.rows
+        if self.window is not None:
+            inside = [r for t, r in rows if self.window[0] <= t <= self.window[1]]
+            rows = inside if inside else [r for _, r in rows]
+        else:
+            rows = [r for _, r in rows]
+        for r in rows:
             try:
                 sm.append(float(r[1]))
                 smax.append(float(r[2]))
@@ -325,6 +335,10 @@ def run_ours(a):
     sweep = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     fused_launches = (cfg.ep + max(1, 64 // cfg.tp) - 1) // max(1, 64 // cfg.tp)
+    variant = bra.bmm_rs_a2a_variant(finp["x"], finp["w"], finp["bias"], cfg.ep, cfg.tp, cfg.E,
+                                     cfg.C, cfg.M, cfg.H, cfg.y_shard_type, yout)
+    fused_kernel = {bra.VARIANT_TC: "fused_tc_kernel", bra.VARIANT_TC2: "fused_tc2_kernel",
+                    bra.VARIANT_SIMT: "fused_simt_kernel"}[variant]
 
     def fused():
         bra.bmm_rs_a2a(finp["x"], finp["w"], finp["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M,
@@ -352,6 +366,7 @@ def run_ours(a):
     time.sleep(0.3)
     dist.barrier()
     torch.cuda.synchronize(dev)
+    wall0 = time.monotonic()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -365,7 +380,10 @@ def run_ours(a):
         ev[k][3].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
+    wall1 = time.monotonic()
     dist.barrier()
+    time.sleep(0.25)
+    sampler.mark(wall0, wall1)
     clocks = sampler.stop()
     if bra.fault_status() != 0:
         raise RuntimeError("watchdog word set during the timed region")
@@ -386,11 +404,12 @@ def run_ours(a):
     tpeak = peaks["bf16_tflops"] if timed_alone else peaks["bf16_tflops_sustained"]
     f_tflops = step_flops / (f_ms / 1e3) / 1e12
     a_gbs = a_bytes / (a_ms / 1e3) / 1e9
-    traffic = _traffic_record("fused_tc_kernel")
+    traffic = _traffic_record(fused_kernel)
     a_traffic = _traffic_record("a2av_kernel")
     roofline = {
-        "kernel": "fused_tc_kernel", "bound": "tensor", "achieved": f_tflops,
+        "kernel": fused_kernel, "bound": "tensor", "achieved": f_tflops,
         "peak": tpeak, "unit": "TFLOP/s", "frac": f_tflops / tpeak,
+        "frac_of_sustained": f_tflops / peaks["bf16_tflops_sustained"],
         "peak_source": f"{peaks['source']} {'burst' if timed_alone else 'sustained'} bf16 "
                        "(fp16 dense rate equals bf16)",
         "traffic": None if traffic is None else traffic["dram_bytes_per_launch"] * fused_launches,

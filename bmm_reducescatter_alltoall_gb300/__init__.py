@@ -15,14 +15,14 @@ import os
 from typing import List, Optional, Sequence
 
 __all__ = [
-    "BraError", "FP16", "BF16", "FP32", "INT8", "VARIANT_TC", "VARIANT_SIMT",
+    "BraError", "FP16", "BF16", "FP32", "INT8", "VARIANT_TC", "VARIANT_TC2", "VARIANT_SIMT",
     "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
     "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked",
     "cal_all_to_all_v_blocks", "l2_flush", "fault_status", "status_str", "version",
 ]
 
 FP16, BF16, FP32, INT8 = 0, 1, 2, 3
-VARIANT_TC, VARIANT_SIMT = 1, 2
+VARIANT_TC, VARIANT_SIMT, VARIANT_TC2 = 1, 2, 3
 OK, ERR_NULLPTR, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = (
     0, 161001, 161002, 161003, 161100, 161101)
 
@@ -196,7 +196,7 @@ def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
 
 
 def bmm_rs_a2a_variant(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out) -> int:
-    """VARIANT_TC or VARIANT_SIMT; raises BraError if the call would be rejected."""
+    """VARIANT_TC, VARIANT_TC2 or VARIANT_SIMT; raises BraError if rejected."""
     xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out)
     v = library().bmm_rs_a2a_variant(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp)
     if v < 0:

@@ -51,13 +51,15 @@ struct FusedProblem {
 };
 
 cudaError_t launch_fused_simt(const FusedProblem& f, cudaStream_t st);
-// Returns cudaErrorInvalidValue if a TMA descriptor cannot be encoded.
-cudaError_t launch_fused_tc(const FusedProblem& f, cudaStream_t st);
+// Both return cudaErrorInvalidValue if a TMA descriptor cannot be encoded.
+cudaError_t launch_fused_tc(const FusedProblem& f, cudaStream_t st);    // one CTA per tile
+cudaError_t launch_fused_tc2(const FusedProblem& f, cudaStream_t st);   // CTA pair per tile
 // Shape / alignment predicate of the tensor-core variant.
 bool fused_tc_eligible(const FusedProblem& f);
 
 cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t st);
 cudaError_t read_fault_word(int32_t* code, int clear);        // tensor-core kernel
+cudaError_t read_fault_word2(int32_t* code, int clear);       // CTA-pair tensor-core kernel
 cudaError_t read_a2av_fault_word(int32_t* code, int clear);   // all_to_all_v kernel
 
 }  // namespace bra

@@ -1,0 +1,314 @@
+// CTA-pair form of the tensor-core fused BMM -> TP ReduceScatter -> bias Add
+// -> EP AllToAll kernel (sm_103a): a cluster of two CTAs computes one
+// 256 x 256 output tile with tcgen05.mma.cta_group::2 (M=256, N=256, K=16).
+//
+// Same dataflow as fused_tc.cu (CANN guide "BatchMatMulReduceScatterAllToAll
+// 原理、shape 约束与 aclnn 两段式调用", 功能说明与计算流程): the K loop of a
+// tile spans the tp shards t = 0..tp-1 (the reduce-scatter sum, fp32, in t
+// order) and the epilogue adds the sender's bias and stores to the all-to-all
+// destination.  What changes is the split of one tile over two SMs:
+//   * CTA rank r of the pair loads A rows [256*mt + 128r, +128) and B columns
+//     [256*nt + 128r, +128) of every K block into its own shared memory; the
+//     pair MMA reads A by M and B by N from both CTAs, so each SM's shared
+//     memory carries 32 KiB per K block instead of 48 KiB for a one-CTA
+//     128 x 256 tile (operand reads plus TMA writes fit the shared-memory
+//     bandwidth).
+//   * Both CTAs' TMA loads complete on the leader's (rank 0) full barrier;
+//     the leader posts the expected bytes of both halves.
+//   * Only the leader issues MMAs; its commits multicast to the empty and
+//     accumulator-full barriers of both CTAs.
+//   * Each CTA's epilogue drains its own TMEM (its 128 rows x 256 columns)
+//     and arrives on the leader's accumulator-empty barrier (remote arrive
+//     for the peer).
+//   * TMEM: 512 columns allocated by the pair (tcgen05.alloc.cta_group::2 in
+//     both CTAs; both get the same column range): two accumulators.
+// Every wait is bounded (about 4 s by %globaltimer) and reports through the
+// device fault word; both CTAs always reach the closing cluster barrier and
+// free their tensor memory.
+#include <cstring>
+#include <memory>
+#include <mutex>
+
+#include "tc_ptx.cuh"
+
+namespace bra {
+
+__device__ int32_t g_bra_fault_word2 = 0;
+
+namespace {
+
+using namespace tc;
+
+#ifndef BRA_TC2_STAGES
+#define BRA_TC2_STAGES 6
+#endif
+#ifndef BRA_TC2_GROUP_M
+#define BRA_TC2_GROUP_M 16
+#endif
+constexpr int BM = 256;                           // rows per pair tile
+constexpr int BM_CTA = 128;                       // rows per CTA
+constexpr int BN = 256, BN_CTA = 128, BK = 64, STAGES = BRA_TC2_STAGES;
+constexpr int kGroupM = BRA_TC2_GROUP_M;
+constexpr int A_BYTES = BM_CTA * BK * 2;          // 16 KiB
+constexpr int B_BOX_BYTES = 64 * BK * 2;          // 8 KiB
+constexpr int B_BYTES = BN_CTA * BK * 2;          // 16 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 32 KiB per CTA
+constexpr int THREADS = 256;
+constexpr int EPI_WARP0 = 4;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int BAR_BYTES = 256;
+// B_BYTES of slack after the ring (barriers sit at its start): every operand
+// read of the last stage stays inside the allocation even for a full-width
+// B read.
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + B_BYTES + BAR_BYTES + 1024;
+
+template <typename T>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    fused_tc2_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t smem_base = smem_u32(smem);
+  uint8_t* bars = smem + STAGES * STAGE_BYTES;
+  const uint32_t bar_base = smem_u32(bars);
+  // barrier layout (8 bytes each): full[STAGES], empty[STAGES], tfull[2], tempty[2]
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 * (2 * STAGES + 4));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 8 * (2 * STAGES + 4) + 8);
+  int32_t* fault = &g_bra_fault_word2;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);     // leader: its expect_tx; both halves' bytes
+      mbar_init(empty_bar(s), 1);    // one multicast commit per use
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);    // one multicast commit per tile
+      mbar_init(tempty_bar(a), 8);   // leader: 4 epilogue warps of each CTA
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    for (int r = 0; r < p.nranks; ++r) {
+      tma_prefetch_desc(&p.tx[r]);
+      tma_prefetch_desc(&p.tw[r]);
+    }
+  }
+  if (warp == 2) {
+    tmem_alloc<2>(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish<2>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // barriers of both CTAs initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    const uint32_t leader_full0 = map_to_rank(full_bar(0), 0);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+      const TileCoord tc = tile_coord(tile, p.m_tiles, p.n_tiles, kGroupM);
+      const int sl = tc.g / p.El, e = tc.g % p.El;
+      const int a_row = tc.mt * BM + (int)rank * BM_CTA;
+      const int b_col = tc.nt * BN + (int)rank * BN_CTA;
+      for (int t = 0; ok && t < p.tp; ++t) {
+        const int r = sl * p.tp + t;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, fault)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+          const uint32_t fb = leader_full0 + 8u * stage;
+          const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          tma_load_3d_pair(a_dst, &p.tx[r], fb, kb * BK, a_row, e);
+#pragma unroll
+          for (int c = 0; c < BN_CTA / 64; ++c)
+            tma_load_3d_pair(b_dst + c * B_BOX_BYTES, &p.tw[r], fb, b_col + c * 64, kb * BK, e);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    if (!ok) spin_ns(2000000ull);   // let copies already issued land
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------- MMA issuer (leader only) ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+      if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, fault)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      const int kk_total = p.tp * p.k_blocks;
+      for (int kk = 0; kk < kk_total; ++kk) {
+        if (!mbar_wait(full_bar(stage), phase, abort_flag, fault)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = smem_base + stage * STAGE_BYTES;
+        const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(b_addr + k * 2048, p.b_lbo, p.b_sbo);
+          tc_mma<2>(d_tmem, ad, bd, p.idesc, (kk > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit_pair(empty_bar(stage), 0x3);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc_commit_pair(tfull_bar(acc), 0x3);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok) spin_ns(2000000ull);   // let MMAs already issued complete
+  } else if (warp >= EPI_WARP0) {
+    // ---------------- epilogue (both CTAs) ----------------
+    const int q = warp & 3;
+    const uint32_t leader_tempty0 = map_to_rank(tempty_bar(0), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = pair; tile < p.num_tiles; tile += npairs) {
+      const TileCoord tc = tile_coord(tile, p.m_tiles, p.n_tiles, kGroupM);
+      const int sl = tc.g / p.El, e = tc.g % p.El;
+      const bool waited = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, fault);
+      if (!__all_sync(0xffffffffu, waited)) break;
+      tc_fence_after();
+      const uint32_t t_base = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      const int m = tc.mt * BM + (int)rank * BM_CTA + q * 32 + lane;
+      epilogue_rows<T, BN>(p, t_base, m, sl, e, tc.nt * BN);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(tempty_bar(acc));
+        else
+          mbar_arrive_cluster(leader_tempty0 + 8u * acc);
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // no remote arrive or MMA of the pair still pending
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc<2>(tmem_base, TMEM_COLS);
+  }
+}
+
+struct DeviceInfo2 {
+  int pairs = 0;
+  bool ready = false;
+};
+
+template <typename T>
+cudaError_t setup_kernel(int* pairs) {
+  cudaError_t e = cudaFuncSetAttribute(fused_tc2_kernel<T>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, fused_tc2_kernel<T>, &cfg);
+  if (e != cudaSuccess) return e;
+  *pairs = n;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_fused_tc2(const FusedProblem& f, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static DeviceInfo2 info[64];
+  int pairs = 1;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    DeviceInfo2& di = info[dev & 63];
+    if (!di.ready) {
+      int a = 0, b = 0;
+      e = setup_kernel<__half>(&a);
+      if (e != cudaSuccess) return e;
+      e = setup_kernel<__nv_bfloat16>(&b);
+      if (e != cudaSuccess) return e;
+      di.pairs = a < b ? a : b;
+      if (di.pairs < 1) di.pairs = 1;
+      di.ready = true;
+    }
+    pairs = di.pairs;
+  }
+
+  std::unique_ptr<TcParams> p(new TcParams);
+  std::memset(p.get(), 0, sizeof(TcParams));
+  fill_common(p.get(), f, BM, BN, BK);
+  const bool bf16 = f.dtype == BRA_BF16;
+  p->idesc = make_idesc(bf16, BM, BN);
+  p->b_lbo = B_BOX_BYTES;
+  p->b_sbo = 1024;
+  const int s_per_launch = kChunkRanks / f.tp > 0 ? kChunkRanks / f.tp : 1;
+  for (int s0 = 0; s0 < f.ep; s0 += s_per_launch) {
+    const int s1 = s0 + s_per_launch < f.ep ? s0 + s_per_launch : f.ep;
+    if (!fill_chunk(p.get(), f, s0, s1, BM_CTA, 64, BK)) return cudaErrorInvalidValue;
+    p->num_tiles = (s1 - s0) * f.El * p->m_tiles * p->n_tiles;
+    const int np = p->num_tiles < pairs ? p->num_tiles : pairs;
+    if (bf16)
+      fused_tc2_kernel<__nv_bfloat16><<<2 * np, THREADS, SMEM_BYTES, st>>>(*p);
+    else
+      fused_tc2_kernel<__half><<<2 * np, THREADS, SMEM_BYTES, st>>>(*p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t read_fault_word2(int32_t* code, int clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(code, g_bra_fault_word2, sizeof(int32_t));
+  if (e != cudaSuccess) return e;
+  if (clear) {
+    const int32_t z = 0;
+    e = cudaMemcpyToSymbol(g_bra_fault_word2, &z, sizeof(int32_t));
+  }
+  return e;
+}
+
+}  // namespace bra

@@ -1,0 +1,471 @@
+// Inline-PTX building blocks shared by the sm_103a tensor-core fused kernels
+// (fused_tc.cu: one CTA per tile; fused_tc2.cu: a CTA pair per tile).
+//
+// mbarrier, TMA (cp.async.bulk.tensor), tcgen05 (alloc / mma / commit / ld),
+// the 128-byte-swizzle shared-memory matrix descriptor, cluster helpers, the
+// tile raster and the epilogue that turns one accumulator row into stores at
+// the all-to-all destinations.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "bra_internal.h"
+
+namespace bra {
+namespace tc {
+
+constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;
+
+// Kernel parameters of both tensor-core kernels (passed as __grid_constant__).
+struct TcParams {
+  CUtensorMap tx[kChunkRanks];   // x_r: dims {Kp, ep*C, El}
+  CUtensorMap tw[kChunkRanks];   // w_r: dims {H, Kp, El}
+  const void* bias[kChunkRanks];
+  void* y[kMaxRanks];
+  int ep, tp, El, C, Kp, H, type, has_bias;
+  int s0;                        // first source EP rank of this launch
+  int nranks;                    // ranks of this launch (x / weight / bias)
+  int rows;                      // ep * C
+  int m_tiles, n_tiles, k_blocks, num_tiles;
+  uint32_t idesc;                // tcgen05 instruction descriptor
+  uint32_t b_lbo, b_sbo;         // B operand strides (bytes)
+};
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Arrive on a barrier given by its shared::cluster address (any CTA of the
+// cluster), with release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for the phase with the given parity.  False when the CTA was
+// flagged by another role or the wait ran out (then this call flags the CTA
+// and records BRA_ERR_TIMEOUT in *fault_word).
+static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              int32_t* fault_word) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int k = 0; k < 64; ++k)
+      if (mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1;
+      atomicExch(fault_word, (int32_t)BRA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void spin_ns(unsigned long long ns) {
+  const unsigned long long t0 = global_ns();
+  while (global_ns() - t0 < ns) {
+  }
+}
+
+// ---------------------------------------------------------------------------
+// cluster
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+// Whole-cluster barrier; every thread of every CTA, converged warps.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// TMA
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// Load into this CTA's shared memory, completing on a barrier that may live
+// in either CTA of the pair (cluster_bar is a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t cluster_bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// With CG == 2 one warp of each CTA of the pair issues these together; the
+// pair gets the same column range in both CTAs.
+template <int CG>
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_relinquish() {
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// D (TMEM) [+]= A (smem) x B (smem), kind::f16 (fp16 or bf16 in, fp32 acc).
+template <int CG>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  if constexpr (CG == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every tcgen05 operation this thread issued so
+// far has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+// Pair form: arrive on the barrier at the same shared offset in every CTA
+// of `cta_mask`.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), version
+// 1: start address, leading and stride byte offsets in 16-byte units.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// tcgen05 instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
+// type (bits 7-9, 10-12: 0 fp16, 1 bf16), A K-major (bit 15 = 0), B N-major
+// (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+inline uint32_t make_idesc(bool bf16, int M, int N) {
+  const uint32_t ab = bf16 ? 1u : 0u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | (0u << 15) | (1u << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// Tile raster: within a group the tiles are walked in super-rows of kGroupM
+// m tiles: n tile by n tile, and inside each n tile down the super-row's m
+// tiles.  CTAs running at the same time then share a few weight column bands
+// and a few token row bands, and the next wave reuses the super-row's token
+// rows from L2.
+// ---------------------------------------------------------------------------
+struct TileCoord {
+  int g, mt, nt;
+};
+__device__ __forceinline__ TileCoord tile_coord(int tile, int m_tiles, int n_tiles, int group_m) {
+  TileCoord c;
+  const int per_group = m_tiles * n_tiles;
+  c.g = tile / per_group;
+  const int t = tile - c.g * per_group;
+  if (group_m <= 0) {
+    c.mt = t / n_tiles;
+    c.nt = t - c.mt * n_tiles;
+    return c;
+  }
+  const int span = group_m * n_tiles;
+  const int sr = t / span;
+  const int first_m = sr * group_m;
+  const int rows = min(group_m, m_tiles - first_m);
+  const int u = t - sr * span;
+  c.mt = first_m + u % rows;
+  c.nt = u / rows;
+  return c;
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Out;
+template <>
+struct Out<__half> {
+  static __device__ __forceinline__ uint32_t pack(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  // 8 bias values (fp16) starting at p.
+  static __device__ __forceinline__ void bias8(const void* p, float (&b)[8]) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __half22float2(h[k]);
+      b[2 * k] = f.x;
+      b[2 * k + 1] = f.y;
+    }
+  }
+  static constexpr int kBiasBytes = 2;
+};
+template <>
+struct Out<__nv_bfloat16> {
+  static __device__ __forceinline__ uint32_t pack(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  // 8 bias values (fp32) starting at p.
+  static __device__ __forceinline__ void bias8(const void* p, float (&b)[8]) {
+    const float4 u = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    b[0] = u.x; b[1] = u.y; b[2] = u.z; b[3] = u.w;
+    b[4] = v.x; b[5] = v.y; b[6] = v.z; b[7] = v.w;
+  }
+  static constexpr int kBiasBytes = 4;
+};
+
+// One epilogue warp drains its 32 TMEM lanes (32 accumulator rows) of a
+// BN-column accumulator: row m of Z_{s,e} (global row in ep*C), columns
+// n0 .. n0+BN-1.  Adds the sender's bias in fp32, rounds once, and stores
+// 16-byte vectors at the all-to-all destination
+//   yShardType 0: y[j*tp + n/Hp][s*El+e, m%C, n%Hp]
+//   yShardType 1: y[j*tp + (m%C)/Cp][s*El+e, (m%C)%Cp, n]      (j = m / C).
+// Every lane runs the tcgen05.ld (warp-wide); stores are masked per row.
+template <typename T, int BN>
+__device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base, int m, int sl,
+                                              int e, int n0) {
+  const int s = p.s0 + sl;
+  const bool row_ok = m < p.rows;
+  const int j = row_ok ? m / p.C : 0;
+  const int cm = row_ok ? m % p.C : 0;
+  const int Hp = p.H / p.tp;
+  int t1 = 0;
+  int64_t row1 = 0;
+  if (p.type == 1) {
+    const int Cp = p.C / p.tp;
+    t1 = cm / Cp;
+    row1 = ((int64_t)(s * p.El + e) * Cp + (cm % Cp)) * p.H;
+  }
+#pragma unroll 1
+  for (int ch = 0; ch < BN / 32; ++ch) {
+    uint32_t v[32];
+    tmem_ld32(t_base + ch * 32, v);
+    tmem_ld_wait();
+    if (!row_ok) continue;
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8) {
+      const int n = n0 + ch * 32 + g8 * 8;
+      if (n >= p.H) continue;
+      int t;
+      int64_t off, boff;
+      if (p.type == 0) {
+        t = n / Hp;
+        const int h = n - t * Hp;
+        off = ((int64_t)(s * p.El + e) * p.C + cm) * Hp + h;
+        boff = (int64_t)e * Hp + h;
+      } else {
+        t = t1;
+        off = row1 + n;
+        boff = (int64_t)e * p.H + n;
+      }
+      float f[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(v[g8 * 8 + k]);
+      if (p.has_bias) {
+        float b[8];
+        Out<T>::bias8(static_cast<const uint8_t*>(p.bias[sl * p.tp + t]) + boff * Out<T>::kBiasBytes,
+                      b);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] += b[k];
+      }
+      uint4 o;
+      o.x = Out<T>::pack(f[0], f[1]);
+      o.y = Out<T>::pack(f[2], f[3]);
+      o.z = Out<T>::pack(f[4], f[5]);
+      o.w = Out<T>::pack(f[6], f[7]);
+      T* yd = static_cast<T*>(p.y[j * p.tp + t]);
+      *reinterpret_cast<uint4*>(yd + off) = o;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host helpers
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 3-D 16-bit tensor {d0 (contiguous), d1, d2}, box {b0, b1, 1}, 128-byte
+// swizzle, zero fill outside the tensor.
+inline bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0,
+                      uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint32_t box[3] = {b0, b1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Fill the fields of TcParams common to every launch of one problem.
+inline void fill_common(TcParams* p, const FusedProblem& f, int bm, int bn, int bk) {
+  const int P = f.ep * f.tp;
+  for (int d = 0; d < P; ++d) p->y[d] = f.y[d];
+  p->ep = f.ep;
+  p->tp = f.tp;
+  p->El = f.El;
+  p->C = f.C;
+  p->Kp = f.Kp;
+  p->H = f.H;
+  p->type = f.type;
+  p->has_bias = f.bias != nullptr;
+  p->rows = f.ep * f.C;
+  p->m_tiles = (p->rows + bm - 1) / bm;
+  p->n_tiles = (f.H + bn - 1) / bn;
+  p->k_blocks = (f.Kp + bk - 1) / bk;
+}
+
+// Descriptors and bias pointers of the source ranks [s0, s1).
+inline bool fill_chunk(TcParams* p, const FusedProblem& f, int s0, int s1, uint32_t a_rows,
+                       uint32_t b_cols, int bk) {
+  const CUtensorMapDataType dt =
+      f.dtype == BRA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  p->s0 = s0;
+  p->nranks = (s1 - s0) * f.tp;
+  for (int r = 0; r < p->nranks; ++r) {
+    const int gr = s0 * f.tp + r;
+    if (!encode_3d(&p->tx[r], dt, f.x[gr], (uint64_t)f.Kp, (uint64_t)p->rows, (uint64_t)f.El,
+                   (uint32_t)bk, a_rows))
+      return false;
+    if (!encode_3d(&p->tw[r], dt, f.w[gr], (uint64_t)f.H, (uint64_t)f.Kp, (uint64_t)f.El,
+                   b_cols, (uint32_t)bk))
+      return false;
+    p->bias[r] = f.bias ? f.bias[gr] : nullptr;
+  }
+  return true;
+}
+
+}  // namespace tc
+}  // namespace bra

@@ -61,8 +61,9 @@ typedef enum { BRA_FP16 = 0, BRA_BF16 = 1, BRA_FP32 = 2, BRA_INT8 = 3 } bra_dtyp
 /* Kernel variants of bmm_rs_a2a (see bmm_rs_a2a_variant). */
 typedef enum {
   BRA_VARIANT_AUTO = 0,
-  BRA_VARIANT_TC = 1,    /* tcgen05 / TMEM / TMA tensor-core kernel        */
-  BRA_VARIANT_SIMT = 2   /* generic kernel: any alignment, any size        */
+  BRA_VARIANT_TC = 1,    /* tcgen05 / TMEM / TMA kernel, one CTA per tile  */
+  BRA_VARIANT_SIMT = 2,  /* generic kernel: any alignment, any size        */
+  BRA_VARIANT_TC2 = 3    /* tcgen05 kernel, a CTA pair per 256x256 tile    */
 } bra_variant;
 
 /* ------------------------------------------------------------------------ */
@@ -113,11 +114,13 @@ typedef enum {
  *                    input range or another output range.
  *   BRA_ERR_UNSUPPORTED  ep*C >= 2^31.
  *   BRA_ERR_CUDA     the launch failed (cudaGetLastError).
- * Variant: the tensor-core kernel runs when every row stride and pointer is
+ * Variant: a tensor-core kernel runs when every row stride and pointer is
  * 16-byte aligned (Kp % 8 == 0, H % 8 == 0, and Hp % 8 == 0 for yShardType
- * 0); otherwise the generic kernel.  Both launch once per 64 source ranks.  The environment variable
- * BRA_FORCE_VARIANT=tc|simt overrides the choice (tc on an ineligible shape
- * returns BRA_ERR_UNSUPPORTED).
+ * 0): the CTA-pair kernel when the problem has at least 64 output tiles of
+ * 256 x 256, else the one-CTA kernel; otherwise the generic kernel.  Each
+ * launches once per 64 source ranks.
+ * The environment variable BRA_FORCE_VARIANT=tc|tc2|simt overrides the
+ * choice (tc or tc2 on an ineligible shape returns BRA_ERR_UNSUPPORTED).
  */
 BRA_API int bmm_rs_a2a(const void* const x[], const void* const weight[],
                const void* const bias[], int64_t ep, int64_t tp, int64_t E,
@@ -139,7 +142,7 @@ BRA_API int bmm_rs_a2a_infer_shape(int64_t ep, int64_t tp, int64_t E, int64_t C,
 
 /*
  * bmm_rs_a2a_variant -- which kernel bmm_rs_a2a would launch for these
- * arguments (BRA_VARIANT_TC or BRA_VARIANT_SIMT), honouring
+ * arguments (BRA_VARIANT_TC, BRA_VARIANT_TC2 or BRA_VARIANT_SIMT), honouring
  * BRA_FORCE_VARIANT.  Pointers are only inspected for alignment.  Returns the
  * variant, or a negative bra_status (e.g. -BRA_ERR_INVALID) when bmm_rs_a2a
  * would reject the call.  Pure host function.
@@ -244,7 +247,7 @@ BRA_API int bra_l2_flush(void* buf, size_t bytes, bra_stream_t stream);
 
 /*
  * bra_fault_status -- the watchdog words of the current device: 0, or the
- * BRA_ERR_TIMEOUT code a kernel (tensor-core fused or all_to_all_v) recorded
+ * BRA_ERR_TIMEOUT code a kernel (a tensor-core fused kernel or all_to_all_v) recorded
  * when one of its bounded waits gave up (the kernel then stops early and its
  * output is incomplete).
  * Synchronous (reads device memory after prior work on the legacy stream).

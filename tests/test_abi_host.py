@@ -161,12 +161,16 @@ def test_valid_shapes_choose_a_variant(lib):
     f = Fake(4, 2, 16, 12, 12, 4, 1)                  # M/tp = 6: not 16-byte rows
     assert _variant(lib, f) == bra.VARIANT_SIMT
     g = Fake(8, 4, 64, 512, 8192, 4096, 1)
-    assert _variant(lib, g) == bra.VARIANT_TC
-    assert _variant(lib, Fake(8, 2, 64, 256, 4096, 4096, 0), bra.BF16) == bra.VARIANT_TC
+    assert _variant(lib, g) == bra.VARIANT_TC2
+    assert _variant(lib, Fake(8, 2, 64, 256, 4096, 4096, 0), bra.BF16) == bra.VARIANT_TC2
+    assert _variant(lib, Fake(2, 2, 4, 96, 256, 512, 0)) == bra.VARIANT_TC     # 4 pair tiles
     assert _variant(lib, Fake(2, 2, 4, 4, 16, 20, 0)) == bra.VARIANT_SIMT   # H/tp = 10
 
 
 def test_forced_variant(lib, monkeypatch):
+    monkeypatch.setenv("BRA_FORCE_VARIANT", "tc2")
+    assert _variant(lib, Fake(8, 4, 64, 512, 8192, 4096, 1)) == bra.VARIANT_TC2
+    assert _variant(lib, Fake(4, 2, 16, 12, 12, 4, 1)) == -UNSUPPORTED
     monkeypatch.setenv("BRA_FORCE_VARIANT", "simt")
     assert _variant(lib, Fake(8, 4, 64, 512, 8192, 4096, 1)) == bra.VARIANT_SIMT
     monkeypatch.setenv("BRA_FORCE_VARIANT", "tc")
@@ -243,7 +247,7 @@ def test_aliasing_rules(lib):
 
 def test_tc_alignment_predicate(lib):
     g = Fake(2, 2, 8, 128, 128, 256, 0)
-    assert _variant(lib, g) == bra.VARIANT_TC
+    assert _variant(lib, g) in (bra.VARIANT_TC, bra.VARIANT_TC2)
     g.x[1] += 2                                   # 2-byte aligned only
     assert _variant(lib, g) == bra.VARIANT_SIMT
 

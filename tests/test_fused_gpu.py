@@ -87,9 +87,10 @@ TC_CASES = [
 ]
 
 
+@pytest.mark.parametrize("variant", ["tc", "tc2"])
 @pytest.mark.parametrize("case", TC_CASES)
 @pytest.mark.parametrize("bias", [True, False])
-def test_tensor_core_kernel(case, bias, monkeypatch):
+def test_tensor_core_kernels(case, bias, variant, monkeypatch):
     ep, tp, E, C, M, H, t, dt = case
     cfg = FusedConfig("tc", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
                       seed=sum(case[:6]), has_bias=bias)
@@ -97,12 +98,14 @@ def test_tensor_core_kernel(case, bias, monkeypatch):
     dinp = _to_dev(inp)
     ys = bra.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t)["y"]
     probe = [torch.empty(ys, dtype=dinp["x"][0].dtype, device="cuda") for _ in range(cfg.P)]
+    monkeypatch.setenv("BRA_FORCE_VARIANT", variant)
+    want = bra.VARIANT_TC2 if variant == "tc2" else bra.VARIANT_TC
     assert bra.bmm_rs_a2a_variant(dinp["x"], dinp["w"], dinp["bias"], ep, tp, E, C, M, H, t,
-                                  probe) == bra.VARIANT_TC
+                                  probe) == want
     ref = _oracle(cfg, inp)
-    out = _run(cfg, dinp, "tc", monkeypatch)
+    out = _run(cfg, dinp, variant, monkeypatch)
     err = _rel_err(out, ref)
-    assert err <= TOL[dt], f"{case} bias={bias}: rel err {err:.3e}"
+    assert err <= TOL[dt], f"{case} bias={bias} {variant}: rel err {err:.3e}"
 
 
 @pytest.mark.parametrize("case", TC_CASES[:5])
@@ -127,11 +130,12 @@ def test_generic_kernel_unaligned_shapes(case, monkeypatch):
     _check_small(cfg.replace(has_bias=False), monkeypatch)
 
 
-def test_tc_and_generic_agree(monkeypatch):
+@pytest.mark.parametrize("variant", ["tc", "tc2"])
+def test_tc_and_generic_agree(variant, monkeypatch):
     cfg = FusedConfig("x", ep=4, tp=2, E=8, C=128, M=256, H=512, y_shard_type=1,
                       dtype="bf16", seed=3)
     dinp = _to_dev(fused_inputs_host(cfg))
-    a = _run(cfg, dinp, "tc", monkeypatch)
+    a = _run(cfg, dinp, variant, monkeypatch)
     b = _run(cfg, dinp, "simt", monkeypatch)
     ref = [t.float().cpu().numpy().astype(np.float64) for t in b]
     assert _rel_err(a, ref) <= TOL["bf16"]
@@ -173,15 +177,16 @@ def _sampled_check(cfg, dinp, out, rng, per_rank):
     return float(np.max(np.abs(got - want)) / np.max(np.abs(want)))
 
 
+@pytest.mark.parametrize("variant", [None, "tc", "tc2"])
 @pytest.mark.parametrize("name", ["ep8tp2_E64_C256_M4096_H4096_t0_bf16",
                                   "ep8tp4_E64_C512_M8192_H4096_t1_fp16"])
-def test_full_size_workloads_sampled(name):
+def test_full_size_workloads_sampled(name, variant, monkeypatch):
     cfg = FUSED_CONFIGS[name]
     rng = np.random.default_rng(99)
     for bias in (True, False):
         c = cfg.replace(has_bias=bias)
         dinp = fused_inputs_device(c)
-        out = _run(c, dinp)
+        out = _run(c, dinp, variant, monkeypatch)
         for y in out:                                  # every element written
             assert not torch.isnan(y).any().item()
         err = _sampled_check(c, dinp, out, rng, per_rank=12 if cfg.P > 16 else 24)

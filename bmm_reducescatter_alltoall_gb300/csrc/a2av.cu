@@ -44,8 +44,17 @@ __device__ int32_t g_a2av_fault_word = 0;
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kStages = 4;
-constexpr int kTileVecs = 1024;                          // 16 KiB of destination
+#ifndef BRA_A2AV_STAGES
+#define BRA_A2AV_STAGES 4
+#endif
+#ifndef BRA_A2AV_TILE_VECS
+#define BRA_A2AV_TILE_VECS 1024
+#endif
+#ifndef BRA_A2AV_MIN_CTAS
+#define BRA_A2AV_MIN_CTAS 2
+#endif
+constexpr int kStages = BRA_A2AV_STAGES;
+constexpr int kTileVecs = BRA_A2AV_TILE_VECS;            // 16-byte destination vectors
 constexpr int kStageBytes = (kTileVecs + 1) * 16;        // + one word when shifted
 constexpr int kStageStride = (kStageBytes + 127) / 128 * 128;
 constexpr int kRingBytes = kStages * kStageStride;
@@ -158,7 +167,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-__global__ void __launch_bounds__(kA2avThreads, 2)
+__global__ void __launch_bounds__(kA2avThreads, BRA_A2AV_MIN_CTAS)
 a2av_kernel(const __grid_constant__ A2avArgs a) {
   extern __shared__ __align__(128) uint8_t ring[];   // kStages x kStageStride
   __shared__ int64_t s_sc[kA2avMaxP * (kA2avMaxP + 1)];   // row stride P + 1
@@ -286,18 +295,6 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   }
   __syncthreads();
 
-  // Head and tail bytes of every piece.
-#pragma unroll 1
-  for (int k = tid; k < P * 32; k += blockDim.x) {
-    const int j = k >> 5, b = k & 31;
-    if (b < 16) {
-      if (b < s_head[j]) s_dst[j][b] = s_src[j][b];
-    } else if (b - 16 < s_tail[j]) {
-      const int64_t off = s_head[j] + s_nvec[j] * 16 + (b - 16);
-      s_dst[j][off] = s_src[j][off];
-    }
-  }
-
   // Vector parts: a bulk-copy producer and kConsumerWarps consumer warps.
   const int64_t ntiles = s_tile0[P];
   volatile int* abort_flag = &s_abort;
@@ -336,6 +333,17 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
     }
   } else {
     const int ctid = tid - 32, nct = kConsumerWarps * 32;
+    // Head and tail bytes of every piece, while the first tiles are in flight.
+#pragma unroll 1
+    for (int k = ctid; k < P * 32; k += nct) {
+      const int jj = k >> 5, b = k & 31;
+      if (b < 16) {
+        if (b < s_head[jj]) s_dst[jj][b] = s_src[jj][b];
+      } else if (b - 16 < s_tail[jj]) {
+        const int64_t off = s_head[jj] + s_nvec[jj] * 16 + (b - 16);
+        s_dst[jj][off] = s_src[jj][off];
+      }
+    }
     int j = 0, stage = 0;
     uint32_t phase = 0;
 #pragma unroll 1

@@ -43,7 +43,7 @@ using namespace tc;
 #define BRA_TC2_STAGES 6
 #endif
 #ifndef BRA_TC2_GROUP_M
-#define BRA_TC2_GROUP_M 16
+#define BRA_TC2_GROUP_M 8
 #endif
 constexpr int BM = 256;                           // rows per pair tile
 constexpr int BM_CTA = 128;                       // rows per CTA

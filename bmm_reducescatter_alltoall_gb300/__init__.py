@@ -16,7 +16,7 @@ from typing import List, Optional, Sequence
 
 __all__ = [
     "BraError", "FP16", "BF16", "FP32", "INT8", "VARIANT_TC", "VARIANT_TC2", "VARIANT_SIMT",
-    "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
+    "FusedOptions", "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
     "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked",
     "cal_all_to_all_v_blocks", "l2_flush", "fault_status", "status_str", "version",
 ]
@@ -29,6 +29,12 @@ OK, ERR_NULLPTR, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = (
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "lib", "libbmmrsa2a.so")
 _lib = None
+
+
+class FusedOptions(ctypes.Structure):
+    """bra_fused_options of the C header."""
+    _fields_ = [("transpose_weight", ctypes.c_int32), ("variant", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 6)]
 
 
 class BraError(RuntimeError):
@@ -52,7 +58,11 @@ def library() -> ctypes.CDLL:
     i64p = ctypes.POINTER(ctypes.c_int64)
     lib.bmm_rs_a2a.argtypes = [pp, pp, pp, i64, i64, i64, i64, i64, i64, i64, c_int, pp, vp]
     lib.bmm_rs_a2a.restype = c_int
-    lib.bmm_rs_a2a_variant.argtypes = [pp, pp, pp, i64, i64, i64, i64, i64, i64, i64, c_int, pp]
+    optp = ctypes.POINTER(FusedOptions)
+    lib.bmm_rs_a2a_ex.argtypes = [pp, pp, pp, i64, i64, i64, i64, i64, i64, i64, c_int, pp, optp, vp]
+    lib.bmm_rs_a2a_ex.restype = c_int
+    lib.bmm_rs_a2a_variant.argtypes = [pp, pp, pp, i64, i64, i64, i64, i64, i64, i64, c_int, pp,
+                                       optp]
     lib.bmm_rs_a2a_variant.restype = c_int
     lib.bmm_rs_a2a_infer_shape.argtypes = [i64] * 7 + [i64p] * 4
     lib.bmm_rs_a2a_infer_shape.restype = c_int
@@ -141,15 +151,31 @@ def _shape_check(t, want, what):
         raise ValueError(f"{what} has shape {tuple(t.shape)}, expected {tuple(want)}")
 
 
-def _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out):
+_VARIANTS = {None: 0, "auto": 0, "tc": VARIANT_TC, "tc2": VARIANT_TC2, "simt": VARIANT_SIMT}
+
+
+def _options(transpose_weight: bool, variant) -> "FusedOptions":
+    if variant not in _VARIANTS:
+        raise ValueError(f"variant must be one of {sorted(k for k in _VARIANTS if k)}")
+    o = FusedOptions()
+    o.transpose_weight = 1 if transpose_weight else 0
+    o.variant = _VARIANTS[variant]
+    return o
+
+
+def _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
+                transpose_weight=False):
     P = ep * tp
     if len(x) != P or len(weight) != P:
         raise ValueError(f"x and weight need ep*tp = {P} entries")
     shapes = bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type)
+    wshape = shapes["w"]
+    if transpose_weight:                      # stored as (El, H, Kp)
+        wshape = (wshape[0], wshape[2], wshape[1])
     dt = x[0].dtype
     for r in range(P):
         _shape_check(_dev_tensor(x[r], f"x[{r}]", dt), shapes["x"], f"x[{r}]")
-        _shape_check(_dev_tensor(weight[r], f"weight[{r}]", dt), shapes["w"], f"weight[{r}]")
+        _shape_check(_dev_tensor(weight[r], f"weight[{r}]", dt), wshape, f"weight[{r}]")
     bptr = None
     if bias is not None:
         if len(bias) != P:
@@ -178,27 +204,36 @@ def _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out):
 
 def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int, tp: int,
                E: int, C: int, M: int, H: int, y_shard_type: int,
-               out: Optional[Sequence] = None, stream=None) -> List:
+               out: Optional[Sequence] = None, stream=None, transpose_weight: bool = False,
+               variant: Optional[str] = None) -> List:
     """Fused BMM -> ReduceScatter -> Add -> AllToAll over P = ep*tp ranks.
 
     x[r], weight[r], bias[r] (or bias None) and out[r] are CUDA tensors of
     the shapes `bmm_rs_a2a_infer_shape` gives; out is allocated when None.
+    transpose_weight: weight[r] is stored as (El, H, Kp) instead of
+    (El, Kp, H).  variant: None/"auto", "tc", "tc2" or "simt".
     Returns out.  Asynchronous on `stream` (default: current stream).
     """
     torch = _torch()
     if out is None:
         ys = bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type)["y"]
         out = [torch.empty(ys, dtype=x[0].dtype, device=x[0].device) for _ in range(ep * tp)]
-    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out)
-    _check(library().bmm_rs_a2a(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp,
-                                _stream_handle(stream)), "bmm_rs_a2a")
+    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
+                                     transpose_weight)
+    opts = _options(transpose_weight, variant)
+    _check(library().bmm_rs_a2a_ex(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp,
+                                   ctypes.byref(opts), _stream_handle(stream)), "bmm_rs_a2a")
     return out
 
 
-def bmm_rs_a2a_variant(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out) -> int:
+def bmm_rs_a2a_variant(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
+                       transpose_weight: bool = False, variant: Optional[str] = None) -> int:
     """VARIANT_TC, VARIANT_TC2 or VARIANT_SIMT; raises BraError if rejected."""
-    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out)
-    v = library().bmm_rs_a2a_variant(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp)
+    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
+                                     transpose_weight)
+    opts = _options(transpose_weight, variant)
+    v = library().bmm_rs_a2a_variant(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp,
+                                     ctypes.byref(opts))
     if v < 0:
         raise BraError(-v, "bmm_rs_a2a_variant")
     return v

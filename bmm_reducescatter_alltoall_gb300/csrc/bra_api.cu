@@ -42,9 +42,17 @@ struct Range {
 int validate_fused(const void* const x[], const void* const weight[],
                    const void* const bias[], int64_t ep, int64_t tp, int64_t E,
                    int64_t C, int64_t M, int64_t H, int64_t type, int dtype,
-                   void* const out[], bra::FusedProblem* prob) {
+                   void* const out[], const bra_fused_options* opts,
+                   bra::FusedProblem* prob) {
   if (!x || !weight || !out) return BRA_ERR_NULLPTR;
   if (dtype != BRA_FP16 && dtype != BRA_BF16) return BRA_ERR_INVALID;
+  if (opts) {
+    for (int k = 0; k < 6; ++k)
+      if (opts->reserved[k] != 0) return BRA_ERR_INVALID;
+    if (opts->variant != BRA_VARIANT_AUTO && opts->variant != BRA_VARIANT_TC &&
+        opts->variant != BRA_VARIANT_TC2 && opts->variant != BRA_VARIANT_SIMT)
+      return BRA_ERR_INVALID;
+  }
   int rc = check_fused_attrs(ep, tp, E, C, M, H, type);
   if (rc != BRA_OK) return rc;
   const int64_t P = ep * tp;
@@ -98,6 +106,7 @@ int validate_fused(const void* const x[], const void* const weight[],
   prob->H = (int)H;
   prob->type = (int)type;
   prob->dtype = dtype;
+  prob->wt = (opts && opts->transpose_weight) ? 1 : 0;
   return BRA_OK;
 }
 
@@ -111,8 +120,8 @@ int forced_variant() {
   return BRA_VARIANT_AUTO;
 }
 
-int choose_variant(const bra::FusedProblem& p) {
-  const int f = forced_variant();
+int choose_variant(const bra::FusedProblem& p, const bra_fused_options* opts) {
+  const int f = (opts && opts->variant != BRA_VARIANT_AUTO) ? opts->variant : forced_variant();
   const bool tc_ok = bra::fused_tc_eligible(p);
   if (f == BRA_VARIANT_SIMT) return BRA_VARIANT_SIMT;
   if (f == BRA_VARIANT_TC || f == BRA_VARIANT_TC2) return tc_ok ? f : -BRA_ERR_UNSUPPORTED;
@@ -185,14 +194,14 @@ int a2av_common(const void* const input[], const int64_t* send_counts,
 
 extern "C" {
 
-int bmm_rs_a2a(const void* const x[], const void* const weight[],
-               const void* const bias[], int64_t ep, int64_t tp, int64_t E,
-               int64_t C, int64_t M, int64_t H, int64_t yShardType, int dtype,
-               void* const out[], bra_stream_t stream) {
+int bmm_rs_a2a_ex(const void* const x[], const void* const weight[],
+                  const void* const bias[], int64_t ep, int64_t tp, int64_t E,
+                  int64_t C, int64_t M, int64_t H, int64_t yShardType, int dtype,
+                  void* const out[], const bra_fused_options* opts, bra_stream_t stream) {
   bra::FusedProblem p;
-  int rc = validate_fused(x, weight, bias, ep, tp, E, C, M, H, yShardType, dtype, out, &p);
+  int rc = validate_fused(x, weight, bias, ep, tp, E, C, M, H, yShardType, dtype, out, opts, &p);
   if (rc != BRA_OK) return rc;
-  const int v = choose_variant(p);
+  const int v = choose_variant(p, opts);
   if (v < 0) return -v;
   if (log_enabled())
     std::fprintf(stderr, "[bra] bmm_rs_a2a ep=%lld tp=%lld E=%lld C=%lld M=%lld H=%lld type=%lld -> %s\n",
@@ -205,14 +214,23 @@ int bmm_rs_a2a(const void* const x[], const void* const weight[],
   return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
 }
 
+int bmm_rs_a2a(const void* const x[], const void* const weight[],
+               const void* const bias[], int64_t ep, int64_t tp, int64_t E,
+               int64_t C, int64_t M, int64_t H, int64_t yShardType, int dtype,
+               void* const out[], bra_stream_t stream) {
+  return bmm_rs_a2a_ex(x, weight, bias, ep, tp, E, C, M, H, yShardType, dtype, out, nullptr,
+                       stream);
+}
+
 int bmm_rs_a2a_variant(const void* const x[], const void* const weight[],
                        const void* const bias[], int64_t ep, int64_t tp,
                        int64_t E, int64_t C, int64_t M, int64_t H,
-                       int64_t yShardType, int dtype, void* const out[]) {
+                       int64_t yShardType, int dtype, void* const out[],
+                       const bra_fused_options* opts) {
   bra::FusedProblem p;
-  int rc = validate_fused(x, weight, bias, ep, tp, E, C, M, H, yShardType, dtype, out, &p);
+  int rc = validate_fused(x, weight, bias, ep, tp, E, C, M, H, yShardType, dtype, out, opts, &p);
   if (rc != BRA_OK) return -rc;
-  return choose_variant(p);
+  return choose_variant(p, opts);
 }
 
 int bmm_rs_a2a_infer_shape(int64_t ep, int64_t tp, int64_t E, int64_t C,

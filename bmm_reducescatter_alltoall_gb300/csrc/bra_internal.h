@@ -48,6 +48,7 @@ struct FusedProblem {
   int ep, tp, El, C, Kp, H;
   int type;                  // yShardType
   int dtype;                 // BRA_FP16 | BRA_BF16
+  int wt;                    // weight stored transposed: (El, H, Kp)
 };
 
 cudaError_t launch_fused_simt(const FusedProblem& f, cudaStream_t st);

@@ -33,6 +33,7 @@ struct SimtParams {
   const void* bias[kChunkRanks];
   void* y[kMaxRanks];
   int ep, tp, El, C, Kp, H, type, has_bias;
+  int wt;       // weight stored transposed: (El, H, Kp)
   int s0;       // first source EP rank of this launch
   int rows;     // ep * C
   int m_tiles;
@@ -86,7 +87,8 @@ fused_simt_kernel(const __grid_constant__ SimtParams p) {
           As[ak][am] = (gm < p.rows && gk < p.Kp) ? to_f<T>(X[(int64_t)gm * p.Kp + gk]) : 0.f;
           const int bk = idx / kTile, bn = idx % kTile;
           const int gk2 = k0 + bk, gn = n0 + bn;
-          Bs[bk][bn] = (gk2 < p.Kp && gn < p.H) ? to_f<T>(W[(int64_t)gk2 * p.H + gn]) : 0.f;
+          const int64_t widx = p.wt ? (int64_t)gn * p.Kp + gk2 : (int64_t)gk2 * p.H + gn;
+          Bs[bk][bn] = (gk2 < p.Kp && gn < p.H) ? to_f<T>(W[widx]) : 0.f;
         }
         __syncthreads();
         const int kn = min(kTk, p.Kp - k0);
@@ -157,6 +159,7 @@ cudaError_t launch_fused_simt(const FusedProblem& f, cudaStream_t st) {
   p->H = f.H;
   p->type = f.type;
   p->has_bias = f.bias != nullptr;
+  p->wt = f.wt;
   p->rows = f.ep * f.C;
   p->m_tiles = (p->rows + kTile - 1) / kTile;
   const int s_per_launch = kChunkRanks / f.tp > 0 ? kChunkRanks / f.tp : 1;

@@ -18,8 +18,10 @@
 //
 // Kernel shape: persistent, one 256-thread CTA per SM.
 //   warp 0 (one lane)  TMA producer: per K block one 128x64 A box and four
-//                      64x64 B boxes (B is the weight, N-contiguous) into a
-//                      4-stage ring guarded by full/empty mbarriers.
+//                      64x64 B boxes (B is the weight, N-contiguous; one
+//                      64x256 K-major box when the weight is stored
+//                      transposed) into a 4-stage ring guarded by full/empty
+//                      mbarriers.
 //   warp 1 (one lane)  MMA issuer: tcgen05.mma.cta_group::1.kind::f16,
 //                      M=128 N=256 K=16, four per K block; commits free the
 //                      stage and, at the end of a tile, publish the
@@ -131,9 +133,13 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_const
           const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
           tma_load_3d(a_dst, &p.tx[r], fb, kb * BK, tc.mt * BM, e);
+          if (p.b_kmajor) {
+            tma_load_3d(b_dst, &p.tw[r], fb, kb * BK, tc.nt * BN, e);   // BN rows x 128 B
+          } else {
 #pragma unroll
-          for (int c = 0; c < BN / 64; ++c)
-            tma_load_3d(b_dst + c * B_BOX_BYTES, &p.tw[r], fb, tc.nt * BN + c * 64, kb * BK, e);
+            for (int c = 0; c < BN / 64; ++c)
+              tma_load_3d(b_dst + c * B_BOX_BYTES, &p.tw[r], fb, tc.nt * BN + c * 64, kb * BK, e);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -166,9 +172,7 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_const
         for (int k = 0; k < BK / 16; ++k) {
           // A: K-major, 128-byte rows; K step of 16 elements = 32 bytes.
           const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
-          // B: N-major boxes of 64(N) x 64(K); K step of 16 rows = 2048 bytes.
-          const uint64_t bd = smem_desc_sw128(b_addr + k * 2048, p.b_lbo, p.b_sbo);
-          tc_mma<1>(d_tmem, ad, bd, p.idesc, (kk > 0 || k > 0) ? 1u : 0u);
+          tc_mma<1>(d_tmem, ad, b_desc(p, b_addr, k), p.idesc, (kk > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit(empty_bar(stage));
         if (++stage == STAGES) {
@@ -265,13 +269,13 @@ cudaError_t launch_fused_tc(const FusedProblem& f, cudaStream_t st) {
   std::memset(p.get(), 0, sizeof(TcParams));
   fill_common(p.get(), f, BM, BN, BK);
   const bool bf16 = f.dtype == BRA_BF16;
-  p->idesc = make_idesc(bf16, BM, BN);
+  p->idesc = make_idesc(bf16, BM, BN, f.wt != 0);
   p->b_lbo = B_BOX_BYTES;   // next 64-wide N group
   p->b_sbo = 1024;          // next 8 K rows
   const int s_per_launch = kChunkRanks / f.tp > 0 ? kChunkRanks / f.tp : 1;
   for (int s0 = 0; s0 < f.ep; s0 += s_per_launch) {
     const int s1 = s0 + s_per_launch < f.ep ? s0 + s_per_launch : f.ep;
-    if (!fill_chunk(p.get(), f, s0, s1, BM, 64, BK)) return cudaErrorInvalidValue;
+    if (!fill_chunk(p.get(), f, s0, s1, BM, 64, BK, BN)) return cudaErrorInvalidValue;
     p->num_tiles = (s1 - s0) * f.El * p->m_tiles * p->n_tiles;
     const int grid = p->num_tiles < sms ? p->num_tiles : sms;
     if (bf16)

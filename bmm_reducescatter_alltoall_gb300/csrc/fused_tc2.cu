@@ -135,9 +135,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
           tma_load_3d_pair(a_dst, &p.tx[r], fb, kb * BK, a_row, e);
+          if (p.b_kmajor) {
+            tma_load_3d_pair(b_dst, &p.tw[r], fb, kb * BK, b_col, e);   // 128 rows x 128 B
+          } else {
 #pragma unroll
-          for (int c = 0; c < BN_CTA / 64; ++c)
-            tma_load_3d_pair(b_dst + c * B_BOX_BYTES, &p.tw[r], fb, b_col + c * 64, kb * BK, e);
+            for (int c = 0; c < BN_CTA / 64; ++c)
+              tma_load_3d_pair(b_dst + c * B_BOX_BYTES, &p.tw[r], fb, b_col + c * 64, kb * BK, e);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -169,8 +173,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
           const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(b_addr + k * 2048, p.b_lbo, p.b_sbo);
-          tc_mma<2>(d_tmem, ad, bd, p.idesc, (kk > 0 || k > 0) ? 1u : 0u);
+          tc_mma<2>(d_tmem, ad, b_desc(p, b_addr, k), p.idesc, (kk > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit_pair(empty_bar(stage), 0x3);
         if (++stage == STAGES) {
@@ -282,13 +285,13 @@ cudaError_t launch_fused_tc2(const FusedProblem& f, cudaStream_t st) {
   std::memset(p.get(), 0, sizeof(TcParams));
   fill_common(p.get(), f, BM, BN, BK);
   const bool bf16 = f.dtype == BRA_BF16;
-  p->idesc = make_idesc(bf16, BM, BN);
+  p->idesc = make_idesc(bf16, BM, BN, f.wt != 0);
   p->b_lbo = B_BOX_BYTES;
   p->b_sbo = 1024;
   const int s_per_launch = kChunkRanks / f.tp > 0 ? kChunkRanks / f.tp : 1;
   for (int s0 = 0; s0 < f.ep; s0 += s_per_launch) {
     const int s1 = s0 + s_per_launch < f.ep ? s0 + s_per_launch : f.ep;
-    if (!fill_chunk(p.get(), f, s0, s1, BM_CTA, 64, BK)) return cudaErrorInvalidValue;
+    if (!fill_chunk(p.get(), f, s0, s1, BM_CTA, 64, BK, BN_CTA)) return cudaErrorInvalidValue;
     p->num_tiles = (s1 - s0) * f.El * p->m_tiles * p->n_tiles;
     const int np = p->num_tiles < pairs ? p->num_tiles : pairs;
     if (bf16)

@@ -33,7 +33,8 @@ struct TcParams {
   int rows;                      // ep * C
   int m_tiles, n_tiles, k_blocks, num_tiles;
   uint32_t idesc;                // tcgen05 instruction descriptor
-  uint32_t b_lbo, b_sbo;         // B operand strides (bytes)
+  uint32_t b_lbo, b_sbo;         // B operand strides (bytes), N-major weight
+  int b_kmajor;                  // weight stored transposed: B is K-major
 };
 
 // ---------------------------------------------------------------------------
@@ -250,11 +251,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 
 // tcgen05 instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
 // type (bits 7-9, 10-12: 0 fp16, 1 bf16), A K-major (bit 15 = 0), B N-major
-// (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-inline uint32_t make_idesc(bool bf16, int M, int N) {
+// (bit 16 = 1) or K-major (bit 16 = 0, transposed weight), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+inline uint32_t make_idesc(bool bf16, int M, int N, bool b_kmajor = false) {
   const uint32_t ab = bf16 ? 1u : 0u;
-  return (1u << 4) | (ab << 7) | (ab << 10) | (0u << 15) | (1u << 16) |
+  return (1u << 4) | (ab << 7) | (ab << 10) | (0u << 15) | ((b_kmajor ? 0u : 1u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Shared-memory descriptor of the B operand for K step k (16 elements):
+// N-major boxes of 64(N) x 64(K) -> 16 K rows = 2048 bytes further;
+// K-major rows of 128 bytes (transposed weight) -> 32 bytes further.
+__device__ __forceinline__ uint64_t b_desc(const TcParams& p, uint32_t b_addr, int k) {
+  return p.b_kmajor ? smem_desc_sw128(b_addr + k * 32, 16, 1024)
+                    : smem_desc_sw128(b_addr + k * 2048, p.b_lbo, p.b_sbo);
 }
 
 // ---------------------------------------------------------------------------
@@ -441,15 +451,18 @@ inline void fill_common(TcParams* p, const FusedProblem& f, int bm, int bn, int 
   p->H = f.H;
   p->type = f.type;
   p->has_bias = f.bias != nullptr;
+  p->b_kmajor = f.wt;
   p->rows = f.ep * f.C;
   p->m_tiles = (p->rows + bm - 1) / bm;
   p->n_tiles = (f.H + bn - 1) / bn;
   p->k_blocks = (f.Kp + bk - 1) / bk;
 }
 
-// Descriptors and bias pointers of the source ranks [s0, s1).
+// Descriptors and bias pointers of the source ranks [s0, s1).  The weight
+// box is 64 columns x bk rows for the N-major weight, or bk x b_rows_t
+// (K x N) for the transposed (K-major) weight.
 inline bool fill_chunk(TcParams* p, const FusedProblem& f, int s0, int s1, uint32_t a_rows,
-                       uint32_t b_cols, int bk) {
+                       uint32_t b_cols, int bk, uint32_t b_rows_t) {
   const CUtensorMapDataType dt =
       f.dtype == BRA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   p->s0 = s0;
@@ -459,9 +472,11 @@ inline bool fill_chunk(TcParams* p, const FusedProblem& f, int s0, int s1, uint3
     if (!encode_3d(&p->tx[r], dt, f.x[gr], (uint64_t)f.Kp, (uint64_t)p->rows, (uint64_t)f.El,
                    (uint32_t)bk, a_rows))
       return false;
-    if (!encode_3d(&p->tw[r], dt, f.w[gr], (uint64_t)f.H, (uint64_t)f.Kp, (uint64_t)f.El,
-                   b_cols, (uint32_t)bk))
-      return false;
+    const bool ok = f.wt ? encode_3d(&p->tw[r], dt, f.w[gr], (uint64_t)f.Kp, (uint64_t)f.H,
+                                     (uint64_t)f.El, (uint32_t)bk, b_rows_t)
+                         : encode_3d(&p->tw[r], dt, f.w[gr], (uint64_t)f.H, (uint64_t)f.Kp,
+                                     (uint64_t)f.El, b_cols, (uint32_t)bk);
+    if (!ok) return false;
     p->bias[r] = f.bias ? f.bias[gr] : nullptr;
   }
   return true;

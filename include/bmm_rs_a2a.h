@@ -127,6 +127,31 @@ BRA_API int bmm_rs_a2a(const void* const x[], const void* const weight[],
                int64_t C, int64_t M, int64_t H, int64_t yShardType, int dtype,
                void* const out[], bra_stream_t stream);
 
+/* Options of bmm_rs_a2a_ex.  Zero-initialise; unused fields must stay 0. */
+typedef struct {
+  /* Non-zero: weight[r] is stored transposed, as (El, H, Kp) row-major (the
+   * layout of a view of the (El, Kp, H) weight with its last two dims
+   * swapped, the transpose_weight attribute of [CANN] §参数说明 / §op_api 层
+   * TransTensor).  The values are the same; only the storage differs. */
+  int32_t transpose_weight;
+  /* BRA_VARIANT_AUTO (0) or a bra_variant to force; takes precedence over
+   * the BRA_FORCE_VARIANT environment variable. */
+  int32_t variant;
+  int32_t reserved[6];
+} bra_fused_options;
+
+/*
+ * bmm_rs_a2a_ex -- bmm_rs_a2a with options (NULL opts = all defaults, same
+ * as bmm_rs_a2a).  Errors as bmm_rs_a2a, plus BRA_ERR_INVALID for an
+ * unknown variant or a non-zero reserved field, and BRA_ERR_UNSUPPORTED when
+ * a forced tensor-core variant cannot take the shape or alignment.
+ */
+BRA_API int bmm_rs_a2a_ex(const void* const x[], const void* const weight[],
+                          const void* const bias[], int64_t ep, int64_t tp, int64_t E,
+                          int64_t C, int64_t M, int64_t H, int64_t yShardType, int dtype,
+                          void* const out[], const bra_fused_options* opts,
+                          bra_stream_t stream);
+
 /*
  * bmm_rs_a2a_infer_shape -- per-rank shapes from the attributes ([CANN]
  * §约束说明 and the infershape of §op_api 层): yShardType 0 gives
@@ -141,16 +166,17 @@ BRA_API int bmm_rs_a2a_infer_shape(int64_t ep, int64_t tp, int64_t E, int64_t C,
                            int64_t bias_shape[3], int64_t y_shape[3]);
 
 /*
- * bmm_rs_a2a_variant -- which kernel bmm_rs_a2a would launch for these
- * arguments (BRA_VARIANT_TC, BRA_VARIANT_TC2 or BRA_VARIANT_SIMT), honouring
- * BRA_FORCE_VARIANT.  Pointers are only inspected for alignment.  Returns the
- * variant, or a negative bra_status (e.g. -BRA_ERR_INVALID) when bmm_rs_a2a
- * would reject the call.  Pure host function.
+ * bmm_rs_a2a_variant -- which kernel bmm_rs_a2a_ex would launch for these
+ * arguments and options (BRA_VARIANT_TC, BRA_VARIANT_TC2 or
+ * BRA_VARIANT_SIMT), honouring BRA_FORCE_VARIANT.  Pointers are only
+ * inspected for alignment.  Returns the variant, or a negative bra_status
+ * (e.g. -BRA_ERR_INVALID) when the call would be rejected.  Pure host.
  */
 BRA_API int bmm_rs_a2a_variant(const void* const x[], const void* const weight[],
                        const void* const bias[], int64_t ep, int64_t tp,
                        int64_t E, int64_t C, int64_t M, int64_t H,
-                       int64_t yShardType, int dtype, void* const out[]);
+                       int64_t yShardType, int dtype, void* const out[],
+                       const bra_fused_options* opts);
 
 /* ------------------------------------------------------------------------ */
 /* all_to_all_v                                                              */

@@ -136,13 +136,13 @@ class Fake:
         return mk(self.x), mk(self.w), mk(self.b), mk(self.y)
 
 
-def _variant(lib, f, dtype=bra.FP16, **over):
+def _variant(lib, f, dtype=bra.FP16, opts=None, **over):
     x, w, b, y = f.arrays()
     ep, tp, E, C, M, H, t = f.args
     p = dict(ep=ep, tp=tp, E=E, C=C, M=M, H=H, t=t)
     p.update(over)
     return lib.bmm_rs_a2a_variant(x, w, b, p["ep"], p["tp"], p["E"], p["C"], p["M"], p["H"],
-                                  p["t"], dtype, y)
+                                  p["t"], dtype, y, None if opts is None else ctypes.byref(opts))
 
 
 def _call_rejected(lib, f, dtype=bra.FP16, **over):
@@ -243,6 +243,26 @@ def test_aliasing_rules(lib):
     g.y[3] = g.b[0]
     x, w, b, y = g.arrays()
     assert lib.bmm_rs_a2a(x, w, b, 2, 2, 8, 4, 8, 8, 0, bra.FP16, y, None) == INVALID
+
+
+def test_options_select_the_variant_and_are_checked(lib, monkeypatch):
+    monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
+    g = Fake(8, 4, 64, 512, 8192, 4096, 1)
+    assert _variant(lib, g, opts=bra._options(False, "tc")) == bra.VARIANT_TC
+    assert _variant(lib, g, opts=bra._options(True, "simt")) == bra.VARIANT_SIMT
+    monkeypatch.setenv("BRA_FORCE_VARIANT", "simt")           # options win over the env
+    assert _variant(lib, g, opts=bra._options(False, "tc2")) == bra.VARIANT_TC2
+    bad = bra._options(False, None)
+    bad.variant = 9
+    assert _variant(lib, g, opts=bad) == -INVALID
+    bad = bra._options(False, None)
+    bad.reserved[3] = 1
+    assert _variant(lib, g, opts=bad) == -INVALID
+    x, w, b, y = g.arrays()
+    assert lib.bmm_rs_a2a_ex(x, w, b, 8, 4, 64, 512, 8192, 4096, 1, bra.FP16, y,
+                             ctypes.byref(bad), None) == INVALID
+    with pytest.raises(ValueError):
+        bra._options(False, "fastest")
 
 
 def test_tc_alignment_predicate(lib):

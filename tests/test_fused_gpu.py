@@ -193,3 +193,59 @@ def test_full_size_workloads_sampled(name, variant, monkeypatch):
         assert err <= TOL[cfg.dtype], f"{name} bias={bias}: sampled rel err {err:.3e}"
         del dinp, out
         torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------
+# transpose_weight: weight[r] stored as (El, H, Kp)
+# --------------------------------------------------------------------------
+
+TW_CASES = [
+    (2, 2, 4, 96, 256, 512, 0, "fp16"),
+    (4, 2, 8, 40, 208, 328, 1, "bf16"),
+    (8, 4, 16, 64, 256, 256, 1, "fp16"),
+    (2, 2, 4, 6, 12, 10, 0, "bf16"),          # unaligned: generic kernel only
+]
+
+
+@pytest.mark.parametrize("variant", ["tc", "tc2", "simt"])
+@pytest.mark.parametrize("case", TW_CASES)
+def test_transposed_weight(case, variant):
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("tw", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=sum(case[:6]) + 5)
+    inp = fused_inputs_host(cfg)
+    ref = _oracle(cfg, inp)
+    dinp = _to_dev(inp)
+    wt = [w.transpose(1, 2).contiguous() for w in dinp["w"]]
+    ys = bra.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t)["y"]
+    out = [torch.full(ys, float("nan"), dtype=dinp["x"][0].dtype, device="cuda")
+           for _ in range(cfg.P)]
+    aligned = (M // tp) % 8 == 0 and H % 8 == 0 and (t == 1 or (H // tp) % 8 == 0)
+    if variant != "simt" and not aligned:
+        with pytest.raises(bra.BraError):
+            bra.bmm_rs_a2a(dinp["x"], wt, dinp["bias"], ep, tp, E, C, M, H, t, out=out,
+                           transpose_weight=True, variant=variant)
+        return
+    bra.bmm_rs_a2a(dinp["x"], wt, dinp["bias"], ep, tp, E, C, M, H, t, out=out,
+                   transpose_weight=True, variant=variant)
+    torch.cuda.synchronize()
+    assert bra.fault_status() == 0
+    err = _rel_err(out, ref)
+    assert err <= TOL[dt], f"{case} {variant} transposed: rel err {err:.3e}"
+
+
+def test_transposed_weight_full_size_sampled():
+    cfg = FUSED_CONFIGS["ep8tp2_E64_C256_M4096_H4096_t0_bf16"]
+    dinp = fused_inputs_device(cfg)
+    wt = [w.transpose(1, 2).contiguous() for w in dinp["w"]]
+    ys = bra.bmm_rs_a2a_infer_shape(cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H, 0)["y"]
+    out = [torch.full(ys, float("nan"), dtype=torch.bfloat16, device="cuda")
+           for _ in range(cfg.P)]
+    bra.bmm_rs_a2a(dinp["x"], wt, dinp["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H, 0,
+                   out=out, transpose_weight=True)
+    torch.cuda.synchronize()
+    assert bra.fault_status() == 0
+    for y in out:
+        assert not torch.isnan(y).any().item()
+    err = _sampled_check(cfg, dinp, out, np.random.default_rng(7), per_rank=16)
+    assert err <= TOL["bf16"], f"sampled rel err {err:.3e}"

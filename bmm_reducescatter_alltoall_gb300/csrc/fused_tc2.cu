@@ -1,14 +1,17 @@
 // CTA-pair form of the tensor-core fused BMM -> TP ReduceScatter -> bias Add
 // -> EP AllToAll kernel (sm_103a): a cluster of two CTAs computes one
-// 256 x 256 output tile with tcgen05.mma.cta_group::2 (M=256, N=256, K=16).
+// 256 x 256 (or 256 x 512) output tile with tcgen05.mma.cta_group::2
+// (M=256, N=256, K=16; two such MMAs per K step share the A slice for the
+// 512-wide tile).
 //
 // Same dataflow as fused_tc.cu (CANN guide "BatchMatMulReduceScatterAllToAll
 // 原理、shape 约束与 aclnn 两段式调用", 功能说明与计算流程): the K loop of a
 // tile spans the tp shards t = 0..tp-1 (the reduce-scatter sum, fp32, in t
 // order) and the epilogue adds the sender's bias and stores to the all-to-all
 // destination.  What changes is the split of one tile over two SMs:
-//   * CTA rank r of the pair loads A rows [256*mt + 128r, +128) and B columns
-//     [256*nt + 128r, +128) of every K block into its own shared memory; the
+//   * CTA rank r of the pair loads A rows [256*mt + 128r, +128) and, for each
+//     N=256 sub-tile, B columns [.. + 128r, +128) of every K block into its
+//     own shared memory; the
 //     pair MMA reads A by M and B by N from both CTAs, so each SM's shared
 //     memory carries 32 KiB per K block instead of 48 KiB for a one-CTA
 //     128 x 256 tile (operand reads plus TMA writes fit the shared-memory
@@ -21,7 +24,8 @@
 //     and arrives on the leader's accumulator-empty barrier (remote arrive
 //     for the peer).
 //   * TMEM: 512 columns allocated by the pair (tcgen05.alloc.cta_group::2 in
-//     both CTAs; both get the same column range): two accumulators.
+//     both CTAs; both get the same column range): two 256-column
+//     accumulators, or one 512-column accumulator for the wide tile.
 // Every wait is bounded (about 4 s by %globaltimer) and reports through the
 // device fault word; both CTAs always reach the closing cluster barrier and
 // free their tensor memory.
@@ -39,32 +43,41 @@ namespace {
 
 using namespace tc;
 
-#ifndef BRA_TC2_STAGES
-#define BRA_TC2_STAGES 6
-#endif
 #ifndef BRA_TC2_GROUP_M
 #define BRA_TC2_GROUP_M 8
 #endif
 constexpr int BM = 256;                           // rows per pair tile
 constexpr int BM_CTA = 128;                       // rows per CTA
-constexpr int BN = 256, BN_CTA = 128, BK = 64, STAGES = BRA_TC2_STAGES;
+constexpr int BK = 64;
 constexpr int kGroupM = BRA_TC2_GROUP_M;
 constexpr int A_BYTES = BM_CTA * BK * 2;          // 16 KiB
-constexpr int B_BOX_BYTES = 64 * BK * 2;          // 8 KiB
-constexpr int B_BYTES = BN_CTA * BK * 2;          // 16 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 32 KiB per CTA
+constexpr int B_BOX_BYTES = 64 * BK * 2;          // 8 KiB: 64 N-major columns
+constexpr int B_SUB_BYTES = 128 * BK * 2;         // 16 KiB: one CTA's half of N = 256
 constexpr int THREADS = 256;
 constexpr int EPI_WARP0 = 4;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
-// B_BYTES of slack after the ring (barriers sit at its start): every operand
-// read of the last stage stays inside the allocation even for a full-width
-// B read.
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + B_BYTES + BAR_BYTES + 1024;
 
-template <typename T>
+// A pair tile is 256 rows x (256 * NSUB) columns: NSUB N=256 MMAs per K step
+// share each A slice.  NSUB = 1: 6-stage ring of 32 KiB, two TMEM
+// accumulators (epilogue overlaps the next tile).  NSUB = 2: 4-stage ring of
+// 48 KiB, one 128 x 512 accumulator per CTA (all of TMEM), a quarter less
+// operand traffic per FLOP from L2 and through shared memory.
+template <int NSUB>
+struct Shape {
+  static constexpr int BN = 256 * NSUB;
+  static constexpr int B_BYTES = NSUB * B_SUB_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = NSUB == 1 ? 6 : 4;
+  static constexpr int NACC = NSUB == 1 ? 2 : 1;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+};
+
+template <typename T, int NSUB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fused_tc2_kernel(const __grid_constant__ TcParams p) {
+  using S = Shape<NSUB>;
+  constexpr int STAGES = S::STAGES, STAGE_BYTES = S::STAGE_BYTES, BN = S::BN, NACC = S::NACC;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -79,6 +92,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 * (2 * STAGES + 4));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 8 * (2 * STAGES + 4) + 8);
   int32_t* fault = &g_bra_fault_word2;
+  static_assert(8 * (2 * STAGES + 4) + 16 <= BAR_BYTES, "barrier area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -89,7 +103,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mbar_init(full_bar(s), 1);     // leader: its expect_tx; both halves' bytes
       mbar_init(empty_bar(s), 1);    // one multicast commit per use
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NACC; ++a) {
       mbar_init(tfull_bar(a), 1);    // one multicast commit per tile
       mbar_init(tempty_bar(a), 8);   // leader: 4 epilogue warps of each CTA
     }
@@ -122,7 +136,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const TileCoord tc = tile_coord(tile, p.m_tiles, p.n_tiles, kGroupM);
       const int sl = tc.g / p.El, e = tc.g % p.El;
       const int a_row = tc.mt * BM + (int)rank * BM_CTA;
-      const int b_col = tc.nt * BN + (int)rank * BN_CTA;
       for (int t = 0; ok && t < p.tp; ++t) {
         const int r = sl * p.tp + t;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -135,12 +148,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
           tma_load_3d_pair(a_dst, &p.tx[r], fb, kb * BK, a_row, e);
-          if (p.b_kmajor) {
-            tma_load_3d_pair(b_dst, &p.tw[r], fb, kb * BK, b_col, e);   // 128 rows x 128 B
-          } else {
 #pragma unroll
-            for (int c = 0; c < BN_CTA / 64; ++c)
-              tma_load_3d_pair(b_dst + c * B_BOX_BYTES, &p.tw[r], fb, b_col + c * 64, kb * BK, e);
+          for (int sub = 0; sub < NSUB; ++sub) {
+            // this CTA's 128 columns of N=256 sub-tile `sub`
+            const int b_col = tc.nt * BN + sub * 256 + (int)rank * 128;
+            const uint32_t bs = b_dst + sub * B_SUB_BYTES;
+            if (p.b_kmajor) {
+              tma_load_3d_pair(bs, &p.tw[r], fb, kb * BK, b_col, e);   // 128 rows x 128 B
+            } else {
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d_pair(bs + c * B_BOX_BYTES, &p.tw[r], fb, b_col + c * 64, kb * BK, e);
+            }
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -160,7 +179,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
       if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, fault)) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);   // acc = 0 when NACC = 1
       const int kk_total = p.tp * p.k_blocks;
       for (int kk = 0; kk < kk_total; ++kk) {
         if (!mbar_wait(full_bar(stage), phase, abort_flag, fault)) {
@@ -173,7 +192,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
           const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
-          tc_mma<2>(d_tmem, ad, b_desc(p, b_addr, k), p.idesc, (kk > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub)
+            tc_mma<2>(d_tmem + sub * 256, ad, b_desc(p, b_addr + sub * B_SUB_BYTES, k), p.idesc,
+                      (kk > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit_pair(empty_bar(stage), 0x3);
         if (++stage == STAGES) {
@@ -183,7 +205,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       if (!ok) break;
       tc_commit_pair(tfull_bar(acc), 0x3);
-      if (++acc == 2) {
+      if (++acc == NACC) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -212,7 +234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         else
           mbar_arrive_cluster(leader_tempty0 + 8u * acc);
       }
-      if (++acc == 2) {
+      if (++acc == NACC) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -229,19 +251,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 struct DeviceInfo2 {
-  int pairs = 0;
+  int pairs = 0;    // co-resident clusters, N = 256 pair tiles
+  int pairs2 = 0;   // co-resident clusters, N = 512 pair tiles
   bool ready = false;
 };
 
-template <typename T>
+template <typename T, int NSUB>
 cudaError_t setup_kernel(int* pairs) {
-  cudaError_t e = cudaFuncSetAttribute(fused_tc2_kernel<T>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  constexpr int smem = Shape<NSUB>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(fused_tc2_kernel<T, NSUB>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = 2;
@@ -250,9 +274,48 @@ cudaError_t setup_kernel(int* pairs) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, fused_tc2_kernel<T>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, fused_tc2_kernel<T, NSUB>, &cfg);
   if (e != cudaSuccess) return e;
   *pairs = n;
+  return cudaSuccess;
+}
+
+// Wide pair tiles (N = 512) when the columns fill them and the contraction
+// is long enough to hide the single accumulator's epilogue (measured: +13%
+// at M = 8192, -12% at M = 4096 against N = 256 tiles).
+#ifndef BRA_TC2_NSUB
+#define BRA_TC2_NSUB 0   // 0: choose by shape
+#endif
+int choose_nsub(const FusedProblem& f) {
+  if (BRA_TC2_NSUB == 1 || BRA_TC2_NSUB == 2) return BRA_TC2_NSUB;
+  const bool fills = f.H % 512 == 0 || f.H >= 2048;
+  const bool long_k = (int64_t)f.tp * f.Kp >= 6144;
+  return fills && long_k ? 2 : 1;
+}
+
+template <int NSUB>
+cudaError_t launch_nsub(const FusedProblem& f, int pairs, cudaStream_t st) {
+  using S = Shape<NSUB>;
+  std::unique_ptr<TcParams> p(new TcParams);
+  std::memset(p.get(), 0, sizeof(TcParams));
+  fill_common(p.get(), f, BM, S::BN, BK);
+  const bool bf16 = f.dtype == BRA_BF16;
+  p->idesc = make_idesc(bf16, BM, 256, f.wt != 0);
+  p->b_lbo = B_BOX_BYTES;
+  p->b_sbo = 1024;
+  const int s_per_launch = kChunkRanks / f.tp > 0 ? kChunkRanks / f.tp : 1;
+  for (int s0 = 0; s0 < f.ep; s0 += s_per_launch) {
+    const int s1 = s0 + s_per_launch < f.ep ? s0 + s_per_launch : f.ep;
+    if (!fill_chunk(p.get(), f, s0, s1, BM_CTA, 64, BK, 128)) return cudaErrorInvalidValue;
+    p->num_tiles = (s1 - s0) * f.El * p->m_tiles * p->n_tiles;
+    const int np = p->num_tiles < pairs ? p->num_tiles : pairs;
+    if (bf16)
+      fused_tc2_kernel<__nv_bfloat16, NSUB><<<2 * np, THREADS, S::SMEM_BYTES, st>>>(*p);
+    else
+      fused_tc2_kernel<__half, NSUB><<<2 * np, THREADS, S::SMEM_BYTES, st>>>(*p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   return cudaSuccess;
 }
 
@@ -264,44 +327,26 @@ cudaError_t launch_fused_tc2(const FusedProblem& f, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   static std::mutex mu;
   static DeviceInfo2 info[64];
-  int pairs = 1;
+  int pairs1 = 1, pairs2 = 1;
   {
     std::lock_guard<std::mutex> lk(mu);
     DeviceInfo2& di = info[dev & 63];
     if (!di.ready) {
-      int a = 0, b = 0;
-      e = setup_kernel<__half>(&a);
-      if (e != cudaSuccess) return e;
-      e = setup_kernel<__nv_bfloat16>(&b);
-      if (e != cudaSuccess) return e;
+      int a = 0, b = 0, c = 0, d = 0;
+      if ((e = setup_kernel<__half, 1>(&a)) != cudaSuccess) return e;
+      if ((e = setup_kernel<__nv_bfloat16, 1>(&b)) != cudaSuccess) return e;
+      if ((e = setup_kernel<__half, 2>(&c)) != cudaSuccess) return e;
+      if ((e = setup_kernel<__nv_bfloat16, 2>(&d)) != cudaSuccess) return e;
       di.pairs = a < b ? a : b;
+      di.pairs2 = c < d ? c : d;
       if (di.pairs < 1) di.pairs = 1;
+      if (di.pairs2 < 1) di.pairs2 = 1;
       di.ready = true;
     }
-    pairs = di.pairs;
+    pairs1 = di.pairs;
+    pairs2 = di.pairs2;
   }
-
-  std::unique_ptr<TcParams> p(new TcParams);
-  std::memset(p.get(), 0, sizeof(TcParams));
-  fill_common(p.get(), f, BM, BN, BK);
-  const bool bf16 = f.dtype == BRA_BF16;
-  p->idesc = make_idesc(bf16, BM, BN, f.wt != 0);
-  p->b_lbo = B_BOX_BYTES;
-  p->b_sbo = 1024;
-  const int s_per_launch = kChunkRanks / f.tp > 0 ? kChunkRanks / f.tp : 1;
-  for (int s0 = 0; s0 < f.ep; s0 += s_per_launch) {
-    const int s1 = s0 + s_per_launch < f.ep ? s0 + s_per_launch : f.ep;
-    if (!fill_chunk(p.get(), f, s0, s1, BM_CTA, 64, BK, BN_CTA)) return cudaErrorInvalidValue;
-    p->num_tiles = (s1 - s0) * f.El * p->m_tiles * p->n_tiles;
-    const int np = p->num_tiles < pairs ? p->num_tiles : pairs;
-    if (bf16)
-      fused_tc2_kernel<__nv_bfloat16><<<2 * np, THREADS, SMEM_BYTES, st>>>(*p);
-    else
-      fused_tc2_kernel<__half><<<2 * np, THREADS, SMEM_BYTES, st>>>(*p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  return choose_nsub(f) == 2 ? launch_nsub<2>(f, pairs2, st) : launch_nsub<1>(f, pairs1, st);
 }
 
 cudaError_t read_fault_word2(int32_t* code, int clear) {

@@ -84,6 +84,9 @@ TC_CASES = [
     (16, 8, 16, 8, 64, 128, 0, "bf16"),       # P = 128: two launches
     (2, 4, 4, 200, 96, 40, 1, "fp16"),        # H = 40 < one column tile
     (2, 2, 2, 1, 16, 16, 0, "fp16"),          # one token
+    (2, 2, 4, 64, 128, 2056, 1, "bf16"),
+    (2, 2, 4, 64, 6144, 2056, 1, "bf16"),     # 512-wide pair tiles (long K), ragged last tile
+    (2, 4, 4, 32, 8192, 512, 0, "fp16"),      # 512-wide pair tiles, tp = 4
 ]
 
 

@@ -65,7 +65,7 @@ constexpr int THREADS = 256;
 constexpr int EPI_WARP0 = 4;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 4 * kEpiStageBytes + 1024;
 
 template <typename T>
 __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_constant__ TcParams p) {
@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_const
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 * (2 * STAGES + 4));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 8 * (2 * STAGES + 4) + 8);
   int32_t* fault = &g_bra_fault_word;
+  // epilogue staging tiles (one per epilogue warp) after the barrier block
+  const uint32_t epi_stage_base = bar_base + BAR_BYTES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_const
   } else if (warp >= EPI_WARP0) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;                      // TMEM lane quarter
+    const uint32_t epi_stage = epi_stage_base + (uint32_t)q * kEpiStageBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_const
       if (!__all_sync(0xffffffffu, waited)) break;
       tc_fence_after();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      epilogue_rows<T, BN>(p, t_base, tc.mt * BM + q * 32 + lane, sl, e, tc.nt * BN);
+      epilogue_rows<T, BN>(p, t_base, tc.mt * BM + q * 32, sl, e, tc.nt * BN, epi_stage, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));

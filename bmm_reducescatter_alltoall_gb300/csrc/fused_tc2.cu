@@ -70,7 +70,7 @@ struct Shape {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = NSUB == 1 ? 6 : 4;
   static constexpr int NACC = NSUB == 1 ? 2 : 1;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 4 * kEpiStageBytes + 1024;
 };
 
 template <typename T, int NSUB>
@@ -92,6 +92,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 * (2 * STAGES + 4));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 8 * (2 * STAGES + 4) + 8);
   int32_t* fault = &g_bra_fault_word2;
+  // epilogue staging tiles (one per epilogue warp) after the barrier block
+  const uint32_t epi_stage_base = bar_base + BAR_BYTES;
   static_assert(8 * (2 * STAGES + 4) + 16 <= BAR_BYTES, "barrier area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -214,6 +216,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp >= EPI_WARP0) {
     // ---------------- epilogue (both CTAs) ----------------
     const int q = warp & 3;
+    const uint32_t epi_stage = epi_stage_base + (uint32_t)q * kEpiStageBytes;
     const uint32_t leader_tempty0 = map_to_rank(tempty_bar(0), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -224,8 +227,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (!__all_sync(0xffffffffu, waited)) break;
       tc_fence_after();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      const int m = tc.mt * BM + (int)rank * BM_CTA + q * 32 + lane;
-      epilogue_rows<T, BN>(p, t_base, m, sl, e, tc.nt * BN);
+      const int row0 = tc.mt * BM + (int)rank * BM_CTA + q * 32;
+      epilogue_rows<T, BN>(p, t_base, row0, sl, e, tc.nt * BN, epi_stage, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

@@ -337,56 +337,118 @@ struct Out<__nv_bfloat16> {
   static constexpr int kBiasBytes = 4;
 };
 
-// One epilogue warp drains its 32 TMEM lanes (32 accumulator rows) of a
-// BN-column accumulator: row m of Z_{s,e} (global row in ep*C), columns
-// n0 .. n0+BN-1.  Adds the sender's bias in fp32, rounds once, and stores
-// 16-byte vectors at the all-to-all destination
-//   yShardType 0: y[j*tp + n/Hp][s*El+e, m%C, n%Hp]
-//   yShardType 1: y[j*tp + (m%C)/Cp][s*El+e, (m%C)%Cp, n]      (j = m / C).
-// Every lane runs the tcgen05.ld (warp-wide); stores are masked per row.
+// Shared-memory staging per epilogue warp: 32 rows x 64 columns of the
+// output dtype (128 bytes) with rows 144 bytes apart, so the row-per-lane
+// writes and the row-segment reads are both free of bank conflicts.
+constexpr int kEpiRowStride = 144;
+constexpr int kEpiBiasBytes = 512 * 4;                // bias of up to 512 columns, fp32
+constexpr int kEpiStageBytes = 32 * kEpiRowStride + kEpiBiasBytes;   // per warp
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds128e(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// One epilogue warp drains its 32 TMEM lanes (accumulator rows row0 ..
+// row0+31 of Z_{s,e}, the global row index in ep*C) of a BN-column
+// accumulator, columns n0 .. n0+BN-1, 64 columns at a time:
+//   1. lane l holds row row0+l: tcgen05.ld two 32-column slices, add the
+//      sender's bias in fp32, round once, write the 128-byte row segment to
+//      the warp's staging tile;
+//   2. the warp stores the staging tile row segment by row segment: lanes
+//      8r'..8r'+7 write the 8 x 16 bytes of one row, 4 rows per instruction,
+//      each to its all-to-all destination
+//        yShardType 0: y[j*tp + n/Hp][s*El+e, m%C, n%Hp]
+//        yShardType 1: y[j*tp + (m%C)/Cp][s*El+e, (m%C)%Cp, n]   (j = m / C).
+// Every lane runs the warp-wide tcgen05.ld; stores are masked per row and
+// per 8 columns (H is a multiple of 8).
 template <typename T, int BN>
-__device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base, int m, int sl,
-                                              int e, int n0) {
+__device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base, int row0, int sl,
+                                              int e, int n0, uint32_t stage, int lane) {
+  static_assert(BN * 4 <= kEpiBiasBytes, "bias staging");
   const int s = p.s0 + sl;
-  const bool row_ok = m < p.rows;
-  const int j = row_ok ? m / p.C : 0;
-  const int cm = row_ok ? m % p.C : 0;
   const int Hp = p.H / p.tp;
-  int t1 = 0;
-  int64_t row1 = 0;
-  if (p.type == 1) {
-    const int Cp = p.C / p.tp;
-    t1 = cm / Cp;
-    row1 = ((int64_t)(s * p.El + e) * Cp + (cm % Cp)) * p.H;
-  }
-#pragma unroll 1
-  for (int ch = 0; ch < BN / 32; ++ch) {
-    uint32_t v[32];
-    tmem_ld32(t_base + ch * 32, v);
-    tmem_ld_wait();
-    if (!row_ok) continue;
-#pragma unroll
-    for (int g8 = 0; g8 < 4; ++g8) {
-      const int n = n0 + ch * 32 + g8 * 8;
-      if (n >= p.H) continue;
-      int t;
-      int64_t off, boff;
-      if (p.type == 0) {
-        t = n / Hp;
-        const int h = n - t * Hp;
-        off = ((int64_t)(s * p.El + e) * p.C + cm) * Hp + h;
-        boff = (int64_t)e * Hp + h;
-      } else {
-        t = t1;
-        off = row1 + n;
-        boff = (int64_t)e * p.H + n;
+  const int Cp = p.type == 1 ? p.C / p.tp : 1;
+  // yShardType 0: the bias depends on the column only, so the warp stages the
+  // tile's BN bias values (fp32) once and every row reads them by broadcast.
+  const uint32_t bias_stage = stage + 32 * kEpiRowStride;
+  const bool bias_staged = p.has_bias && p.type == 0;
+  if (bias_staged) {
+    for (int g = lane; g < BN / 8; g += 32) {
+      const int n = n0 + g * 8;
+      float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (n < p.H) {
+        const int t = n / Hp;
+        Out<T>::bias8(static_cast<const uint8_t*>(p.bias[sl * p.tp + t]) +
+                          ((int64_t)e * Hp + (n - t * Hp)) * Out<T>::kBiasBytes,
+                      b);
       }
+      sts128(bias_stage + g * 32, make_uint4(__float_as_uint(b[0]), __float_as_uint(b[1]),
+                                             __float_as_uint(b[2]), __float_as_uint(b[3])));
+      sts128(bias_stage + g * 32 + 16, make_uint4(__float_as_uint(b[4]), __float_as_uint(b[5]),
+                                                  __float_as_uint(b[6]), __float_as_uint(b[7])));
+    }
+    __syncwarp();
+  }
+  // this lane's own row (phase 1)
+  const int m_own = row0 + lane;
+  const bool own_ok = m_own < p.rows;
+  const int t_own = (own_ok && p.type == 1) ? (m_own % p.C) / Cp : 0;
+  // the 8 rows this lane stores (phase 2): r = 4q + lane/8
+  const int kc = lane & 7;
+  int64_t rbase[8];
+  int rdest[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int m = row0 + 4 * q + (lane >> 3);
+    if (m < p.rows) {
+      const int j = m / p.C, cm = m % p.C;
+      if (p.type == 0) {
+        rbase[q] = ((int64_t)(s * p.El + e) * p.C + cm) * Hp;
+        rdest[q] = j * p.tp;
+      } else {
+        rbase[q] = ((int64_t)(s * p.El + e) * Cp + (cm % Cp)) * p.H;
+        rdest[q] = j * p.tp + cm / Cp;
+      }
+    } else {
+      rdest[q] = -1;
+    }
+  }
+  const uint32_t my_row = stage + (uint32_t)lane * kEpiRowStride;
+#pragma unroll 1
+  for (int ch = 0; ch < BN / 64; ++ch) {
+    uint32_t v[64];
+    tmem_ld32(t_base + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+    tmem_ld32(t_base + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+    tmem_ld_wait();
+    // phase 1: bias, convert, stage the row segment
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) {
+      const int n = n0 + ch * 64 + g8 * 8;
       float f[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(v[g8 * 8 + k]);
-      if (p.has_bias) {
+      if (bias_staged) {
+        const uint32_t ba = bias_stage + (uint32_t)(ch * 64 + g8 * 8) * 4;
+        const uint4 b0 = lds128e(ba), b1 = lds128e(ba + 16);
+        f[0] += __uint_as_float(b0.x); f[1] += __uint_as_float(b0.y);
+        f[2] += __uint_as_float(b0.z); f[3] += __uint_as_float(b0.w);
+        f[4] += __uint_as_float(b1.x); f[5] += __uint_as_float(b1.y);
+        f[6] += __uint_as_float(b1.z); f[7] += __uint_as_float(b1.w);
+      } else if (p.has_bias && own_ok && n < p.H) {
+        // yShardType 1: the row picks the TP rank, hence the bias row.
         float b[8];
-        Out<T>::bias8(static_cast<const uint8_t*>(p.bias[sl * p.tp + t]) + boff * Out<T>::kBiasBytes,
+        Out<T>::bias8(static_cast<const uint8_t*>(p.bias[sl * p.tp + t_own]) +
+                          ((int64_t)e * p.H + n) * Out<T>::kBiasBytes,
                       b);
 #pragma unroll
         for (int k = 0; k < 8; ++k) f[k] += b[k];
@@ -396,9 +458,33 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base
       o.y = Out<T>::pack(f[2], f[3]);
       o.z = Out<T>::pack(f[4], f[5]);
       o.w = Out<T>::pack(f[6], f[7]);
-      T* yd = static_cast<T*>(p.y[j * p.tp + t]);
-      *reinterpret_cast<uint4*>(yd + off) = o;
+      sts128(my_row + g8 * 16, o);
     }
+    __syncwarp();
+    // phase 2: row segments to their destinations
+    const int n = n0 + ch * 64 + kc * 8;
+    if (n < p.H) {
+      const int t0 = p.type == 0 ? n / Hp : 0;
+      const int h0 = n - t0 * Hp;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (rdest[q] < 0) continue;
+        const int r = 4 * q + (lane >> 3);
+        const uint4 val = lds128e(stage + (uint32_t)r * kEpiRowStride + kc * 16);
+        int d;
+        int64_t off;
+        if (p.type == 0) {
+          d = rdest[q] + t0;
+          off = rbase[q] + h0;
+        } else {
+          d = rdest[q];
+          off = rbase[q] + n;
+        }
+        T* yd = static_cast<T*>(p.y[d]);
+        *reinterpret_cast<uint4*>(yd + off) = val;
+      }
+    }
+    __syncwarp();
   }
 }
 

@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_const
     if (!ok) spin_ns(2000000ull);   // let copies already issued land
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
+    const RingDescs rd = ring_descs(p, smem_base, smem_base + A_BYTES);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -168,14 +169,11 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_const
           break;
         }
         tc_fence_after();
-        const uint32_t a_addr = smem_base + stage * STAGE_BYTES;
-        const uint32_t b_addr = a_addr + A_BYTES;
+        const uint64_t so = (uint64_t)((stage * STAGE_BYTES) >> 4);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          // A: K-major, 128-byte rows; K step of 16 elements = 32 bytes.
-          const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
-          tc_mma<1>(d_tmem, ad, b_desc(p, b_addr, k), p.idesc, (kk > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < BK / 16; ++k)
+          tc_mma<1>(d_tmem, rd.a0 + so + 2 * k, rd.b0 + so + rd.b_kstep * k, p.idesc,
+                    (kk > 0 || k > 0) ? 1u : 0u);
         tc_commit(empty_bar(stage));
         if (++stage == STAGES) {
           stage = 0;

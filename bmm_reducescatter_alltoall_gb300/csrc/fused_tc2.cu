@@ -173,6 +173,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (!ok) spin_ns(2000000ull);   // let copies already issued land
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------- MMA issuer (leader only) ----------------
+    const RingDescs rd = ring_descs(p, smem_base, smem_base + A_BYTES);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -189,14 +190,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a_addr = smem_base + stage * STAGE_BYTES;
-        const uint32_t b_addr = a_addr + A_BYTES;
+        const uint64_t so = (uint64_t)((stage * STAGE_BYTES) >> 4);
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
 #pragma unroll
           for (int sub = 0; sub < NSUB; ++sub)
-            tc_mma<2>(d_tmem + sub * 256, ad, b_desc(p, b_addr + sub * B_SUB_BYTES, k), p.idesc,
+            tc_mma<2>(d_tmem + sub * 256, rd.a0 + so + 2 * k,
+                      rd.b0 + so + (uint64_t)((sub * B_SUB_BYTES) >> 4) + rd.b_kstep * k, p.idesc,
                       (kk > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit_pair(empty_bar(stage), 0x3);
@@ -283,18 +283,14 @@ cudaError_t setup_kernel(int* pairs) {
   return cudaSuccess;
 }
 
-// Wide pair tiles (N = 512) when the columns fill them and the contraction
-// is long enough to hide the single accumulator's epilogue (measured: +13%
-// at M = 8192, -12% at M = 4096 against N = 256 tiles).
+// Pair tiles 256 wide by default: with the MMA issue loop down to one add per
+// MMA, the double-buffered accumulator of the 256-wide tile beats the single
+// 512-wide accumulator on both workloads measured (M = 4096 and 8192).
+// BRA_TC2_NSUB=2 selects the 512-wide tile.
 #ifndef BRA_TC2_NSUB
-#define BRA_TC2_NSUB 0   // 0: choose by shape
+#define BRA_TC2_NSUB 1
 #endif
-int choose_nsub(const FusedProblem& f) {
-  if (BRA_TC2_NSUB == 1 || BRA_TC2_NSUB == 2) return BRA_TC2_NSUB;
-  const bool fills = f.H % 512 == 0 || f.H >= 2048;
-  const bool long_k = (int64_t)f.tp * f.Kp >= 6144;
-  return fills && long_k ? 2 : 1;
-}
+int choose_nsub(const FusedProblem&) { return BRA_TC2_NSUB == 2 ? 2 : 1; }
 
 template <int NSUB>
 cudaError_t launch_nsub(const FusedProblem& f, int pairs, cudaStream_t st) {

@@ -77,9 +77,10 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 // Bounded wait for the phase with the given parity.  False when the CTA was
 // flagged by another role or the wait ran out (then this call flags the CTA
-// and records BRA_ERR_TIMEOUT in *fault_word).
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                              int32_t* fault_word) {
+// and records BRA_ERR_TIMEOUT in *fault_word).  mbar_wait below checks the
+// phase inline first and only calls this slow path when it has to wait.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort_flag, int32_t* fault_word) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
@@ -93,6 +94,10 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int32_t* fault_word) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, fault_word);
 }
 __device__ __forceinline__ void spin_ns(unsigned long long ns) {
   const unsigned long long t0 = global_ns();
@@ -259,12 +264,24 @@ inline uint32_t make_idesc(bool bf16, int M, int N, bool b_kmajor = false) {
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Shared-memory descriptor of the B operand for K step k (16 elements):
-// N-major boxes of 64(N) x 64(K) -> 16 K rows = 2048 bytes further;
-// K-major rows of 128 bytes (transposed weight) -> 32 bytes further.
-__device__ __forceinline__ uint64_t b_desc(const TcParams& p, uint32_t b_addr, int k) {
-  return p.b_kmajor ? smem_desc_sw128(b_addr + k * 32, 16, 1024)
-                    : smem_desc_sw128(b_addr + k * 2048, p.b_lbo, p.b_sbo);
+// Operand descriptors of one CTA's ring, built once: the descriptor of any
+// stage / K step is the base descriptor plus the byte offset in 16-byte
+// units (the 14-bit start-address field; shared memory is below 256 KiB, so
+// the add never carries out of it).  A is K-major (K step of 16 elements =
+// 32 bytes); B is N-major boxes of 64(N) x 64(K) (K step = 16 rows = 2048
+// bytes) or, for a transposed weight, K-major (32 bytes).
+struct RingDescs {
+  uint64_t a0, b0;        // stage 0, K step 0
+  uint32_t b_kstep;       // B K step, 16-byte units
+};
+__device__ __forceinline__ RingDescs ring_descs(const TcParams& p, uint32_t a_addr0,
+                                                uint32_t b_addr0) {
+  RingDescs d;
+  d.a0 = smem_desc_sw128(a_addr0, 16, 1024);
+  d.b0 = p.b_kmajor ? smem_desc_sw128(b_addr0, 16, 1024)
+                    : smem_desc_sw128(b_addr0, p.b_lbo, p.b_sbo);
+  d.b_kstep = p.b_kmajor ? 2u : 128u;
+  return d;
 }
 
 // ---------------------------------------------------------------------------

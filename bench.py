@@ -42,6 +42,10 @@ def _args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused", default=FUSED_NAME)
     ap.add_argument("--a2av", default=A2AV_NAME)
+    ap.add_argument("--a2av-sweep", action="store_true",
+                    help="instead of the step: all_to_all_v alone over a range of sizes "
+                         "(L2 swept before every timed call), plus a CUDA graph of 100 "
+                         "back-to-back calls per size; one JSON line per size")
     return ap.parse_args(argv)
 
 
@@ -524,11 +528,120 @@ def run_ours(a):
         print(json.dumps(line), flush=True)
     dist.close()
 
+# --------------------------------------------------------------------------
+# all_to_all_v size sweep (not the step: a measurement of the exchange alone)
+# --------------------------------------------------------------------------
+
+# (base workload, field scaled, values): int8 P=32 Dirichlet rows from 64 KiB
+# to 32 MiB sent per rank, fp32 P=8 uniform counts from the workload's 4096
+# up to 8M per pair.
+SWEEP = [
+    ("P32_L64_int8_dirichlet0.3", "scale", [1 << 16, 1 << 18, 1 << 21, 1 << 23, 1 << 25]),
+    ("P8_L10_fp32_uniform4096", "count_max", [4096, 1 << 16, 1 << 20, 1 << 23]),
+]
+
+
+def run_a2av_sweep(a):
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from bmm_reducescatter_alltoall_gb300 import _build
+    _build.build()
+    import bmm_reducescatter_alltoall_gb300 as bra
+    from workloads import A2AV_CONFIGS, a2av_counts
+
+    peaks = _peaks()
+    sweep = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    timed = max(a.steps, 20)
+    for base, field, values in SWEEP:
+        for v in values:
+            cfg = A2AV_CONFIGS[base].replace(**{field: v})
+            sc = a2av_counts(cfg)
+            dt = torch.int8 if cfg.dtype == "int8" else torch.float32
+            g = torch.Generator(device=dev)
+            g.manual_seed(cfg.seed)
+            ins = []
+            for i in range(cfg.P):
+                n = int(sc[i].sum())
+                if dt == torch.int8:
+                    ins.append(torch.randint(-128, 128, (n,), generator=g, device=dev,
+                                             dtype=torch.int8))
+                else:
+                    ins.append(torch.randn(n, generator=g, device=dev))
+            outs = [torch.empty(int(c), dtype=dt, device=dev) for c in sc.sum(axis=0)]
+            sc_d = torch.from_numpy(sc).to(dev)
+            book = [torch.empty((cfg.P, cfg.P), dtype=torch.int64, device=dev)
+                    for _ in range(3)]
+
+            def call():
+                bra.all_to_all_v(ins, sc_d, outs, cfg.L, send_displs=book[0],
+                                 recv_counts=book[1], recv_displs=book[2])
+
+            for _ in range(max(a.warmup, 3)):
+                bra.l2_flush(sweep, stream=stream)
+                call()
+            torch.cuda.synchronize(dev)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(timed)]
+            for e0, e1 in ev:
+                torch.cuda._sleep(20_000_000)   # keeps the GPU busy so the host runs ahead
+                bra.l2_flush(sweep, stream=stream)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            us = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
+            med = statistics.median(us)
+
+            # 100 back-to-back calls in one CUDA graph: launch cost amortised,
+            # inputs warm in L2 where they fit
+            graph = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                call()
+            stream.wait_stream(side)
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(graph):
+                for _ in range(100):
+                    call()
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            for _ in range(3):
+                graph.replay()
+            g1.record(stream)
+            torch.cuda.synchronize(dev)
+            graph_us = g0.elapsed_time(g1) * 1e3 / 300
+            if bra.fault_status() != 0:
+                raise RuntimeError("watchdog word set during the sweep")
+
+            nbytes = 2 * int(sc.sum()) * ins[0].element_size() + 4 * sc.size * 8
+            gbs = nbytes / (med * 1e-6) / 1e9
+            print(json.dumps({
+                "sweep": "all_to_all_v", "workload": base, field: v, "P": cfg.P, "L": cfg.L,
+                "dtype": cfg.dtype, "bytes_moved": nbytes, "calls": timed,
+                "median_us": med, "min_us": us[0], "GB/s": gbs,
+                "frac_of_hbm": gbs / peaks["hbm_gbs"],
+                "graph_us_per_call": graph_us,
+                "graph_GB/s": nbytes / (graph_us * 1e-6) / 1e9,
+                "l2": "256 MiB read-only sweep before every timed call (not in the time); "
+                      "the graph replays run back to back without it",
+            }), flush=True)
+            del ins, outs, sc_d, book, graph
+            torch.cuda.empty_cache()
+
 
 def main(argv=None):
     a = _args(argv)
     if a.impl == "reference":
         run_reference(a)
+    elif a.a2av_sweep:
+        run_a2av_sweep(a)
     else:
         run_ours(a)
 

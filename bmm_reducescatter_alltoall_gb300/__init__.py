@@ -313,7 +313,8 @@ def all_to_all_v_checked(inputs: Sequence, send_counts, out: Sequence, core_num:
 
 
 def l2_flush(buf, stream=None) -> None:
-    """Zero `buf` (a CUDA tensor larger than L2) to evict earlier data from L2."""
+    """Read all of `buf` (a CUDA tensor larger than L2, contents unchanged) so
+    that earlier data is evicted from L2."""
     _dev_tensor(buf, "buf")
     _check(library().bra_l2_flush(buf.data_ptr(), buf.numel() * buf.element_size(),
                                   _stream_handle(stream)), "bra_l2_flush")

@@ -179,10 +179,9 @@ int a2av_common(const void* const input[], const int64_t* send_counts,
   a.rd = recv_displs;
   a.status = checked ? status_dev : nullptr;
   a.P = (int)P;
-  a.B = (int)B;
   a.esize = dtype == BRA_FP32 ? 4 : 1;
   a.check_cap = checked ? 1 : 0;
-  const int ctas = bra::a2av_ctas_per_rank((int)P, (int)B);
+  const int ctas = bra::a2av_ctas_per_rank((int)P);
   if (log_enabled())
     std::fprintf(stderr, "[bra] all_to_all_v P=%lld L=%lld B=%lld ctas/rank=%d grid=(%d,%lld)\n",
                  (long long)P, (long long)core_num, (long long)B, ctas, ctas, (long long)P);

@@ -29,15 +29,14 @@ struct A2avArgs {
   int64_t* rd;              // recv_displs [P][P]
   int32_t* status;          // optional device status word
   int P;
-  int B;                    // CalAllToAllVBlocks(P, L)
   int esize;                // element size in bytes (4 or 1)
   int check_cap;            // compare received totals against cap[]
 };
 
 // Launch the exchange with `ctas_per_rank` CTAs per source rank.
 cudaError_t launch_a2av(const A2avArgs& a, int ctas_per_rank, cudaStream_t st);
-// CTAs per rank that fill the GPU about once (never more than B).
-int a2av_ctas_per_rank(int P, int B);
+// CTAs per rank that fill the GPU once.
+int a2av_ctas_per_rank(int P);
 
 // Problem description shared by both fused variants.
 struct FusedProblem {

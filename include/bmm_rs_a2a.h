@@ -212,9 +212,11 @@ BRA_API int64_t cal_all_to_all_v_blocks(int64_t P, int64_t L);
  *                (the caller's obligation here; see all_to_all_v_checked);
  *                may be NULL when that sum is 0.
  *   P            number of ranks, 1 <= P <= 64.
- *   core_num     requested block count L per rank, in [1, INT32_MAX]; the
- *                exchange splits each rank's send buffer into
- *                B = cal_all_to_all_v_blocks(P, L) equal ranges.
+ *   core_num     requested block count L per rank, in [1, INT32_MAX],
+ *                validated with B = cal_all_to_all_v_blocks(P, L).  B is an
+ *                Ascend launch width; here each rank's send buffer is split
+ *                into as many equal ranges as fill the GPU once, which the
+ *                results do not depend on.
  *   dtype        BRA_FP32 or BRA_INT8 ([PTO] §约束与诊断 allowlist).
  * Errors (nothing launched):
  *   BRA_ERR_NULLPTR  input, out, send_counts or a bookkeeping array is NULL.

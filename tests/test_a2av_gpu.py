@@ -121,6 +121,18 @@ def test_workloads_bit_exact(name):
     del got
 
 
+@pytest.mark.parametrize("name,field,value", [
+    ("P32_L64_int8_dirichlet0.3", "scale", 1 << 23),     # ~8 MiB sent per rank
+    ("P8_L10_fp32_uniform4096", "count_max", 1 << 20),   # ~2 MiB per pair
+])
+def test_large_sizes_bit_exact(name, field, value):
+    """Sizes from the upper part of the bench's size sweep (256 MiB moved)."""
+    cfg = A2AV_CONFIGS[name].replace(**{field: value})
+    sc, inputs = a2av_inputs(cfg)
+    check_exact(sc, inputs, cfg.dtype, cfg.L, guard=5)
+    assert bra.fault_status() == 0
+
+
 @pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 32, 64])
 @pytest.mark.parametrize("dt", ["fp32", "int8"])
 def test_rank_counts_and_launch_widths(P, dt):

@@ -10,32 +10,36 @@
 // the launch width B = CalAllToAllVBlocks(P, L): B is the number of vector
 // cores an Ascend launch uses, which has no counterpart here, and the results
 // do not depend on how the copy is spread over CTAs.
-// Every CTA of source rank i:
-//   1. stages the whole P x P count matrix in shared memory (P <= 64, rows
-//      padded to P+1 so column reads hit distinct banks) and rejects the call
-//      if any count is negative, a non-zero count would touch a NULL buffer
-//      or (checked variant) a receive total is over capacity (every CTA sees
-//      the same matrix, so all take the same decision without a grid sync);
-//   2. warp-scans row i (its send displacements) and sums, per column j, the
-//      counts of sources k < i (its receive displacement at rank j) and of
-//      all sources (what rank j receives);
-//   3. CTA 0 of rank i writes row i of send_displs and column i of
-//      recv_counts / recv_displs;
-//   4. copies: rank i's send buffer is split into one equal element range
-//      per CTA, cut at the destination boundaries into at most P pieces; a
-//      piece is its 16-byte-aligned destination vectors plus head and tail
-//      bytes before the first / after the last vector.  The CTA's source
-//      bytes are contiguous, so one thread streams them through a
-//      kStages-deep shared-memory ring in chunks of kChunk bytes (16-byte
-//      granules, each chunk staged with one granule of overlap) with
-//      cp.async.bulk (TMA bulk copies, completion on an mbarrier).  For each
-//      chunk, seven consumer warps write every vector of every piece whose
-//      first source byte lies in the chunk, shifting the words into
-//      destination alignment (int8 can be off by any byte, fp32 by whole
-//      words), and 32 lanes write the head and tail bytes that lie in it.  A
-//      granule holding a byte of the buffer never crosses a page the buffer
-//      does not touch, so the granule-wide loads stay in bounds.  Up to
-//      kStages chunks per CTA are in flight without holding registers.
+//
+// A CTA of source rank i takes an equal element range [lo, hi) of rank i's
+// send buffer.  That range is contiguous in the source (the buffer is
+// ordered by destination) and cut at the destination boundaries into at
+// most P pieces; a piece is its 16-byte-aligned destination vectors plus
+// head and tail bytes before the first / after the last vector.  Roles:
+//   warp 0   reads row i of the counts from global memory, scans it (the
+//            send displacements), fixes [lo, hi) and publishes them; lane 0
+//            then streams the range through a kStages-deep shared-memory
+//            ring in chunks of kChunk bytes (16-byte granules, each chunk
+//            staged with one granule of overlap) with cp.async.bulk (TMA
+//            bulk copies, completion on an mbarrier), starting before the
+//            rest of the set-up is done;
+//   warps 1-7 (consumers) stage the whole P x P count matrix (P <= 64, rows
+//            padded to P+1 so column reads hit distinct banks) in the ring
+//            stages the producer fills last, reject the call if any count
+//            is negative, a non-zero count would touch a NULL buffer or
+//            (checked variant) a receive total is over capacity (every CTA
+//            sees the same matrix, so all take the same decision without a
+//            grid sync), sum every column below row i (the receive
+//            displacements) and over all rows, write the bookkeeping (CTA 0
+//            of each rank), build the pieces, hand the count stages to the
+//            producer, and then, for each chunk, write every vector of every
+//            piece whose first source byte lies in the chunk, shifting the
+//            words into destination alignment (int8 can be off by any byte,
+//            fp32 by whole words), while 32 lanes write the head and tail
+//            bytes that lie in it.
+// A granule holding a byte of a buffer never crosses a page the buffer does
+// not touch, so the granule-wide loads stay in bounds.  If the call is
+// rejected the producer waits for the copies it issued before the CTA ends.
 // Every wait is bounded (about 2 s by %globaltimer); a wait that runs out
 // records BRA_ERR_TIMEOUT in this file's device word, flags the CTA, and all
 // roles leave their loops.
@@ -58,7 +62,7 @@ constexpr unsigned kFull = 0xffffffffu;
 #define BRA_A2AV_TILE_VECS 1024
 #endif
 #ifndef BRA_A2AV_MIN_CTAS
-#define BRA_A2AV_MIN_CTAS 2
+#define BRA_A2AV_MIN_CTAS 3
 #endif
 constexpr int kStages = BRA_A2AV_STAGES;
 constexpr int kTileVecs = BRA_A2AV_TILE_VECS;            // 16-byte destination vectors
@@ -68,16 +72,14 @@ constexpr int kStageBytes = kChunk + 16;
 constexpr int kStageStride = (kStageBytes + 127) / 128 * 128;
 constexpr int kRingBytes = kStages * kStageStride;
 static_assert(kRingBytes >= kA2avMaxP * (kA2avMaxP + 1) * 8, "the ring also holds the counts");
-constexpr int kConsumerWarps = kA2avThreads / 32 - 1;
-// The warp that scans this CTA's own row of counts.
-constexpr int kRowWarp = kA2avThreads / 32 - 1;
-#ifndef BRA_A2AV_PREFETCH_KB
-#define BRA_A2AV_PREFETCH_KB 256
+#ifndef BRA_A2AV_THREADS
+#define BRA_A2AV_THREADS 256
 #endif
-// Bytes of a CTA's source range prefetched into L2 during the set-up.
-constexpr uint32_t kPrefetchBytes = BRA_A2AV_PREFETCH_KB * 1024u;
-// Count-matrix entries (P x P) per thread.
-constexpr int kCountIters = kA2avMaxP * kA2avMaxP / kA2avThreads;
+constexpr int kA2avThreads = BRA_A2AV_THREADS;   // one producer warp + consumer warps
+constexpr int kConsumerWarps = kA2avThreads / 32 - 1;
+constexpr int kConsumers = kConsumerWarps * 32;
+// Count-matrix entries (P x P) per consumer thread.
+constexpr int kCountIters = (kA2avMaxP * kA2avMaxP + kConsumers - 1) / kConsumers;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
 // Exclusive scan of 64 values held as (lane, lane + 32) by one warp.
@@ -171,6 +173,28 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
     }
   }
 }
+// Bounded wait that does not leave early when another role gave up: used
+// where the CTA must still observe the phase (copies in flight, set-up
+// hand-offs).  Running out records BRA_ERR_TIMEOUT like mbar_wait.
+__device__ __noinline__ bool mbar_wait_plain(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int k = 0; k < 64; ++k)
+      if (mbar_try(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1;
+      atomicExch(&g_a2av_fault_word, (int32_t)BRA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+// Barrier among the consumer warps only (named barrier 1).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+}
 // Bulk copy of `bytes` (a multiple of 16) from a 16-byte-aligned global
 // address into shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -179,13 +203,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
-}
-// Hint: bring `bytes` (a multiple of 16) from a 16-byte-aligned global
-// address into L2.
-__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-               ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
-               : "memory");
 }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -214,13 +231,10 @@ __device__ __forceinline__ void shifted_copy(uint4* d4, uint32_t buf, int n, int
 __global__ void __launch_bounds__(kA2avThreads, BRA_A2AV_MIN_CTAS)
 a2av_kernel(const __grid_constant__ A2avArgs a) {
   extern __shared__ __align__(128) uint8_t ring[];   // kStages x kStageStride
-  // The P x P counts (row stride P + 1) live in the ring's memory: they are
-  // dead before the first chunk is staged.
-  int64_t* const s_sc = reinterpret_cast<int64_t*>(ring);
   __shared__ int64_t s_row[kA2avMaxP];   // row i of the counts
   __shared__ int64_t s_sd[kA2avMaxP];    // send displacement of rank i to j
   __shared__ int64_t s_rd[kA2avMaxP];    // receive displacement of i at j
-  __shared__ int64_t s_part[2][kA2avThreads];   // column partial sums per row group
+  __shared__ int64_t s_part[2][kConsumers];   // column partial sums per row group
   // This CTA's share of rank i's send buffer, cut at destination
   // boundaries: one piece per destination j (possibly empty).
   __shared__ const char* s_src[kA2avMaxP];   // first source byte of the piece
@@ -233,46 +247,67 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   __shared__ int s_nul[kA2avMaxP];           // bit 0: in[r] NULL, bit 1: out[r] NULL
   __shared__ __align__(8) uint64_t s_full[kStages];
   __shared__ __align__(8) uint64_t s_empty[kStages];
+  __shared__ __align__(8) uint64_t s_row_ready;    // warp 0 has published row i
+  __shared__ __align__(8) uint64_t s_setup_done;   // the counts are no longer read
+  __shared__ int64_t s_lo, s_hi;
   __shared__ int s_npieces;
   __shared__ int s_bad;
-  __shared__ int s_abort;
+  __shared__ int s_reject;   // the consumers rejected the call
+  __shared__ int s_abort;    // a bounded wait ran out
 
   const int P = a.P;
   const int i = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ctid = tid - 32;   // consumer thread index (warps 1..7)
+  // The P x P counts (row stride P + 1, so column reads hit distinct banks)
+  // sit at the end of the ring, in the stages the producer fills last.
+  const int ld = P + 1;
+  const uint32_t sc_off = (uint32_t)(kRingBytes - P * ld * 8) & ~127u;
+  int64_t* const s_sc = reinterpret_cast<int64_t*>(ring + sc_off);
 
-  // Loads first: this thread's share of the count matrix (all of it is
-  // issued before any is used, so it costs one memory round trip), while
-  // thread 0 sets up the barriers.
+  // Loads first, so they overlap the barrier set-up: row i (warp 0) and
+  // each consumer thread's share of the count matrix, all issued before any
+  // is used.
+  int64_t r0 = 0, r1 = 0;
   int64_t v[kCountIters];
+  if (warp == 0) {
+    const int64_t* row = a.sc + (int64_t)i * P;
+    r0 = lane < P ? __ldg(row + lane) : 0;
+    r1 = lane + 32 < P ? __ldg(row + lane + 32) : 0;
+  } else {
 #pragma unroll
-  for (int m = 0; m < kCountIters; ++m) {
-    const int k = tid + m * kA2avThreads;
-    v[m] = k < P * P ? __ldg(a.sc + k) : 0;
+    for (int m = 0; m < kCountIters; ++m) {
+      const int k = ctid + m * kConsumers;
+      v[m] = k < P * P ? __ldg(a.sc + k) : 0;
+    }
+    // Per-rank pointers into shared memory once: kernel-parameter arrays
+    // read with a different index per lane serialise across the warp.
+    if (ctid < P) {
+      char* o = static_cast<char*>(a.out[ctid]);
+      s_outp[ctid] = o;
+      s_nul[ctid] = (a.in[ctid] == nullptr ? 1 : 0) | (o == nullptr ? 2 : 0);
+    }
   }
   if (tid == 0) {
     s_bad = 0;
+    s_reject = 0;
     s_abort = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&s_full[s]), 1);
       mbar_init(smem_u32(&s_empty[s]), kConsumerWarps);
     }
+    mbar_init(smem_u32(&s_row_ready), 1);
+    mbar_init(smem_u32(&s_setup_done), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // Per-rank pointers into shared memory once: kernel-parameter arrays read
-  // with a different index per lane serialise across the warp.
-  if (tid < P) {
-    char* o = static_cast<char*>(a.out[tid]);
-    s_outp[tid] = o;
-    s_nul[tid] = (a.in[tid] == nullptr ? 1 : 0) | (o == nullptr ? 2 : 0);
-  }
-  // Row i straight from global memory: its prefix sums are the send
-  // displacements, and its total fixes this CTA's source range, whose start
-  // is prefetched into L2 while the rest of the set-up runs.
-  if (warp == kRowWarp) {
-    const int64_t* row = a.sc + (int64_t)i * P;
-    const int64_t r0 = lane < P ? __ldg(row + lane) : 0;
-    const int64_t r1 = lane + 32 < P ? __ldg(row + lane + 32) : 0;
+  __syncthreads();   // the only CTA-wide barrier: roles split from here
+  volatile int* abort_flag = &s_abort;
+  const uint32_t ring_base = smem_u32(ring);
+  const int64_t es = a.esize;
+
+  if (warp == 0) {
+    // Row i: its prefix sums are the send displacements, and its total fixes
+    // this CTA's source range, which lane 0 starts streaming at once.
     int64_t e0, e1, tot;
     warp_exscan64(r0, r1, lane, e0, e1, tot);
     if (lane < P) {
@@ -284,25 +319,78 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
       s_row[lane + 32] = r1;
     }
     const bool row_ok = __all_sync(kFull, r0 >= 0 && r1 >= 0);
-    if (kPrefetchBytes > 0 && lane == 0 && row_ok && a.in[i] != nullptr) {
-      const int64_t lo = split_point(tot, gridDim.x, blockIdx.x);
-      int64_t hi = split_point(tot, gridDim.x, blockIdx.x + 1);
-      const uintptr_t base = reinterpret_cast<uintptr_t>(a.in[i]);
-      const uintptr_t b0 = (base + (uintptr_t)(lo * a.esize) + 15) & ~(uintptr_t)15;
-      uintptr_t b1 = (base + (uintptr_t)(hi * a.esize)) & ~(uintptr_t)15;
-      if (b1 > b0 + kPrefetchBytes) b1 = b0 + kPrefetchBytes;
-      if (b1 > b0) l2_prefetch(reinterpret_cast<const void*>(b0), (uint32_t)(b1 - b0));
+    const int64_t lo = row_ok ? split_point(tot, gridDim.x, blockIdx.x) : 0;
+    const int64_t hi = row_ok ? split_point(tot, gridDim.x, blockIdx.x + 1) : 0;
+    __syncwarp();
+    if (lane != 0) return;
+    s_lo = lo;
+    s_hi = hi;
+    mbar_arrive(smem_u32(&s_row_ready));
+
+    // Producer.  Nothing is streamed for a row with a negative count or a
+    // NULL buffer; the consumers reject such calls.
+    const bool go = row_ok && hi > lo && a.in[i] != nullptr;
+    const uintptr_t S = go ? reinterpret_cast<uintptr_t>(a.in[i]) + (uintptr_t)(lo * es) : 0;
+    const uintptr_t E = go ? reinterpret_cast<uintptr_t>(a.in[i]) + (uintptr_t)(hi * es) : 0;
+    const uintptr_t G0 = S & ~(uintptr_t)15, G1 = (E + 15) & ~(uintptr_t)15;
+    const int64_t ntiles = go ? (int64_t)((G1 - G0 + kChunk - 1) / kChunk) : 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true, setup_seen = false;
+    int64_t issued = 0;
+#pragma unroll 1
+    for (int64_t t = 0; t < ntiles; ++t) {
+      if (!mbar_wait(smem_u32(&s_empty[stage]), phase ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (!setup_seen && (uint32_t)stage * kStageStride + kStageBytes > sc_off) {
+        // This stage holds the counts until the consumers are done with them.
+        if (!mbar_wait_plain(smem_u32(&s_setup_done), 0, abort_flag)) {
+          ok = false;
+          break;
+        }
+        setup_seen = true;
+        if (s_reject) break;
+        // Order the consumers' generic accesses before the bulk copies.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      const uintptr_t c0 = G0 + (uintptr_t)t * kChunk;
+      const uintptr_t ce = c0 + kChunk + 16 < G1 ? c0 + kChunk + 16 : G1;
+      const uint32_t fb = smem_u32(&s_full[stage]);
+      mbar_expect_tx(fb, (uint32_t)(ce - c0));
+      bulk_load(ring_base + stage * kStageStride, reinterpret_cast<const void*>(c0),
+                (uint32_t)(ce - c0), fb);
+      ++issued;
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
+    // The CTA may not finish while copies it issued are in flight.  If the
+    // call was rejected nothing consumes them (and no stage was reused):
+    // wait for each to land.
+    if (ok && !setup_seen) ok = mbar_wait_plain(smem_u32(&s_setup_done), 0, abort_flag);
+    if (ok && s_reject) {
+      for (int s = 0; s < kStages && s < issued; ++s)
+        if (!mbar_wait_plain(smem_u32(&s_full[s]), 0, abort_flag)) break;
+    }
+    if (!ok) {   // a wait ran out: give copies already issued time to land
+      const unsigned long long t0 = global_ns();
+      while (global_ns() - t0 < 2000000ull) {
+      }
+    }
+    return;
   }
-  __syncthreads();
-  const int ld = P + 1;   // padded row stride: column reads hit distinct banks
+
+  // Consumers (warps 1..7): the count matrix, the checks and the pieces,
+  // synchronised among themselves by named barrier 1.
   {
-    // (src, dst) of entry tid + m * kA2avThreads, stepped without dividing.
-    const int step_rows = kA2avThreads / P, step_cols = kA2avThreads - step_rows * P;
-    int src = tid / P, dst = tid - (tid / P) * P;
+    const int step_rows = kConsumers / P, step_cols = kConsumers - step_rows * P;
+    int src = ctid / P, dst = ctid - (ctid / P) * P;   // entry ctid + m * kConsumers
 #pragma unroll
     for (int m = 0; m < kCountIters; ++m) {
-      const int k = tid + m * kA2avThreads;
+      const int k = ctid + m * kConsumers;
       if (m > 0) {
         src += step_rows;
         dst += step_cols;
@@ -318,57 +406,60 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
       }
     }
   }
-  __syncthreads();
+  consumer_sync();
 
-  // Bookkeeping: the sums of column j over source rows k < i (rank i's
-  // receive displacement at j) and over all rows (what j receives), as
-  // G = blockDim / P groups of threads each summing every G-th row, then
-  // one combine per column.
-  const int G = blockDim.x / P;   // >= 4 (P <= 64)
-  if (tid < G * P) {
-    const int j = tid % P, g = tid / P;
+  // The sums of column j over source rows k < i (rank i's receive
+  // displacement at j) and over all rows (what j receives), as G groups of
+  // threads each summing every G-th row, then one combine per column.
+  const int G = kConsumers / P;   // >= 3 (P <= 64)
+  if (ctid < G * P) {
+    const int j = ctid % P, g = ctid / P;
     int64_t before = 0, all = 0;
     for (int k = g; k < P; k += G) {
-      const int64_t v = s_sc[k * ld + j];
-      all += v;
-      if (k < i) before += v;
+      const int64_t c = s_sc[k * ld + j];
+      all += c;
+      if (k < i) before += c;
     }
     s_part[0][g * P + j] = before;
     s_part[1][g * P + j] = all;
   }
-  __syncthreads();
-  if (tid < P) {
+  consumer_sync();
+  if (ctid < P) {
     int64_t before = 0, all = 0;
     for (int g = 0; g < G; ++g) {
-      before += s_part[0][g * P + tid];
-      all += s_part[1][g * P + tid];
+      before += s_part[0][g * P + ctid];
+      all += s_part[1][g * P + ctid];
     }
-    s_rd[tid] = before;
+    s_rd[ctid] = before;
     // Checked variant: a receive total over capacity (every CTA decides alike).
-    if (a.check_cap && all > a.cap[tid]) s_bad = 1;
+    if (a.check_cap && all > a.cap[ctid]) s_bad = 1;
   }
-  __syncthreads();
+  // Row i as warp 0 published it (it does so without waiting on anything;
+  // one thread observes the hand-off and the barrier spreads it, so a
+  // timeout here would send every consumer the same way).
+  if (ctid == 0 && !mbar_wait_plain(smem_u32(&s_row_ready), 0, abort_flag)) s_bad = 1;
+  consumer_sync();
   const bool bad = s_bad != 0;
-  if (a.status && blockIdx.x == 0 && i == 0 && tid == 0)
+  if (a.status && blockIdx.x == 0 && i == 0 && ctid == 0)
     *a.status = bad ? BRA_ERR_INVALID : BRA_OK;
-  if (bad) return;
+  if (bad) {
+    if (ctid == 0) {
+      s_reject = 1;
+      mbar_arrive(smem_u32(&s_setup_done));
+    }
+    return;
+  }
+  const int64_t lo = s_lo, hi = s_hi;
 
   if (blockIdx.x == 0) {
-    for (int j = tid; j < P; j += blockDim.x) {
+    for (int j = ctid; j < P; j += kConsumers) {
       a.sd[(int64_t)i * P + j] = s_sd[j];
       a.rc[(int64_t)j * P + i] = s_row[j];
       a.rd[(int64_t)j * P + i] = s_rd[j];
     }
   }
 
-  // This CTA's contiguous range: equal range blockIdx.x of gridDim.x over
-  // rank i's send buffer.
-  const int64_t total = s_sd[P - 1] + s_row[P - 1];
-  const int64_t lo = split_point(total, gridDim.x, blockIdx.x);
-  const int64_t hi = split_point(total, gridDim.x, blockIdx.x + 1);
-  const int64_t es = a.esize;
-
-  if (warp == 0) {
+  if (warp == 1) {
     bool has[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -399,7 +490,8 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
     if (has[1]) s_list[__popc(m0) + __popc(m1 & below)] = lane + 32;
     if (lane == 0) s_npieces = __popc(m0) + __popc(m1);
   }
-  __syncthreads();
+  consumer_sync();
+  if (ctid == 0) mbar_arrive(smem_u32(&s_setup_done));   // the counts are dead
 
   // The CTA's source bytes [S, E) are contiguous (the send buffer is ordered
   // by destination).  They stream through the ring as chunks of kChunk bytes
@@ -411,102 +503,67 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   const uintptr_t E = reinterpret_cast<uintptr_t>(a.in[i]) + (uintptr_t)(hi * es);
   const uintptr_t G0 = S & ~(uintptr_t)15, G1 = (E + 15) & ~(uintptr_t)15;
   const int64_t ntiles = hi > lo ? (int64_t)((G1 - G0 + kChunk - 1) / kChunk) : 0;
-  volatile int* abort_flag = &s_abort;
-  const uint32_t ring_base = smem_u32(ring);
-  if (warp == 0) {
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      // The ring held the counts: order those generic accesses before the
-      // bulk copies overwrite it.
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  const int nct = kConsumers;
+  int q = 0, stage = 0;   // q: first listed piece not yet finished
+  uint32_t phase = 0;
 #pragma unroll 1
-      for (int64_t t = 0; t < ntiles; ++t) {
-        if (!mbar_wait(smem_u32(&s_empty[stage]), phase ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uintptr_t c0 = G0 + (uintptr_t)t * kChunk;
-        const uintptr_t ce = c0 + kChunk + 16 < G1 ? c0 + kChunk + 16 : G1;
-        const uint32_t fb = smem_u32(&s_full[stage]);
-        mbar_expect_tx(fb, (uint32_t)(ce - c0));
-        bulk_load(ring_base + stage * kStageStride, reinterpret_cast<const void*>(c0),
-                  (uint32_t)(ce - c0), fb);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      if (!ok) {   // let copies already issued land before the CTA exits
-        const unsigned long long t0 = global_ns();
-        while (global_ns() - t0 < 2000000ull) {
-        }
-      }
-    }
-  } else {
-    const int ctid = tid - 32, nct = kConsumerWarps * 32;
-    int q = 0, stage = 0;   // q: first listed piece not yet finished
-    uint32_t phase = 0;
+  for (int64_t t = 0; t < ntiles; ++t) {
+    const bool waited = mbar_wait(smem_u32(&s_full[stage]), phase, abort_flag);
+    if (!__all_sync(kFull, waited)) break;
+    const uintptr_t c0 = G0 + (uintptr_t)t * kChunk;
+    const uintptr_t c1 = c0 + kChunk < G1 ? c0 + kChunk : G1;   // bytes this chunk writes
+    const uint32_t buf = ring_base + stage * kStageStride;      // holds source byte c0 + o at o
 #pragma unroll 1
-    for (int64_t t = 0; t < ntiles; ++t) {
-      const bool waited = mbar_wait(smem_u32(&s_full[stage]), phase, abort_flag);
-      if (!__all_sync(kFull, waited)) break;
-      const uintptr_t c0 = G0 + (uintptr_t)t * kChunk;
-      const uintptr_t c1 = c0 + kChunk < G1 ? c0 + kChunk : G1;   // bytes this chunk writes
-      const uint32_t buf = ring_base + stage * kStageStride;      // holds source byte c0 + o at o
-#pragma unroll 1
-      for (int qq = q; qq < npieces; ++qq) {
-        const int j = s_list[qq];
-        const uintptr_t ps = reinterpret_cast<uintptr_t>(s_src[j]);
-        if (ps >= c1) break;   // starts in a later chunk
-        const int64_t head = s_head[j], nvec = s_nvec[j];
-        const int tail = s_tail[j];
-        char* const dj = s_dst[j];
-        // Vectors v whose first source byte base + 16 v lies in [c0, c1).
-        const uintptr_t base = ps + (uintptr_t)head;
-        const int64_t vlo = base >= c0 ? 0 : (int64_t)((c0 - base + 15) >> 4);
-        int64_t vhi = base >= c1 ? 0 : (int64_t)((c1 - base + 15) >> 4);
-        if (vhi > nvec) vhi = nvec;
-        if (vhi > vlo) {
-          const uint32_t o = (uint32_t)(base + (uintptr_t)(vlo * 16) - c0);
-          const uint32_t vbuf = buf + (o & ~15u), delta = o & 15u, r = (delta & 3u) * 8u;
-          uint4* d4 = reinterpret_cast<uint4*>(dj + head) + vlo;
-          const int n = (int)(vhi - vlo);
-          switch (delta >> 2) {
-            case 0:
-              if (r == 0) {
+    for (int qq = q; qq < npieces; ++qq) {
+      const int j = s_list[qq];
+      const uintptr_t ps = reinterpret_cast<uintptr_t>(s_src[j]);
+      if (ps >= c1) break;   // starts in a later chunk
+      const int64_t head = s_head[j], nvec = s_nvec[j];
+      const int tail = s_tail[j];
+      char* const dj = s_dst[j];
+      // Vectors v whose first source byte base + 16 v lies in [c0, c1).
+      const uintptr_t base = ps + (uintptr_t)head;
+      const int64_t vlo = base >= c0 ? 0 : (int64_t)((c0 - base + 15) >> 4);
+      int64_t vhi = base >= c1 ? 0 : (int64_t)((c1 - base + 15) >> 4);
+      if (vhi > nvec) vhi = nvec;
+      if (vhi > vlo) {
+        const uint32_t o = (uint32_t)(base + (uintptr_t)(vlo * 16) - c0);
+        const uint32_t vbuf = buf + (o & ~15u), delta = o & 15u, r = (delta & 3u) * 8u;
+        uint4* d4 = reinterpret_cast<uint4*>(dj + head) + vlo;
+        const int n = (int)(vhi - vlo);
+        switch (delta >> 2) {
+          case 0:
+            if (r == 0) {
 #pragma unroll 2
-                for (int k = ctid; k < n; k += nct) d4[k] = lds128(vbuf + 16u * k);
-              } else {
-                shifted_copy<0>(d4, vbuf, n, ctid, nct, r);
-              }
-              break;
-            case 1: shifted_copy<1>(d4, vbuf, n, ctid, nct, r); break;
-            case 2: shifted_copy<2>(d4, vbuf, n, ctid, nct, r); break;
-            default: shifted_copy<3>(d4, vbuf, n, ctid, nct, r); break;
-          }
+              for (int k = ctid; k < n; k += nct) d4[k] = lds128(vbuf + 16u * k);
+            } else {
+              shifted_copy<0>(d4, vbuf, n, ctid, nct, r);
+            }
+            break;
+          case 1: shifted_copy<1>(d4, vbuf, n, ctid, nct, r); break;
+          case 2: shifted_copy<2>(d4, vbuf, n, ctid, nct, r); break;
+          default: shifted_copy<3>(d4, vbuf, n, ctid, nct, r); break;
         }
-        // Head bytes (lanes 0-15) and tail bytes (lanes 16-31) of the first
-        // consumer warp, each written by the chunk holding its source byte.
-        if (warp == 1) {
-          const int b = lane & 15;
-          const int64_t off = lane < 16 ? (b < head ? b : -1)
-                                        : (b < tail ? head + nvec * 16 + b : -1);
-          if (off >= 0) {
-            const uintptr_t sb = ps + (uintptr_t)off;
-            if (sb >= c0 && sb < c1) dj[off] = (char)lds8(buf + (uint32_t)(sb - c0));
-          }
+      }
+      // Head bytes (lanes 0-15) and tail bytes (lanes 16-31) of the first
+      // consumer warp, each written by the chunk holding its source byte.
+      if (warp == 1) {
+        const int b = lane & 15;
+        const int64_t off = lane < 16 ? (b < head ? b : -1)
+                                      : (b < tail ? head + nvec * 16 + b : -1);
+        if (off >= 0) {
+          const uintptr_t sb = ps + (uintptr_t)off;
+          if (sb >= c0 && sb < c1) dj[off] = (char)lds8(buf + (uint32_t)(sb - c0));
         }
-        if (base + (uintptr_t)(nvec * 16) + (uintptr_t)tail > c1) break;   // continues
-        q = qq + 1;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s_empty[stage]));
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
-      }
+      if (base + (uintptr_t)(nvec * 16) + (uintptr_t)tail > c1) break;   // continues
+      q = qq + 1;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s_empty[stage]));
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
     }
   }
 }

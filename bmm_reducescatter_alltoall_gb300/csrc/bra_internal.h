@@ -12,7 +12,6 @@ namespace bra {
 
 // all_to_all_v keeps the whole P x P count matrix of int64 in shared memory.
 constexpr int kA2avMaxP = 64;
-constexpr int kA2avThreads = 256;   // one producer warp + seven consumer warps
 
 // Fused kernels: one launch covers the TP groups of up to kChunkRanks source
 // ranks (their x / weight / bias), and may write to any of kMaxRanks outputs.

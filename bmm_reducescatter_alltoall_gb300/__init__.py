@@ -78,6 +78,8 @@ def library() -> ctypes.CDLL:
     lib.bra_l2_flush.restype = c_int
     lib.bra_fault_status.argtypes = [ctypes.POINTER(i32), c_int]
     lib.bra_fault_status.restype = c_int
+    lib.bra_wait_selftest.argtypes = [c_int, vp, vp]
+    lib.bra_wait_selftest.restype = c_int
     lib.bra_version.argtypes = []
     lib.bra_version.restype = ctypes.c_char_p
     _lib = lib
@@ -318,6 +320,21 @@ def l2_flush(buf, stream=None) -> None:
     _dev_tensor(buf, "buf")
     _check(library().bra_l2_flush(buf.data_ptr(), buf.numel() * buf.element_size(),
                                   _stream_handle(stream)), "bra_l2_flush")
+
+
+WAIT_A2AV, WAIT_TC = 0, 1
+
+
+def wait_selftest(which: str, status, stream=None) -> None:
+    """Run one bounded wait that nothing completes with the wait helper of the
+    all_to_all_v kernel (which='a2av', ~2 s) or of the tensor-core fused
+    kernels (which='tc', ~4 s).  `status` (CUDA int32, 1 element) receives
+    ERR_TIMEOUT and the watchdog word read by fault_status() is set."""
+    torch = _torch()
+    code = {"a2av": WAIT_A2AV, "tc": WAIT_TC}[which]
+    _dev_tensor(status, "status", torch.int32)
+    _check(library().bra_wait_selftest(code, status.data_ptr(), _stream_handle(stream)),
+           "bra_wait_selftest")
 
 
 def fault_status(clear: bool = False) -> int:

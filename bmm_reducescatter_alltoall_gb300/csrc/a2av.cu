@@ -568,6 +568,25 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   }
 }
 
+// Diagnostic: one bounded wait (the same helper the exchange uses) on a
+// barrier nothing arrives at.  It runs out after kWaitTimeoutNs, records
+// BRA_ERR_TIMEOUT in this file's fault word and returns; *status gets the
+// outcome.
+__global__ void a2av_wait_probe_kernel(int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool done = mbar_wait_plain(smem_u32(&bar), 0, &abort_flag);
+    *status = done ? BRA_OK : BRA_ERR_TIMEOUT;
+  }
+}
+
 int device_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -619,6 +638,11 @@ cudaError_t launch_a2av(const A2avArgs& a, int ctas_per_rank, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   dim3 grid(ctas_per_rank, a.P);
   a2av_kernel<<<grid, kA2avThreads, kRingBytes, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_a2av_wait_probe(int32_t* status, cudaStream_t st) {
+  a2av_wait_probe_kernel<<<1, 32, 0, st>>>(status);
   return cudaGetLastError();
 }
 

@@ -317,6 +317,18 @@ int bra_fault_status(int32_t* code, int clear) {
   return BRA_OK;
 }
 
+int bra_wait_selftest(int which, int32_t* status_dev, bra_stream_t stream) {
+  if (!status_dev) return BRA_ERR_NULLPTR;
+  cudaError_t e;
+  if (which == BRA_WAIT_A2AV)
+    e = bra::launch_a2av_wait_probe(status_dev, (cudaStream_t)stream);
+  else if (which == BRA_WAIT_TC)
+    e = bra::launch_tc_wait_probe(status_dev, (cudaStream_t)stream);
+  else
+    return BRA_ERR_INVALID;
+  return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
+}
+
 const char* bra_version(void) { return "0.1.0"; }
 
 }  // extern "C"

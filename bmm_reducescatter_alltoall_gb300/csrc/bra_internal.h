@@ -60,5 +60,8 @@ cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t st);
 cudaError_t read_fault_word(int32_t* code, int clear);        // tensor-core kernel
 cudaError_t read_fault_word2(int32_t* code, int clear);       // CTA-pair tensor-core kernel
 cudaError_t read_a2av_fault_word(int32_t* code, int clear);   // all_to_all_v kernel
+// One bounded wait that nothing completes, with each family's wait helper.
+cudaError_t launch_a2av_wait_probe(int32_t* status, cudaStream_t st);
+cudaError_t launch_tc_wait_probe(int32_t* status, cudaStream_t st);
 
 }  // namespace bra

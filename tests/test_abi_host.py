@@ -323,3 +323,10 @@ def test_binding_rejects_host_tensors():
     with pytest.raises(ValueError):
         bra.all_to_all_v([torch.zeros(4)] * 2, torch.zeros(2, 2, dtype=torch.int64),
                          [torch.zeros(4)] * 2, 2)
+
+
+def test_wait_selftest_argument_checks(lib):
+    """Rejections happen on the host before any launch."""
+    assert lib.bra_wait_selftest(bra.WAIT_A2AV, None, None) == NULLPTR
+    assert lib.bra_wait_selftest(7, 1 << 32, None) == INVALID
+    assert lib.bra_wait_selftest(-1, 1 << 32, None) == INVALID

@@ -1,0 +1,44 @@
+"""Failure detection on the GPU without a fault: a bounded wait runs out.
+
+Each kernel family's wait helper (the one every mbarrier wait of
+all_to_all_v, or of the tensor-core fused kernels, goes through) is run on a
+barrier phase that nothing completes.  The wait gives up after its limit
+(about 2 s / 4 s), the kernel reports BRA_ERR_TIMEOUT in its status word and
+in the watchdog word the host reads, and returns; nothing traps, and the
+context stays usable, which the exact exchange run afterwards checks.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bmm_reducescatter_alltoall_gb300 as bra
+from oracle import a2av as oa
+from workloads import A2AV_CONFIGS, a2av_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _exchange_is_exact():
+    cfg = A2AV_CONFIGS["P8_L10_fp32_uniform4096"]
+    sc, inputs = a2av_inputs(cfg)
+    ins = [torch.from_numpy(a).cuda() for a in inputs]
+    outs = [torch.zeros(int(c), dtype=torch.float32, device="cuda") for c in sc.sum(axis=0)]
+    bra.all_to_all_v(ins, torch.from_numpy(sc).cuda(), outs, cfg.L)
+    torch.cuda.synchronize()
+    ref = oa.all_to_all_v(inputs, sc, [np.zeros(int(c), np.float32) for c in sc.sum(axis=0)])
+    return all(np.array_equal(o.cpu().numpy().view(np.uint32), r.view(np.uint32))
+               for o, r in zip(outs, ref["out"]))
+
+
+@pytest.mark.parametrize("which", ["a2av", "tc"])
+def test_bounded_wait_runs_out_and_reports(which):
+    bra.fault_status(clear=True)
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    bra.wait_selftest(which, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == bra.ERR_TIMEOUT
+    assert bra.fault_status() == bra.ERR_TIMEOUT
+    bra.fault_status(clear=True)
+    assert bra.fault_status() == 0
+    assert _exchange_is_exact()
+    assert bra.fault_status() == 0

@@ -16,13 +16,14 @@ from typing import List, Optional, Sequence
 
 __all__ = [
     "BraError", "FP16", "BF16", "FP32", "INT8", "VARIANT_TC", "VARIANT_TC2", "VARIANT_SIMT",
+    "VARIANT_TCU", "wait_selftest",
     "FusedOptions", "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
     "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked",
     "cal_all_to_all_v_blocks", "l2_flush", "fault_status", "status_str", "version",
 ]
 
 FP16, BF16, FP32, INT8 = 0, 1, 2, 3
-VARIANT_TC, VARIANT_SIMT, VARIANT_TC2 = 1, 2, 3
+VARIANT_TC, VARIANT_SIMT, VARIANT_TC2, VARIANT_TCU = 1, 2, 3, 4
 OK, ERR_NULLPTR, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = (
     0, 161001, 161002, 161003, 161100, 161101)
 
@@ -153,7 +154,8 @@ def _shape_check(t, want, what):
         raise ValueError(f"{what} has shape {tuple(t.shape)}, expected {tuple(want)}")
 
 
-_VARIANTS = {None: 0, "auto": 0, "tc": VARIANT_TC, "tc2": VARIANT_TC2, "simt": VARIANT_SIMT}
+_VARIANTS = {None: 0, "auto": 0, "tc": VARIANT_TC, "tc2": VARIANT_TC2, "simt": VARIANT_SIMT,
+             "tcu": VARIANT_TCU}
 
 
 def _options(transpose_weight: bool, variant) -> "FusedOptions":
@@ -230,7 +232,7 @@ def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
 
 def bmm_rs_a2a_variant(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
                        transpose_weight: bool = False, variant: Optional[str] = None) -> int:
-    """VARIANT_TC, VARIANT_TC2 or VARIANT_SIMT; raises BraError if rejected."""
+    """VARIANT_TC, VARIANT_TC2, VARIANT_TCU or VARIANT_SIMT; raises BraError if rejected."""
     xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
                                      transpose_weight)
     opts = _options(transpose_weight, variant)

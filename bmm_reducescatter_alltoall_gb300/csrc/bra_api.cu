@@ -50,7 +50,8 @@ int validate_fused(const void* const x[], const void* const weight[],
     for (int k = 0; k < 6; ++k)
       if (opts->reserved[k] != 0) return BRA_ERR_INVALID;
     if (opts->variant != BRA_VARIANT_AUTO && opts->variant != BRA_VARIANT_TC &&
-        opts->variant != BRA_VARIANT_TC2 && opts->variant != BRA_VARIANT_SIMT)
+        opts->variant != BRA_VARIANT_TC2 && opts->variant != BRA_VARIANT_SIMT &&
+        opts->variant != BRA_VARIANT_TCU)
       return BRA_ERR_INVALID;
   }
   int rc = check_fused_attrs(ep, tp, E, C, M, H, type);
@@ -110,31 +111,39 @@ int validate_fused(const void* const x[], const void* const weight[],
   return BRA_OK;
 }
 
-// BRA_FORCE_VARIANT=tc|tc2|simt, read at every call.
+// BRA_FORCE_VARIANT=tc|tc2|tcu|simt, read at every call.
 int forced_variant() {
   const char* v = std::getenv("BRA_FORCE_VARIANT");
   if (!v || !*v) return BRA_VARIANT_AUTO;
   if (!std::strcmp(v, "tc")) return BRA_VARIANT_TC;
   if (!std::strcmp(v, "tc2")) return BRA_VARIANT_TC2;
   if (!std::strcmp(v, "simt")) return BRA_VARIANT_SIMT;
+  if (!std::strcmp(v, "tcu")) return BRA_VARIANT_TCU;
   return BRA_VARIANT_AUTO;
 }
 
 int choose_variant(const bra::FusedProblem& p, const bra_fused_options* opts) {
   const int f = (opts && opts->variant != BRA_VARIANT_AUTO) ? opts->variant : forced_variant();
   const bool tc_ok = bra::fused_tc_eligible(p);
+  const bool tcu_ok = bra::fused_tcu_eligible(p);
   if (f == BRA_VARIANT_SIMT) return BRA_VARIANT_SIMT;
   if (f == BRA_VARIANT_TC || f == BRA_VARIANT_TC2) return tc_ok ? f : -BRA_ERR_UNSUPPORTED;
-  if (!tc_ok) return BRA_VARIANT_SIMT;
+  if (f == BRA_VARIANT_TCU) return tcu_ok ? f : -BRA_ERR_UNSUPPORTED;
+  // Rows TMA cannot describe: the tensor-core kernel that stages operands
+  // with loads; pointers not even element-aligned: the generic kernel.
+  if (!tc_ok) return tcu_ok ? BRA_VARIANT_TCU : BRA_VARIANT_SIMT;
   // The CTA-pair kernel moves a third less shared-memory traffic per FLOP;
-  // with few 256 x 256 tiles the one-CTA kernel spreads over more SMs.
-  const int64_t pair_tiles = (int64_t)p.ep * p.El * ((int64_t)p.ep * p.C + 255) / 256 *
+  // with few 256 x 256 tiles the one-CTA kernel spreads over more SMs, and
+  // with at most 128 token rows per group (a weight-streaming, HBM-bound
+  // problem) the pair's 256-row tile would be half empty.
+  const int64_t rows = (int64_t)p.ep * p.C;
+  const int64_t pair_tiles = (int64_t)p.ep * p.El * ((rows + 255) / 256) *
                              (((int64_t)p.H + 255) / 256);
-  return pair_tiles >= 64 ? BRA_VARIANT_TC2 : BRA_VARIANT_TC;
+  return pair_tiles >= 64 && rows > 128 ? BRA_VARIANT_TC2 : BRA_VARIANT_TC;
 }
 
 const char* variant_name(int v) {
-  return v == BRA_VARIANT_TC2 ? "tc2" : v == BRA_VARIANT_TC ? "tc" : "simt";
+  return v == BRA_VARIANT_TC2 ? "tc2" : v == BRA_VARIANT_TC ? "tc" : v == BRA_VARIANT_TCU ? "tcu" : "simt";
 }
 
 bool log_enabled() {
@@ -206,8 +215,9 @@ int bmm_rs_a2a_ex(const void* const x[], const void* const weight[],
     std::fprintf(stderr, "[bra] bmm_rs_a2a ep=%lld tp=%lld E=%lld C=%lld M=%lld H=%lld type=%lld -> %s\n",
                  (long long)ep, (long long)tp, (long long)E, (long long)C, (long long)M,
                  (long long)H, (long long)yShardType, variant_name(v));
-  cudaError_t e = v == BRA_VARIANT_TC2  ? bra::launch_fused_tc2(p, (cudaStream_t)stream)
-                  : v == BRA_VARIANT_TC ? bra::launch_fused_tc(p, (cudaStream_t)stream)
+  cudaError_t e = v == BRA_VARIANT_TC2   ? bra::launch_fused_tc2(p, (cudaStream_t)stream)
+                  : v == BRA_VARIANT_TC  ? bra::launch_fused_tc(p, (cudaStream_t)stream)
+                  : v == BRA_VARIANT_TCU ? bra::launch_fused_tcu(p, (cudaStream_t)stream)
                                         : bra::launch_fused_simt(p, (cudaStream_t)stream);
   if (e == cudaErrorInvalidValue && v != BRA_VARIANT_SIMT) return BRA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
@@ -309,11 +319,12 @@ int bra_l2_flush(void* buf, size_t bytes, bra_stream_t stream) {
 
 int bra_fault_status(int32_t* code, int clear) {
   if (!code) return BRA_ERR_NULLPTR;
-  int32_t a = 0, b = 0, c = 0;
+  int32_t a = 0, b = 0, c = 0, d = 0;
   if (bra::read_fault_word(&a, clear) != cudaSuccess) return BRA_ERR_CUDA;
   if (bra::read_fault_word2(&c, clear) != cudaSuccess) return BRA_ERR_CUDA;
+  if (bra::read_fault_word3(&d, clear) != cudaSuccess) return BRA_ERR_CUDA;
   if (bra::read_a2av_fault_word(&b, clear) != cudaSuccess) return BRA_ERR_CUDA;
-  *code = a ? a : (c ? c : b);
+  *code = a ? a : (c ? c : (d ? d : b));
   return BRA_OK;
 }
 

@@ -55,10 +55,14 @@ cudaError_t launch_fused_tc(const FusedProblem& f, cudaStream_t st);    // one C
 cudaError_t launch_fused_tc2(const FusedProblem& f, cudaStream_t st);   // CTA pair per tile
 // Shape / alignment predicate of the tensor-core variant.
 bool fused_tc_eligible(const FusedProblem& f);
+// Tensor-core variant for rows of any alignment (operands staged by loads).
+cudaError_t launch_fused_tcu(const FusedProblem& f, cudaStream_t st);
+bool fused_tcu_eligible(const FusedProblem& f);
 
 cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t st);
 cudaError_t read_fault_word(int32_t* code, int clear);        // tensor-core kernel
 cudaError_t read_fault_word2(int32_t* code, int clear);       // CTA-pair tensor-core kernel
+cudaError_t read_fault_word3(int32_t* code, int clear);       // unaligned tensor-core kernel
 cudaError_t read_a2av_fault_word(int32_t* code, int clear);   // all_to_all_v kernel
 // One bounded wait that nothing completes, with each family's wait helper.
 cudaError_t launch_a2av_wait_probe(int32_t* status, cudaStream_t st);

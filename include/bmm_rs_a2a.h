@@ -63,7 +63,9 @@ typedef enum {
   BRA_VARIANT_AUTO = 0,
   BRA_VARIANT_TC = 1,    /* tcgen05 / TMEM / TMA kernel, one CTA per tile  */
   BRA_VARIANT_SIMT = 2,  /* generic kernel: any alignment, any size        */
-  BRA_VARIANT_TC2 = 3    /* tcgen05 kernel, a CTA pair per 256x256 tile    */
+  BRA_VARIANT_TC2 = 3,   /* tcgen05 kernel, a CTA pair per 256x256 tile    */
+  BRA_VARIANT_TCU = 4    /* tcgen05 kernel for rows of any alignment:
+                            operands staged by loads, not TMA             */
 } bra_variant;
 
 /* ------------------------------------------------------------------------ */
@@ -167,8 +169,8 @@ BRA_API int bmm_rs_a2a_infer_shape(int64_t ep, int64_t tp, int64_t E, int64_t C,
 
 /*
  * bmm_rs_a2a_variant -- which kernel bmm_rs_a2a_ex would launch for these
- * arguments and options (BRA_VARIANT_TC, BRA_VARIANT_TC2 or
- * BRA_VARIANT_SIMT), honouring BRA_FORCE_VARIANT.  Pointers are only
+ * arguments and options (BRA_VARIANT_TC, BRA_VARIANT_TC2, BRA_VARIANT_TCU
+ * or BRA_VARIANT_SIMT), honouring BRA_FORCE_VARIANT.  Pointers are only
  * inspected for alignment.  Returns the variant, or a negative bra_status
  * (e.g. -BRA_ERR_INVALID) when the call would be rejected.  Pure host.
  */

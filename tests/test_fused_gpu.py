@@ -90,7 +90,11 @@ TC_CASES = [
 ]
 
 
-@pytest.mark.parametrize("variant", ["tc", "tc2"])
+_WANT = {"tc": bra.VARIANT_TC, "tc2": bra.VARIANT_TC2, "tcu": bra.VARIANT_TCU,
+         "simt": bra.VARIANT_SIMT}
+
+
+@pytest.mark.parametrize("variant", ["tc", "tc2", "tcu"])
 @pytest.mark.parametrize("case", TC_CASES)
 @pytest.mark.parametrize("bias", [True, False])
 def test_tensor_core_kernels(case, bias, variant, monkeypatch):
@@ -102,7 +106,7 @@ def test_tensor_core_kernels(case, bias, variant, monkeypatch):
     ys = bra.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t)["y"]
     probe = [torch.empty(ys, dtype=dinp["x"][0].dtype, device="cuda") for _ in range(cfg.P)]
     monkeypatch.setenv("BRA_FORCE_VARIANT", variant)
-    want = bra.VARIANT_TC2 if variant == "tc2" else bra.VARIANT_TC
+    want = _WANT[variant]
     assert bra.bmm_rs_a2a_variant(dinp["x"], dinp["w"], dinp["bias"], ep, tp, E, C, M, H, t,
                                   probe) == want
     ref = _oracle(cfg, inp)
@@ -125,15 +129,61 @@ def test_generic_kernel_on_the_same_shapes(case, monkeypatch):
     (2, 1, 2, 3, 5, 7, 1, "fp16"),
     (4, 4, 8, 8, 20, 36, 0, "bf16"),
 ])
-def test_generic_kernel_unaligned_shapes(case, monkeypatch):
+@pytest.mark.parametrize("variant", [None, "simt"])
+def test_unaligned_shapes_small(case, variant, monkeypatch):
+    """Rows TMA cannot describe: the load-staged tensor-core kernel (the
+    automatic choice) and the generic kernel."""
     ep, tp, E, C, M, H, t, dt = case
     cfg = FusedConfig("u", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
                       seed=sum(case[:6]) + 2)
-    _check_small(cfg, monkeypatch)
-    _check_small(cfg.replace(has_bias=False), monkeypatch)
+    _check_small(cfg, monkeypatch, variant=variant)
+    _check_small(cfg.replace(has_bias=False), monkeypatch, variant=variant)
 
 
-@pytest.mark.parametrize("variant", ["tc", "tc2"])
+# Unaligned shapes over several tiles, with ragged row / column / K tails:
+# K per shard, H or H/tp not a multiple of 8 elements.
+UNALIGNED_CASES = [
+    # ep, tp, E, C, M, H, type, dtype
+    (2, 2, 4, 40, 130, 70, 0, "fp16"),        # Kp = 65, H/tp = 35
+    (2, 2, 4, 40, 130, 70, 1, "bf16"),
+    (4, 2, 8, 96, 200, 300, 0, "bf16"),       # Kp = 100 (200-byte rows), 3 m-tiles, 2 n-tiles
+    (2, 4, 4, 260, 1028, 516, 1, "fp16"),     # Kp = 257, ragged 5 m-tiles x 3 n-tiles
+    (4, 4, 8, 33 * 4, 36, 4, 1, "fp16"),      # Kp = 9, H = 4: K and N far below one block
+    (8, 2, 16, 16, 2050, 1030, 0, "bf16"),    # P = 16, Kp = 1025, H/tp = 515
+]
+
+
+@pytest.mark.parametrize("case", UNALIGNED_CASES)
+@pytest.mark.parametrize("bias", [True, False])
+def test_unaligned_shapes_tensor_core(case, bias, monkeypatch):
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("ut", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=sum(case[:6]) + 11, has_bias=bias)
+    inp = fused_inputs_host(cfg)
+    dinp = _to_dev(inp)
+    ys = bra.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t)["y"]
+    probe = [torch.empty(ys, dtype=dinp["x"][0].dtype, device="cuda") for _ in range(cfg.P)]
+    monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
+    assert bra.bmm_rs_a2a_variant(dinp["x"], dinp["w"], dinp["bias"], ep, tp, E, C, M, H, t,
+                                  probe) == bra.VARIANT_TCU
+    ref = _oracle(cfg, inp)
+    out = _run(cfg, dinp, None, monkeypatch)
+    err = _rel_err(out, ref)
+    assert err <= TOL[dt], f"{case} bias={bias}: rel err {err:.3e}"
+
+
+def test_unaligned_2d_bias_and_generic_agree(monkeypatch):
+    cfg = FusedConfig("u2", ep=4, tp=2, E=8, C=96, M=200, H=300, y_shard_type=1, dtype="fp16",
+                      seed=21)
+    _check_small(cfg, monkeypatch, bias_ndim=2)
+    dinp = _to_dev(fused_inputs_host(cfg))
+    a = _run(cfg, dinp, "tcu", monkeypatch)
+    b = _run(cfg, dinp, "simt", monkeypatch)
+    ref = [u.float().cpu().numpy().astype(np.float64) for u in b]
+    assert _rel_err(a, ref) <= TOL["fp16"]
+
+
+@pytest.mark.parametrize("variant", ["tc", "tc2", "tcu"])
 def test_tc_and_generic_agree(variant, monkeypatch):
     cfg = FusedConfig("x", ep=4, tp=2, E=8, C=128, M=256, H=512, y_shard_type=1,
                       dtype="bf16", seed=3)
@@ -206,11 +256,12 @@ TW_CASES = [
     (2, 2, 4, 96, 256, 512, 0, "fp16"),
     (4, 2, 8, 40, 208, 328, 1, "bf16"),
     (8, 4, 16, 64, 256, 256, 1, "fp16"),
-    (2, 2, 4, 6, 12, 10, 0, "bf16"),          # unaligned: generic kernel only
+    (2, 2, 4, 6, 12, 10, 0, "bf16"),          # unaligned: not for the TMA kernels
+    (2, 2, 4, 40, 130, 70, 1, "fp16"),        # unaligned, several K blocks
 ]
 
 
-@pytest.mark.parametrize("variant", ["tc", "tc2", "simt"])
+@pytest.mark.parametrize("variant", ["tc", "tc2", "tcu", "simt"])
 @pytest.mark.parametrize("case", TW_CASES)
 def test_transposed_weight(case, variant):
     ep, tp, E, C, M, H, t, dt = case
@@ -224,7 +275,7 @@ def test_transposed_weight(case, variant):
     out = [torch.full(ys, float("nan"), dtype=dinp["x"][0].dtype, device="cuda")
            for _ in range(cfg.P)]
     aligned = (M // tp) % 8 == 0 and H % 8 == 0 and (t == 1 or (H // tp) % 8 == 0)
-    if variant != "simt" and not aligned:
+    if variant in ("tc", "tc2") and not aligned:
         with pytest.raises(bra.BraError):
             bra.bmm_rs_a2a(dinp["x"], wt, dinp["bias"], ep, tp, E, C, M, H, t, out=out,
                            transpose_weight=True, variant=variant)
@@ -251,4 +302,28 @@ def test_transposed_weight_full_size_sampled():
     for y in out:
         assert not torch.isnan(y).any().item()
     err = _sampled_check(cfg, dinp, out, np.random.default_rng(7), per_rank=16)
+    assert err <= TOL["bf16"], f"sampled rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+def test_unaligned_large_sampled(transposed, monkeypatch):
+    """A large shape with 4100-byte token rows and 8200-byte weight rows (no
+    TMA): the load-staged tensor-core kernel, sampled against the oracle."""
+    cfg = FUSED_CONFIGS["ep8tp2_E64_C256_M4096_H4096_t0_bf16"].replace(E=16, M=4100, H=4100)
+    dinp = fused_inputs_device(cfg)
+    w = [u.transpose(1, 2).contiguous() for u in dinp["w"]] if transposed else dinp["w"]
+    ys = bra.bmm_rs_a2a_infer_shape(cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H, 0)["y"]
+    out = [torch.full(ys, float("nan"), dtype=torch.bfloat16, device="cuda")
+           for _ in range(cfg.P)]
+    monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
+    assert bra.bmm_rs_a2a_variant(dinp["x"], w, dinp["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C,
+                                  cfg.M, cfg.H, 0, out, transpose_weight=transposed) == \
+        bra.VARIANT_TCU
+    bra.bmm_rs_a2a(dinp["x"], w, dinp["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H, 0,
+                   out=out, transpose_weight=transposed)
+    torch.cuda.synchronize()
+    assert bra.fault_status() == 0
+    for y in out:
+        assert not torch.isnan(y).any().item()
+    err = _sampled_check(cfg, dinp, out, np.random.default_rng(11), per_rank=16)
     assert err <= TOL["bf16"], f"sampled rel err {err:.3e}"

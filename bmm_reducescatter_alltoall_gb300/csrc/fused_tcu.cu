@@ -56,9 +56,11 @@ constexpr int PROD_THREADS = PROD_WARPS * 32;
 constexpr int CHUNKS_PER_THREAD = (A_CHUNKS + B_CHUNKS) / PROD_THREADS;   // 12
 static_assert(CHUNKS_PER_THREAD * PROD_THREADS == A_CHUNKS + B_CHUNKS, "chunk split");
 // Chunks whose loads are in flight together (13 warps leave 128 registers a
-// thread: an SM sub-partition holds four of them).
+// thread: an SM sub-partition holds four of them).  Four spill a few bytes
+// and still beat two and three, since throughput is set by the loads in
+// flight.
 #ifndef BRA_TCU_BATCH
-#define BRA_TCU_BATCH 2
+#define BRA_TCU_BATCH 4
 #endif
 constexpr int BATCH = BRA_TCU_BATCH;
 static_assert(CHUNKS_PER_THREAD % BATCH == 0, "batches");

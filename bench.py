@@ -35,11 +35,13 @@ METRIC = "fused BMM-RS-A2A TFLOP/s & all_to_all_v GB/s (1 GB300) vs roofline"
 def _args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--a2av-alone-calls", type=int, default=30,
+                    help="all_to_all_v calls timed alone after the step loop (0: none)")
     ap.add_argument("--fused", default=FUSED_NAME)
     ap.add_argument("--a2av", default=A2AV_NAME)
     ap.add_argument("--a2av-sweep", action="store_true",
@@ -342,6 +344,7 @@ def run_ours(a):
     variant = bra.bmm_rs_a2a_variant(finp["x"], finp["w"], finp["bias"], cfg.ep, cfg.tp, cfg.E,
                                      cfg.C, cfg.M, cfg.H, cfg.y_shard_type, yout)
     fused_kernel = {bra.VARIANT_TC: "fused_tc_kernel", bra.VARIANT_TC2: "fused_tc2_kernel",
+                    bra.VARIANT_TCU: "fused_tcu_kernel",
                     bra.VARIANT_SIMT: "fused_simt_kernel"}[variant]
 
     def fused():
@@ -426,6 +429,30 @@ def run_ours(a):
         "traffic": None if a_traffic is None else a_traffic["dram_bytes_per_launch"],
         "algorithmic_bytes_per_launch": a_bytes, "mean_ms": a_ms, "min_ms": min(a2av_ms),
         "B": bra.cal_all_to_all_v_blocks(acfg.P, acfg.L),
+    }
+
+    # ---- all_to_all_v timed alone: each call after the L2 sweep, with the GPU
+    # idle between calls (not following the fused kernel's power draw) ----
+    a_alone = []
+    for _ in range(a.a2av_alone_calls):
+        torch.cuda._sleep(20_000_000)     # keeps the GPU busy so the host runs ahead
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        a2av()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        a_alone.append(e0.elapsed_time(e1))
+    # the mean, not the median: event times come in ~2 us steps at this size
+    a_alone_ms = statistics.mean(a_alone) if a_alone else float("nan")
+    a2av_line["alone"] = None if not a_alone else {
+        "achieved": a_bytes / (a_alone_ms / 1e3) / 1e9, "unit": "GB/s",
+        "frac": a_bytes / (a_alone_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+        "mean_ms": a_alone_ms, "min_ms": min(a_alone), "calls": len(a_alone),
+        "note": "each call after the read-only L2 sweep, timed alone (CUDA events, ~2 us "
+                "resolution); the in-step figure above follows the fused kernel at its "
+                "power-capped clock, which also slows L2",
     }
 
     # ---- end to end through the public API with host buffers ----

@@ -104,6 +104,13 @@ FUSED_CONFIGS = {
         "ep8tp2_E8_C256_M4096_H4096_t0_bf16", ep=8, tp=2, E=8, C=256,
         M=4096, H=4096, y_shard_type=0, dtype="bf16", seed=2,
         x_std=0.02, w_std=0.02, bias_std=1.0),
+    # The bf16 profiling size with 4100-byte token rows and 8200-byte weight
+    # rows (M/tp = H/tp = 2050): no TMA descriptor fits, the tensor-core
+    # kernel that stages operands with loads runs.
+    "ep8tp2_E8_C256_M4100_H4100_t0_bf16": FusedConfig(
+        "ep8tp2_E8_C256_M4100_H4100_t0_bf16", ep=8, tp=2, E=8, C=256,
+        M=4100, H=4100, y_shard_type=0, dtype="bf16", seed=2,
+        x_std=0.02, w_std=0.02, bias_std=1.0),
     # Profiling size of the workload above: the same per-expert GEMMs, one
     # local expert per rank (E = ep), 1/8 of the FLOPs, 1.3 GB on the device.
     "ep8tp4_E8_C512_M8192_H4096_t1_fp16": FusedConfig(

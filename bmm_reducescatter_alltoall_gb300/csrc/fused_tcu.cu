@@ -50,20 +50,23 @@ constexpr int B_BOX_BYTES = 64 * BK * 2;          // 64(N) x 64(K), 8 KiB
 constexpr int B_BYTES = BN * BK * 2;              // 32 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 48 KiB
 constexpr int A_CHUNKS = A_BYTES / 16, B_CHUNKS = B_BYTES / 16;
-constexpr int EPI_WARPS = 4, MMA_WARP = 4, PROD_WARP0 = 5, PROD_WARPS = 8;
-constexpr int THREADS = (PROD_WARP0 + PROD_WARPS) * 32;   // 416
+#ifndef BRA_TCU_PROD_WARPS
+#define BRA_TCU_PROD_WARPS 7
+#endif
+constexpr int EPI_WARPS = 4, MMA_WARP = 4, PROD_WARP0 = 5, PROD_WARPS = BRA_TCU_PROD_WARPS;
+constexpr int THREADS = (PROD_WARP0 + PROD_WARPS) * 32;
 constexpr int PROD_THREADS = PROD_WARPS * 32;
-constexpr int CHUNKS_PER_THREAD = (A_CHUNKS + B_CHUNKS) / PROD_THREADS;   // 12
-static_assert(CHUNKS_PER_THREAD * PROD_THREADS == A_CHUNKS + B_CHUNKS, "chunk split");
+constexpr int CHUNKS_PER_THREAD = (A_CHUNKS + B_CHUNKS + PROD_THREADS - 1) / PROD_THREADS;
 // Chunks whose loads are in flight together (13 warps leave 128 registers a
 // thread: an SM sub-partition holds four of them).  Four spill a few bytes
 // and still beat two and three, since throughput is set by the loads in
 // flight.
 #ifndef BRA_TCU_BATCH
-#define BRA_TCU_BATCH 4
+#define BRA_TCU_BATCH 7
 #endif
 constexpr int BATCH = BRA_TCU_BATCH;
 static_assert(CHUNKS_PER_THREAD % BATCH == 0, "batches");
+constexpr int ALL_CHUNKS = A_CHUNKS + B_CHUNKS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
 // Epilogue staging per warp: 32 rows x 32 rounded 16-bit outputs (64 bytes,
@@ -239,7 +242,10 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tcu_kernel(const __grid_cons
 #pragma unroll
             for (int i = 0; i < BATCH; ++i) {
               const int id = ptid + (bt * BATCH + i) * PROD_THREADS;
-              if (id < A_CHUNKS) {
+              if (id >= ALL_CHUNKS) {
+                ld[i].n = 0;
+                dst[i] = 0;
+              } else if (id < A_CHUNKS) {
                 // A: token row m, K elements k0 + 8 kc ..
                 const int rr = id >> 3, kc = id & 7;
                 const int m = tc.mt * BM + rr;
@@ -263,7 +269,9 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tcu_kernel(const __grid_cons
               }
             }
 #pragma unroll
-            for (int i = 0; i < BATCH; ++i) sts128(dst[i], chunk_value(ld[i]));
+            for (int i = 0; i < BATCH; ++i)
+              if (ptid + (bt * BATCH + i) * PROD_THREADS < ALL_CHUNKS)
+                sts128(dst[i], chunk_value(ld[i]));
           }
           // generic-proxy writes -> visible to the tensor core, then publish
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -327,3 +327,32 @@ def test_unaligned_large_sampled(transposed, monkeypatch):
         assert not torch.isnan(y).any().item()
     err = _sampled_check(cfg, dinp, out, np.random.default_rng(11), per_rank=16)
     assert err <= TOL["bf16"], f"sampled rel err {err:.3e}"
+
+
+# --------------------------------------------------------------------------
+# The limits the guide's constraints allow (约束说明 / 数据关系与取值范围说明)
+# --------------------------------------------------------------------------
+
+MAX_CASES = [
+    # ep, tp, E, C, M, H, type, dtype, variants
+    (32, 32, 32, 2, 256, 256, 0, "fp16", ("tc", "tcu", "simt")),     # P = 1024 virtual ranks
+    (32, 32, 32, 32, 256, 256, 1, "bf16", ("tc", "tcu")),            # P = 1024, C/tp = 1
+    (16, 2, 512, 1, 16, 16, 0, "fp16", ("tc", "tcu")),               # E = 512: 32 local experts
+    (2, 1, 2, 2, 16, 65535, 0, "bf16", ("tcu", "simt")),             # H = 65535 (odd)
+    (2, 1, 2, 2, 65535, 16, 1, "fp16", ("tcu",)),                    # M/tp = 65535 (odd)
+]
+
+
+@pytest.mark.parametrize("case", MAX_CASES)
+def test_maximum_sizes(case, monkeypatch):
+    ep, tp, E, C, M, H, t, dt, variants = case
+    cfg = FusedConfig("max", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=ep + tp + E + C)
+    inp = fused_inputs_host(cfg)
+    ref = _oracle(cfg, inp)
+    dinp = _to_dev(inp)
+    for v in variants:
+        out = _run(cfg, dinp, v, monkeypatch)
+        err = _rel_err(out, ref)
+        assert err <= TOL[dt], f"{case[:8]} {v}: rel err {err:.3e}"
+        del out

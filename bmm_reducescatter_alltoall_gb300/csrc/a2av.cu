@@ -23,16 +23,15 @@
 //            staged with one granule of overlap) with cp.async.bulk (TMA
 //            bulk copies, completion on an mbarrier), starting before the
 //            rest of the set-up is done;
-//   warps 1-7 (consumers) stage the whole P x P count matrix (P <= 64, rows
-//            padded to P+1 so column reads hit distinct banks) in the ring
-//            stages the producer fills last, reject the call if any count
+//   warps 1-7 (consumers) read the whole P x P count matrix (P <= 64),
+//            each thread a slice of one column, reject the call if any count
 //            is negative, a non-zero count would touch a NULL buffer or
 //            (checked variant) a receive total is over capacity (every CTA
 //            sees the same matrix, so all take the same decision without a
 //            grid sync), sum every column below row i (the receive
 //            displacements) and over all rows, write the bookkeeping (CTA 0
-//            of each rank), build the pieces, hand the count stages to the
-//            producer, and then, for each chunk, write every vector of every
+//            of each rank), build the pieces, tell the producer the verdict,
+//            and then, for each chunk, write every vector of every
 //            piece whose first source byte lies in the chunk, shifting the
 //            words into destination alignment (int8 can be off by any byte,
 //            fp32 by whole words), while 32 lanes write the head and tail
@@ -71,15 +70,15 @@ constexpr uint32_t kChunk = kTileVecs * 16;
 constexpr int kStageBytes = kChunk + 16;
 constexpr int kStageStride = (kStageBytes + 127) / 128 * 128;
 constexpr int kRingBytes = kStages * kStageStride;
-static_assert(kRingBytes >= kA2avMaxP * (kA2avMaxP + 1) * 8, "the ring also holds the counts");
 #ifndef BRA_A2AV_THREADS
 #define BRA_A2AV_THREADS 256
 #endif
 constexpr int kA2avThreads = BRA_A2AV_THREADS;   // one producer warp + consumer warps
 constexpr int kConsumerWarps = kA2avThreads / 32 - 1;
 constexpr int kConsumers = kConsumerWarps * 32;
-// Count-matrix entries (P x P) per consumer thread.
-constexpr int kCountIters = (kA2avMaxP * kA2avMaxP + kConsumers - 1) / kConsumers;
+// Count rows per consumer thread: rows g, g + G, ... of one column, with
+// G = kConsumers / P >= kConsumers / kA2avMaxP row groups.
+constexpr int kColIters = (kA2avMaxP + kConsumers / kA2avMaxP - 1) / (kConsumers / kA2avMaxP);
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
 // Exclusive scan of 64 values held as (lane, lane + 32) by one warp.
@@ -248,7 +247,7 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   __shared__ __align__(8) uint64_t s_full[kStages];
   __shared__ __align__(8) uint64_t s_empty[kStages];
   __shared__ __align__(8) uint64_t s_row_ready;    // warp 0 has published row i
-  __shared__ __align__(8) uint64_t s_setup_done;   // the counts are no longer read
+  __shared__ __align__(8) uint64_t s_setup_done;   // the consumers' verdict (accept / reject)
   __shared__ int64_t s_lo, s_hi;
   __shared__ int s_npieces;
   __shared__ int s_bad;
@@ -259,26 +258,27 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   const int i = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ctid = tid - 32;   // consumer thread index (warps 1..7)
-  // The P x P counts (row stride P + 1, so column reads hit distinct banks)
-  // sit at the end of the ring, in the stages the producer fills last.
-  const int ld = P + 1;
-  const uint32_t sc_off = (uint32_t)(kRingBytes - P * ld * 8) & ~127u;
-  int64_t* const s_sc = reinterpret_cast<int64_t*>(ring + sc_off);
+  // Consumer thread (j, g) = (ctid % P, ctid / P), ctid < G * P, owns
+  // column j of the counts on the rows k = g, g + G, ... (a warp reads whole
+  // rows, so the loads coalesce).
+  const int G = kConsumers / P;   // >= 3 (P <= 64)
+  const int cj = ctid % P, cg = ctid / P;
+  const bool col_owner = warp > 0 && ctid < G * P;
 
   // Loads first, so they overlap the barrier set-up: row i (warp 0) and
   // each consumer thread's share of the count matrix, all issued before any
   // is used.
   int64_t r0 = 0, r1 = 0;
-  int64_t v[kCountIters];
+  int64_t v[kColIters];
   if (warp == 0) {
     const int64_t* row = a.sc + (int64_t)i * P;
     r0 = lane < P ? __ldg(row + lane) : 0;
     r1 = lane + 32 < P ? __ldg(row + lane + 32) : 0;
   } else {
 #pragma unroll
-    for (int m = 0; m < kCountIters; ++m) {
-      const int k = ctid + m * kConsumers;
-      v[m] = k < P * P ? __ldg(a.sc + k) : 0;
+    for (int m = 0; m < kColIters; ++m) {
+      const int k = cg + m * G;
+      v[m] = (col_owner && k < P) ? __ldg(a.sc + (int64_t)k * P + cj) : 0;
     }
     // Per-rank pointers into shared memory once: kernel-parameter arrays
     // read with a different index per lane serialise across the warp.
@@ -336,24 +336,14 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
     const int64_t ntiles = go ? (int64_t)((G1 - G0 + kChunk - 1) / kChunk) : 0;
     int stage = 0;
     uint32_t phase = 0;
-    bool ok = true, setup_seen = false;
+    bool ok = true;
     int64_t issued = 0;
 #pragma unroll 1
     for (int64_t t = 0; t < ntiles; ++t) {
+      // Also leaves when the consumers reject the call (they raise the flag).
       if (!mbar_wait(smem_u32(&s_empty[stage]), phase ^ 1u, abort_flag)) {
         ok = false;
         break;
-      }
-      if (!setup_seen && (uint32_t)stage * kStageStride + kStageBytes > sc_off) {
-        // This stage holds the counts until the consumers are done with them.
-        if (!mbar_wait_plain(smem_u32(&s_setup_done), 0, abort_flag)) {
-          ok = false;
-          break;
-        }
-        setup_seen = true;
-        if (s_reject) break;
-        // Order the consumers' generic accesses before the bulk copies.
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
       const uintptr_t c0 = G0 + (uintptr_t)t * kChunk;
       const uintptr_t ce = c0 + kChunk + 16 < G1 ? c0 + kChunk + 16 : G1;
@@ -367,15 +357,14 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
         phase ^= 1u;
       }
     }
-    // The CTA may not finish while copies it issued are in flight.  If the
-    // call was rejected nothing consumes them (and no stage was reused):
-    // wait for each to land.
-    if (ok && !setup_seen) ok = mbar_wait_plain(smem_u32(&s_setup_done), 0, abort_flag);
-    if (ok && s_reject) {
+    // The CTA may not finish while copies it issued are in flight, so learn
+    // the consumers' verdict.  A rejected call consumes nothing (and so no
+    // stage was reused): wait for each issued copy to land.
+    const bool told = mbar_wait_plain(smem_u32(&s_setup_done), 0, abort_flag);
+    if (told && s_reject) {
       for (int s = 0; s < kStages && s < issued; ++s)
         if (!mbar_wait_plain(smem_u32(&s_full[s]), 0, abort_flag)) break;
-    }
-    if (!ok) {   // a wait ran out: give copies already issued time to land
+    } else if (!ok || !told) {   // a wait ran out: give copies already issued time to land
       const unsigned long long t0 = global_ns();
       while (global_ns() - t0 < 2000000ull) {
       }
@@ -383,45 +372,28 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
     return;
   }
 
-  // Consumers (warps 1..7): the count matrix, the checks and the pieces,
-  // synchronised among themselves by named barrier 1.
-  {
-    const int step_rows = kConsumers / P, step_cols = kConsumers - step_rows * P;
-    int src = ctid / P, dst = ctid - (ctid / P) * P;   // entry ctid + m * kConsumers
-#pragma unroll
-    for (int m = 0; m < kCountIters; ++m) {
-      const int k = ctid + m * kConsumers;
-      if (m > 0) {
-        src += step_rows;
-        dst += step_cols;
-        if (dst >= P) {
-          dst -= P;
-          ++src;
-        }
-      }
-      if (k < P * P) {
-        s_sc[src * ld + dst] = v[m];
-        // A negative count, or a count that would read or write a NULL buffer.
-        if (v[m] < 0 || (v[m] > 0 && ((s_nul[src] & 1) | (s_nul[dst] & 2)))) s_bad = 1;
-      }
-    }
-  }
-  consumer_sync();
-
-  // The sums of column j over source rows k < i (rank i's receive
-  // displacement at j) and over all rows (what j receives), as G groups of
-  // threads each summing every G-th row, then one combine per column.
-  const int G = kConsumers / P;   // >= 3 (P <= 64)
-  if (ctid < G * P) {
-    const int j = ctid % P, g = ctid / P;
+  // Consumers (warps 1..7): the checks, the column sums and the pieces,
+  // synchronised among themselves by named barrier 1.  Thread (j, g) checks
+  // its counts (negative, or non-zero with a NULL buffer at either end) and
+  // sums column j over its rows below i (rank i's receive displacement at
+  // j) and over all its rows (what j receives); one combine per column.
+  if (col_owner) {
     int64_t before = 0, all = 0;
-    for (int k = g; k < P; k += G) {
-      const int64_t c = s_sc[k * ld + j];
-      all += c;
-      if (k < i) before += c;
+    bool bad_here = false;
+    const bool out_nul = (s_nul[cj] & 2) != 0;
+#pragma unroll
+    for (int m = 0; m < kColIters; ++m) {
+      const int k = cg + m * G;
+      if (k < P) {
+        const int64_t c = v[m];
+        all += c;
+        if (k < i) before += c;
+        bad_here |= c < 0 || (c > 0 && ((s_nul[k] & 1) || out_nul));
+      }
     }
-    s_part[0][g * P + j] = before;
-    s_part[1][g * P + j] = all;
+    if (bad_here) s_bad = 1;
+    s_part[0][cg * P + cj] = before;
+    s_part[1][cg * P + cj] = all;
   }
   consumer_sync();
   if (ctid < P) {
@@ -445,6 +417,7 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   if (bad) {
     if (ctid == 0) {
       s_reject = 1;
+      *abort_flag = 1;   // a producer waiting for a free stage leaves its loop
       mbar_arrive(smem_u32(&s_setup_done));
     }
     return;
@@ -491,7 +464,7 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
     if (lane == 0) s_npieces = __popc(m0) + __popc(m1);
   }
   consumer_sync();
-  if (ctid == 0) mbar_arrive(smem_u32(&s_setup_done));   // the counts are dead
+  if (ctid == 0) mbar_arrive(smem_u32(&s_setup_done));   // accepted
 
   // The CTA's source bytes [S, E) are contiguous (the send buffer is ordered
   // by destination).  They stream through the ring as chunks of kChunk bytes

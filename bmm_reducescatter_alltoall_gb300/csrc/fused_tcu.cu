@@ -364,6 +364,20 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tcu_kernel(const __grid_cons
       const int t_own = (m_own < p.rows && p.type == 1) ? (m_own % p.C) / Cp : 0;
       // yShardType 1: the row picks the TP rank, hence the bias row.
       const void* brow = (p.has_bias && p.type == 1) ? p.bias[sl * p.tp + t_own] : nullptr;
+      // This lane's row, once per tile: destination rank (without the
+      // column's TP rank for yShardType 0) and element offset of its start.
+      int d_own = 0;
+      int64_t off_own = 0;
+      if (m_own < p.rows) {
+        const int j = m_own / p.C, cm = m_own - j * p.C;
+        if (p.type == 0) {
+          d_own = j * p.tp;
+          off_own = ((int64_t)(s * p.El + e) * p.C + cm) * Hp;
+        } else {
+          d_own = j * p.tp + cm / Cp;
+          off_own = ((int64_t)(s * p.El + e) * Cp + (cm % Cp)) * p.H;
+        }
+      }
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t v[32];
@@ -383,27 +397,17 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tcu_kernel(const __grid_cons
           stg[lane * (kURowStride / 2) + c] = Elt<T>::cvt(f);
         }
         __syncwarp();
-        // phase 2: row by row, lanes on consecutive elements
+        // phase 2: row by row, lanes on consecutive elements; the row's
+        // destination comes from its lane, the column's part is per lane
+        const int n = n0 + ch * 32 + lane;
+        const int t_n = p.type == 0 ? n / Hp : 0;
+        const int h_n = n - t_n * (p.type == 0 ? Hp : 0);
 #pragma unroll 1
         for (int rr = 0; rr < 32; ++rr) {
-          const int m = row0 + rr;
-          if (m >= p.rows) break;
-          const int j = m / p.C, cm = m - j * p.C;
-          const int c = lane;
-          const int n = n0 + ch * 32 + c;
-          if (n < p.H) {
-            int d;
-            int64_t off;
-            if (p.type == 0) {
-              const int t = n / Hp;
-              d = j * p.tp + t;
-              off = ((int64_t)(s * p.El + e) * p.C + cm) * Hp + (n - t * Hp);
-            } else {
-              d = j * p.tp + cm / Cp;
-              off = ((int64_t)(s * p.El + e) * Cp + (cm % Cp)) * p.H + n;
-            }
-            static_cast<uint16_t*>(p.y[d])[off] = stg[rr * (kURowStride / 2) + c];
-          }
+          if (row0 + rr >= p.rows) break;
+          const int d = __shfl_sync(0xffffffffu, d_own, rr) + t_n;
+          const int64_t off = __shfl_sync(0xffffffffu, off_own, rr) + h_n;
+          if (n < p.H) static_cast<uint16_t*>(p.y[d])[off] = stg[rr * (kURowStride / 2) + lane];
         }
         __syncwarp();
       }

@@ -215,7 +215,7 @@ def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
     x[r], weight[r], bias[r] (or bias None) and out[r] are CUDA tensors of
     the shapes `bmm_rs_a2a_infer_shape` gives; out is allocated when None.
     transpose_weight: weight[r] is stored as (El, H, Kp) instead of
-    (El, Kp, H).  variant: None/"auto", "tc", "tc2" or "simt".
+    (El, Kp, H).  variant: None/"auto", "tc", "tc2", "tcu" or "simt".
     Returns out.  Asynchronous on `stream` (default: current stream).
     """
     torch = _torch()

@@ -116,13 +116,17 @@ typedef enum {
  *                    input range or another output range.
  *   BRA_ERR_UNSUPPORTED  ep*C >= 2^31.
  *   BRA_ERR_CUDA     the launch failed (cudaGetLastError).
- * Variant: a tensor-core kernel runs when every row stride and pointer is
- * 16-byte aligned (Kp % 8 == 0, H % 8 == 0, and Hp % 8 == 0 for yShardType
- * 0): the CTA-pair kernel when the problem has at least 64 output tiles of
- * 256 x 256, else the one-CTA kernel; otherwise the generic kernel.  Each
- * launches once per 64 source ranks.
- * The environment variable BRA_FORCE_VARIANT=tc|tc2|simt overrides the
- * choice (tc or tc2 on an ineligible shape returns BRA_ERR_UNSUPPORTED).
+ * Variant: when every row stride and pointer is 16-byte aligned (Kp % 8 ==
+ * 0, H % 8 == 0, and Hp % 8 == 0 for yShardType 0) a TMA-fed tensor-core
+ * kernel runs: the CTA-pair kernel when the problem has at least 64 output
+ * tiles of 256 x 256 and more than 128 token rows (ep*C) per expert group,
+ * else the one-CTA kernel.  Other shapes with element-aligned pointers run
+ * the tensor-core kernel that stages operands with loads; pointers that are
+ * not even element-aligned run the generic kernel.  Each launches once per
+ * 64 source ranks.
+ * The environment variable BRA_FORCE_VARIANT=tc|tc2|tcu|simt overrides the
+ * choice (tc, tc2 or tcu on an ineligible shape returns
+ * BRA_ERR_UNSUPPORTED).
  */
 BRA_API int bmm_rs_a2a(const void* const x[], const void* const weight[],
                const void* const bias[], int64_t ep, int64_t tp, int64_t E,

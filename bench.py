@@ -40,6 +40,8 @@ def _args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true",
+                    help="skip the unfused torch (cuBLAS bmm + elementwise) context timing")
     ap.add_argument("--a2av-alone-calls", type=int, default=30,
                     help="all_to_all_v calls timed alone after the step loop (0: none)")
     ap.add_argument("--fused", default=FUSED_NAME)
@@ -304,6 +306,36 @@ def run_reference(a):
 
 
 # --------------------------------------------------------------------------
+# Context: the same op unfused, from torch ops (cuBLAS bmm per rank, the tp
+# sum, the bias add and the all-to-all as copies).  Measurement only; the
+# intermediate tensors temp1 / temp2 / temp3 are materialised as the
+# reference op's dataflow describes.
+# --------------------------------------------------------------------------
+
+def unfused_torch(cfg, x, w, bias, out):
+    import torch
+    ep, tp, El, C, H, t_ = cfg.ep, cfg.tp, cfg.E // cfg.ep, cfg.C, cfg.H, cfg.y_shard_type
+    Hp, Cp = H // tp, C // tp
+    for s in range(ep):
+        temp2 = None
+        for t in range(tp):
+            temp1 = torch.bmm(x[s * tp + t], w[s * tp + t])            # (El, ep*C, H)
+            temp2 = temp1 if temp2 is None else temp2.add_(temp1)       # the reduce-scatter's sum
+        for t in range(tp):
+            r = s * tp + t
+            if t_ == 0:
+                chunk = temp2[:, :, t * Hp:(t + 1) * Hp]                # (El, ep*C, Hp)
+                b = None if bias is None else bias[r].reshape(El, 1, Hp)
+            else:
+                chunk = temp2.view(El, ep, tp, Cp, H)[:, :, t]          # (El, ep, Cp, H)
+                b = None if bias is None else bias[r].reshape(El, 1, 1, H)
+            temp3 = chunk if b is None else (chunk.float() + b.float()).to(chunk.dtype)
+            for j in range(ep):
+                blk = temp3[:, j * C:(j + 1) * C] if t_ == 0 else temp3[:, j]
+                out[j * tp + t][s * El:(s + 1) * El].copy_(blk)
+
+
+# --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
 
@@ -430,6 +462,33 @@ def run_ours(a):
         "algorithmic_bytes_per_launch": a_bytes, "mean_ms": a_ms, "min_ms": min(a2av_ms),
         "B": bra.cal_all_to_all_v_blocks(acfg.P, acfg.L),
     }
+
+    # ---- context: the same op unfused from torch ops (after the timed region) ----
+    unfused = None
+    if not a.no_unfused:
+        yref = [torch.empty_like(t) for t in yout]
+        unfused_torch(cfg, finp["x"], finp["w"], finp["bias"], yref)      # warm-up
+        torch.cuda.synchronize(dev)
+        u0 = torch.cuda.Event(enable_timing=True)
+        u1 = torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        for _ in range(3):
+            unfused_torch(cfg, finp["x"], finp["w"], finp["bias"], yref)
+        u1.record(stream)
+        torch.cuda.synchronize(dev)
+        u_ms = u0.elapsed_time(u1) / 3
+        diff = max(float((a_.float() - b_.float()).abs().max()) for a_, b_ in zip(yref, yout))
+        scale = max(float(b_.float().abs().max()) for b_ in yout)
+        unfused = {
+            "ms": u_ms, "tflops": step_flops / (u_ms / 1e3) / 1e12,
+            "fused_speedup": u_ms / f_ms,
+            "max_rel_diff_vs_fused": diff / scale,
+            "what": "torch.bmm per rank (cuBLAS) with temp1/temp2/temp3 materialised, the tp "
+                    "sum, bias add and the all-to-all as copies; 3 iterations after the timed "
+                    "region (context, not a product path)",
+        }
+        del yref
+        torch.cuda.empty_cache()
 
     # ---- all_to_all_v timed alone: each call after the L2 sweep, with the GPU
     # idle between calls (not following the fused kernel's power draw) ----
@@ -600,6 +659,7 @@ def run_ours(a):
             },
             "roofline": roofline,
             "all_to_all_v": a2av_line,
+            "unfused_torch": unfused,
             "cpu_baseline": cpu_baseline,
             "e2e": e2e,
             "clocks": clocks,

@@ -65,16 +65,46 @@ KERNEL_SOURCES = {
 }
 
 
+def code_text(src: bytes) -> bytes:
+    """C/C++/CUDA source with comments removed and whitespace normalised
+    (runs of blanks become one space, blank lines dropped); string and
+    character literals are kept verbatim.  Two sources with the same code
+    text compile to the same program."""
+    out = bytearray()
+    i, n = 0, len(src)
+    while i < n:
+        c = src[i:i + 1]
+        if c == b"/" and src[i + 1:i + 2] == b"/":
+            j = src.find(b"\n", i)
+            i = n if j < 0 else j
+        elif c == b"/" and src[i + 1:i + 2] == b"*":
+            j = src.find(b"*/", i + 2)
+            i = n if j < 0 else j + 2
+            out += b" "
+        elif c in (b'"', b"'"):
+            j = i + 1
+            while j < n and src[j:j + 1] != c:
+                j += 2 if src[j:j + 1] == b"\\" else 1
+            out += src[i:j + 1]
+            i = j + 1
+        else:
+            out += c
+            i += 1
+    lines = (b" ".join(line.split()) for line in bytes(out).split(b"\n"))
+    return b"\n".join(line for line in lines if line)
+
+
 def source_digest(kernel: str = None) -> str:
-    """Hash identifying a kernel build: the kernel's translation unit plus
-    every header (all sources when `kernel` is None)."""
+    """Hash identifying a kernel build: the code text (comments and
+    whitespace ignored) of the kernel's translation unit plus every header,
+    and the compile flags (all sources, verbatim, when `kernel` is None)."""
     if kernel is None:
         return _digest([])
     h = hashlib.sha256()
     for p in [os.path.join(CSRC, KERNEL_SOURCES[kernel])] + _headers():
         h.update(os.path.basename(p).encode())
         with open(p, "rb") as f:
-            h.update(f.read())
+            h.update(code_text(f.read()))
     h.update(" ".join(ARCH + CFLAGS).encode())
     return h.hexdigest()
 

@@ -377,6 +377,7 @@ def run_ours(a):
                                      cfg.C, cfg.M, cfg.H, cfg.y_shard_type, yout)
     fused_kernel = {bra.VARIANT_TC: "fused_tc_kernel", bra.VARIANT_TC2: "fused_tc2_kernel",
                     bra.VARIANT_TCU: "fused_tcu_kernel",
+                    bra.VARIANT_TCR: "fused_tcr_kernel",
                     bra.VARIANT_SIMT: "fused_simt_kernel"}[variant]
 
     def fused():

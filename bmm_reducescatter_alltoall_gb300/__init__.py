@@ -16,14 +16,14 @@ from typing import List, Optional, Sequence
 
 __all__ = [
     "BraError", "FP16", "BF16", "FP32", "INT8", "VARIANT_TC", "VARIANT_TC2", "VARIANT_SIMT",
-    "VARIANT_TCU", "wait_selftest",
+    "VARIANT_TCU", "VARIANT_TCR", "wait_selftest",
     "FusedOptions", "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
     "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked",
     "cal_all_to_all_v_blocks", "l2_flush", "fault_status", "status_str", "version",
 ]
 
 FP16, BF16, FP32, INT8 = 0, 1, 2, 3
-VARIANT_TC, VARIANT_SIMT, VARIANT_TC2, VARIANT_TCU = 1, 2, 3, 4
+VARIANT_TC, VARIANT_SIMT, VARIANT_TC2, VARIANT_TCU, VARIANT_TCR = 1, 2, 3, 4, 5
 OK, ERR_NULLPTR, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = (
     0, 161001, 161002, 161003, 161100, 161101)
 
@@ -155,7 +155,7 @@ def _shape_check(t, want, what):
 
 
 _VARIANTS = {None: 0, "auto": 0, "tc": VARIANT_TC, "tc2": VARIANT_TC2, "simt": VARIANT_SIMT,
-             "tcu": VARIANT_TCU}
+             "tcu": VARIANT_TCU, "tcr": VARIANT_TCR}
 
 
 def _options(transpose_weight: bool, variant) -> "FusedOptions":
@@ -215,7 +215,7 @@ def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
     x[r], weight[r], bias[r] (or bias None) and out[r] are CUDA tensors of
     the shapes `bmm_rs_a2a_infer_shape` gives; out is allocated when None.
     transpose_weight: weight[r] is stored as (El, H, Kp) instead of
-    (El, Kp, H).  variant: None/"auto", "tc", "tc2", "tcu" or "simt".
+    (El, Kp, H).  variant: None/"auto", "tc", "tc2", "tcr", "tcu" or "simt".
     Returns out.  Asynchronous on `stream` (default: current stream).
     """
     torch = _torch()
@@ -232,7 +232,7 @@ def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
 
 def bmm_rs_a2a_variant(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
                        transpose_weight: bool = False, variant: Optional[str] = None) -> int:
-    """VARIANT_TC, VARIANT_TC2, VARIANT_TCU or VARIANT_SIMT; raises BraError if rejected."""
+    """VARIANT_TC, VARIANT_TC2, VARIANT_TCR, VARIANT_TCU or VARIANT_SIMT; raises BraError if rejected."""
     xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
                                      transpose_weight)
     opts = _options(transpose_weight, variant)

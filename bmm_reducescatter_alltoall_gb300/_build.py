@@ -59,6 +59,7 @@ KERNEL_SOURCES = {
     "fused_tc_kernel": "fused_tc.cu",
     "fused_tc2_kernel": "fused_tc2.cu",
     "fused_tcu_kernel": "fused_tcu.cu",
+    "fused_tcr_kernel": "fused_tcr.cu",
     "l2_flush_kernel": "l2_flush.cu",
     "fused_simt_kernel": "fused_simt.cu",
     "a2av_kernel": "a2av.cu",

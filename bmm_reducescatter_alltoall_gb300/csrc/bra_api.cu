@@ -51,7 +51,7 @@ int validate_fused(const void* const x[], const void* const weight[],
       if (opts->reserved[k] != 0) return BRA_ERR_INVALID;
     if (opts->variant != BRA_VARIANT_AUTO && opts->variant != BRA_VARIANT_TC &&
         opts->variant != BRA_VARIANT_TC2 && opts->variant != BRA_VARIANT_SIMT &&
-        opts->variant != BRA_VARIANT_TCU)
+        opts->variant != BRA_VARIANT_TCU && opts->variant != BRA_VARIANT_TCR)
       return BRA_ERR_INVALID;
   }
   int rc = check_fused_attrs(ep, tp, E, C, M, H, type);
@@ -111,7 +111,7 @@ int validate_fused(const void* const x[], const void* const weight[],
   return BRA_OK;
 }
 
-// BRA_FORCE_VARIANT=tc|tc2|tcu|simt, read at every call.
+// BRA_FORCE_VARIANT=tc|tc2|tcr|tcu|simt, read at every call.
 int forced_variant() {
   const char* v = std::getenv("BRA_FORCE_VARIANT");
   if (!v || !*v) return BRA_VARIANT_AUTO;
@@ -119,6 +119,7 @@ int forced_variant() {
   if (!std::strcmp(v, "tc2")) return BRA_VARIANT_TC2;
   if (!std::strcmp(v, "simt")) return BRA_VARIANT_SIMT;
   if (!std::strcmp(v, "tcu")) return BRA_VARIANT_TCU;
+  if (!std::strcmp(v, "tcr")) return BRA_VARIANT_TCR;
   return BRA_VARIANT_AUTO;
 }
 
@@ -126,12 +127,16 @@ int choose_variant(const bra::FusedProblem& p, const bra_fused_options* opts) {
   const int f = (opts && opts->variant != BRA_VARIANT_AUTO) ? opts->variant : forced_variant();
   const bool tc_ok = bra::fused_tc_eligible(p);
   const bool tcu_ok = bra::fused_tcu_eligible(p);
+  const bool tcr_ok = bra::fused_tcr_eligible(p);
   if (f == BRA_VARIANT_SIMT) return BRA_VARIANT_SIMT;
   if (f == BRA_VARIANT_TC || f == BRA_VARIANT_TC2) return tc_ok ? f : -BRA_ERR_UNSUPPORTED;
   if (f == BRA_VARIANT_TCU) return tcu_ok ? f : -BRA_ERR_UNSUPPORTED;
-  // Rows TMA cannot describe: the tensor-core kernel that stages operands
-  // with loads; pointers not even element-aligned: the generic kernel.
-  if (!tc_ok) return tcu_ok ? BRA_VARIANT_TCU : BRA_VARIANT_SIMT;
+  if (f == BRA_VARIANT_TCR) return tcr_ok ? f : -BRA_ERR_UNSUPPORTED;
+  // Rows without a 16-byte pitch: the CTA-pair kernel fed by row-class TMA
+  // maps; when a launch cannot hold the maps of one TP group, the kernel
+  // that stages operands with loads; pointers not even element-aligned: the
+  // generic kernel.
+  if (!tc_ok) return tcr_ok ? BRA_VARIANT_TCR : tcu_ok ? BRA_VARIANT_TCU : BRA_VARIANT_SIMT;
   // The CTA-pair kernel moves a third less shared-memory traffic per FLOP;
   // with few 256 x 256 tiles the one-CTA kernel spreads over more SMs, and
   // with at most 128 token rows per group (a weight-streaming, HBM-bound
@@ -143,7 +148,11 @@ int choose_variant(const bra::FusedProblem& p, const bra_fused_options* opts) {
 }
 
 const char* variant_name(int v) {
-  return v == BRA_VARIANT_TC2 ? "tc2" : v == BRA_VARIANT_TC ? "tc" : v == BRA_VARIANT_TCU ? "tcu" : "simt";
+  return v == BRA_VARIANT_TC2   ? "tc2"
+         : v == BRA_VARIANT_TC  ? "tc"
+         : v == BRA_VARIANT_TCR ? "tcr"
+         : v == BRA_VARIANT_TCU ? "tcu"
+                                : "simt";
 }
 
 bool log_enabled() {
@@ -217,6 +226,7 @@ int bmm_rs_a2a_ex(const void* const x[], const void* const weight[],
                  (long long)H, (long long)yShardType, variant_name(v));
   cudaError_t e = v == BRA_VARIANT_TC2   ? bra::launch_fused_tc2(p, (cudaStream_t)stream)
                   : v == BRA_VARIANT_TC  ? bra::launch_fused_tc(p, (cudaStream_t)stream)
+                  : v == BRA_VARIANT_TCR ? bra::launch_fused_tcr(p, (cudaStream_t)stream)
                   : v == BRA_VARIANT_TCU ? bra::launch_fused_tcu(p, (cudaStream_t)stream)
                                         : bra::launch_fused_simt(p, (cudaStream_t)stream);
   if (e == cudaErrorInvalidValue && v != BRA_VARIANT_SIMT) return BRA_ERR_UNSUPPORTED;
@@ -319,12 +329,13 @@ int bra_l2_flush(void* buf, size_t bytes, bra_stream_t stream) {
 
 int bra_fault_status(int32_t* code, int clear) {
   if (!code) return BRA_ERR_NULLPTR;
-  int32_t a = 0, b = 0, c = 0, d = 0;
+  int32_t a = 0, b = 0, c = 0, d = 0, g = 0;
   if (bra::read_fault_word(&a, clear) != cudaSuccess) return BRA_ERR_CUDA;
   if (bra::read_fault_word2(&c, clear) != cudaSuccess) return BRA_ERR_CUDA;
   if (bra::read_fault_word3(&d, clear) != cudaSuccess) return BRA_ERR_CUDA;
+  if (bra::read_fault_word4(&g, clear) != cudaSuccess) return BRA_ERR_CUDA;
   if (bra::read_a2av_fault_word(&b, clear) != cudaSuccess) return BRA_ERR_CUDA;
-  *code = a ? a : (c ? c : (d ? d : b));
+  *code = a ? a : c ? c : d ? d : g ? g : b;
   return BRA_OK;
 }
 

@@ -58,11 +58,16 @@ bool fused_tc_eligible(const FusedProblem& f);
 // Tensor-core variant for rows of any alignment (operands staged by loads).
 cudaError_t launch_fused_tcu(const FusedProblem& f, cudaStream_t st);
 bool fused_tcu_eligible(const FusedProblem& f);
+// CTA-pair tensor-core variant for rows without a 16-byte pitch, fed by TMA
+// through row-class maps (cudaErrorInvalidValue if a map cannot be encoded).
+cudaError_t launch_fused_tcr(const FusedProblem& f, cudaStream_t st);
+bool fused_tcr_eligible(const FusedProblem& f);
 
 cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t st);
 cudaError_t read_fault_word(int32_t* code, int clear);        // tensor-core kernel
 cudaError_t read_fault_word2(int32_t* code, int clear);       // CTA-pair tensor-core kernel
-cudaError_t read_fault_word3(int32_t* code, int clear);       // unaligned tensor-core kernel
+cudaError_t read_fault_word3(int32_t* code, int clear);       // load-staged unaligned kernel
+cudaError_t read_fault_word4(int32_t* code, int clear);       // row-class TMA unaligned kernel
 cudaError_t read_a2av_fault_word(int32_t* code, int clear);   // all_to_all_v kernel
 // One bounded wait that nothing completes, with each family's wait helper.
 cudaError_t launch_a2av_wait_probe(int32_t* status, cudaStream_t st);

@@ -33,7 +33,7 @@
 #include <memory>
 #include <mutex>
 
-#include "tc_ptx.cuh"
+#include "tcu_epilogue.cuh"
 
 namespace bra {
 
@@ -69,11 +69,6 @@ static_assert(CHUNKS_PER_THREAD % BATCH == 0, "batches");
 constexpr int ALL_CHUNKS = A_CHUNKS + B_CHUNKS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
-// Epilogue staging per warp: 32 rows x 32 rounded 16-bit outputs (64 bytes,
-// rows 68 bytes apart so row-per-lane writes and per-row reads avoid bank
-// conflicts) plus the tile's yShardType-0 bias (fp32).
-constexpr int kURowStride = 68;
-constexpr int kUStageBytes = 32 * kURowStride + BN * 4;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + EPI_WARPS * kUStageBytes + 1024;
 
 struct UParams {
@@ -85,27 +80,6 @@ struct UParams {
   int s0, rows, m_tiles, n_tiles, k_blocks, num_tiles;
   int b_kmajor;
   uint32_t idesc;
-};
-
-template <typename T>
-struct Elt;
-template <>
-struct Elt<__half> {
-  static __device__ __forceinline__ uint16_t cvt(float v) {
-    return __half_as_ushort(__float2half_rn(v));
-  }
-  static __device__ __forceinline__ float bias(const void* p, int64_t i) {
-    return __half2float(static_cast<const __half*>(p)[i]);
-  }
-};
-template <>
-struct Elt<__nv_bfloat16> {
-  static __device__ __forceinline__ uint16_t cvt(float v) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  }
-  static __device__ __forceinline__ float bias(const void* p, int64_t i) {
-    return static_cast<const float*>(p)[i];
-  }
 };
 
 __device__ __forceinline__ uint4 ldg128(uintptr_t a) {
@@ -332,85 +306,17 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tcu_kernel(const __grid_cons
   } else {
     // ---------------- epilogue (warps 0..3 = TMEM lane quarters) ----------------
     const int q = warp;
-    uint16_t* stg = reinterpret_cast<uint16_t*>(epi_smem + q * kUStageBytes);
-    float* bias_stg = reinterpret_cast<float*>(epi_smem + q * kUStageBytes + 32 * kURowStride);
-    const int Hp = p.H / p.tp;
-    const int Cp = p.type == 1 ? p.C / p.tp : 1;
+    uint8_t* stg = epi_smem + q * kUStageBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       const TileCoord tc = tile_coord(tile, p.m_tiles, p.n_tiles, kGroupM);
       const int sl = tc.g / p.El, e = tc.g % p.El;
-      const int s = p.s0 + sl;
-      const int n0 = tc.nt * BN, row0 = tc.mt * BM + q * 32;
       const bool waited = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, fault);
       if (!__all_sync(0xffffffffu, waited)) break;
       tc_fence_after();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      // yShardType 0: the bias depends on the column only.
-      if (p.has_bias && p.type == 0) {
-        for (int c = lane; c < BN; c += 32) {
-          const int n = n0 + c;
-          float b = 0.f;
-          if (n < p.H) {
-            const int t = n / Hp;
-            b = Elt<T>::bias(p.bias[sl * p.tp + t], (int64_t)e * Hp + (n - t * Hp));
-          }
-          bias_stg[c] = b;
-        }
-        __syncwarp();
-      }
-      const int m_own = row0 + lane;
-      const int t_own = (m_own < p.rows && p.type == 1) ? (m_own % p.C) / Cp : 0;
-      // yShardType 1: the row picks the TP rank, hence the bias row.
-      const void* brow = (p.has_bias && p.type == 1) ? p.bias[sl * p.tp + t_own] : nullptr;
-      // This lane's row, once per tile: destination rank (without the
-      // column's TP rank for yShardType 0) and element offset of its start.
-      int d_own = 0;
-      int64_t off_own = 0;
-      if (m_own < p.rows) {
-        const int j = m_own / p.C, cm = m_own - j * p.C;
-        if (p.type == 0) {
-          d_own = j * p.tp;
-          off_own = ((int64_t)(s * p.El + e) * p.C + cm) * Hp;
-        } else {
-          d_own = j * p.tp + cm / Cp;
-          off_own = ((int64_t)(s * p.El + e) * Cp + (cm % Cp)) * p.H;
-        }
-      }
-#pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(t_base + ch * 32, v);
-        tmem_ld_wait();
-        // phase 1: lane = row; bias in fp32, one rounding, staged
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float f = __uint_as_float(v[c]);
-          const int n = n0 + ch * 32 + c;
-          if (p.has_bias) {
-            if (p.type == 0)
-              f += bias_stg[ch * 32 + c];
-            else if (m_own < p.rows && n < p.H)
-              f += Elt<T>::bias(brow, (int64_t)e * p.H + n);
-          }
-          stg[lane * (kURowStride / 2) + c] = Elt<T>::cvt(f);
-        }
-        __syncwarp();
-        // phase 2: row by row, lanes on consecutive elements; the row's
-        // destination comes from its lane, the column's part is per lane
-        const int n = n0 + ch * 32 + lane;
-        const int t_n = p.type == 0 ? n / Hp : 0;
-        const int h_n = n - t_n * (p.type == 0 ? Hp : 0);
-#pragma unroll 1
-        for (int rr = 0; rr < 32; ++rr) {
-          if (row0 + rr >= p.rows) break;
-          const int d = __shfl_sync(0xffffffffu, d_own, rr) + t_n;
-          const int64_t off = __shfl_sync(0xffffffffu, off_own, rr) + h_n;
-          if (n < p.H) static_cast<uint16_t*>(p.y[d])[off] = stg[rr * (kURowStride / 2) + lane];
-        }
-        __syncwarp();
-      }
+      epilogue_rows_u<T>(p, t_base, tc.mt * BM + q * 32, sl, e, tc.nt * BN, stg, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));

@@ -64,8 +64,11 @@ typedef enum {
   BRA_VARIANT_TC = 1,    /* tcgen05 / TMEM / TMA kernel, one CTA per tile  */
   BRA_VARIANT_SIMT = 2,  /* generic kernel: any alignment, any size        */
   BRA_VARIANT_TC2 = 3,   /* tcgen05 kernel, a CTA pair per 256x256 tile    */
-  BRA_VARIANT_TCU = 4    /* tcgen05 kernel for rows of any alignment:
+  BRA_VARIANT_TCU = 4,   /* tcgen05 kernel for rows of any alignment:
                             operands staged by loads, not TMA             */
+  BRA_VARIANT_TCR = 5    /* tcgen05 CTA-pair kernel for rows of any
+                            alignment: row-class TMA maps, rows shifted
+                            into place in shared memory                   */
 } bra_variant;
 
 /* ------------------------------------------------------------------------ */
@@ -121,11 +124,16 @@ typedef enum {
  * kernel runs: the CTA-pair kernel when the problem has at least 64 output
  * tiles of 256 x 256 and more than 128 token rows (ep*C) per expert group,
  * else the one-CTA kernel.  Other shapes with element-aligned pointers run
- * the tensor-core kernel that stages operands with loads; pointers that are
- * not even element-aligned run the generic kernel.  Each launches once per
- * 64 source ranks.
- * The environment variable BRA_FORCE_VARIANT=tc|tc2|tcu|simt overrides the
- * choice (tc, tc2 or tcu on an ineligible shape returns
+ * the CTA-pair tensor-core kernel fed by row-class TMA maps (one map per
+ * class of rows that start at the same offset past a 16-byte boundary, the
+ * rows shifted into place in shared memory); when the maps of one TP group
+ * do not fit a launch ((n_x + n_w) * tp > 176, n = 1, 2, 4 or 8 classes per
+ * operand) the tensor-core kernel that stages operands with loads runs
+ * instead.  Pointers that are not even element-aligned run the generic
+ * kernel.  Each launches once per 64 source ranks (the row-class kernel once
+ * per 176 / (n_x + n_w) ranks).
+ * The environment variable BRA_FORCE_VARIANT=tc|tc2|tcr|tcu|simt overrides
+ * the choice (tc, tc2, tcr or tcu on an ineligible shape returns
  * BRA_ERR_UNSUPPORTED).
  */
 BRA_API int bmm_rs_a2a(const void* const x[], const void* const weight[],
@@ -173,8 +181,8 @@ BRA_API int bmm_rs_a2a_infer_shape(int64_t ep, int64_t tp, int64_t E, int64_t C,
 
 /*
  * bmm_rs_a2a_variant -- which kernel bmm_rs_a2a_ex would launch for these
- * arguments and options (BRA_VARIANT_TC, BRA_VARIANT_TC2, BRA_VARIANT_TCU
- * or BRA_VARIANT_SIMT), honouring BRA_FORCE_VARIANT.  Pointers are only
+ * arguments and options (BRA_VARIANT_TC, BRA_VARIANT_TC2, BRA_VARIANT_TCR,
+ * BRA_VARIANT_TCU or BRA_VARIANT_SIMT), honouring BRA_FORCE_VARIANT.  Pointers are only
  * inspected for alignment.  Returns the variant, or a negative bra_status
  * (e.g. -BRA_ERR_INVALID) when the call would be rejected.  Pure host.
  */

@@ -159,7 +159,7 @@ def _call_rejected(lib, f, dtype=bra.FP16, **over):
 
 def test_valid_shapes_choose_a_variant(lib):
     f = Fake(4, 2, 16, 12, 12, 4, 1)                  # M/tp = 6: not 16-byte rows
-    assert _variant(lib, f) == bra.VARIANT_TCU        # tensor cores, operands staged by loads
+    assert _variant(lib, f) == bra.VARIANT_TCR        # tensor cores fed by row-class TMA maps
     g = Fake(8, 4, 64, 512, 8192, 4096, 1)
     assert _variant(lib, g) == bra.VARIANT_TC2
     assert _variant(lib, Fake(8, 2, 64, 256, 4096, 4096, 0), bra.BF16) == bra.VARIANT_TC2
@@ -167,7 +167,11 @@ def test_valid_shapes_choose_a_variant(lib):
     # decode-like token counts: <= 128 rows per group stream weights on one-CTA tiles
     assert _variant(lib, Fake(8, 4, 64, 16, 8192, 4096, 1)) == bra.VARIANT_TC
     assert _variant(lib, Fake(8, 4, 64, 32, 8192, 4096, 1)) == bra.VARIANT_TC2
-    assert _variant(lib, Fake(2, 2, 4, 4, 16, 20, 0)) == bra.VARIANT_TCU    # H/tp = 10
+    assert _variant(lib, Fake(2, 2, 4, 4, 16, 20, 0)) == bra.VARIANT_TCR    # H/tp = 10
+    # odd M/tp and H: 8 row classes each; 16 maps a rank fit one TP group of 8
+    # ranks in a launch (176 maps), not one of 16: operands staged by loads
+    assert _variant(lib, Fake(2, 8, 4, 16, 8 * 3, 5, 1)) == bra.VARIANT_TCR
+    assert _variant(lib, Fake(2, 16, 4, 16, 16 * 3, 5, 1)) == bra.VARIANT_TCU
     # an operand that is not even element-aligned: only the generic kernel
     odd = Fake(4, 2, 16, 12, 12, 4, 1)
     odd.x[3] += 1
@@ -188,6 +192,11 @@ def test_forced_variant(lib, monkeypatch):
     odd = Fake(4, 2, 16, 12, 12, 4, 1)
     odd.w[0] += 1
     assert _variant(lib, odd) == -UNSUPPORTED
+    monkeypatch.setenv("BRA_FORCE_VARIANT", "tcr")
+    assert _variant(lib, Fake(8, 4, 64, 512, 8192, 4096, 1)) == bra.VARIANT_TCR
+    assert _variant(lib, Fake(4, 2, 16, 12, 12, 4, 1)) == bra.VARIANT_TCR
+    assert _variant(lib, odd) == -UNSUPPORTED
+    assert _variant(lib, Fake(2, 16, 4, 16, 16 * 3, 5, 1)) == -UNSUPPORTED
 
 
 @pytest.mark.parametrize("over", [
@@ -281,8 +290,8 @@ def test_options_select_the_variant_and_are_checked(lib, monkeypatch):
 def test_tc_alignment_predicate(lib):
     g = Fake(2, 2, 8, 128, 128, 256, 0)
     assert _variant(lib, g) in (bra.VARIANT_TC, bra.VARIANT_TC2)
-    g.x[1] += 2                                   # 2-byte aligned only: no TMA
-    assert _variant(lib, g) == bra.VARIANT_TCU
+    g.x[1] += 2                                   # 2-byte aligned only: row-class TMA
+    assert _variant(lib, g) == bra.VARIANT_TCR
     g.x[1] += 1                                   # not even element-aligned
     assert _variant(lib, g) == bra.VARIANT_SIMT
 

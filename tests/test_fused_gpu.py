@@ -91,10 +91,10 @@ TC_CASES = [
 
 
 _WANT = {"tc": bra.VARIANT_TC, "tc2": bra.VARIANT_TC2, "tcu": bra.VARIANT_TCU,
-         "simt": bra.VARIANT_SIMT}
+         "tcr": bra.VARIANT_TCR, "simt": bra.VARIANT_SIMT}
 
 
-@pytest.mark.parametrize("variant", ["tc", "tc2", "tcu"])
+@pytest.mark.parametrize("variant", ["tc", "tc2", "tcr", "tcu"])
 @pytest.mark.parametrize("case", TC_CASES)
 @pytest.mark.parametrize("bias", [True, False])
 def test_tensor_core_kernels(case, bias, variant, monkeypatch):
@@ -129,10 +129,10 @@ def test_generic_kernel_on_the_same_shapes(case, monkeypatch):
     (2, 1, 2, 3, 5, 7, 1, "fp16"),
     (4, 4, 8, 8, 20, 36, 0, "bf16"),
 ])
-@pytest.mark.parametrize("variant", [None, "simt"])
+@pytest.mark.parametrize("variant", [None, "tcu", "simt"])
 def test_unaligned_shapes_small(case, variant, monkeypatch):
-    """Rows TMA cannot describe: the load-staged tensor-core kernel (the
-    automatic choice) and the generic kernel."""
+    """Rows without a 16-byte pitch: the row-class TMA kernel (the automatic
+    choice), the load-staged tensor-core kernel and the generic kernel."""
     ep, tp, E, C, M, H, t, dt = case
     cfg = FusedConfig("u", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
                       seed=sum(case[:6]) + 2)
@@ -153,9 +153,10 @@ UNALIGNED_CASES = [
 ]
 
 
+@pytest.mark.parametrize("variant", [None, "tcu"])
 @pytest.mark.parametrize("case", UNALIGNED_CASES)
 @pytest.mark.parametrize("bias", [True, False])
-def test_unaligned_shapes_tensor_core(case, bias, monkeypatch):
+def test_unaligned_shapes_tensor_core(case, bias, variant, monkeypatch):
     ep, tp, E, C, M, H, t, dt = case
     cfg = FusedConfig("ut", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
                       seed=sum(case[:6]) + 11, has_bias=bias)
@@ -165,11 +166,11 @@ def test_unaligned_shapes_tensor_core(case, bias, monkeypatch):
     probe = [torch.empty(ys, dtype=dinp["x"][0].dtype, device="cuda") for _ in range(cfg.P)]
     monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
     assert bra.bmm_rs_a2a_variant(dinp["x"], dinp["w"], dinp["bias"], ep, tp, E, C, M, H, t,
-                                  probe) == bra.VARIANT_TCU
+                                  probe) == bra.VARIANT_TCR
     ref = _oracle(cfg, inp)
-    out = _run(cfg, dinp, None, monkeypatch)
+    out = _run(cfg, dinp, variant, monkeypatch)
     err = _rel_err(out, ref)
-    assert err <= TOL[dt], f"{case} bias={bias}: rel err {err:.3e}"
+    assert err <= TOL[dt], f"{case} bias={bias} {variant}: rel err {err:.3e}"
 
 
 def test_unaligned_2d_bias_and_generic_agree(monkeypatch):
@@ -177,13 +178,14 @@ def test_unaligned_2d_bias_and_generic_agree(monkeypatch):
                       seed=21)
     _check_small(cfg, monkeypatch, bias_ndim=2)
     dinp = _to_dev(fused_inputs_host(cfg))
-    a = _run(cfg, dinp, "tcu", monkeypatch)
     b = _run(cfg, dinp, "simt", monkeypatch)
     ref = [u.float().cpu().numpy().astype(np.float64) for u in b]
-    assert _rel_err(a, ref) <= TOL["fp16"]
+    for v in ("tcr", "tcu"):
+        a = _run(cfg, dinp, v, monkeypatch)
+        assert _rel_err(a, ref) <= TOL["fp16"], v
 
 
-@pytest.mark.parametrize("variant", ["tc", "tc2", "tcu"])
+@pytest.mark.parametrize("variant", ["tc", "tc2", "tcr", "tcu"])
 def test_tc_and_generic_agree(variant, monkeypatch):
     cfg = FusedConfig("x", ep=4, tp=2, E=8, C=128, M=256, H=512, y_shard_type=1,
                       dtype="bf16", seed=3)
@@ -261,7 +263,7 @@ TW_CASES = [
 ]
 
 
-@pytest.mark.parametrize("variant", ["tc", "tc2", "tcu", "simt"])
+@pytest.mark.parametrize("variant", ["tc", "tc2", "tcr", "tcu", "simt"])
 @pytest.mark.parametrize("case", TW_CASES)
 def test_transposed_weight(case, variant):
     ep, tp, E, C, M, H, t, dt = case
@@ -305,10 +307,12 @@ def test_transposed_weight_full_size_sampled():
     assert err <= TOL["bf16"], f"sampled rel err {err:.3e}"
 
 
+@pytest.mark.parametrize("variant", [None, "tcu"])
 @pytest.mark.parametrize("transposed", [False, True])
-def test_unaligned_large_sampled(transposed, monkeypatch):
-    """A large shape with 4100-byte token rows and 8200-byte weight rows (no
-    TMA): the load-staged tensor-core kernel, sampled against the oracle."""
+def test_unaligned_large_sampled(transposed, variant, monkeypatch):
+    """A large shape with 4100-byte token rows and 8200-byte weight rows: the
+    row-class TMA kernel (the automatic choice) and the load-staged kernel,
+    sampled against the oracle."""
     cfg = FUSED_CONFIGS["ep8tp2_E64_C256_M4096_H4096_t0_bf16"].replace(E=16, M=4100, H=4100)
     dinp = fused_inputs_device(cfg)
     w = [u.transpose(1, 2).contiguous() for u in dinp["w"]] if transposed else dinp["w"]
@@ -318,9 +322,9 @@ def test_unaligned_large_sampled(transposed, monkeypatch):
     monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
     assert bra.bmm_rs_a2a_variant(dinp["x"], w, dinp["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C,
                                   cfg.M, cfg.H, 0, out, transpose_weight=transposed) == \
-        bra.VARIANT_TCU
+        bra.VARIANT_TCR
     bra.bmm_rs_a2a(dinp["x"], w, dinp["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H, 0,
-                   out=out, transpose_weight=transposed)
+                   out=out, transpose_weight=transposed, variant=variant)
     torch.cuda.synchronize()
     assert bra.fault_status() == 0
     for y in out:
@@ -329,17 +333,59 @@ def test_unaligned_large_sampled(transposed, monkeypatch):
     assert err <= TOL["bf16"], f"sampled rel err {err:.3e}"
 
 
+def _shifted(t, off):
+    """A copy of t whose storage starts `off` elements past an allocation
+    (16-byte aligned) start."""
+    buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+    v = buf[off:off + t.numel()].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+@pytest.mark.parametrize("M,H", [(272, 264), (130, 70)])
+def test_element_aligned_pointers(M, H, transposed, monkeypatch):
+    """x, weight and y of every rank start 1..7 elements past a 16-byte
+    boundary (a different offset per rank), with 16-byte and with unaligned
+    row pitches: the row-class maps start below each row and the rows are
+    shifted into place."""
+    cfg = FusedConfig("ptr", ep=4, tp=2, E=8, C=96, M=M, H=H, y_shard_type=1, dtype="bf16",
+                      seed=M + H)
+    inp = fused_inputs_host(cfg)
+    ref = _oracle(cfg, inp)
+    dinp = _to_dev(inp)
+    xs = [_shifted(x, 1 + r % 7) for r, x in enumerate(dinp["x"])]
+    w0 = [w.transpose(1, 2).contiguous() for w in dinp["w"]] if transposed else dinp["w"]
+    ws = [_shifted(w, 7 - r % 7) for r, w in enumerate(w0)]
+    ys = bra.bmm_rs_a2a_infer_shape(cfg.ep, cfg.tp, cfg.E, cfg.C, M, H, 1)["y"]
+    outs = [_shifted(torch.full(ys, float("nan"), dtype=torch.bfloat16, device="cuda"), 3)
+            for _ in range(cfg.P)]
+    monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
+    for v in (None, "tcu"):
+        assert v or bra.bmm_rs_a2a_variant(xs, ws, dinp["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C,
+                                           M, H, 1, outs, transpose_weight=transposed) == \
+            bra.VARIANT_TCR
+        for o in outs:
+            o.fill_(float("nan"))
+        bra.bmm_rs_a2a(xs, ws, dinp["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C, M, H, 1, out=outs,
+                       transpose_weight=transposed, variant=v)
+        torch.cuda.synchronize()
+        assert bra.fault_status() == 0
+        err = _rel_err(outs, ref)
+        assert err <= TOL["bf16"], f"M={M} H={H} transposed={transposed} {v}: {err:.3e}"
+
+
 # --------------------------------------------------------------------------
 # The limits the guide's constraints allow (约束说明 / 数据关系与取值范围说明)
 # --------------------------------------------------------------------------
 
 MAX_CASES = [
     # ep, tp, E, C, M, H, type, dtype, variants
-    (32, 32, 32, 2, 256, 256, 0, "fp16", ("tc", "tcu", "simt")),     # P = 1024 virtual ranks
-    (32, 32, 32, 32, 256, 256, 1, "bf16", ("tc", "tcu")),            # P = 1024, C/tp = 1
-    (16, 2, 512, 1, 16, 16, 0, "fp16", ("tc", "tcu")),               # E = 512: 32 local experts
-    (2, 1, 2, 2, 16, 65535, 0, "bf16", ("tcu", "simt")),             # H = 65535 (odd)
-    (2, 1, 2, 2, 65535, 16, 1, "fp16", ("tcu",)),                    # M/tp = 65535 (odd)
+    (32, 32, 32, 2, 256, 256, 0, "fp16", ("tc", "tcr", "tcu", "simt")),  # P = 1024 virtual ranks
+    (32, 32, 32, 32, 256, 256, 1, "bf16", ("tc", "tcr", "tcu")),         # P = 1024, C/tp = 1
+    (16, 2, 512, 1, 16, 16, 0, "fp16", ("tc", "tcr", "tcu")),            # E = 512: 32 local experts
+    (2, 1, 2, 2, 16, 65535, 0, "bf16", ("tcr", "tcu", "simt")),          # H = 65535 (odd)
+    (2, 1, 2, 2, 65535, 16, 1, "fp16", ("tcr", "tcu")),                  # M/tp = 65535 (odd)
 ]
 
 

@@ -74,7 +74,13 @@ constexpr int RWARPS = BRA_TCR_RWARPS;       // realign warps per group
 constexpr int RGROUPS = BRA_TCR_RGROUPS;     // groups take K blocks in turn
 constexpr int RAW_STAGES = BRA_TCR_RAW_STAGES, SW_STAGES = BRA_TCR_SW_STAGES;
 constexpr int TMA_WARP = 0, MMA_WARP = 1, RW0 = 2;
-constexpr int EPI_WARP0 = ((RW0 + RGROUPS * RWARPS + 3) / 4) * 4;   // lane quarter = warp % 4
+// Warps between the realign warps and the epilogue signal the leader for the
+// peer CTA (at least two, taking stages in turn).
+constexpr int SIG_WARP0 = RW0 + RGROUPS * RWARPS;
+constexpr int EPI_WARP0 = ((SIG_WARP0 + 2 + 3) / 4) * 4;   // lane quarter = warp % 4
+constexpr int NSIG = EPI_WARP0 - SIG_WARP0;
+constexpr int NBW = 16 / RWARPS;                           // realign batches per warp and stage
+static_assert(16 % RWARPS == 0, "realign batches");
 constexpr int THREADS = (EPI_WARP0 + 4) * 32;
 // canonical stage: A 128 x 64 K-major; B 64 x 128 N-major (two 64 x 64 boxes)
 // or, transposed weight, 128 x 64 K-major
@@ -153,12 +159,12 @@ __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 }
 
 // One realign batch: four warp steps of one class box, each lane moving one
-// 16-byte chunk per step: the 16 bytes that start D elements (2D bytes) into
-// the raw granule pair at src[s] go to dst[s], or zeros where bit s of
-// `zero` is set.  All loads are issued before the first is used.
+// 16-byte chunk per step: o[s] = the 16 bytes that start D elements (2D
+// bytes) into the raw granule pair at src[s], or zeros where bit s of `zero`
+// is set.  All loads are issued before the first is used.
 template <int D>
-__device__ __forceinline__ void shift_batch(const uint32_t (&src)[4], const uint32_t (&dst)[4],
-                                            uint32_t zero) {
+__device__ __forceinline__ void shift_batch(const uint32_t (&src)[4], uint32_t zero,
+                                            uint4 (&o)[4]) {
   uint4 a[4], b[4];
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
@@ -167,36 +173,34 @@ __device__ __forceinline__ void shift_batch(const uint32_t (&src)[4], const uint
   }
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
-    uint4 o;
     if constexpr (D == 0) {
-      o = a[s];
+      o[s] = a[s];
     } else {
       const uint32_t x[8] = {a[s].x, a[s].y, a[s].z, a[s].w, b[s].x, b[s].y, b[s].z, b[s].w};
       constexpr int w = D / 2;
       if constexpr (D % 2 == 0) {
-        o = make_uint4(x[w], x[w + 1], x[w + 2], x[w + 3]);
+        o[s] = make_uint4(x[w], x[w + 1], x[w + 2], x[w + 3]);
       } else {
-        o.x = __funnelshift_r(x[w], x[w + 1], 16);
-        o.y = __funnelshift_r(x[w + 1], x[w + 2], 16);
-        o.z = __funnelshift_r(x[w + 2], x[w + 3], 16);
-        o.w = __funnelshift_r(x[w + 3], x[w + 4], 16);
+        o[s].x = __funnelshift_r(x[w], x[w + 1], 16);
+        o[s].y = __funnelshift_r(x[w + 1], x[w + 2], 16);
+        o[s].z = __funnelshift_r(x[w + 2], x[w + 3], 16);
+        o[s].w = __funnelshift_r(x[w + 3], x[w + 4], 16);
       }
     }
-    if ((zero >> s) & 1u) o = make_uint4(0u, 0u, 0u, 0u);
-    sts128(dst[s], o);
+    if ((zero >> s) & 1u) o[s] = make_uint4(0u, 0u, 0u, 0u);
   }
 }
-__device__ __forceinline__ void shift_batch_rt(int d, const uint32_t (&src)[4],
-                                               const uint32_t (&dst)[4], uint32_t zero) {
+__device__ __forceinline__ void shift_batch_rt(int d, const uint32_t (&src)[4], uint32_t zero,
+                                               uint4 (&o)[4]) {
   switch (d) {
-    case 1: shift_batch<1>(src, dst, zero); break;
-    case 2: shift_batch<2>(src, dst, zero); break;
-    case 3: shift_batch<3>(src, dst, zero); break;
-    case 4: shift_batch<4>(src, dst, zero); break;
-    case 5: shift_batch<5>(src, dst, zero); break;
-    case 6: shift_batch<6>(src, dst, zero); break;
-    case 7: shift_batch<7>(src, dst, zero); break;
-    default: shift_batch<0>(src, dst, zero); break;
+    case 1: shift_batch<1>(src, zero, o); break;
+    case 2: shift_batch<2>(src, zero, o); break;
+    case 3: shift_batch<3>(src, zero, o); break;
+    case 4: shift_batch<4>(src, zero, o); break;
+    case 5: shift_batch<5>(src, zero, o); break;
+    case 6: shift_batch<6>(src, zero, o); break;
+    case 7: shift_batch<7>(src, zero, o); break;
+    default: shift_batch<0>(src, zero, o); break;
   }
 }
 
@@ -231,11 +235,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t raw_base = sw_base + SW_STAGES * SW_BYTES;
   uint8_t* bars = smem + SW_STAGES * SW_BYTES + RAW_STAGES * RAW_BYTES;
   const uint32_t bar_base = smem_u32(bars);
-  constexpr int NB = 2 * RAW_STAGES + 2 * SW_STAGES;
+  constexpr int NB = 2 * RAW_STAGES + 3 * SW_STAGES;
   auto raw_full = [&](int s) { return bar_base + 8u * s; };
   auto raw_empty = [&](int s) { return bar_base + 8u * (RAW_STAGES + s); };
   auto sw_full = [&](int s) { return bar_base + 8u * (2 * RAW_STAGES + s); };
   auto sw_empty = [&](int s) { return bar_base + 8u * (2 * RAW_STAGES + SW_STAGES + s); };
+  auto ready = [&](int s) { return bar_base + 8u * (2 * RAW_STAGES + 2 * SW_STAGES + s); };
   auto tfull_bar = [&](int a) { return bar_base + 8u * (NB + a); };
   auto tempty_bar = [&](int a) { return bar_base + 8u * (NB + 2 + a); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 * (NB + 4));
@@ -252,11 +257,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RAW_STAGES; ++s) {
       mbar_init(raw_full(s), 1);            // expect_tx of this CTA's producer
-      mbar_init(raw_empty(s), 1);           // this CTA's realign warps, once all are done
+      mbar_init(raw_empty(s), RWARPS);      // each realign warp of the stage's group
     }
     for (int s = 0; s < SW_STAGES; ++s) {
       mbar_init(sw_full(s), 2);             // leader: one arrival per CTA of the pair
       mbar_init(sw_empty(s), 1);            // one multicast commit per use
+      mbar_init(ready(s), 1);               // peer: its realign group is done
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -386,11 +392,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // 64 warp steps per K block (32 for A, 32 for B) in 16 batches of four
     // steps inside one class box; group g takes the K blocks n with
     // n % RGROUPS == g (n counts the CTA's K blocks), and its warp rw the
-    // batches rw, rw + RWARPS, ...
+    // batches rw, rw + RWARPS, ...  A warp frees the raw stage as soon as its
+    // rows are in registers, then waits for the canonical slot.
     const int grp = (warp - RW0) / RWARPS, rw = (warp - RW0) % RWARPS;
     int n = 0;
     const int rg = lane >> 3, c = lane & 7;
-    const uint32_t leader_sw_full0 = map_to_rank(sw_full(0), 0);
     const int sx = 5 - p.lgx, sw = 5 - p.lgw;   // log2 of warp steps per class box
     int rs = 0, ss = 0;
     uint32_t rph = 0, sph = 0;
@@ -405,82 +411,114 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int8_t* xd = &p.delta[rl * mpr];
         const int8_t* wd = xd + ncx;
         for (int kb = 0; kb < p.k_blocks; ++kb, ++n) {
-          if (n % RGROUPS != grp) {
-            if (++rs == RAW_STAGES) {
-              rs = 0;
-              rph ^= 1u;
+          if (n % RGROUPS == grp) {
+            // all warps of the group go on, or all leave (a wait that gave up)
+            if (!realign_all(grp, mbar_wait(raw_full(rs), rph, abort_flag, fault))) {
+              ok = false;
+              break;
             }
-            if (++ss == SW_STAGES) {
-              ss = 0;
-              sph ^= 1u;
+            const uint32_t ra = raw_base + rs * RAW_BYTES, rb = ra + RAW_A;
+            const uint32_t sa = sw_base + ss * SW_BYTES, sb = sa + A_BYTES;
+            const int k0 = kb * BK;
+            const int fbk = e * p.Kp + k0;
+            uint4 val[NBW][4];
+            uint32_t dst[NBW][4];
+#pragma unroll
+            for (int h = 0; h < NBW; ++h) {
+              const int bt = rw + h * RWARPS;
+              uint32_t src[4], zero = 0;
+              int d;
+              if (bt < 8) {
+                // A: rows i = b + n_x * j, eight lanes a row, four rows a step
+                const int it0 = bt * 4, b = it0 >> sx, v0 = it0 & ((1 << sx) - 1);
+                const uint32_t box = ra + b * (RAW_A >> p.lgx);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                  const int j = 4 * (v0 + s) + rg, i = b + (j << p.lgx);
+                  src[s] = box + j * KROW + c * 16;
+                  dst[h][s] = sa + i * 128 + ((c ^ (i & 7)) << 4);
+                }
+                d = xd[(fa + b) & (ncx - 1)];
+              } else if (p.b_kmajor) {
+                // B, transposed weight: N rows, as A
+                const int it0 = (bt - 8) * 4, b = it0 >> sw, v0 = it0 & ((1 << sw) - 1);
+                const uint32_t box = rb + b * (RAW_B >> p.lgw);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                  const int j = 4 * (v0 + s) + rg, i = b + (j << p.lgw);
+                  src[s] = box + j * KROW + c * 16;
+                  dst[h][s] = sb + i * 128 + ((c ^ (i & 7)) << 4);
+                }
+                d = wd[(fbn + b) & (ncw - 1)];
+              } else {
+                // B, weight (Kp, H): two K rows a step, both 64-column halves;
+                // K rows past Kp become zeros
+                const int it0 = (bt - 8) * 4, b = it0 >> sw, v0 = it0 & ((1 << sw) - 1);
+                const uint32_t box = rb + b * ((BK * NROW) >> p.lgw);
+                const int half = rg & 1;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                  const int j = 2 * (v0 + s) + (rg >> 1), kr = b + (j << p.lgw);
+                  src[s] = box + j * NROW + (half * 8 + c) * 16;
+                  dst[h][s] = sb + half * B_BOX_BYTES + kr * 128 + ((c ^ (kr & 7)) << 4);
+                  if (k0 + kr >= p.Kp) zero |= 1u << s;
+                }
+                d = wd[(fbk + b) & (ncw - 1)];
+              }
+              shift_batch_rt(d, src, zero, val[h]);
             }
-            continue;
-          }
-          // all warps of the group go on, or all leave (a wait that gave up)
-          const bool got = mbar_wait(raw_full(rs), rph, abort_flag, fault) &&
-                           mbar_wait(sw_empty(ss), sph ^ 1u, abort_flag, fault);
-          if (!realign_all(grp, got)) {
-            ok = false;
-            break;
-          }
-          const uint32_t ra = raw_base + rs * RAW_BYTES, rb = ra + RAW_A;
-          const uint32_t sa = sw_base + ss * SW_BYTES, sb = sa + A_BYTES;
-          const int k0 = kb * BK;
-          const int fbk = e * p.Kp + k0;
-#pragma unroll 1
-          for (int bt = rw; bt < 16; bt += RWARPS) {
-            uint32_t src[4], dst[4], zero = 0;
-            int d;
-            if (bt < 8) {
-              // A: rows i = b + n_x * j, eight lanes a row, four rows a step
-              const int it0 = bt * 4, b = it0 >> sx, v0 = it0 & ((1 << sx) - 1);
-              const uint32_t box = ra + b * (RAW_A >> p.lgx);
+            // this warp's reads of the raw stage are done
+            __syncwarp();
+            if (lane == 0) mbar_arrive(raw_empty(rs));
+            const bool got = mbar_wait(sw_empty(ss), sph ^ 1u, abort_flag, fault);
+            if (got) {
 #pragma unroll
-              for (int s = 0; s < 4; ++s) {
-                const int j = 4 * (v0 + s) + rg, i = b + (j << p.lgx);
-                src[s] = box + j * KROW + c * 16;
-                dst[s] = sa + i * 128 + ((c ^ (i & 7)) << 4);
-              }
-              d = xd[(fa + b) & (ncx - 1)];
-            } else if (p.b_kmajor) {
-              // B, transposed weight: N rows, as A
-              const int it0 = (bt - 8) * 4, b = it0 >> sw, v0 = it0 & ((1 << sw) - 1);
-              const uint32_t box = rb + b * (RAW_B >> p.lgw);
+              for (int h = 0; h < NBW; ++h)
 #pragma unroll
-              for (int s = 0; s < 4; ++s) {
-                const int j = 4 * (v0 + s) + rg, i = b + (j << p.lgw);
-                src[s] = box + j * KROW + c * 16;
-                dst[s] = sb + i * 128 + ((c ^ (i & 7)) << 4);
-              }
-              d = wd[(fbn + b) & (ncw - 1)];
-            } else {
-              // B, weight (Kp, H): two K rows a step, both 64-column halves;
-              // K rows past Kp become zeros
-              const int it0 = (bt - 8) * 4, b = it0 >> sw, v0 = it0 & ((1 << sw) - 1);
-              const uint32_t box = rb + b * ((BK * NROW) >> p.lgw);
-              const int half = rg & 1;
-#pragma unroll
-              for (int s = 0; s < 4; ++s) {
-                const int j = 2 * (v0 + s) + (rg >> 1), kr = b + (j << p.lgw);
-                src[s] = box + j * NROW + (half * 8 + c) * 16;
-                dst[s] = sb + half * B_BOX_BYTES + kr * 128 + ((c ^ (kr & 7)) << 4);
-                if (k0 + kr >= p.Kp) zero |= 1u << s;
-              }
-              d = wd[(fbk + b) & (ncw - 1)];
+                for (int s = 0; s < 4; ++s) sts128(dst[h][s], val[h][s]);
             }
-            shift_batch_rt(d, src, dst, zero);
-          }
-          // generic-proxy writes -> visible to the tensor core; once every
-          // realign warp is done, one thread publishes the stage
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          realign_sync(grp);
-          if (rw == 0 && lane == 0) {
-            mbar_arrive_cluster(leader_sw_full0 + 8u * ss);
-            mbar_arrive(raw_empty(rs));
+            // generic-proxy writes -> visible to the tensor core; the barrier
+            // also tells the group whether every wait succeeded
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (!realign_all(grp, got)) {
+              ok = false;
+              break;
+            }
+            // publish: the leader arrives on its own barrier; the peer tells
+            // a signal warp, which makes the release at cluster scope
+            if (rw == 0 && lane == 0) mbar_arrive(rank == 0 ? sw_full(ss) : ready(ss));
           }
           if (++rs == RAW_STAGES) {
             rs = 0;
             rph ^= 1u;
+          }
+          if (++ss == SW_STAGES) {
+            ss = 0;
+            sph ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp >= SIG_WARP0 && warp < EPI_WARP0) {
+    // ---------------- peer signal warps ----------------
+    // Signal warp k takes the stages n with n % NSIG == k: once the peer's
+    // realign group is done (ready), one release arrive at cluster scope on
+    // the leader's sw_full makes those writes visible to the leader's MMA.
+    // These arrives take a while each; several warps keep them overlapped.
+    if (rank == 1 && lane == 0) {
+      const int k = warp - SIG_WARP0;
+      const uint32_t leader_sw_full0 = map_to_rank(sw_full(0), 0);
+      int n = 0, ss = 0;
+      uint32_t sph = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+        for (int kk = 0; kk < p.tp * p.k_blocks; ++kk, ++n) {
+          if (n % NSIG == k) {
+            if (!mbar_wait(ready(ss), sph, abort_flag, fault)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_cluster(leader_sw_full0 + 8u * ss);
           }
           if (++ss == SW_STAGES) {
             ss = 0;

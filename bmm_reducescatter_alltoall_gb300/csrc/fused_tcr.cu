@@ -204,14 +204,9 @@ __device__ __forceinline__ void shift_batch_rt(int d, const uint32_t (&src)[4], 
   }
 }
 
-// Named barrier of realign group g (id 1 + g); every thread of the group
-// reaches each use, since the group leaves its loop only as a whole
-// (realign_all).
-__device__ __forceinline__ void realign_sync(int g) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "n"(RWARPS * 32) : "memory");
-}
-// The same barrier as a reduction: true on every thread of the group iff v
-// is true on all of them.
+// Named barrier of realign group g (id 1 + g) as a reduction: true on every
+// thread of the group iff v is true on all of them.  Every thread of the
+// group reaches each use, since the group leaves its loop only as a whole.
 __device__ __forceinline__ bool realign_all(int g, bool v) {
   uint32_t r;
   asm volatile(

@@ -95,14 +95,40 @@ def code_text(src: bytes) -> bytes:
     return b"\n".join(line for line in lines if line)
 
 
+def included_files(path: str) -> list:
+    """`path` and every header it includes with #include "..." (found in
+    csrc/ or include/), transitively, each once, in a stable order."""
+    seen, order = set(), []
+
+    def visit(p):
+        if p in seen:
+            return
+        seen.add(p)
+        order.append(p)
+        with open(p, "rb") as f:
+            text = code_text(f.read()).decode("utf-8", "replace")
+        for line in text.splitlines():
+            line = line.strip()
+            if line.startswith("#include") and '"' in line:
+                name = line.split('"')[1]
+                for d in (os.path.dirname(p), CSRC, INCLUDE):
+                    q = os.path.join(d, name)
+                    if os.path.exists(q):
+                        visit(os.path.normpath(q))
+                        break
+    visit(os.path.normpath(path))
+    return order
+
+
 def source_digest(kernel: str = None) -> str:
     """Hash identifying a kernel build: the code text (comments and
-    whitespace ignored) of the kernel's translation unit plus every header,
-    and the compile flags (all sources, verbatim, when `kernel` is None)."""
+    whitespace ignored) of the kernel's translation unit and of the headers
+    it includes, and the compile flags (all sources, verbatim, when `kernel`
+    is None)."""
     if kernel is None:
         return _digest([])
     h = hashlib.sha256()
-    for p in [os.path.join(CSRC, KERNEL_SOURCES[kernel])] + _headers():
+    for p in included_files(os.path.join(CSRC, KERNEL_SOURCES[kernel])):
         h.update(os.path.basename(p).encode())
         with open(p, "rb") as f:
             h.update(code_text(f.read()))

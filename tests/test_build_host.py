@@ -33,3 +33,13 @@ def test_literals_survive_and_comments_go():
     assert b'"a // not a comment /* nor this */"' in t
     assert b"header comment" not in t and b"trailing" not in t and b"block" not in t
     assert b"#define TILE 128\n" in t
+
+
+def test_digest_follows_the_included_headers(tmp_path):
+    from bmm_reducescatter_alltoall_gb300._build import included_files
+    (tmp_path / "k.cu").write_text('#include "a.h"\n// #include "gone.h"\nint k;\n')
+    (tmp_path / "a.h").write_text('#pragma once\n#include "b.h"\n/* #include "c.h" */\n')
+    (tmp_path / "b.h").write_text('#include "a.h"\nint b;\n')
+    (tmp_path / "c.h").write_text("int c;\n")
+    names = [p.rsplit("/", 1)[-1] for p in included_files(str(tmp_path / "k.cu"))]
+    assert names == ["k.cu", "a.h", "b.h"]        # commented includes and cycles handled

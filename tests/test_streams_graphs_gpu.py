@@ -15,8 +15,8 @@ from workloads import A2AV_CONFIGS, FusedConfig, a2av_inputs, fused_inputs_host
 pytestmark = pytest.mark.gpu
 
 
-def _fused_case(seed, t=1, dt="fp16"):
-    cfg = FusedConfig("s", ep=4, tp=2, E=8, C=128, M=512, H=768, y_shard_type=t, dtype=dt,
+def _fused_case(seed, t=1, dt="fp16", M=512, H=768):
+    cfg = FusedConfig("s", ep=4, tp=2, E=8, C=128, M=M, H=H, y_shard_type=t, dtype=dt,
                       seed=seed)
     inp = fused_inputs_host(cfg)
     d = {k: (None if v is None else [u.cuda() for u in v]) for k, v in inp.items()}
@@ -45,52 +45,62 @@ def _same_bits(a, b):
                for x, y in zip(a, b))
 
 
-def test_concurrent_calls_on_two_streams():
+def test_concurrent_calls_on_three_streams():
     c1, d1, mk1 = _fused_case(1, t=1, dt="fp16")
     c2, d2, mk2 = _fused_case(2, t=0, dt="bf16")
+    c3, d3, mk3 = _fused_case(4, t=1, dt="bf16", M=514, H=774)   # Kp = 257: row-class kernel
+    assert bra.bmm_rs_a2a_variant(d3["x"], d3["w"], d3["bias"], c3.ep, c3.tp, c3.E, c3.C, c3.M,
+                                  c3.H, 1, mk3()) == bra.VARIANT_TCR
     ca, ins, scd, mka = _a2av_case()
-    ref1, ref2, refa = mk1(), mk2(), mka()
+    ref1, ref2, ref3, refa = mk1(), mk2(), mk3(), mka()
     _call(c1, d1, ref1)
     _call(c2, d2, ref2)
+    _call(c3, d3, ref3)
     bra.all_to_all_v(ins, scd, refa, ca.L)
     torch.cuda.synchronize()
-    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1, s2, s3 = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     for _ in range(3):
-        o1, o2, oa = mk1(), mk2(), mka()
+        o1, o2, o3, oa = mk1(), mk2(), mk3(), mka()
         torch.cuda.synchronize()
         _call(c1, d1, o1, stream=s1)
         _call(c2, d2, o2, stream=s2)
+        _call(c3, d3, o3, stream=s3)
         bra.all_to_all_v(ins, scd, oa, ca.L, stream=s2)
         torch.cuda.synchronize()
-        assert _same_bits(o1, ref1) and _same_bits(o2, ref2) and _same_bits(oa, refa)
+        assert _same_bits(o1, ref1) and _same_bits(o2, ref2) and _same_bits(o3, ref3)
+        assert _same_bits(oa, refa)
     assert bra.fault_status() == 0
 
 
 def test_step_captured_in_a_cuda_graph():
     c1, d1, mk1 = _fused_case(3, t=1, dt="fp16")
+    c3, d3, mk3 = _fused_case(5, t=0, dt="fp16", M=514, H=774)   # row-class kernel
     ca, ins, scd, mka = _a2av_case()
-    ref1, refa = mk1(), mka()
+    ref1, ref3, refa = mk1(), mk3(), mka()
     _call(c1, d1, ref1)
+    _call(c3, d3, ref3)
     bra.all_to_all_v(ins, scd, refa, ca.L)
     torch.cuda.synchronize()
-    o1, oa = mk1(), mka()
+    o1, o3, oa = mk1(), mk3(), mka()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):          # warm the library's per-device set-up
         _call(c1, d1, o1)
+        _call(c3, d3, o3)
         bra.all_to_all_v(ins, scd, oa, ca.L)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    for t_ in o1 + oa:
+    for t_ in o1 + o3 + oa:
         t_.zero_()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         _call(c1, d1, o1)
+        _call(c3, d3, o3)
         bra.all_to_all_v(ins, scd, oa, ca.L)
     for _ in range(2):
-        for t_ in o1 + oa:
+        for t_ in o1 + o3 + oa:
             t_.zero_()
         g.replay()
         torch.cuda.synchronize()
-        assert _same_bits(o1, ref1) and _same_bits(oa, refa)
+        assert _same_bits(o1, ref1) and _same_bits(o3, ref3) and _same_bits(oa, refa)
     assert bra.fault_status() == 0

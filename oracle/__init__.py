@@ -16,7 +16,8 @@ Sources (pages, cited by title and section):
 Modules:
   fused     -- infer_shapes, bmm_rs_a2a (sender view, the four steps in order),
                y_source / bmm_rs_a2a_point (receiver view, per element)
-  a2av      -- cal_all_to_all_v_blocks, a2av_bookkeeping, all_to_all_v
+  a2av      -- cal_all_to_all_v_blocks, a2av_bookkeeping, all_to_all_v,
+               indexed_all_to_all_v (gather through the index, then exchange)
   rounding  -- float64 -> fp16 / bf16 round-to-nearest-even
 
 Pins (tests/test_oracle.py): the printed CalAllToAllVBlocks example and rule

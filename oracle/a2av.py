@@ -94,3 +94,51 @@ def received_totals(send_counts: np.ndarray) -> np.ndarray:
         for j in range(P):
             tot[j] += sc[i, j]
     return tot
+
+
+def indexed_all_to_all_v(inputs: Sequence[np.ndarray], index: Sequence[np.ndarray],
+                         send_counts: np.ndarray, out_init: Sequence[np.ndarray]) -> dict:
+    """Indexed exchange ([PTO] §A5 URMA 索引交换): the page names the operands
+    (input, send_counts, recv_counts, index) and says the cores share the
+    local data movement before the remote transfers; it does not define
+    `index`.  Reading taken here: the local movement gathers rank i's send
+    list from its input through its index, then the send lists are exchanged
+    as in all_to_all_v:
+
+        send_i[k] = inputs[i][index[i][k]]        k < sum_j send_counts[i][j]
+        out[j][rd[j][i] + m] = send_i[sd[i][j] + m]   m < send_counts[i][j]
+
+    An index value outside [0, len(inputs[i])) is an error: that element is
+    not delivered (its destination keeps the initial value) and is counted in
+    "invalid".  Negative counts reject the whole call, as in all_to_all_v.
+    """
+    sc = np.asarray(send_counts, dtype=np.int64)
+    P = sc.shape[0]
+    if (sc < 0).any():
+        raise ValueError("negative send count")
+    sd, rc, rd = a2av_bookkeeping(sc)
+    out: List[np.ndarray] = [np.array(o, copy=True) for o in out_init]
+    invalid = 0
+    for i in range(P):
+        src = np.asarray(inputs[i])
+        idx = np.asarray(index[i], dtype=np.int64)
+        n = int(sc[i].sum())
+        if len(idx) < n:
+            raise ValueError(f"rank {i}: index shorter than its send list")
+        # local movement: the send list and which of its entries exist
+        ok = (idx[:n] >= 0) & (idx[:n] < len(src))
+        invalid += int((~ok).sum())
+        send = np.zeros(n, dtype=src.dtype)
+        send[ok] = src[idx[:n][ok]]
+        # the exchange of the send list
+        for j in range(P):
+            c = int(sc[i, j])
+            if c == 0:
+                continue
+            a, b = int(sd[i, j]), int(rd[j, i])
+            if b + c > len(out[j]):
+                raise ValueError(f"pair ({i},{j}) exceeds a buffer")
+            keep = ok[a:a + c]
+            out[j][b:b + c][keep] = send[a:a + c][keep]
+    return {"out": out, "send_displs": sd, "recv_counts": rc, "recv_displs": rd,
+            "invalid": invalid}

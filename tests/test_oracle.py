@@ -122,6 +122,84 @@ def test_exchange_brute_force_by_tags():
             np.testing.assert_array_equal(out[j], np.array(expect, dtype=np.float64))
 
 
+# --------------------------------------------------------------------------
+# indexed all_to_all_v (reading: gather through the index, then exchange)
+# --------------------------------------------------------------------------
+
+def _indexed_case(P, seed, hi=5, extra=3):
+    rng = np.random.default_rng(seed)
+    sc = rng.integers(0, hi + 1, size=(P, P)).astype(np.int64)
+    lens = [int(sc[i].sum()) + int(rng.integers(0, extra + 1)) for i in range(P)]
+    inputs = [rng.standard_normal(n) for n in lens]
+    index = [rng.integers(0, max(n, 1), size=int(sc[i].sum())) for i, n in enumerate(lens)]
+    return sc, inputs, index
+
+
+def test_indexed_with_identity_index_is_all_to_all_v():
+    for P in (1, 2, 3, 8):
+        sc, inputs = _a2av_case(P, seed=40 + P)
+        cols = sc.sum(axis=0)
+        init = [np.full(int(n) + 2, -7.0) for n in cols]
+        ident = [np.arange(len(a), dtype=np.int64) for a in inputs]
+        a = oa.all_to_all_v(inputs, sc, init)
+        b = oa.indexed_all_to_all_v(inputs, ident, sc, init)
+        assert b["invalid"] == 0
+        for u, v in zip(a["out"], b["out"]):
+            np.testing.assert_array_equal(u, v)
+        for k in ("send_displs", "recv_counts", "recv_displs"):
+            np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_indexed_brute_force_by_tags():
+    # Input element p of rank i carries the tag i * 1000 + p.  Walking each
+    # sender's destinations in rank order with a running position, the m-th
+    # element rank j receives from rank i must carry the tag of the input
+    # element that rank i's index names at that position.
+    for P, seed in itertools.product((1, 2, 3, 4), range(4)):
+        sc, inputs, index = _indexed_case(P, seed=200 + 10 * P + seed)
+        tagged = [np.array([i * 1000 + q for q in range(len(inputs[i]))], dtype=np.float64)
+                  for i in range(P)]
+        expect = [[] for _ in range(P)]
+        for j in range(P):
+            for i in range(P):
+                pos = 0
+                for jj in range(P):
+                    for m in range(int(sc[i, jj])):
+                        if jj == j:
+                            expect[j].append(i * 1000 + int(index[i][pos]))
+                        pos += 1
+        cols = sc.sum(axis=0)
+        out = oa.indexed_all_to_all_v(tagged, index, sc, [np.zeros(int(n)) for n in cols])["out"]
+        for j in range(P):
+            np.testing.assert_array_equal(out[j], np.array(expect[j], dtype=np.float64))
+
+
+def test_indexed_permutation_conserves_the_elements():
+    for P in (2, 5, 8):
+        rng = np.random.default_rng(300 + P)
+        sc = rng.integers(0, 9, size=(P, P)).astype(np.int64)
+        inputs = [rng.standard_normal(int(sc[i].sum())) for i in range(P)]
+        index = [rng.permutation(len(a)) for a in inputs]
+        cols = sc.sum(axis=0)
+        r = oa.indexed_all_to_all_v(inputs, index, sc, [np.zeros(int(n)) for n in cols])
+        assert r["invalid"] == 0
+        np.testing.assert_array_equal(np.sort(np.concatenate(r["out"])),
+                                      np.sort(np.concatenate(inputs)))
+
+
+def test_indexed_out_of_range_not_delivered_and_counted():
+    sc = np.array([[2, 1], [1, 2]], dtype=np.int64)
+    inputs = [np.array([10.0, 11.0, 12.0]), np.array([20.0, 21.0, 22.0, 23.0])]
+    index = [np.array([2, -1, 0]), np.array([4, 1, 3])]   # -1 and 4 are outside
+    init = [np.full(3, -5.0), np.full(3, -5.0)]
+    r = oa.indexed_all_to_all_v(inputs, index, sc, init)
+    assert r["invalid"] == 2
+    np.testing.assert_array_equal(r["out"][0], [12.0, -5.0, -5.0])   # from 0: 12, bad; from 1: bad
+    np.testing.assert_array_equal(r["out"][1], [10.0, 21.0, 23.0])
+    with pytest.raises(ValueError):
+        oa.indexed_all_to_all_v(inputs, index, np.array([[1, -1], [0, 1]]), init)
+
+
 def test_negative_counts_rejected():
     sc = np.array([[1, -1], [0, 2]], dtype=np.int64)
     with pytest.raises(ValueError):

@@ -44,6 +44,8 @@ def _args(argv=None):
                     help="skip the unfused torch (cuBLAS bmm + elementwise) context timing")
     ap.add_argument("--a2av-alone-calls", type=int, default=30,
                     help="all_to_all_v calls timed alone after the step loop (0: none)")
+    ap.add_argument("--indexed-calls", type=int, default=30,
+                    help="indexed all_to_all_v calls timed alone after the step loop (0: none)")
     ap.add_argument("--fused", default=FUSED_NAME)
     ap.add_argument("--a2av", default=A2AV_NAME)
     ap.add_argument("--a2av-sweep", action="store_true",
@@ -349,7 +351,7 @@ def run_ours(a):
     from bmm_reducescatter_alltoall_gb300 import _build
     _build.build()
     import bmm_reducescatter_alltoall_gb300 as bra
-    from workloads import A2AV_CONFIGS, FUSED_CONFIGS, a2av_inputs, fused_inputs_device
+    from workloads import A2AV_CONFIGS, FUSED_CONFIGS, a2av_index, a2av_inputs, fused_inputs_device
 
     cfg = FUSED_CONFIGS[a.fused]
     acfg = A2AV_CONFIGS[a.a2av]
@@ -515,6 +517,48 @@ def run_ours(a):
                 "power-capped clock, which also slows L2",
     }
 
+    # ---- indexed all_to_all_v timed alone: the same counts and payload, each
+    # sender's list gathered through a permutation of its input ----
+    indexed = None
+    if a.indexed_calls > 0:
+        perm = a2av_index(sc, [len(v) for v in a_inputs], "perm", seed=acfg.seed)
+        ix = [torch.from_numpy(v).to(dev) for v in perm]
+
+        def ia2av():
+            bra.indexed_all_to_all_v(a_in, ix, sc_d, a_out, acfg.L, send_displs=book[0],
+                                     recv_counts=book[1], recv_displs=book[2], stream=stream)
+
+        for _ in range(3):
+            ia2av()
+        ia_ms = []
+        for _ in range(a.indexed_calls):
+            torch.cuda._sleep(20_000_000)
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ia2av()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ia_ms.append(e0.elapsed_time(e1))
+        n_el = int(sc.sum())
+        ia_bytes = 2 * n_el * a_in[0].element_size() + 8 * n_el + 4 * sc.size * 8
+        m = statistics.mean(ia_ms)
+        indexed = {
+            "kernel": "ia2av_kernel", "workload": f"{a.a2av}, index = a permutation of each "
+                                                  "sender's input (seeded)",
+            "achieved": ia_bytes / (m / 1e3) / 1e9, "unit": "GB/s",
+            "frac": ia_bytes / (m / 1e3) / 1e9 / peaks["hbm_gbs"], "peak": peaks["hbm_gbs"],
+            "algorithmic_bytes_per_launch": ia_bytes, "mean_ms": m, "min_ms": min(ia_ms),
+            "calls": len(ia_ms),
+            "note": "bytes = payload read + write + 8-byte index per element + bookkeeping; "
+                    "each call after the read-only L2 sweep, timed alone; the gathers are "
+                    "random, one 32-byte sector per element",
+        }
+        del ix
+        if bra.fault_status() != 0:
+            raise RuntimeError("watchdog word set by the indexed exchange")
+
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if a.e2e_steps > 0:
@@ -660,6 +704,7 @@ def run_ours(a):
             },
             "roofline": roofline,
             "all_to_all_v": a2av_line,
+            "indexed_all_to_all_v": indexed,
             "unfused_torch": unfused,
             "cpu_baseline": cpu_baseline,
             "e2e": e2e,

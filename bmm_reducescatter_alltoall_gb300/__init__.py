@@ -16,7 +16,7 @@ from typing import List, Optional, Sequence
 
 __all__ = [
     "BraError", "FP16", "BF16", "FP32", "INT8", "VARIANT_TC", "VARIANT_TC2", "VARIANT_SIMT",
-    "VARIANT_TCU", "VARIANT_TCR", "wait_selftest",
+    "VARIANT_TCU", "VARIANT_TCR", "wait_selftest", "indexed_all_to_all_v",
     "FusedOptions", "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
     "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked",
     "cal_all_to_all_v_blocks", "l2_flush", "fault_status", "status_str", "version",
@@ -73,6 +73,9 @@ def library() -> ctypes.CDLL:
     lib.all_to_all_v.restype = c_int
     lib.all_to_all_v_checked.argtypes = [pp, vp, vp, vp, vp, pp, i64, i64, c_int, i64p, vp, vp]
     lib.all_to_all_v_checked.restype = c_int
+    lib.indexed_all_to_all_v.argtypes = [pp, i64p, pp, vp, vp, vp, vp, pp, i64, i64, c_int, vp,
+                                         vp]
+    lib.indexed_all_to_all_v.restype = c_int
     lib.bra_status_str.argtypes = [c_int]
     lib.bra_status_str.restype = ctypes.c_char_p
     lib.bra_l2_flush.argtypes = [vp, ctypes.c_size_t, vp]
@@ -312,6 +315,37 @@ def all_to_all_v_checked(inputs: Sequence, send_counts, out: Sequence, core_num:
         rc.data_ptr(), rd.data_ptr(), _ptr_array([t.data_ptr() for t in out]), P,
         int(core_num), code, cap, status.data_ptr(), _stream_handle(stream)),
         "all_to_all_v_checked")
+    return {"out": out, "send_displs": sd, "recv_counts": rc, "recv_displs": rd,
+            "status": status}
+
+
+def indexed_all_to_all_v(inputs: Sequence, index: Sequence, send_counts, out: Sequence,
+                         core_num: int, status=None, send_displs=None, recv_counts=None,
+                         recv_displs=None, stream=None) -> dict:
+    """Indexed exchange (see the C header): rank i sends inputs[i][index[i][k]]
+    in the order of its send list, split by send_counts as in all_to_all_v.
+
+    index[i]: CUDA int64 with at least sum_j send_counts[i][j] entries.
+    status: optional CUDA int32 (1 element) set to 0, or ERR_INVALID when an
+    index was out of range or the call was rejected on the device.
+    Returns {'out', 'send_displs', 'recv_counts', 'recv_displs', 'status'}.
+    """
+    torch = _torch()
+    P, code, sd, rc, rd = _a2av_args(inputs, send_counts, out, send_displs, recv_counts,
+                                     recv_displs)
+    if len(index) != P:
+        raise ValueError(f"index has {len(index)} entries for {P} ranks")
+    for t in index:
+        _dev_tensor(t, "index", torch.int64)
+    lens = (ctypes.c_int64 * P)(*[t.numel() for t in inputs])
+    if status is not None:
+        _dev_tensor(status, "status", torch.int32)
+    _check(library().indexed_all_to_all_v(
+        _ptr_array([t.data_ptr() for t in inputs]), lens,
+        _ptr_array([t.data_ptr() for t in index]), send_counts.data_ptr(), sd.data_ptr(),
+        rc.data_ptr(), rd.data_ptr(), _ptr_array([t.data_ptr() for t in out]), P,
+        int(core_num), code, None if status is None else status.data_ptr(),
+        _stream_handle(stream)), "indexed_all_to_all_v")
     return {"out": out, "send_displs": sd, "recv_counts": rc, "recv_displs": rd,
             "status": status}
 

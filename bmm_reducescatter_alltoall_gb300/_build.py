@@ -63,6 +63,7 @@ KERNEL_SOURCES = {
     "l2_flush_kernel": "l2_flush.cu",
     "fused_simt_kernel": "fused_simt.cu",
     "a2av_kernel": "a2av.cu",
+    "ia2av_kernel": "ia2av.cu",
 }
 
 

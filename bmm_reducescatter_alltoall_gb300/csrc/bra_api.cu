@@ -207,9 +207,71 @@ int a2av_common(const void* const input[], const int64_t* send_counts,
   return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
 }
 
+int ia2av_common(const void* const input[], const int64_t in_len[],
+                 const int64_t* const index[], const int64_t* send_counts,
+                 int64_t* send_displs, int64_t* recv_counts, int64_t* recv_displs,
+                 void* const out[], int64_t P, int64_t core_num, int dtype,
+                 int32_t* status_dev, cudaStream_t stream) {
+  if (!input || !in_len || !index || !send_counts || !send_displs || !recv_counts ||
+      !recv_displs || !out)
+    return BRA_ERR_NULLPTR;
+  if (P < 1) return BRA_ERR_INVALID;
+  if (core_num < 1 || core_num > kInt32Max) return BRA_ERR_INVALID;
+  if (dtype != BRA_FP32 && dtype != BRA_INT8) return BRA_ERR_INVALID;
+  if (P > bra::kA2avMaxP) return BRA_ERR_UNSUPPORTED;
+  for (int64_t i = 0; i < P; ++i) {
+    if (in_len[i] < 0) return BRA_ERR_INVALID;
+    if (in_len[i] > 0 && !input[i]) return BRA_ERR_NULLPTR;
+  }
+  // An output may alias no input, no index array and no other output.
+  for (int64_t j = 0; j < P; ++j) {
+    if (!out[j]) continue;
+    for (int64_t i = 0; i < P; ++i)
+      if (out[j] == input[i] || out[j] == static_cast<const void*>(index[i]))
+        return BRA_ERR_INVALID;
+    for (int64_t k = 0; k < j; ++k)
+      if (out[j] == out[k]) return BRA_ERR_INVALID;
+  }
+  const int64_t B = cal_all_to_all_v_blocks(P, core_num);
+  if (B < 1 || B * P > kInt32Max) return BRA_ERR_INVALID;
+
+  bra::IA2avArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int64_t r = 0; r < P; ++r) {
+    a.in[r] = input[r];
+    a.idx[r] = index[r];
+    a.in_len[r] = in_len[r];
+    a.out[r] = out[r];
+  }
+  a.sc = send_counts;
+  a.sd = send_displs;
+  a.rc = recv_counts;
+  a.rd = recv_displs;
+  a.status = status_dev;
+  a.P = (int)P;
+  a.esize = dtype == BRA_FP32 ? 4 : 1;
+  const int ctas = bra::ia2av_ctas_per_rank((int)P);
+  if (log_enabled())
+    std::fprintf(stderr, "[bra] indexed_all_to_all_v P=%lld L=%lld B=%lld grid=(%d,%lld)\n",
+                 (long long)P, (long long)core_num, (long long)B, ctas, (long long)P);
+  cudaError_t e = cudaSuccess;
+  if (status_dev) e = cudaMemsetAsync(status_dev, 0, sizeof(int32_t), stream);
+  if (e == cudaSuccess) e = bra::launch_ia2av(a, ctas, stream);
+  return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
+
+int indexed_all_to_all_v(const void* const input[], const int64_t in_len[],
+                         const int64_t* const index[], const int64_t* send_counts,
+                         int64_t* send_displs, int64_t* recv_counts, int64_t* recv_displs,
+                         void* const out[], int64_t P, int64_t core_num, int dtype,
+                         int32_t* status_dev, bra_stream_t stream) {
+  return ia2av_common(input, in_len, index, send_counts, send_displs, recv_counts, recv_displs,
+                      out, P, core_num, dtype, status_dev, (cudaStream_t)stream);
+}
 
 int bmm_rs_a2a_ex(const void* const x[], const void* const weight[],
                   const void* const bias[], int64_t ep, int64_t tp, int64_t E,

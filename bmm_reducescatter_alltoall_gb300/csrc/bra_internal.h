@@ -34,6 +34,23 @@ struct A2avArgs {
 
 // Launch the exchange with `ctas_per_rank` CTAs per source rank.
 cudaError_t launch_a2av(const A2avArgs& a, int ctas_per_rank, cudaStream_t st);
+
+// Indexed exchange: rank i's send list is input[i] gathered through idx[i].
+struct IA2avArgs {
+  const void* in[kA2avMaxP];
+  const int64_t* idx[kA2avMaxP];
+  int64_t in_len[kA2avMaxP];  // elements of in[i]; index values must lie below
+  void* out[kA2avMaxP];
+  const int64_t* sc;          // send_counts [P][P]
+  int64_t* sd;                // send_displs [P][P]
+  int64_t* rc;                // recv_counts [P][P]
+  int64_t* rd;                // recv_displs [P][P]
+  int32_t* status;            // optional device status word
+  int P;
+  int esize;                  // element size in bytes (4 or 1)
+};
+cudaError_t launch_ia2av(const IA2avArgs& a, int ctas_per_rank, cudaStream_t st);
+int ia2av_ctas_per_rank(int P);
 // CTAs per rank that fill the GPU once.
 int a2av_ctas_per_rank(int P);
 

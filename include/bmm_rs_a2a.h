@@ -267,6 +267,50 @@ BRA_API int all_to_all_v_checked(const void* const input[], const int64_t* send_
                          const int64_t* out_capacity, int32_t* status_dev,
                          bra_stream_t stream);
 
+/*
+ * indexed_all_to_all_v -- the URMA indexed exchange ([PTO] §A5 URMA
+ * 索引交换).  The page names the operands and says the cores share the local
+ * data movement before the remote transfers, but does not define `index`;
+ * the reading implemented: rank i's send list is its input gathered through
+ * its index, and the send lists are exchanged as in all_to_all_v:
+ *   n_i = sum_j send_counts[i][j]
+ *   send_i[k] = input[i][index[i][k]],                        0 <= k < n_i
+ *   out[j][recv_displs[j][i] + m] = send_i[send_displs[i][j] + m],
+ *       0 <= m < send_counts[i][j]
+ * with send_displs, recv_counts, recv_displs as in all_to_all_v (written by
+ * the kernel).  Elements of out[j] past its received total are not written.
+ *
+ * Arguments:
+ *   input[P]     device; input[i] holds in_len[i] elements of `dtype` (may be
+ *                NULL when in_len[i] is 0).
+ *   in_len[P]    host; element counts of the inputs (copied at the call).
+ *   index[P]     device int64; index[i] holds at least n_i entries (may be
+ *                NULL when n_i is 0).
+ *   send_counts, send_displs, recv_counts, recv_displs, out, P, core_num,
+ *   dtype        as for all_to_all_v.
+ *   status_dev   optional device int32: set to BRA_OK on the stream before
+ *                the kernel, then to BRA_ERR_INVALID if the call was rejected
+ *                on the device or an index value was out of range.
+ * Errors (nothing launched):
+ *   BRA_ERR_NULLPTR  input, in_len, index, out, send_counts or a bookkeeping
+ *                    array is NULL; input[i] NULL with in_len[i] > 0.
+ *   BRA_ERR_INVALID  P < 1; core_num outside [1, INT32_MAX]; dtype not
+ *                    FP32/INT8; in_len[i] < 0; an out[j] equal to an input,
+ *                    an index array or another output; B*P > INT32_MAX.
+ *   BRA_ERR_UNSUPPORTED  P > 64.
+ *   BRA_ERR_CUDA     the launch failed.
+ * Device-side data checks: a negative send count, or a NULL index[i] /
+ * out[j] that would be used, rejects the call (nothing written at all).  An
+ * index value outside [0, in_len[i]) is never dereferenced: that position is
+ * not delivered (its destination keeps its value) and the rest is.
+ */
+BRA_API int indexed_all_to_all_v(const void* const input[], const int64_t in_len[],
+                         const int64_t* const index[], const int64_t* send_counts,
+                         int64_t* send_displs, int64_t* recv_counts,
+                         int64_t* recv_displs, void* const out[], int64_t P,
+                         int64_t core_num, int dtype, int32_t* status_dev,
+                         bra_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Utilities                                                                 */
 /* ------------------------------------------------------------------------ */

@@ -339,6 +339,46 @@ def test_a2av_rejections(lib, checked):
         assert _a2av(lib, status=None, **kw) == NULLPTR
 
 
+def _ia2av(lib, P=4, L=4, dtype=bra.INT8, ins=None, lens=None, idx=None, outs=None,
+           sc=1 << 30, sd=2 << 30, rc=3 << 30, rd=4 << 30, status=None):
+    ins = [(10 + k) << 32 for k in range(P)] if ins is None else ins
+    idx = [(20 + k) << 32 for k in range(P)] if idx is None else idx
+    outs = [(100 + k) << 32 for k in range(P)] if outs is None else outs
+    lens = [16] * max(P, 1) if lens is None else lens
+    ip = bra._ptr_array(ins) if ins != "null" else None
+    xp = bra._ptr_array(idx) if idx != "null" else None
+    op = bra._ptr_array(outs) if outs != "null" else None
+    lp = (ctypes.c_int64 * len(lens))(*lens) if lens != "null" else None
+    return lib.indexed_all_to_all_v(ip, lp, xp, sc, sd, rc, rd, op, P, L, dtype, status, None)
+
+
+def test_indexed_a2av_rejections(lib):
+    """Every rejection of the indexed exchange happens on the host, before any
+    launch."""
+    assert _ia2av(lib, P=0) == INVALID
+    assert _ia2av(lib, L=0) == INVALID
+    assert _ia2av(lib, L=2**31) == INVALID
+    for dt in (bra.FP16, bra.BF16, 9):
+        assert _ia2av(lib, dtype=dt) == INVALID
+    for key in ("ins", "idx", "outs", "lens"):
+        assert _ia2av(lib, **{key: "null"}) == NULLPTR
+    for key in ("sc", "sd", "rc", "rd"):
+        assert _ia2av(lib, **{key: None}) == NULLPTR
+    assert _ia2av(lib, lens=[16, -1, 16, 16]) == INVALID
+    assert _ia2av(lib, ins=[1 << 32, 0, 3 << 32, 4 << 32]) == NULLPTR   # in_len 16, NULL input
+    ins = [(10 + k) << 32 for k in range(4)]
+    idx = [(20 + k) << 32 for k in range(4)]
+    assert _ia2av(lib, outs=[5 << 40, ins[2], 6 << 40, 7 << 40]) == INVALID
+    assert _ia2av(lib, outs=[5 << 40, 6 << 40, idx[3], 7 << 40]) == INVALID
+    assert _ia2av(lib, outs=[5 << 40, 6 << 40, 5 << 40, 7 << 40]) == INVALID
+    assert _ia2av(lib, P=65, L=65, lens=[1] * 65) == UNSUPPORTED
+    assert _ia2av(lib, P=64, L=2**31 - 1, lens=[1] * 64) == INVALID
+    # a NULL input is fine when it holds no element: the call gets as far as
+    # the aliasing rule
+    assert _ia2av(lib, ins=[0] * 4, lens=[0] * 4,
+                  outs=[5 << 40, 6 << 40, 5 << 40, 7 << 40]) == INVALID
+
+
 def test_binding_rejects_host_tensors():
     import torch
     x = [torch.zeros(1, 8, 8, dtype=torch.float16) for _ in range(4)]

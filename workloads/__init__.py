@@ -31,7 +31,7 @@ from typing import List, Optional
 import numpy as np
 
 __all__ = [
-    "FusedConfig", "A2AVConfig", "FUSED_CONFIGS", "A2AV_CONFIGS",
+    "FusedConfig", "A2AVConfig", "FUSED_CONFIGS", "A2AV_CONFIGS", "a2av_index",
     "fused_shapes", "fused_inputs_host", "fused_inputs_device",
     "a2av_counts", "a2av_inputs",
 ]
@@ -229,3 +229,25 @@ def a2av_inputs(cfg: A2AVConfig, extra: int = 0):
         else:
             raise ValueError(cfg.dtype)
     return counts, inputs
+
+
+def a2av_index(counts: np.ndarray, in_lens, kind: str = "perm", seed: int = 0):
+    """Index arrays for the indexed exchange: index[i] has one int64 entry per
+    element rank i sends (its row total).  kind "perm": a permutation of
+    rank i's input positions (needs in_lens[i] == the row total); "random":
+    uniform positions in [0, in_lens[i]), repeats allowed; "identity": 0, 1, ..."""
+    out = []
+    for i in range(len(in_lens)):
+        n = int(np.asarray(counts)[i].sum())
+        rng = np.random.default_rng([seed, i])
+        if kind == "perm":
+            assert int(in_lens[i]) == n
+            out.append(rng.permutation(n).astype(np.int64))
+        elif kind == "random":
+            out.append(rng.integers(0, max(int(in_lens[i]), 1), size=n, dtype=np.int64))
+        elif kind == "identity":
+            out.append(np.arange(n, dtype=np.int64))
+        else:
+            raise ValueError(kind)
+    return out
+

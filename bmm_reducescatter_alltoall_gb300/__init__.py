@@ -1,5 +1,5 @@
-"""GB300-native fused MoE BMM -> TP ReduceScatter -> bias Add -> EP AllToAll
-and all_to_all_v over virtual ranks on one GPU.
+"""GB300-native fused MoE BMM -> TP ReduceScatter -> bias Add -> EP AllToAll,
+all_to_all_v and its indexed form over virtual ranks on one GPU.
 
 Thin Python binding over libbmmrsa2a.so (the C ABI in include/bmm_rs_a2a.h):
 it checks tensors (device, dtype, contiguity), passes their data pointers and

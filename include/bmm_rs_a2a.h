@@ -1,8 +1,9 @@
 /*
  * bmm_rs_a2a.h -- C ABI of libbmmrsa2a.so: the MoE expert-parallel x
  * tensor-parallel dataflow BatchMatMul -> TP ReduceScatter -> bias Add -> EP
- * AllToAll, and the variable-count all_to_all_v exchange, with all ep*tp ranks
- * resident on one GPU as virtual ranks (one buffer partition per rank).
+ * AllToAll, the variable-count all_to_all_v exchange and its indexed form,
+ * with all ep*tp ranks resident on one GPU as virtual ranks (one buffer
+ * partition per rank).
  *
  * Pages cited (by title and section):
  *   [CANN] "CANN ops-transformer 通算融合算子实战 BatchMatMulReduceScatterAllToAll

@@ -108,11 +108,14 @@ def test_identity_index_equals_all_to_all_v():
     np.testing.assert_array_equal(book[2], plain["recv_displs"].cpu().numpy())
 
 
-def test_full_size_workload_permutation():
-    cfg = A2AV_CONFIGS["P32_L64_int8_dirichlet0.3"]
-    sc, inputs = a2av_inputs(cfg)
-    index = a2av_index(sc, [len(a) for a in inputs], "perm", seed=5)
-    _check_against_oracle(sc, inputs, index, "int8", L=cfg.L, guard=64)
+@pytest.mark.parametrize("name,kind", [("P32_L64_int8_dirichlet0.3", "perm"),
+                                       ("P8_L10_fp32_uniform4096", "perm"),
+                                       ("P8_L10_fp32_uniform4096", "random")])
+def test_full_size_workloads(name, kind):
+    cfg = A2AV_CONFIGS[name]
+    sc, inputs = a2av_inputs(cfg, extra=0 if kind == "perm" else 1000)
+    index = a2av_index(sc, [len(a) for a in inputs], kind, seed=5)
+    _check_against_oracle(sc, inputs, index, cfg.dtype, L=cfg.L, guard=64)
 
 
 @pytest.mark.parametrize("in_off,out_off", [(1, 3), (3, 1), (2, 2)])

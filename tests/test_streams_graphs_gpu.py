@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import bmm_reducescatter_alltoall_gb300 as bra
-from workloads import A2AV_CONFIGS, FusedConfig, a2av_inputs, fused_inputs_host
+from workloads import A2AV_CONFIGS, FusedConfig, a2av_index, a2av_inputs, fused_inputs_host
 
 pytestmark = pytest.mark.gpu
 
@@ -39,6 +39,17 @@ def _a2av_case():
     return cfg, ins, scd, mk
 
 
+def _indexed_case():
+    cfg = A2AV_CONFIGS["P8_L10_fp32_uniform4096"]
+    sc, inputs = a2av_inputs(cfg, extra=100)
+    idx = [torch.from_numpy(x).cuda()
+           for x in a2av_index(sc, [len(a) for a in inputs], "random", seed=2)]
+    ins = [torch.from_numpy(a).cuda() for a in inputs]
+    scd = torch.from_numpy(sc).cuda()
+    mk = lambda: [torch.zeros(int(c), dtype=torch.float32, device="cuda") for c in sc.sum(axis=0)]
+    return cfg, ins, idx, scd, mk
+
+
 def _same_bits(a, b):
     return all(torch.equal(x.view(torch.int16) if x.dtype != torch.float32 else x.view(torch.int32),
                            y.view(torch.int16) if y.dtype != torch.float32 else y.view(torch.int32))
@@ -52,23 +63,26 @@ def test_concurrent_calls_on_three_streams():
     assert bra.bmm_rs_a2a_variant(d3["x"], d3["w"], d3["bias"], c3.ep, c3.tp, c3.E, c3.C, c3.M,
                                   c3.H, 1, mk3()) == bra.VARIANT_TCR
     ca, ins, scd, mka = _a2av_case()
-    ref1, ref2, ref3, refa = mk1(), mk2(), mk3(), mka()
+    ci, iins, iidx, iscd, mki = _indexed_case()
+    ref1, ref2, ref3, refa, refi = mk1(), mk2(), mk3(), mka(), mki()
     _call(c1, d1, ref1)
     _call(c2, d2, ref2)
     _call(c3, d3, ref3)
     bra.all_to_all_v(ins, scd, refa, ca.L)
+    bra.indexed_all_to_all_v(iins, iidx, iscd, refi, ci.L)
     torch.cuda.synchronize()
     s1, s2, s3 = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     for _ in range(3):
-        o1, o2, o3, oa = mk1(), mk2(), mk3(), mka()
+        o1, o2, o3, oa, oi = mk1(), mk2(), mk3(), mka(), mki()
         torch.cuda.synchronize()
         _call(c1, d1, o1, stream=s1)
         _call(c2, d2, o2, stream=s2)
         _call(c3, d3, o3, stream=s3)
         bra.all_to_all_v(ins, scd, oa, ca.L, stream=s2)
+        bra.indexed_all_to_all_v(iins, iidx, iscd, oi, ci.L, stream=s1)
         torch.cuda.synchronize()
         assert _same_bits(o1, ref1) and _same_bits(o2, ref2) and _same_bits(o3, ref3)
-        assert _same_bits(oa, refa)
+        assert _same_bits(oa, refa) and _same_bits(oi, refi)
     assert bra.fault_status() == 0
 
 
@@ -76,31 +90,36 @@ def test_step_captured_in_a_cuda_graph():
     c1, d1, mk1 = _fused_case(3, t=1, dt="fp16")
     c3, d3, mk3 = _fused_case(5, t=0, dt="fp16", M=514, H=774)   # row-class kernel
     ca, ins, scd, mka = _a2av_case()
-    ref1, ref3, refa = mk1(), mk3(), mka()
+    ci, iins, iidx, iscd, mki = _indexed_case()
+    ref1, ref3, refa, refi = mk1(), mk3(), mka(), mki()
     _call(c1, d1, ref1)
     _call(c3, d3, ref3)
     bra.all_to_all_v(ins, scd, refa, ca.L)
+    bra.indexed_all_to_all_v(iins, iidx, iscd, refi, ci.L)
     torch.cuda.synchronize()
-    o1, o3, oa = mk1(), mk3(), mka()
+    o1, o3, oa, oi = mk1(), mk3(), mka(), mki()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):          # warm the library's per-device set-up
         _call(c1, d1, o1)
         _call(c3, d3, o3)
         bra.all_to_all_v(ins, scd, oa, ca.L)
+        bra.indexed_all_to_all_v(iins, iidx, iscd, oi, ci.L)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    for t_ in o1 + o3 + oa:
+    for t_ in o1 + o3 + oa + oi:
         t_.zero_()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         _call(c1, d1, o1)
         _call(c3, d3, o3)
         bra.all_to_all_v(ins, scd, oa, ca.L)
+        bra.indexed_all_to_all_v(iins, iidx, iscd, oi, ci.L)
     for _ in range(2):
-        for t_ in o1 + o3 + oa:
+        for t_ in o1 + o3 + oa + oi:
             t_.zero_()
         g.replay()
         torch.cuda.synchronize()
         assert _same_bits(o1, ref1) and _same_bits(o3, ref3) and _same_bits(oa, refa)
+        assert _same_bits(oi, refi)
     assert bra.fault_status() == 0

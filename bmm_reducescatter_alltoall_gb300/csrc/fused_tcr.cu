@@ -29,15 +29,23 @@
 //                       accumulators per CTA); in the leader its lane 0
 //                       issues the pair MMAs (M=256, N=256, K=16) and
 //                       commits to both CTAs.
-//   warps 2..2+RWARPS-1 realign: copy each raw row into the 128-byte-swizzle
-//                       layout a TMA box would have produced, shifted by the
-//                       class's delta (a compile-time shift picked per warp:
-//                       the four rows a warp moves at once share a class),
-//                       zero the weight's K rows past Kp, publish with
-//                       fence.proxy.async and an arrival on the leader's
-//                       sw_full barrier (SW_STAGES-deep canonical ring).
-//                       Eight lanes move one row's 128 bytes, so reads and
-//                       writes are free of bank conflicts.
+//   warps 2..           realign (RGROUPS groups of RWARPS warps, taking K
+//                       blocks in turn): shift each raw row into the
+//                       128-byte-swizzle layout a TMA box would have produced,
+//                       by the class's delta (a compile-time shift picked per
+//                       batch: the rows a warp moves at once share a class),
+//                       and zero the weight's K rows past Kp.  A warp frees
+//                       the raw stage once its rows are in registers, waits
+//                       for the canonical slot (SW_STAGES-deep ring), stores,
+//                       and runs fence.proxy.async; the group then meets at a
+//                       named barrier and publishes the stage: the leader's
+//                       group on its own sw_full, the peer's group on a local
+//                       `ready` barrier.  Eight lanes move one row's 128
+//                       bytes, so reads and writes are free of bank conflicts.
+//   warps SIG_WARP0..   in the peer CTA, signal warps take stages in turn: on
+//                       `ready`, one release arrive at cluster scope on the
+//                       leader's sw_full (such an arrive takes ~2k cycles, so
+//                       several are kept in flight, off the realign path).
 //   warps EPI_WARP0..+3 epilogue of the CTA's 128 accumulator rows.
 // Every wait is bounded (about 4 s); a wait that runs out records
 // BRA_ERR_TIMEOUT in a device word and every role leaves its loop; both CTAs

@@ -358,16 +358,17 @@ def l2_flush(buf, stream=None) -> None:
                                   _stream_handle(stream)), "bra_l2_flush")
 
 
-WAIT_A2AV, WAIT_TC = 0, 1
+WAIT_A2AV, WAIT_TC, WAIT_TC_CLUSTER = 0, 1, 2
 
 
 def wait_selftest(which: str, status, stream=None) -> None:
     """Run one bounded wait that nothing completes with the wait helper of the
-    all_to_all_v kernel (which='a2av', ~2 s) or of the tensor-core fused
-    kernels (which='tc', ~4 s).  `status` (CUDA int32, 1 element) receives
+    all_to_all_v kernel (which='a2av', ~2 s), of the tensor-core fused
+    kernels (which='tc', ~4 s) or the cluster-scope one of the row-class
+    kernel (which='tc_cluster', ~4 s).  `status` (CUDA int32, 1 element) receives
     ERR_TIMEOUT and the watchdog word read by fault_status() is set."""
     torch = _torch()
-    code = {"a2av": WAIT_A2AV, "tc": WAIT_TC}[which]
+    code = {"a2av": WAIT_A2AV, "tc": WAIT_TC, "tc_cluster": WAIT_TC_CLUSTER}[which]
     _dev_tensor(status, "status", torch.int32)
     _check(library().bra_wait_selftest(code, status.data_ptr(), _stream_handle(stream)),
            "bra_wait_selftest")

@@ -408,6 +408,8 @@ int bra_wait_selftest(int which, int32_t* status_dev, bra_stream_t stream) {
     e = bra::launch_a2av_wait_probe(status_dev, (cudaStream_t)stream);
   else if (which == BRA_WAIT_TC)
     e = bra::launch_tc_wait_probe(status_dev, (cudaStream_t)stream);
+  else if (which == BRA_WAIT_TC_CLUSTER)
+    e = bra::launch_tcr_wait_probe(status_dev, (cudaStream_t)stream);
   else
     return BRA_ERR_INVALID;
   return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;

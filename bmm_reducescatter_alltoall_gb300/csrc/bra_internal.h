@@ -89,5 +89,6 @@ cudaError_t read_a2av_fault_word(int32_t* code, int clear);   // all_to_all_v ke
 // One bounded wait that nothing completes, with each family's wait helper.
 cudaError_t launch_a2av_wait_probe(int32_t* status, cudaStream_t st);
 cudaError_t launch_tc_wait_probe(int32_t* status, cudaStream_t st);
+cudaError_t launch_tcr_wait_probe(int32_t* status, cudaStream_t st);   // cluster-scope wait
 
 }  // namespace bra

@@ -760,6 +760,32 @@ cudaError_t launch_fused_tcr(const FusedProblem& f, cudaStream_t st) {
   return cudaSuccess;
 }
 
+namespace {
+// Diagnostic: one bounded cluster-scope wait (the helper of this kernel's MMA
+// issuer, which waits for both CTAs' stages) on a barrier nothing arrives
+// at; it runs out, records BRA_ERR_TIMEOUT in this file's fault word and
+// returns; *status gets the outcome.
+__global__ void tcr_wait_probe_kernel(int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool done = mbar_wait_cluster(smem_u32(&bar), 0, &abort_flag, &g_bra_fault_word4);
+    *status = done ? BRA_OK : BRA_ERR_TIMEOUT;
+  }
+}
+}  // namespace
+
+cudaError_t launch_tcr_wait_probe(int32_t* status, cudaStream_t st) {
+  tcr_wait_probe_kernel<<<1, 32, 0, st>>>(status);
+  return cudaGetLastError();
+}
+
 cudaError_t read_fault_word4(int32_t* code, int clear) {
   cudaError_t e = cudaMemcpyFromSymbol(code, g_bra_fault_word4, sizeof(int32_t));
   if (e != cudaSuccess) return e;

@@ -346,8 +346,10 @@ BRA_API int bra_fault_status(int32_t* code, int clear);
  * bra_wait_selftest -- failure-detection check: launches one kernel whose
  * single bounded wait waits on an mbarrier phase that nothing completes,
  * using the wait helper of the all_to_all_v kernel (which =
- * BRA_WAIT_A2AV, gives up after about 2 s) or of the tensor-core fused
- * kernels (BRA_WAIT_TC, about 4 s).  The wait runs out, the kernel writes
+ * BRA_WAIT_A2AV, gives up after about 2 s), of the tensor-core fused
+ * kernels (BRA_WAIT_TC, about 4 s) or the cluster-scope one of the row-class
+ * kernel's MMA issuer (BRA_WAIT_TC_CLUSTER, about 4 s).  The wait runs out,
+ * the kernel writes
  * BRA_ERR_TIMEOUT to *status_dev (device int32, BRA_OK had the phase
  * completed), records BRA_ERR_TIMEOUT in the watchdog word that
  * bra_fault_status reads, and returns; nothing traps and the context stays
@@ -355,7 +357,7 @@ BRA_API int bra_fault_status(int32_t* code, int clear);
  * Returns BRA_ERR_NULLPTR, BRA_ERR_INVALID (unknown `which`), BRA_ERR_CUDA
  * or BRA_OK.
  */
-enum { BRA_WAIT_A2AV = 0, BRA_WAIT_TC = 1 };
+enum { BRA_WAIT_A2AV = 0, BRA_WAIT_TC = 1, BRA_WAIT_TC_CLUSTER = 2 };
 BRA_API int bra_wait_selftest(int which, int32_t* status_dev, bra_stream_t stream);
 
 /* Library version, "major.minor.patch". */

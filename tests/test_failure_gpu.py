@@ -1,8 +1,9 @@
 """Failure detection on the GPU without a fault: a bounded wait runs out.
 
-Each kernel family's wait helper (the one every mbarrier wait of
-all_to_all_v, or of the tensor-core fused kernels, goes through) is run on a
-barrier phase that nothing completes.  The wait gives up after its limit
+Each wait helper (the one every mbarrier wait of all_to_all_v, of the
+tensor-core fused kernels, or the cluster-scope wait of the row-class
+kernel's MMA issuer goes through) is run on a barrier phase that nothing
+completes.  The wait gives up after its limit
 (about 2 s / 4 s), the kernel reports BRA_ERR_TIMEOUT in its status word and
 in the watchdog word the host reads, and returns; nothing traps, and the
 context stays usable, which the exact exchange run afterwards checks.
@@ -30,7 +31,7 @@ def _exchange_is_exact():
                for o, r in zip(outs, ref["out"]))
 
 
-@pytest.mark.parametrize("which", ["a2av", "tc"])
+@pytest.mark.parametrize("which", ["a2av", "tc", "tc_cluster"])
 def test_bounded_wait_runs_out_and_reports(which):
     bra.fault_status(clear=True)
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")

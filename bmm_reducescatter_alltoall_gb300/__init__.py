@@ -11,6 +11,7 @@ calling into a missing library raises `RuntimeError`.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 from typing import List, Optional, Sequence
 
@@ -18,7 +19,8 @@ __all__ = [
     "BraError", "FP16", "BF16", "FP32", "INT8", "VARIANT_TC", "VARIANT_TC2", "VARIANT_SIMT",
     "VARIANT_TCU", "VARIANT_TCR", "wait_selftest", "indexed_all_to_all_v",
     "FusedOptions", "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
-    "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked",
+    "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked", "Plan", "bmm_rs_a2a_plan",
+    "all_to_all_v_plan", "indexed_all_to_all_v_plan",
     "cal_all_to_all_v_blocks", "l2_flush", "fault_status", "status_str", "version",
 ]
 
@@ -109,10 +111,9 @@ def _torch():
 
 
 def _ptr_array(ptrs: Sequence[Optional[int]]):
-    arr = (ctypes.c_void_p * max(1, len(ptrs)))()
-    for k, p in enumerate(ptrs):
-        arr[k] = p if p else None
-    return arr
+    if not ptrs:
+        return (ctypes.c_void_p * 1)()
+    return (ctypes.c_void_p * len(ptrs))(*[p if p else None for p in ptrs])
 
 
 def _stream_handle(stream) -> Optional[int]:
@@ -135,6 +136,23 @@ def _dev_tensor(t, what: str, dtype=None):
     return t
 
 
+def _checked_ptrs(ts, what: str, dtype, shape=None):
+    """Data pointers of the CUDA tensors `ts`, after one pass that checks
+    device, dtype, contiguity and (when given) shape of each; only when that
+    pass fails is the failing entry looked up for the error message."""
+    try:
+        ok = all(t.is_cuda and t.dtype is dtype and t.is_contiguous() and
+                 (shape is None or t.shape == shape) for t in ts)
+    except AttributeError:
+        ok = False
+    if not ok:
+        for r, t in enumerate(ts):
+            _dev_tensor(t, f"{what}[{r}]", dtype)
+            if shape is not None:
+                _shape_check(t, shape, f"{what}[{r}]")
+    return [t.data_ptr() for t in ts]
+
+
 def _fused_dtype(dt) -> int:
     torch = _torch()
     if dt == torch.float16:
@@ -144,12 +162,19 @@ def _fused_dtype(dt) -> int:
     raise TypeError(f"fused op takes float16 or bfloat16, got {dt}")
 
 
-def bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type) -> dict:
-    """Per-rank shapes: {'x','w','bias','y'} as tuples (bias in 3-D form)."""
+@functools.lru_cache(maxsize=256)
+def _infer_shape(ep, tp, E, C, M, H, y_shard_type) -> tuple:
     arrs = [(ctypes.c_int64 * 3)() for _ in range(4)]
     _check(library().bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type, *arrs),
            "bmm_rs_a2a_infer_shape")
-    return {k: tuple(a) for k, a in zip(("x", "w", "bias", "y"), arrs)}
+    return tuple(tuple(a) for a in arrs)
+
+
+def bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type) -> dict:
+    """Per-rank shapes: {'x','w','bias','y'} as tuples (bias in 3-D form)."""
+    return dict(zip(("x", "w", "bias", "y"),
+                    _infer_shape(int(ep), int(tp), int(E), int(C), int(M), int(H),
+                                 int(y_shard_type))))
 
 
 def _shape_check(t, want, what):
@@ -180,9 +205,8 @@ def _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
     if transpose_weight:                      # stored as (El, H, Kp)
         wshape = (wshape[0], wshape[2], wshape[1])
     dt = x[0].dtype
-    for r in range(P):
-        _shape_check(_dev_tensor(x[r], f"x[{r}]", dt), shapes["x"], f"x[{r}]")
-        _shape_check(_dev_tensor(weight[r], f"weight[{r}]", dt), wshape, f"weight[{r}]")
+    xs = _checked_ptrs(x, "x", dt, shapes["x"])
+    ws = _checked_ptrs(weight, "weight", dt, wshape)
     bptr = None
     if bias is not None:
         if len(bias) != P:
@@ -190,23 +214,64 @@ def _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
         torch = _torch()
         bdt = torch.float16 if dt == torch.float16 else torch.float32
         b3 = shapes["bias"]
+        b2 = (b3[0], b3[2])
         ptrs = []
         for r, b in enumerate(bias):
             if b is None:
                 ptrs.append(0)
                 continue
-            _dev_tensor(b, f"bias[{r}]", bdt)
-            if tuple(b.shape) not in (tuple(b3), (b3[0], b3[2])):
+            if not (b.is_cuda and b.dtype is bdt and b.is_contiguous() and
+                    (b.shape == b3 or b.shape == b2)):
+                _dev_tensor(b, f"bias[{r}]", bdt)
                 raise ValueError(f"bias[{r}] has shape {tuple(b.shape)}, expected {b3} "
-                                 f"or {(b3[0], b3[2])}")
+                                 f"or {b2}")
             ptrs.append(b.data_ptr())
         bptr = _ptr_array(ptrs)
     if len(out) != P:
         raise ValueError(f"out needs ep*tp = {P} entries")
-    for r in range(P):
-        _shape_check(_dev_tensor(out[r], f"out[{r}]", dt), shapes["y"], f"out[{r}]")
-    return (_ptr_array([t.data_ptr() for t in x]), _ptr_array([t.data_ptr() for t in weight]),
-            bptr, _ptr_array([t.data_ptr() for t in out]), _fused_dtype(dt))
+    ys = _checked_ptrs(out, "out", dt, shapes["y"])
+    return _ptr_array(xs), _ptr_array(ws), bptr, _ptr_array(ys), _fused_dtype(dt)
+
+
+class Plan:
+    """A library call prepared once.
+
+    The tensors were checked and their data pointers taken when the plan was
+    made; run() (or calling the plan) only calls the library, so repeated
+    calls on the same buffers skip the per-tensor checks of the one-shot
+    functions.  The plan keeps its tensors alive; they must keep their
+    storage between runs (no resize or reallocation), while their values may
+    change.  run() returns `result` (the outputs) and is asynchronous on
+    `stream` (default: the current stream).
+    """
+
+    def __init__(self, fn, args, name: str, result, keep):
+        self._fn, self._args, self._name = fn, args, name
+        self.result = result
+        self._keep = keep
+
+    def run(self, stream=None):
+        _check(self._fn(*self._args, _stream_handle(stream)), self._name)
+        return self.result
+
+    __call__ = run
+
+
+def bmm_rs_a2a_plan(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int, tp: int,
+                    E: int, C: int, M: int, H: int, y_shard_type: int,
+                    out: Optional[Sequence] = None, transpose_weight: bool = False,
+                    variant: Optional[str] = None) -> Plan:
+    """bmm_rs_a2a prepared once (see Plan); plan.run() returns out."""
+    torch = _torch()
+    if out is None:
+        ys = bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type)["y"]
+        out = [torch.empty(ys, dtype=x[0].dtype, device=x[0].device) for _ in range(ep * tp)]
+    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
+                                     transpose_weight)
+    opts = _options(transpose_weight, variant)
+    args = (xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp, ctypes.byref(opts))
+    return Plan(library().bmm_rs_a2a_ex, args, "bmm_rs_a2a", out,
+                (x, weight, bias, opts, xp, wp, bp, yp))
 
 
 def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int, tp: int,
@@ -219,18 +284,11 @@ def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
     the shapes `bmm_rs_a2a_infer_shape` gives; out is allocated when None.
     transpose_weight: weight[r] is stored as (El, H, Kp) instead of
     (El, Kp, H).  variant: None/"auto", "tc", "tc2", "tcr", "tcu" or "simt".
-    Returns out.  Asynchronous on `stream` (default: current stream).
+    Returns out.  Asynchronous on `stream` (default: current stream).  For
+    repeated calls on the same buffers, bmm_rs_a2a_plan skips the checks.
     """
-    torch = _torch()
-    if out is None:
-        ys = bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type)["y"]
-        out = [torch.empty(ys, dtype=x[0].dtype, device=x[0].device) for _ in range(ep * tp)]
-    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
-                                     transpose_weight)
-    opts = _options(transpose_weight, variant)
-    _check(library().bmm_rs_a2a_ex(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp,
-                                   ctypes.byref(opts), _stream_handle(stream)), "bmm_rs_a2a")
-    return out
+    return bmm_rs_a2a_plan(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
+                           transpose_weight, variant).run(stream)
 
 
 def bmm_rs_a2a_variant(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
@@ -262,9 +320,8 @@ def _a2av_args(inputs, send_counts, out, send_displs, recv_counts, recv_displs):
         code = INT8
     else:
         raise TypeError(f"all_to_all_v takes float32 or int8, got {dt}")
-    for r in range(P):
-        _dev_tensor(inputs[r], f"inputs[{r}]", dt)
-        _dev_tensor(out[r], f"out[{r}]", dt)
+    _checked_ptrs(inputs, "inputs", dt)
+    _checked_ptrs(out, "out", dt)
     _dev_tensor(send_counts, "send_counts", torch.int64)
     if tuple(send_counts.shape) != (P, P):
         raise ValueError(f"send_counts must be ({P}, {P})")
@@ -278,6 +335,20 @@ def _a2av_args(inputs, send_counts, out, send_displs, recv_counts, recv_displs):
     return P, code, sd, rc, rd
 
 
+def all_to_all_v_plan(inputs: Sequence, send_counts, out: Sequence, core_num: int,
+                      send_displs=None, recv_counts=None, recv_displs=None) -> Plan:
+    """all_to_all_v prepared once (see Plan); plan.run() returns the result dict."""
+    P, code, sd, rc, rd = _a2av_args(inputs, send_counts, out, send_displs, recv_counts,
+                                     recv_displs)
+    ip = _ptr_array([t.data_ptr() for t in inputs])
+    op = _ptr_array([t.data_ptr() for t in out])
+    args = (ip, send_counts.data_ptr(), sd.data_ptr(), rc.data_ptr(), rd.data_ptr(), op, P,
+            int(core_num), code)
+    result = {"out": out, "send_displs": sd, "recv_counts": rc, "recv_displs": rd}
+    return Plan(library().all_to_all_v, args, "all_to_all_v", result,
+                (inputs, send_counts, ip, op))
+
+
 def all_to_all_v(inputs: Sequence, send_counts, out: Sequence, core_num: int,
                  send_displs=None, recv_counts=None, recv_displs=None, stream=None) -> dict:
     """Variable-count exchange among P = len(inputs) ranks (see the C header).
@@ -285,13 +356,8 @@ def all_to_all_v(inputs: Sequence, send_counts, out: Sequence, core_num: int,
     send_counts: CUDA int64 (P, P).  out[j] must hold what rank j receives.
     Returns {'out', 'send_displs', 'recv_counts', 'recv_displs'}.
     """
-    P, code, sd, rc, rd = _a2av_args(inputs, send_counts, out, send_displs, recv_counts,
-                                     recv_displs)
-    _check(library().all_to_all_v(_ptr_array([t.data_ptr() for t in inputs]),
-                                  send_counts.data_ptr(), sd.data_ptr(), rc.data_ptr(),
-                                  rd.data_ptr(), _ptr_array([t.data_ptr() for t in out]), P,
-                                  int(core_num), code, _stream_handle(stream)), "all_to_all_v")
-    return {"out": out, "send_displs": sd, "recv_counts": rc, "recv_displs": rd}
+    return all_to_all_v_plan(inputs, send_counts, out, core_num, send_displs, recv_counts,
+                             recv_displs).run(stream)
 
 
 def all_to_all_v_checked(inputs: Sequence, send_counts, out: Sequence, core_num: int,
@@ -330,24 +396,33 @@ def indexed_all_to_all_v(inputs: Sequence, index: Sequence, send_counts, out: Se
     index was out of range or the call was rejected on the device.
     Returns {'out', 'send_displs', 'recv_counts', 'recv_displs', 'status'}.
     """
+    return indexed_all_to_all_v_plan(inputs, index, send_counts, out, core_num, status,
+                                     send_displs, recv_counts, recv_displs).run(stream)
+
+
+def indexed_all_to_all_v_plan(inputs: Sequence, index: Sequence, send_counts, out: Sequence,
+                              core_num: int, status=None, send_displs=None, recv_counts=None,
+                              recv_displs=None) -> Plan:
+    """indexed_all_to_all_v prepared once (see Plan); plan.run() returns the
+    result dict."""
     torch = _torch()
     P, code, sd, rc, rd = _a2av_args(inputs, send_counts, out, send_displs, recv_counts,
                                      recv_displs)
     if len(index) != P:
         raise ValueError(f"index has {len(index)} entries for {P} ranks")
-    for t in index:
-        _dev_tensor(t, "index", torch.int64)
+    iptrs = _checked_ptrs(index, "index", torch.int64)
     lens = (ctypes.c_int64 * P)(*[t.numel() for t in inputs])
     if status is not None:
         _dev_tensor(status, "status", torch.int32)
-    _check(library().indexed_all_to_all_v(
-        _ptr_array([t.data_ptr() for t in inputs]), lens,
-        _ptr_array([t.data_ptr() for t in index]), send_counts.data_ptr(), sd.data_ptr(),
-        rc.data_ptr(), rd.data_ptr(), _ptr_array([t.data_ptr() for t in out]), P,
-        int(core_num), code, None if status is None else status.data_ptr(),
-        _stream_handle(stream)), "indexed_all_to_all_v")
-    return {"out": out, "send_displs": sd, "recv_counts": rc, "recv_displs": rd,
-            "status": status}
+    ip = _ptr_array([t.data_ptr() for t in inputs])
+    xp = _ptr_array(iptrs)
+    op = _ptr_array([t.data_ptr() for t in out])
+    args = (ip, lens, xp, send_counts.data_ptr(), sd.data_ptr(), rc.data_ptr(), rd.data_ptr(),
+            op, P, int(core_num), code, None if status is None else status.data_ptr())
+    result = {"out": out, "send_displs": sd, "recv_counts": rc, "recv_displs": rd,
+              "status": status}
+    return Plan(library().indexed_all_to_all_v, args, "indexed_all_to_all_v", result,
+                (inputs, index, send_counts, status, ip, xp, op, lens))
 
 
 def l2_flush(buf, stream=None) -> None:

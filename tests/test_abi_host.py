@@ -387,6 +387,11 @@ def test_binding_rejects_host_tensors():
     with pytest.raises(ValueError):
         bra.all_to_all_v([torch.zeros(4)] * 2, torch.zeros(2, 2, dtype=torch.int64),
                          [torch.zeros(4)] * 2, 2)
+    with pytest.raises(ValueError):                  # plans check when they are made
+        bra.bmm_rs_a2a_plan(x, x, None, 2, 2, 2, 4, 16, 8, 0, out=x)
+    with pytest.raises(ValueError):
+        bra.all_to_all_v_plan([torch.zeros(4)] * 2, torch.zeros(2, 2, dtype=torch.int64),
+                              [torch.zeros(4)] * 2, 2)
 
 
 def test_wait_selftest_argument_checks(lib):

@@ -105,8 +105,15 @@ FUSED_CONFIGS = {
         M=4096, H=4096, y_shard_type=0, dtype="bf16", seed=2,
         x_std=0.02, w_std=0.02, bias_std=1.0),
     # The bf16 profiling size with 4100-byte token rows and 8200-byte weight
-    # rows (M/tp = H/tp = 2050): no TMA descriptor fits, the tensor-core
-    # kernel that stages operands with loads runs.
+    # rows (M/tp = H/tp = 2050): no TMA descriptor of the whole matrices fits;
+    # the row-class TMA kernel runs.
+    # Decode-like token counts at profiling size: C = 16 (128 token rows per
+    # group), one local expert per rank; the weights (0.54 GB) dominate the
+    # bytes, and the one-CTA kernel streams them.
+    "ep8tp4_E8_C16_M8192_H4096_t1_fp16": FusedConfig(
+        "ep8tp4_E8_C16_M8192_H4096_t1_fp16", ep=8, tp=4, E=8, C=16,
+        M=8192, H=4096, y_shard_type=1, dtype="fp16", seed=4,
+        x_std=0.02, w_std=0.02, bias_std=1.0),
     "ep8tp2_E8_C256_M4100_H4100_t0_bf16": FusedConfig(
         "ep8tp2_E8_C256_M4100_H4100_t0_bf16", ep=8, tp=2, E=8, C=256,
         M=4100, H=4100, y_shard_type=0, dtype="bf16", seed=2,

@@ -39,7 +39,7 @@
 #include <memory>
 #include <mutex>
 
-#include "tc_ptx.cuh"
+#include "tcu_epilogue.cuh"
 
 namespace bra {
 
@@ -66,6 +66,7 @@ constexpr int EPI_WARP0 = 4;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 4 * kEpiStageBytes + 1024;
+static_assert(kUStageBytes <= kEpiStageBytes, "element epilogue staging");
 
 template <typename T>
 __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_constant__ TcParams p) {
@@ -203,7 +204,11 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_const
       if (!__all_sync(0xffffffffu, waited)) break;
       tc_fence_after();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      epilogue_rows<T, BN>(p, t_base, tc.mt * BM + q * 32, sl, e, tc.nt * BN, epi_stage, lane);
+      if (p.y_elem)   // outputs or bias without 16-byte alignment: element stores
+        epilogue_rows_u<T>(p, t_base, tc.mt * BM + q * 32, sl, e, tc.nt * BN,
+                           bars + BAR_BYTES + q * kEpiStageBytes, lane);
+      else
+        epilogue_rows<T, BN>(p, t_base, tc.mt * BM + q * 32, sl, e, tc.nt * BN, epi_stage, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -230,14 +235,18 @@ struct DeviceInfo {
 }  // namespace
 
 bool fused_tc_eligible(const FusedProblem& f) {
+  // TMA needs 16-byte x and weight rows and pointers; outputs and bias need
+  // only element alignment (the epilogue stores element by element when they
+  // are not 16-byte aligned).
   if (f.Kp % 8 != 0 || f.H % 8 != 0) return false;
-  if (f.type == 0 && (f.H / f.tp) % 8 != 0) return false;
   const int P = f.ep * f.tp;
   if (P > kMaxRanks) return false;
   auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  const uintptr_t bias_align = f.dtype == BRA_BF16 ? 3u : 1u;
   for (int r = 0; r < P; ++r) {
-    if (!al(f.x[r]) || !al(f.w[r]) || !al(f.y[r])) return false;
-    if (f.bias && !al(f.bias[r])) return false;
+    if (!al(f.x[r]) || !al(f.w[r])) return false;
+    if (reinterpret_cast<uintptr_t>(f.y[r]) & 1u) return false;
+    if (f.bias && (reinterpret_cast<uintptr_t>(f.bias[r]) & bias_align)) return false;
   }
   return true;
 }

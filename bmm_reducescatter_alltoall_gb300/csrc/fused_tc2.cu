@@ -33,7 +33,7 @@
 #include <memory>
 #include <mutex>
 
-#include "tc_ptx.cuh"
+#include "tcu_epilogue.cuh"
 
 namespace bra {
 
@@ -63,6 +63,8 @@ constexpr int BAR_BYTES = 256;
 // accumulators (epilogue overlaps the next tile).  NSUB = 2: 4-stage ring of
 // 48 KiB, one 128 x 512 accumulator per CTA (all of TMEM), a quarter less
 // operand traffic per FLOP from L2 and through shared memory.
+static_assert(kUStageBytes <= kEpiStageBytes, "element epilogue staging");
+
 template <int NSUB>
 struct Shape {
   static constexpr int BN = 256 * NSUB;
@@ -228,7 +230,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       const int row0 = tc.mt * BM + (int)rank * BM_CTA + q * 32;
-      epilogue_rows<T, BN>(p, t_base, row0, sl, e, tc.nt * BN, epi_stage, lane);
+      if (p.y_elem) {   // outputs or bias without 16-byte alignment: element stores
+        uint8_t* stg = bars + BAR_BYTES + q * kEpiStageBytes;
+#pragma unroll 1
+        for (int sub = 0; sub < NSUB; ++sub)
+          epilogue_rows_u<T>(p, t_base + sub * 256, row0, sl, e, tc.nt * BN + sub * 256, stg,
+                             lane);
+      } else {
+        epilogue_rows<T, BN>(p, t_base, row0, sl, e, tc.nt * BN, epi_stage, lane);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

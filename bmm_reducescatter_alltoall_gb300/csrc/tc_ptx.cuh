@@ -35,6 +35,8 @@ struct TcParams {
   uint32_t idesc;                // tcgen05 instruction descriptor
   uint32_t b_lbo, b_sbo;         // B operand strides (bytes), N-major weight
   int b_kmajor;                  // weight stored transposed: B is K-major
+  int y_elem;                    // output rows / pointers or bias not 16-byte aligned:
+                                 // the epilogue stores element by element
 };
 
 // ---------------------------------------------------------------------------
@@ -556,6 +558,15 @@ inline void fill_common(TcParams* p, const FusedProblem& f, int bm, int bn, int 
   p->has_bias = f.bias != nullptr;
   p->b_kmajor = f.wt;
   p->rows = f.ep * f.C;
+  // 16-byte vector stores need 16-byte output rows and pointers, and the
+  // vector bias loads 16-byte bias rows and pointers.
+  {
+    const int Hp = f.H / f.tp;
+    bool vec = f.type == 1 || Hp % 8 == 0;
+    auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    for (int d = 0; vec && d < P; ++d) vec = al(f.y[d]) && (!f.bias || al(f.bias[d]));
+    p->y_elem = vec ? 0 : 1;
+  }
   p->m_tiles = (p->rows + bm - 1) / bm;
   p->n_tiles = (f.H + bn - 1) / bn;
   p->k_blocks = (f.Kp + bk - 1) / bk;

@@ -120,11 +120,14 @@ typedef enum {
  *                    input range or another output range.
  *   BRA_ERR_UNSUPPORTED  ep*C >= 2^31.
  *   BRA_ERR_CUDA     the launch failed (cudaGetLastError).
- * Variant: when every row stride and pointer is 16-byte aligned (Kp % 8 ==
- * 0, H % 8 == 0, and Hp % 8 == 0 for yShardType 0) a TMA-fed tensor-core
+ * Variant: when the operands' rows and pointers are 16-byte aligned (Kp % 8
+ * == 0, H % 8 == 0, x and weight 16-byte aligned) a TMA-fed tensor-core
  * kernel runs: the CTA-pair kernel when the problem has at least 64 output
  * tiles of 256 x 256 and more than 128 token rows (ep*C) per expert group,
- * else the one-CTA kernel.  Other shapes with element-aligned pointers run
+ * else the one-CTA kernel.  Its epilogue stores 16-byte vectors when the
+ * outputs and bias are 16-byte aligned (and Hp % 8 == 0 for yShardType 0),
+ * else element by element (outputs and bias element-aligned).  Other shapes
+ * with element-aligned pointers run
  * the CTA-pair tensor-core kernel fed by row-class TMA maps (one map per
  * class of rows that start at the same offset past a 16-byte boundary, the
  * rows shifted into place in shared memory); when the maps of one TP group

@@ -288,6 +288,14 @@ def test_options_select_the_variant_and_are_checked(lib, monkeypatch):
 
 
 def test_tc_alignment_predicate(lib):
+    # output rows or pointers without 16-byte alignment keep the TMA kernels
+    # (their epilogue stores element by element): H/tp = 12, odd y offsets
+    h = Fake(2, 2, 4, 64, 256, 24, 0)
+    assert _variant(lib, h) == bra.VARIANT_TC
+    h.y[1] += 2
+    assert _variant(lib, h) == bra.VARIANT_TC
+    h.y[1] += 1                                   # not even element-aligned
+    assert _variant(lib, h) == bra.VARIANT_SIMT
     g = Fake(2, 2, 8, 128, 128, 256, 0)
     assert _variant(lib, g) in (bra.VARIANT_TC, bra.VARIANT_TC2)
     g.x[1] += 2                                   # 2-byte aligned only: row-class TMA

@@ -276,7 +276,7 @@ def test_transposed_weight(case, variant):
     ys = bra.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t)["y"]
     out = [torch.full(ys, float("nan"), dtype=dinp["x"][0].dtype, device="cuda")
            for _ in range(cfg.P)]
-    aligned = (M // tp) % 8 == 0 and H % 8 == 0 and (t == 1 or (H // tp) % 8 == 0)
+    aligned = (M // tp) % 8 == 0 and H % 8 == 0          # TMA-ready x and weight rows
     if variant in ("tc", "tc2") and not aligned:
         with pytest.raises(bra.BraError):
             bra.bmm_rs_a2a(dinp["x"], wt, dinp["bias"], ep, tp, E, C, M, H, t, out=out,
@@ -331,6 +331,52 @@ def test_unaligned_large_sampled(transposed, variant, monkeypatch):
         assert not torch.isnan(y).any().item()
     err = _sampled_check(cfg, dinp, out, np.random.default_rng(11), per_rank=16)
     assert err <= TOL["bf16"], f"sampled rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("variant", [None, "tc", "tc2"])
+@pytest.mark.parametrize("case", [
+    (2, 2, 4, 64, 256, 24, 0, "fp16"),        # H/tp = 12: output rows of 24 bytes
+    (4, 2, 8, 256, 512, 1032, 0, "bf16"),     # H/tp = 516, 256 x 256 pair tiles
+    (2, 4, 4, 96, 512, 264, 0, "bf16"),       # H/tp = 66
+])
+def test_tma_kernels_with_unaligned_output_rows(case, variant, monkeypatch):
+    """x and weight rows are TMA-ready, the yShardType-0 output rows are not:
+    the TMA kernels store element by element."""
+    ep, tp, E, C, M, H, t, dt = case
+    for bias in (True, False):
+        cfg = FusedConfig("yo", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                          seed=sum(case[:6]) + 31, has_bias=bias)
+        inp = fused_inputs_host(cfg)
+        dinp = _to_dev(inp)
+        if variant is None:
+            ys = bra.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t)["y"]
+            probe = [torch.empty(ys, dtype=dinp["x"][0].dtype, device="cuda")
+                     for _ in range(cfg.P)]
+            monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
+            assert bra.bmm_rs_a2a_variant(dinp["x"], dinp["w"], dinp["bias"], ep, tp, E, C, M,
+                                          H, t, probe) in (bra.VARIANT_TC, bra.VARIANT_TC2)
+        out = _run(cfg, dinp, variant, monkeypatch)
+        err = _rel_err(out, _oracle(cfg, inp))
+        assert err <= TOL[dt], f"{case} {variant} bias={bias}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("variant", ["tc", "tc2"])
+def test_tma_kernels_with_element_aligned_outputs_and_bias(variant, monkeypatch):
+    """16-byte x and weight, but y and bias views start a few elements past a
+    16-byte boundary: element-wise epilogue, same results as the oracle."""
+    cfg = FusedConfig("yb", ep=4, tp=2, E=8, C=128, M=512, H=768, y_shard_type=1,
+                      dtype="fp16", seed=41)
+    inp = fused_inputs_host(cfg)
+    dinp = _to_dev(inp)
+    bias = [_shifted(b, 1 + r % 5) for r, b in enumerate(dinp["bias"])]
+    ys = bra.bmm_rs_a2a_infer_shape(cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H, 1)["y"]
+    outs = [_shifted(torch.full(ys, float("nan"), dtype=torch.float16, device="cuda"),
+                     1 + r % 7) for r in range(cfg.P)]
+    bra.bmm_rs_a2a(dinp["x"], dinp["w"], bias, cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H, 1,
+                   out=outs, variant=variant)
+    torch.cuda.synchronize()
+    assert bra.fault_status() == 0
+    assert _rel_err(outs, _oracle(cfg, inp)) <= TOL["fp16"]
 
 
 def _shifted(t, off):

@@ -632,7 +632,8 @@ def run_ours(a):
                 h_.copy_(d_, non_blocking=True)
 
         def run_steps(n):
-            ev = {k: [torch.cuda.Event() for _ in range(3)] for k in range(n)}
+            ev = {k: [torch.cuda.Event(), torch.cuda.Event(),
+                      torch.cuda.Event(enable_timing=True)] for k in range(n)}
             for k in range(n):
                 dset = sets[k % 2]
                 up_done, comp_done, down_done = ev[k]
@@ -650,7 +651,7 @@ def run_ours(a):
                 with torch.cuda.stream(down):
                     download(dset)
                 down_done.record(down)
-            return ev[n - 1][2]
+            return ev
 
         run_steps(2)
         torch.cuda.synchronize(dev)
@@ -660,8 +661,8 @@ def run_ours(a):
         e0.record(up)
         stream.wait_event(e0)
         down.wait_event(e0)
-        last = run_steps(a.e2e_steps)
-        down.wait_event(last)
+        evs = run_steps(a.e2e_steps)
+        down.wait_event(evs[a.e2e_steps - 1][2])
         e1.record(down)
         torch.cuda.synchronize(dev)
         dist.barrier()
@@ -670,8 +671,14 @@ def run_ours(a):
         e2e_val, _ = aggregate(dist, step_flops * a.e2e_steps / 1e12, e0.elapsed_time(e1) / 1e3,
                                dev)
         e2e_s = e0.elapsed_time(e1) / 1e3
+        # device time between consecutive read-back ends: the steady step is
+        # bound by the host link; single copies that stall show as outliers
+        ends = [e0.elapsed_time(evs[k][2]) for k in range(a.e2e_steps)]
+        step_ms = [ends[0]] + [b_ - a_ for a_, b_ in zip(ends, ends[1:])]
         e2e = {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": a.e2e_steps,
+               "step_ms": [round(v, 2) for v in step_ms],
+               "median_step_ms": float(np.median(step_ms)),
                "pipelined": "uploads of step k+1 and read-back of step k-1 overlap step k "
                             "(two device sets, copy streams)",
                "bound": "host link",

@@ -50,6 +50,10 @@ def _args(argv=None):
     ap.add_argument("--indexed-calls", type=int, default=30,
                     help="indexed all_to_all_v calls timed alone after the step loop (0: none)")
     ap.add_argument("--fused", default=FUSED_NAME)
+    ap.add_argument("--workspace", action="store_true",
+                    help="give the fused call a workspace of bmm_rs_a2a_workspace_size bytes: "
+                         "shapes whose x or weight rows lack a 16-byte pitch then run the "
+                         "packed variant (operands repacked, then the TMA kernel)")
     ap.add_argument("--a2av", default=A2AV_NAME)
     ap.add_argument("--a2av-sweep", action="store_true",
                     help="instead of the step: all_to_all_v alone over a range of sizes "
@@ -378,16 +382,34 @@ def run_ours(a):
     sweep = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     fused_launches = (cfg.ep + max(1, 64 // cfg.tp) - 1) // max(1, 64 // cfg.tp)
+    ws_bytes = 0
+    workspace = None
+    if a.workspace:
+        ws_bytes = bra.bmm_rs_a2a_workspace_size(finp["x"], finp["w"], finp["bias"], cfg.ep,
+                                                 cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H,
+                                                 cfg.y_shard_type, yout)
+        if ws_bytes > 0:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     variant = bra.bmm_rs_a2a_variant(finp["x"], finp["w"], finp["bias"], cfg.ep, cfg.tp, cfg.E,
-                                     cfg.C, cfg.M, cfg.H, cfg.y_shard_type, yout)
-    fused_kernel = {bra.VARIANT_TC: "fused_tc_kernel", bra.VARIANT_TC2: "fused_tc2_kernel",
-                    bra.VARIANT_TCU: "fused_tcu_kernel",
-                    bra.VARIANT_TCR: "fused_tcr_kernel",
-                    bra.VARIANT_SIMT: "fused_simt_kernel"}[variant]
+                                     cfg.C, cfg.M, cfg.H, cfg.y_shard_type, yout,
+                                     workspace=workspace)
+    names = {bra.VARIANT_TC: "fused_tc_kernel", bra.VARIANT_TC2: "fused_tc2_kernel",
+             bra.VARIANT_TCU: "fused_tcu_kernel", bra.VARIANT_TCR: "fused_tcr_kernel",
+             bra.VARIANT_SIMT: "fused_simt_kernel"}
+    if variant == bra.VARIANT_PACKED:
+        # the library's choice between the TMA kernels, restated: the CTA
+        # pair with >= 64 pair tiles and > 128 token rows per group
+        rows = cfg.ep * cfg.C
+        pair_tiles = cfg.E * ((rows + 255) // 256) * ((cfg.H + 255) // 256)
+        tma = "fused_tc2_kernel" if pair_tiles >= 64 and rows > 128 else "fused_tc_kernel"
+        fused_kernel = "repack_rows_kernel + " + tma
+    else:
+        fused_kernel = names[variant]
 
     # prepared calls: the tensors are checked once, each step only calls the library
     fused_plan = bra.bmm_rs_a2a_plan(finp["x"], finp["w"], finp["bias"], cfg.ep, cfg.tp, cfg.E,
-                                     cfg.C, cfg.M, cfg.H, cfg.y_shard_type, out=yout)
+                                     cfg.C, cfg.M, cfg.H, cfg.y_shard_type, out=yout,
+                                     workspace=workspace)
     a2av_plan = bra.all_to_all_v_plan(a_in, sc_d, a_out, acfg.L, send_displs=book[0],
                                       recv_counts=book[1], recv_displs=book[2])
 
@@ -614,7 +636,7 @@ def run_ours(a):
         for dset in sets:                          # prepared once per device set
             dset["fplan"] = bra.bmm_rs_a2a_plan(dset["x"], dset["w"], dset["b"], cfg.ep, cfg.tp,
                                                 cfg.E, cfg.C, cfg.M, cfg.H, cfg.y_shard_type,
-                                                out=dset["y"])
+                                                out=dset["y"], workspace=workspace)
             dset["aplan"] = bra.all_to_all_v_plan(dset["a_in"], dset["sc"], dset["a_out"],
                                                   acfg.L, send_displs=dset["book"][0],
                                                   recv_counts=dset["book"][1],
@@ -710,12 +732,13 @@ def run_ours(a):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "fp16", "data": "synthetic",
+            "dtype": cfg.dtype, "data": "synthetic",
             "config": {
                 "workload": f"{a.fused} + {a.a2av}",
                 "fused": {"ep": cfg.ep, "tp": cfg.tp, "E": cfg.E, "C": cfg.C, "M": cfg.M,
                           "H": cfg.H, "yShardType": cfg.y_shard_type, "dtype": cfg.dtype,
-                          "tflop_per_step": step_flops / 1e12},
+                          "tflop_per_step": step_flops / 1e12, "variant": fused_kernel,
+                          "workspace_bytes": ws_bytes},
                 "all_to_all_v": {"P": acfg.P, "L": acfg.L, "dtype": acfg.dtype,
                                  "bytes_moved": a_bytes},
                 "parallelism": "replicas" if dist.world > 1 else "single GPU, virtual ranks",

@@ -17,7 +17,8 @@ from typing import List, Optional, Sequence
 
 __all__ = [
     "BraError", "FP16", "BF16", "FP32", "INT8", "VARIANT_TC", "VARIANT_TC2", "VARIANT_SIMT",
-    "VARIANT_TCU", "VARIANT_TCR", "wait_selftest", "indexed_all_to_all_v",
+    "VARIANT_TCU", "VARIANT_TCR", "VARIANT_PACKED", "wait_selftest", "indexed_all_to_all_v",
+    "bmm_rs_a2a_workspace_size",
     "FusedOptions", "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
     "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked", "Plan", "bmm_rs_a2a_plan",
     "all_to_all_v_plan", "indexed_all_to_all_v_plan",
@@ -25,7 +26,7 @@ __all__ = [
 ]
 
 FP16, BF16, FP32, INT8 = 0, 1, 2, 3
-VARIANT_TC, VARIANT_SIMT, VARIANT_TC2, VARIANT_TCU, VARIANT_TCR = 1, 2, 3, 4, 5
+VARIANT_TC, VARIANT_SIMT, VARIANT_TC2, VARIANT_TCU, VARIANT_TCR, VARIANT_PACKED = 1, 2, 3, 4, 5, 6
 OK, ERR_NULLPTR, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = (
     0, 161001, 161002, 161003, 161100, 161101)
 
@@ -37,7 +38,8 @@ _lib = None
 class FusedOptions(ctypes.Structure):
     """bra_fused_options of the C header."""
     _fields_ = [("transpose_weight", ctypes.c_int32), ("variant", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 6)]
+                ("reserved", ctypes.c_int32 * 2), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_int64)]
 
 
 class BraError(RuntimeError):
@@ -67,6 +69,8 @@ def library() -> ctypes.CDLL:
     lib.bmm_rs_a2a_variant.argtypes = [pp, pp, pp, i64, i64, i64, i64, i64, i64, i64, c_int, pp,
                                        optp]
     lib.bmm_rs_a2a_variant.restype = c_int
+    lib.bmm_rs_a2a_workspace_size.argtypes = lib.bmm_rs_a2a_variant.argtypes
+    lib.bmm_rs_a2a_workspace_size.restype = i64
     lib.bmm_rs_a2a_infer_shape.argtypes = [i64] * 7 + [i64p] * 4
     lib.bmm_rs_a2a_infer_shape.restype = c_int
     lib.cal_all_to_all_v_blocks.argtypes = [i64, i64]
@@ -183,15 +187,20 @@ def _shape_check(t, want, what):
 
 
 _VARIANTS = {None: 0, "auto": 0, "tc": VARIANT_TC, "tc2": VARIANT_TC2, "simt": VARIANT_SIMT,
-             "tcu": VARIANT_TCU, "tcr": VARIANT_TCR}
+             "tcu": VARIANT_TCU, "tcr": VARIANT_TCR, "packed": VARIANT_PACKED}
 
 
-def _options(transpose_weight: bool, variant) -> "FusedOptions":
+def _options(transpose_weight: bool, variant, workspace=None) -> "FusedOptions":
     if variant not in _VARIANTS:
         raise ValueError(f"variant must be one of {sorted(k for k in _VARIANTS if k)}")
     o = FusedOptions()
     o.transpose_weight = 1 if transpose_weight else 0
     o.variant = _VARIANTS[variant]
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        o.workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
     return o
 
 
@@ -260,7 +269,7 @@ class Plan:
 def bmm_rs_a2a_plan(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int, tp: int,
                     E: int, C: int, M: int, H: int, y_shard_type: int,
                     out: Optional[Sequence] = None, transpose_weight: bool = False,
-                    variant: Optional[str] = None) -> Plan:
+                    variant: Optional[str] = None, workspace=None) -> Plan:
     """bmm_rs_a2a prepared once (see Plan); plan.run() returns out."""
     torch = _torch()
     if out is None:
@@ -268,35 +277,52 @@ def bmm_rs_a2a_plan(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep:
         out = [torch.empty(ys, dtype=x[0].dtype, device=x[0].device) for _ in range(ep * tp)]
     xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
                                      transpose_weight)
-    opts = _options(transpose_weight, variant)
+    opts = _options(transpose_weight, variant, workspace)
     args = (xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp, ctypes.byref(opts))
     return Plan(library().bmm_rs_a2a_ex, args, "bmm_rs_a2a", out,
-                (x, weight, bias, opts, xp, wp, bp, yp))
+                (x, weight, bias, opts, xp, wp, bp, yp, workspace))
 
 
 def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int, tp: int,
                E: int, C: int, M: int, H: int, y_shard_type: int,
                out: Optional[Sequence] = None, stream=None, transpose_weight: bool = False,
-               variant: Optional[str] = None) -> List:
+               variant: Optional[str] = None, workspace=None) -> List:
     """Fused BMM -> ReduceScatter -> Add -> AllToAll over P = ep*tp ranks.
 
     x[r], weight[r], bias[r] (or bias None) and out[r] are CUDA tensors of
     the shapes `bmm_rs_a2a_infer_shape` gives; out is allocated when None.
     transpose_weight: weight[r] is stored as (El, H, Kp) instead of
-    (El, Kp, H).  variant: None/"auto", "tc", "tc2", "tcr", "tcu" or "simt".
-    Returns out.  Asynchronous on `stream` (default: current stream).  For
+    (El, Kp, H).  variant: None/"auto", "tc", "tc2", "tcr", "tcu", "simt" or
+    "packed".  workspace: an optional contiguous CUDA tensor of at least
+    bmm_rs_a2a_workspace_size(...) bytes; given one, shapes whose x or weight
+    rows lack a 16-byte pitch run the packed variant (operands repacked into
+    it, then the TMA kernel).  Returns out.  Asynchronous on `stream` (default: current stream).  For
     repeated calls on the same buffers, bmm_rs_a2a_plan skips the checks.
     """
     return bmm_rs_a2a_plan(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
-                           transpose_weight, variant).run(stream)
+                           transpose_weight, variant, workspace).run(stream)
+
+
+def bmm_rs_a2a_workspace_size(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
+                              transpose_weight: bool = False) -> int:
+    """Bytes of workspace the packed variant needs for these tensors (0: none)."""
+    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
+                                     transpose_weight)
+    opts = _options(transpose_weight, None)
+    n = library().bmm_rs_a2a_workspace_size(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt,
+                                            yp, ctypes.byref(opts))
+    if n < 0:
+        raise BraError(-n, "bmm_rs_a2a_workspace_size")
+    return n
 
 
 def bmm_rs_a2a_variant(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
-                       transpose_weight: bool = False, variant: Optional[str] = None) -> int:
-    """VARIANT_TC, VARIANT_TC2, VARIANT_TCR, VARIANT_TCU or VARIANT_SIMT; raises BraError if rejected."""
+                       transpose_weight: bool = False, variant: Optional[str] = None,
+                       workspace=None) -> int:
+    """The VARIANT_* constant bmm_rs_a2a would run; raises BraError if rejected."""
     xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
                                      transpose_weight)
-    opts = _options(transpose_weight, variant)
+    opts = _options(transpose_weight, variant, workspace)
     v = library().bmm_rs_a2a_variant(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp,
                                      ctypes.byref(opts))
     if v < 0:

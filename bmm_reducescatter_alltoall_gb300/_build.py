@@ -64,6 +64,7 @@ KERNEL_SOURCES = {
     "fused_simt_kernel": "fused_simt.cu",
     "a2av_kernel": "a2av.cu",
     "ia2av_kernel": "ia2av.cu",
+    "repack_rows_kernel": "repack.cu",
 }
 
 

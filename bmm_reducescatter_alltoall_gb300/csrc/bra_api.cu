@@ -37,6 +37,8 @@ struct Range {
   bool out;
 };
 
+void tensor_ranges(const bra::FusedProblem& p, std::vector<Range>* all);
+
 // Validation in the order of CheckParams: null pointers, dtype, attributes,
 // shapes; then the aliasing rule.  On success fills `prob`.
 int validate_fused(const void* const x[], const void* const weight[],
@@ -47,12 +49,16 @@ int validate_fused(const void* const x[], const void* const weight[],
   if (!x || !weight || !out) return BRA_ERR_NULLPTR;
   if (dtype != BRA_FP16 && dtype != BRA_BF16) return BRA_ERR_INVALID;
   if (opts) {
-    for (int k = 0; k < 6; ++k)
+    for (int k = 0; k < 2; ++k)
       if (opts->reserved[k] != 0) return BRA_ERR_INVALID;
     if (opts->variant != BRA_VARIANT_AUTO && opts->variant != BRA_VARIANT_TC &&
         opts->variant != BRA_VARIANT_TC2 && opts->variant != BRA_VARIANT_SIMT &&
-        opts->variant != BRA_VARIANT_TCU && opts->variant != BRA_VARIANT_TCR)
+        opts->variant != BRA_VARIANT_TCU && opts->variant != BRA_VARIANT_TCR &&
+        opts->variant != BRA_VARIANT_PACKED)
       return BRA_ERR_INVALID;
+    if (opts->workspace_bytes < 0) return BRA_ERR_INVALID;
+    if (!opts->workspace && opts->workspace_bytes != 0) return BRA_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(opts->workspace) & 255u) return BRA_ERR_INVALID;
   }
   int rc = check_fused_attrs(ep, tp, E, C, M, H, type);
   if (rc != BRA_OK) return rc;
@@ -66,35 +72,6 @@ int validate_fused(const void* const x[], const void* const weight[],
   if (ep * C >= (int64_t(1) << 31)) return BRA_ERR_UNSUPPORTED;
 
   const int64_t El = E / ep, Kp = M / tp;
-  const int64_t es = 2;
-  const int64_t bes = dtype == BRA_FP16 ? 2 : 4;
-  const int64_t Hb = type == 0 ? H / tp : H;
-  const int64_t xb = El * ep * C * Kp * es, wb = El * Kp * H * es;
-  const int64_t bb = El * Hb * bes;
-  const int64_t yb = (type == 0 ? E * C * (H / tp) : E * (C / tp) * H) * es;
-  std::vector<Range> in, outs;
-  in.reserve(3 * P);
-  outs.reserve(P);
-  for (int64_t r = 0; r < P; ++r) {
-    in.push_back({(uintptr_t)x[r], (uintptr_t)x[r] + (uintptr_t)xb, false});
-    in.push_back({(uintptr_t)weight[r], (uintptr_t)weight[r] + (uintptr_t)wb, false});
-    if (nb) in.push_back({(uintptr_t)bias[r], (uintptr_t)bias[r] + (uintptr_t)bb, false});
-    outs.push_back({(uintptr_t)out[r], (uintptr_t)out[r] + (uintptr_t)yb, true});
-  }
-  // Outputs may overlap nothing.  Sorted by start, a pair (a before b)
-  // overlaps iff b.lo < a.hi; track the largest end of every earlier range
-  // and of every earlier output.
-  std::vector<Range> all(in);
-  all.insert(all.end(), outs.begin(), outs.end());
-  std::sort(all.begin(), all.end(),
-            [](const Range& a, const Range& b) { return a.lo < b.lo; });
-  uintptr_t max_hi_all = 0, max_hi_out = 0;
-  for (const Range& a : all) {
-    if (a.out ? a.lo < max_hi_all : a.lo < max_hi_out) return BRA_ERR_INVALID;
-    max_hi_all = std::max(max_hi_all, a.hi);
-    if (a.out) max_hi_out = std::max(max_hi_out, a.hi);
-  }
-
   prob->x = x;
   prob->w = weight;
   prob->bias = nb ? bias : nullptr;
@@ -107,8 +84,84 @@ int validate_fused(const void* const x[], const void* const weight[],
   prob->H = (int)H;
   prob->type = (int)type;
   prob->dtype = dtype;
+  // Outputs may overlap nothing.  Sorted by start, a pair (a before b)
+  // overlaps iff b.lo < a.hi; track the largest end of every earlier range
+  // and of every earlier output.
+  std::vector<Range> all;
+  all.reserve(4 * P);
+  tensor_ranges(*prob, &all);
+  std::sort(all.begin(), all.end(),
+            [](const Range& a, const Range& b) { return a.lo < b.lo; });
+  uintptr_t max_hi_all = 0, max_hi_out = 0;
+  for (const Range& a : all) {
+    if (a.out ? a.lo < max_hi_all : a.lo < max_hi_out) return BRA_ERR_INVALID;
+    max_hi_all = std::max(max_hi_all, a.hi);
+    if (a.out) max_hi_out = std::max(max_hi_out, a.hi);
+  }
+
   prob->wt = (opts && opts->transpose_weight) ? 1 : 0;
+  prob->xp = (int)Kp;
+  prob->wp = prob->wt ? (int)Kp : (int)H;
   return BRA_OK;
+}
+
+// Byte ranges of every input and output of a validated problem.
+void tensor_ranges(const bra::FusedProblem& p, std::vector<Range>* all) {
+  const int64_t P = (int64_t)p.ep * p.tp;
+  const int64_t El = p.El, Kp = p.Kp, H = p.H, C = p.C, E = El * p.ep;
+  const int64_t bes = p.dtype == BRA_FP16 ? 2 : 4;
+  const int64_t Hb = p.type == 0 ? H / p.tp : H;
+  const int64_t xb = El * p.ep * C * Kp * 2, wb = El * Kp * H * 2, bb = El * Hb * bes;
+  const int64_t yb = (p.type == 0 ? E * C * (H / p.tp) : E * (C / p.tp) * H) * 2;
+  for (int64_t r = 0; r < P; ++r) {
+    all->push_back({(uintptr_t)p.x[r], (uintptr_t)p.x[r] + (uintptr_t)xb, false});
+    all->push_back({(uintptr_t)p.w[r], (uintptr_t)p.w[r] + (uintptr_t)wb, false});
+    if (p.bias) all->push_back({(uintptr_t)p.bias[r], (uintptr_t)p.bias[r] + (uintptr_t)bb, false});
+    all->push_back({(uintptr_t)p.y[r], (uintptr_t)p.y[r] + (uintptr_t)yb, true});
+  }
+}
+
+// The copies the packed variant makes ([CANN] §调用说明 two-phase workspace):
+// an operand is copied when its rows lack a 16-byte pitch or a pointer is
+// not 16-byte aligned; copies have pitches rounded up to 8 elements and start
+// 256-byte aligned, x copies of all ranks first, then weight copies.
+struct PackPlan {
+  bool ok = false;            // the packed variant can take the call
+  bool px = false, pw = false;
+  int xp = 0, wp = 0;         // pitches of the copies (elements)
+  int64_t x_rows = 0, w_rows = 0;
+  int64_t xbytes = 0, wbytes = 0;   // one rank's copy, rounded up to 256 bytes
+  int64_t total = 0;
+};
+
+int64_t round256(int64_t v) { return (v + 255) / 256 * 256; }
+
+PackPlan pack_plan(const bra::FusedProblem& p) {
+  PackPlan q;
+  const int P = p.ep * p.tp;
+  if (P > bra::kMaxRanks) return q;
+  auto low = [](const void* a, uintptr_t m) { return (reinterpret_cast<uintptr_t>(a) & m) != 0; };
+  const int wlen = p.wt ? p.Kp : p.H;
+  q.px = p.Kp % 8 != 0;
+  q.pw = wlen % 8 != 0;
+  const uintptr_t bias_mask = p.dtype == BRA_BF16 ? 3u : 1u;
+  for (int r = 0; r < P; ++r) {
+    // element alignment everywhere: the repack reads 16-bit elements, the
+    // TMA kernels' element-wise epilogue writes them
+    if (low(p.x[r], 1u) || low(p.w[r], 1u) || low(p.y[r], 1u)) return q;
+    if (p.bias && low(p.bias[r], bias_mask)) return q;
+    if (low(p.x[r], 15u)) q.px = true;
+    if (low(p.w[r], 15u)) q.pw = true;
+  }
+  q.ok = true;
+  q.xp = (p.Kp + 7) / 8 * 8;
+  q.wp = (wlen + 7) / 8 * 8;
+  q.x_rows = (int64_t)p.El * p.ep * p.C;
+  q.w_rows = (int64_t)p.El * (p.wt ? p.H : p.Kp);
+  q.xbytes = round256(q.x_rows * q.xp * 2);
+  q.wbytes = round256(q.w_rows * q.wp * 2);
+  q.total = (int64_t)P * ((q.px ? q.xbytes : 0) + (q.pw ? q.wbytes : 0));
+  return q;
 }
 
 // BRA_FORCE_VARIANT=tc|tc2|tcr|tcu|simt, read at every call.
@@ -120,7 +173,30 @@ int forced_variant() {
   if (!std::strcmp(v, "simt")) return BRA_VARIANT_SIMT;
   if (!std::strcmp(v, "tcu")) return BRA_VARIANT_TCU;
   if (!std::strcmp(v, "tcr")) return BRA_VARIANT_TCR;
+  if (!std::strcmp(v, "packed")) return BRA_VARIANT_PACKED;
   return BRA_VARIANT_AUTO;
+}
+
+// The CTA-pair kernel moves a third less shared-memory traffic per FLOP;
+// with few 256 x 256 tiles the one-CTA kernel spreads over more SMs, and
+// with at most 128 token rows per group (a weight-streaming, HBM-bound
+// problem) the pair's 256-row tile would be half empty.
+int tma_kernel_for(const bra::FusedProblem& p) {
+  const int64_t rows = (int64_t)p.ep * p.C;
+  const int64_t pair_tiles = (int64_t)p.ep * p.El * ((rows + 255) / 256) *
+                             (((int64_t)p.H + 255) / 256);
+  return pair_tiles >= 64 && rows > 128 ? BRA_VARIANT_TC2 : BRA_VARIANT_TC;
+}
+
+// The packed variant for a call that gives `opts`: BRA_VARIANT_PACKED, or a
+// negative status (no workspace where one is needed: UNSUPPORTED; one too
+// small: INVALID).
+int packed_or_status(const bra::FusedProblem& p, const bra_fused_options* opts) {
+  const PackPlan q = pack_plan(p);
+  if (!q.ok) return -BRA_ERR_UNSUPPORTED;
+  if (q.total == 0) return BRA_VARIANT_PACKED;
+  if (!opts || !opts->workspace) return -BRA_ERR_UNSUPPORTED;
+  return opts->workspace_bytes >= q.total ? BRA_VARIANT_PACKED : -BRA_ERR_INVALID;
 }
 
 int choose_variant(const bra::FusedProblem& p, const bra_fused_options* opts) {
@@ -132,23 +208,86 @@ int choose_variant(const bra::FusedProblem& p, const bra_fused_options* opts) {
   if (f == BRA_VARIANT_TC || f == BRA_VARIANT_TC2) return tc_ok ? f : -BRA_ERR_UNSUPPORTED;
   if (f == BRA_VARIANT_TCU) return tcu_ok ? f : -BRA_ERR_UNSUPPORTED;
   if (f == BRA_VARIANT_TCR) return tcr_ok ? f : -BRA_ERR_UNSUPPORTED;
-  // Rows without a 16-byte pitch: the CTA-pair kernel fed by row-class TMA
+  if (f == BRA_VARIANT_PACKED) return packed_or_status(p, opts);
+  // Rows without a 16-byte pitch: with a workspace, the operands repacked
+  // for the TMA kernel; otherwise the CTA-pair kernel fed by row-class TMA
   // maps; when a launch cannot hold the maps of one TP group, the kernel
   // that stages operands with loads; pointers not even element-aligned: the
   // generic kernel.
-  if (!tc_ok) return tcr_ok ? BRA_VARIANT_TCR : tcu_ok ? BRA_VARIANT_TCU : BRA_VARIANT_SIMT;
-  // The CTA-pair kernel moves a third less shared-memory traffic per FLOP;
-  // with few 256 x 256 tiles the one-CTA kernel spreads over more SMs, and
-  // with at most 128 token rows per group (a weight-streaming, HBM-bound
-  // problem) the pair's 256-row tile would be half empty.
-  const int64_t rows = (int64_t)p.ep * p.C;
-  const int64_t pair_tiles = (int64_t)p.ep * p.El * ((rows + 255) / 256) *
-                             (((int64_t)p.H + 255) / 256);
-  return pair_tiles >= 64 && rows > 128 ? BRA_VARIANT_TC2 : BRA_VARIANT_TC;
+  if (!tc_ok) {
+    if (opts && opts->workspace && pack_plan(p).ok) return packed_or_status(p, opts);
+    return tcr_ok ? BRA_VARIANT_TCR : tcu_ok ? BRA_VARIANT_TCU : BRA_VARIANT_SIMT;
+  }
+  return tma_kernel_for(p);
+}
+
+bool log_enabled();
+
+// Repack the operands the plan names into the workspace (after checking
+// that it overlaps no input or output), then run the TMA kernel on the
+// copies.  Everything is enqueued on `st`.
+int run_packed(const bra::FusedProblem& p, const bra_fused_options* opts, cudaStream_t st) {
+  const PackPlan q = pack_plan(p);
+  if (!q.ok) return BRA_ERR_UNSUPPORTED;
+  const int P = p.ep * p.tp;
+  std::vector<const void*> xs(p.x, p.x + P), wsrc(p.w, p.w + P);
+  if (q.total > 0) {
+    std::vector<Range> all;
+    tensor_ranges(p, &all);
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(opts->workspace);
+    const uintptr_t hi = lo + (uintptr_t)q.total;
+    for (const Range& a : all)
+      if (a.lo < hi && lo < a.hi) return BRA_ERR_INVALID;
+    bra::RepackArgs a;
+    std::memset(&a, 0, sizeof(a));
+    uint8_t* cur = static_cast<uint8_t*>(opts->workspace);
+    cudaError_t e = cudaSuccess;
+    auto add = [&](const void* src, void* dst, int64_t rows, int len, int pitch) {
+      if (e != cudaSuccess) return;
+      if (a.njobs == bra::kRepackJobs) {
+        e = bra::launch_repack(a, st);
+        a.njobs = 0;
+        a.total_rows = 0;
+        if (e != cudaSuccess) return;
+      }
+      a.job[a.njobs++] = bra::RepackJob{src, dst, a.total_rows, len, pitch};
+      a.total_rows += rows;
+    };
+    if (q.px)
+      for (int r = 0; r < P; ++r) {
+        add(p.x[r], cur, q.x_rows, p.Kp, q.xp);
+        xs[r] = cur;
+        cur += q.xbytes;
+      }
+    if (q.pw)
+      for (int r = 0; r < P; ++r) {
+        add(p.w[r], cur, q.w_rows, p.wt ? p.Kp : p.H, q.wp);
+        wsrc[r] = cur;
+        cur += q.wbytes;
+      }
+    if (e == cudaSuccess && a.njobs > 0) e = bra::launch_repack(a, st);
+    if (e != cudaSuccess) return BRA_ERR_CUDA;
+  }
+  bra::FusedProblem r = p;
+  r.x = xs.data();
+  r.w = wsrc.data();
+  if (q.px) r.xp = q.xp;
+  if (q.pw) r.wp = q.wp;
+  if (!bra::fused_tc_eligible(r)) return BRA_ERR_UNSUPPORTED;
+  const int v = tma_kernel_for(r);
+  if (log_enabled())
+    std::fprintf(stderr, "[bra] packed: x %s (pitch %d), weight %s (pitch %d), %lld bytes -> %s\n",
+                 q.px ? "copied" : "in place", r.xp, q.pw ? "copied" : "in place", r.wp,
+                 (long long)q.total, v == BRA_VARIANT_TC2 ? "tc2" : "tc");
+  const cudaError_t e = v == BRA_VARIANT_TC2 ? bra::launch_fused_tc2(r, st)
+                                             : bra::launch_fused_tc(r, st);
+  if (e == cudaErrorInvalidValue) return BRA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
 }
 
 const char* variant_name(int v) {
-  return v == BRA_VARIANT_TC2   ? "tc2"
+  return v == BRA_VARIANT_PACKED ? "packed"
+         : v == BRA_VARIANT_TC2 ? "tc2"
          : v == BRA_VARIANT_TC  ? "tc"
          : v == BRA_VARIANT_TCR ? "tcr"
          : v == BRA_VARIANT_TCU ? "tcu"
@@ -286,6 +425,7 @@ int bmm_rs_a2a_ex(const void* const x[], const void* const weight[],
     std::fprintf(stderr, "[bra] bmm_rs_a2a ep=%lld tp=%lld E=%lld C=%lld M=%lld H=%lld type=%lld -> %s\n",
                  (long long)ep, (long long)tp, (long long)E, (long long)C, (long long)M,
                  (long long)H, (long long)yShardType, variant_name(v));
+  if (v == BRA_VARIANT_PACKED) return run_packed(p, opts, (cudaStream_t)stream);
   cudaError_t e = v == BRA_VARIANT_TC2   ? bra::launch_fused_tc2(p, (cudaStream_t)stream)
                   : v == BRA_VARIANT_TC  ? bra::launch_fused_tc(p, (cudaStream_t)stream)
                   : v == BRA_VARIANT_TCR ? bra::launch_fused_tcr(p, (cudaStream_t)stream)
@@ -312,6 +452,24 @@ int bmm_rs_a2a_variant(const void* const x[], const void* const weight[],
   int rc = validate_fused(x, weight, bias, ep, tp, E, C, M, H, yShardType, dtype, out, opts, &p);
   if (rc != BRA_OK) return -rc;
   return choose_variant(p, opts);
+}
+
+int64_t bmm_rs_a2a_workspace_size(const void* const x[], const void* const weight[],
+                                  const void* const bias[], int64_t ep, int64_t tp, int64_t E,
+                                  int64_t C, int64_t M, int64_t H, int64_t yShardType,
+                                  int dtype, void* const out[], const bra_fused_options* opts) {
+  bra_fused_options o;
+  std::memset(&o, 0, sizeof(o));
+  if (opts) o = *opts;
+  o.workspace = nullptr;
+  o.workspace_bytes = 0;
+  bra::FusedProblem p;
+  const int rc = validate_fused(x, weight, bias, ep, tp, E, C, M, H, yShardType, dtype, out, &o,
+                                &p);
+  if (rc != BRA_OK) return -rc;
+  if (bra::fused_tc_eligible(p)) return 0;
+  const PackPlan q = pack_plan(p);
+  return q.ok ? q.total : 0;
 }
 
 int bmm_rs_a2a_infer_shape(int64_t ep, int64_t tp, int64_t E, int64_t C,

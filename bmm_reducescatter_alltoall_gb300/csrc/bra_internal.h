@@ -54,7 +54,7 @@ int ia2av_ctas_per_rank(int P);
 // CTAs per rank that fill the GPU once.
 int a2av_ctas_per_rank(int P);
 
-// Problem description shared by both fused variants.
+// Problem description shared by the fused kernels.
 struct FusedProblem {
   const void* const* x;      // [P]
   const void* const* w;      // [P]
@@ -64,6 +64,11 @@ struct FusedProblem {
   int type;                  // yShardType
   int dtype;                 // BRA_FP16 | BRA_BF16
   int wt;                    // weight stored transposed: (El, H, Kp)
+  // Row pitches in elements: x rows (Kp long) and weight rows (H long, or Kp
+  // when transposed).  Equal to the row lengths for the caller's dense
+  // tensors; larger for repacked copies, whose rows start 16-byte aligned.
+  // Only the TMA kernels (fused_tc*) accept pitches other than the lengths.
+  int xp, wp;
 };
 
 cudaError_t launch_fused_simt(const FusedProblem& f, cudaStream_t st);
@@ -81,6 +86,23 @@ cudaError_t launch_fused_tcr(const FusedProblem& f, cudaStream_t st);
 bool fused_tcr_eligible(const FusedProblem& f);
 
 cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t st);
+
+// Row repacking: copies rows of 16-bit elements that start at any even byte
+// address to rows that start 16-byte aligned, `pitch` elements apart.
+struct RepackJob {
+  const void* src;   // rows of `len` elements, back to back (2-byte aligned)
+  void* dst;         // 16-byte aligned; row k starts at dst + k * pitch * 2
+  int64_t row0;      // index of this job's first row among all rows of the launch
+  int32_t len;       // elements per row
+  int32_t pitch;     // destination row pitch in elements (>= len rounded up to 8)
+};
+constexpr int kRepackJobs = 256;
+struct RepackArgs {
+  RepackJob job[kRepackJobs];   // ordered by row0; job[0].row0 == 0
+  int64_t total_rows;
+  int njobs;
+};
+cudaError_t launch_repack(const RepackArgs& a, cudaStream_t st);
 cudaError_t read_fault_word(int32_t* code, int clear);        // tensor-core kernel
 cudaError_t read_fault_word2(int32_t* code, int clear);       // CTA-pair tensor-core kernel
 cudaError_t read_fault_word3(int32_t* code, int clear);       // load-staged unaligned kernel

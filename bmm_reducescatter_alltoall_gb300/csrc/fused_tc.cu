@@ -235,10 +235,11 @@ struct DeviceInfo {
 }  // namespace
 
 bool fused_tc_eligible(const FusedProblem& f) {
-  // TMA needs 16-byte x and weight rows and pointers; outputs and bias need
-  // only element alignment (the epilogue stores element by element when they
-  // are not 16-byte aligned).
-  if (f.Kp % 8 != 0 || f.H % 8 != 0) return false;
+  // TMA needs x and weight rows with a 16-byte pitch and 16-byte pointers
+  // (the row lengths themselves may be ragged: coordinates past a row's end
+  // read zeros); outputs and bias need only element alignment (the epilogue
+  // stores element by element when they are not 16-byte aligned).
+  if (f.xp % 8 != 0 || f.wp % 8 != 0) return false;
   const int P = f.ep * f.tp;
   if (P > kMaxRanks) return false;
   auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };

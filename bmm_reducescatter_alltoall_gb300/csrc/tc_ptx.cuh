@@ -529,14 +529,15 @@ inline EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D 16-bit tensor {d0 (contiguous), d1, d2}, box {b0, b1, 1}, 128-byte
-// swizzle, zero fill outside the tensor.
+// 3-D 16-bit tensor {d0 (contiguous), d1, d2} whose rows are `pitch`
+// elements apart (pitch >= d0), box {b0, b1, 1}, 128-byte swizzle, zero fill
+// outside the tensor (including columns d0 .. pitch-1).
 inline bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0,
-                      uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+                      uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint64_t pitch) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint64_t strides[2] = {pitch * 2, pitch * d1 * 2};
   const cuuint32_t box[3] = {b0, b1, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -562,7 +563,7 @@ inline void fill_common(TcParams* p, const FusedProblem& f, int bm, int bn, int 
   // vector bias loads 16-byte bias rows and pointers.
   {
     const int Hp = f.H / f.tp;
-    bool vec = f.type == 1 || Hp % 8 == 0;
+    bool vec = (f.type == 1 ? f.H : Hp) % 8 == 0;
     auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
     for (int d = 0; vec && d < P; ++d) vec = al(f.y[d]) && (!f.bias || al(f.bias[d]));
     p->y_elem = vec ? 0 : 1;
@@ -584,12 +585,12 @@ inline bool fill_chunk(TcParams* p, const FusedProblem& f, int s0, int s1, uint3
   for (int r = 0; r < p->nranks; ++r) {
     const int gr = s0 * f.tp + r;
     if (!encode_3d(&p->tx[r], dt, f.x[gr], (uint64_t)f.Kp, (uint64_t)p->rows, (uint64_t)f.El,
-                   (uint32_t)bk, a_rows))
+                   (uint32_t)bk, a_rows, (uint64_t)f.xp))
       return false;
     const bool ok = f.wt ? encode_3d(&p->tw[r], dt, f.w[gr], (uint64_t)f.Kp, (uint64_t)f.H,
-                                     (uint64_t)f.El, (uint32_t)bk, b_rows_t)
+                                     (uint64_t)f.El, (uint32_t)bk, b_rows_t, (uint64_t)f.wp)
                          : encode_3d(&p->tw[r], dt, f.w[gr], (uint64_t)f.H, (uint64_t)f.Kp,
-                                     (uint64_t)f.El, b_cols, (uint32_t)bk);
+                                     (uint64_t)f.El, b_cols, (uint32_t)bk, (uint64_t)f.wp);
     if (!ok) return false;
     p->bias[r] = f.bias ? f.bias[gr] : nullptr;
   }

@@ -67,9 +67,12 @@ typedef enum {
   BRA_VARIANT_TC2 = 3,   /* tcgen05 kernel, a CTA pair per 256x256 tile    */
   BRA_VARIANT_TCU = 4,   /* tcgen05 kernel for rows of any alignment:
                             operands staged by loads, not TMA             */
-  BRA_VARIANT_TCR = 5    /* tcgen05 CTA-pair kernel for rows of any
+  BRA_VARIANT_TCR = 5,   /* tcgen05 CTA-pair kernel for rows of any
                             alignment: row-class TMA maps, rows shifted
                             into place in shared memory                   */
+  BRA_VARIANT_PACKED = 6 /* operands without a 16-byte row pitch copied
+                            into the caller's workspace with one, then the
+                            TMA kernel (TC or TC2 by the same rule)       */
 } bra_variant;
 
 /* ------------------------------------------------------------------------ */
@@ -121,14 +124,16 @@ typedef enum {
  *   BRA_ERR_UNSUPPORTED  ep*C >= 2^31.
  *   BRA_ERR_CUDA     the launch failed (cudaGetLastError).
  * Variant: when the operands' rows and pointers are 16-byte aligned (Kp % 8
- * == 0, H % 8 == 0, x and weight 16-byte aligned) a TMA-fed tensor-core
- * kernel runs: the CTA-pair kernel when the problem has at least 64 output
+ * == 0, the weight's row length H -- Kp when transposed -- % 8 == 0, x and
+ * weight 16-byte aligned) a TMA-fed tensor-core kernel runs: the CTA-pair kernel when the problem has at least 64 output
  * tiles of 256 x 256 and more than 128 token rows (ep*C) per expert group,
  * else the one-CTA kernel.  Its epilogue stores 16-byte vectors when the
  * outputs and bias are 16-byte aligned (and Hp % 8 == 0 for yShardType 0),
  * else element by element (outputs and bias element-aligned).  Other shapes
- * with element-aligned pointers run
- * the CTA-pair tensor-core kernel fed by row-class TMA maps (one map per
+ * with element-aligned pointers run, given a workspace (bmm_rs_a2a_ex), the
+ * packed variant: those operands repacked, then the same TMA kernel.
+ * Without a workspace they run the CTA-pair tensor-core kernel fed by
+ * row-class TMA maps (one map per
  * class of rows that start at the same offset past a 16-byte boundary, the
  * rows shifted into place in shared memory); when the maps of one TP group
  * do not fit a launch ((n_x + n_w) * tp > 176, n = 1, 2, 4 or 8 classes per
@@ -136,9 +141,9 @@ typedef enum {
  * instead.  Pointers that are not even element-aligned run the generic
  * kernel.  Each launches once per 64 source ranks (the row-class kernel once
  * per 176 / (n_x + n_w) ranks).
- * The environment variable BRA_FORCE_VARIANT=tc|tc2|tcr|tcu|simt overrides
- * the choice (tc, tc2, tcr or tcu on an ineligible shape returns
- * BRA_ERR_UNSUPPORTED).
+ * The environment variable BRA_FORCE_VARIANT=tc|tc2|tcr|tcu|simt|packed
+ * overrides the choice (tc, tc2, tcr or tcu on an ineligible shape, or
+ * packed without a large enough workspace, returns BRA_ERR_UNSUPPORTED).
  */
 BRA_API int bmm_rs_a2a(const void* const x[], const void* const weight[],
                const void* const bias[], int64_t ep, int64_t tp, int64_t E,
@@ -155,14 +160,33 @@ typedef struct {
   /* BRA_VARIANT_AUTO (0) or a bra_variant to force; takes precedence over
    * the BRA_FORCE_VARIANT environment variable. */
   int32_t variant;
-  int32_t reserved[6];
+  int32_t reserved[2];
+  /* Device memory the call may use as scratch, in the manner of the second
+   * call of the two-phase aclnn interface ([CANN] §调用说明: the workspace
+   * and its size).  NULL with workspace_bytes 0: no workspace.  Only
+   * BRA_VARIANT_PACKED uses it (see bmm_rs_a2a_workspace_size); it must be
+   * 256-byte aligned, hold at least that many bytes, and overlap no input or
+   * output.  Its contents are scratch: overwritten, never read before being
+   * written.  The caller owns it; it must stay allocated until the call's
+   * work on `stream` completes. */
+  void* workspace;
+  int64_t workspace_bytes;
 } bra_fused_options;
 
 /*
  * bmm_rs_a2a_ex -- bmm_rs_a2a with options (NULL opts = all defaults, same
  * as bmm_rs_a2a).  Errors as bmm_rs_a2a, plus BRA_ERR_INVALID for an
- * unknown variant or a non-zero reserved field, and BRA_ERR_UNSUPPORTED when
- * a forced tensor-core variant cannot take the shape or alignment.
+ * unknown variant, a non-zero reserved field, a workspace that is not
+ * 256-byte aligned, smaller than bmm_rs_a2a_workspace_size, negative in size
+ * or overlapping an input or output (checked when a workspace is given and
+ * the packed variant would use it), and BRA_ERR_UNSUPPORTED when a forced
+ * tensor-core variant cannot take the shape or alignment.
+ * With a workspace of at least bmm_rs_a2a_workspace_size bytes, AUTO takes
+ * BRA_VARIANT_PACKED for every shape whose x or weight rows lack a 16-byte
+ * pitch (and whose pointers are element-aligned): the repack kernel copies
+ * those operands' rows into the workspace at a pitch of a multiple of 8
+ * elements, then the TMA kernel reads the copies (rows past the logical
+ * length read as zeros, so the copies need no zero padding).
  */
 BRA_API int bmm_rs_a2a_ex(const void* const x[], const void* const weight[],
                           const void* const bias[], int64_t ep, int64_t tp, int64_t E,
@@ -184,9 +208,29 @@ BRA_API int bmm_rs_a2a_infer_shape(int64_t ep, int64_t tp, int64_t E, int64_t C,
                            int64_t bias_shape[3], int64_t y_shape[3]);
 
 /*
+ * bmm_rs_a2a_workspace_size -- bytes of workspace the packed variant needs
+ * for these arguments (the first call of the two-phase aclnn interface,
+ * [CANN] §调用说明, without the executor): for every rank, a copy of x[r]
+ * when M/tp % 8 != 0 or x[r] is not 16-byte aligned, and of weight[r] when
+ * its row length (H, or M/tp when transposed) % 8 != 0 or weight[r] is not
+ * 16-byte aligned, each with rows rounded up to a multiple of 8 elements and
+ * each copy starting 256-byte aligned.  0 when no operand needs a copy (the
+ * TMA kernels read the caller's tensors) or when the packed variant cannot
+ * take the call (a pointer not element-aligned, more than 1024 ranks).  The
+ * workspace fields of opts are ignored.  Returns the size, or a negative
+ * bra_status when bmm_rs_a2a_ex would reject the arguments.  Pure host.
+ */
+BRA_API int64_t bmm_rs_a2a_workspace_size(const void* const x[], const void* const weight[],
+                                          const void* const bias[], int64_t ep, int64_t tp,
+                                          int64_t E, int64_t C, int64_t M, int64_t H,
+                                          int64_t yShardType, int dtype, void* const out[],
+                                          const bra_fused_options* opts);
+
+/*
  * bmm_rs_a2a_variant -- which kernel bmm_rs_a2a_ex would launch for these
  * arguments and options (BRA_VARIANT_TC, BRA_VARIANT_TC2, BRA_VARIANT_TCR,
- * BRA_VARIANT_TCU or BRA_VARIANT_SIMT), honouring BRA_FORCE_VARIANT.  Pointers are only
+ * BRA_VARIANT_TCU, BRA_VARIANT_SIMT or BRA_VARIANT_PACKED), honouring
+ * BRA_FORCE_VARIANT.  Pointers are only
  * inspected for alignment.  Returns the variant, or a negative bra_status
  * (e.g. -BRA_ERR_INVALID) when the call would be rejected.  Pure host.
  */

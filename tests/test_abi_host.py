@@ -278,7 +278,7 @@ def test_options_select_the_variant_and_are_checked(lib, monkeypatch):
     bad.variant = 9
     assert _variant(lib, g, opts=bad) == -INVALID
     bad = bra._options(False, None)
-    bad.reserved[3] = 1
+    bad.reserved[1] = 1
     assert _variant(lib, g, opts=bad) == -INVALID
     x, w, b, y = g.arrays()
     assert lib.bmm_rs_a2a_ex(x, w, b, 8, 4, 64, 512, 8192, 4096, 1, bra.FP16, y,
@@ -407,3 +407,131 @@ def test_wait_selftest_argument_checks(lib):
     assert lib.bra_wait_selftest(bra.WAIT_A2AV, None, None) == NULLPTR
     assert lib.bra_wait_selftest(7, 1 << 32, None) == INVALID
     assert lib.bra_wait_selftest(-1, 1 << 32, None) == INVALID
+
+
+# --------------------------------------------------------------------------
+# Workspace (packed variant)
+# --------------------------------------------------------------------------
+
+def test_options_struct_layout():
+    """bra_fused_options: two int32 fields, two reserved int32, then the
+    workspace pointer and its int64 size (32 bytes, 8-byte aligned)."""
+    F = bra.FusedOptions
+    assert ctypes.sizeof(F) == 32 and ctypes.alignment(F) == 8
+    assert [getattr(F, n).offset for n in ("transpose_weight", "variant", "reserved",
+                                           "workspace", "workspace_bytes")] == [0, 4, 8, 16, 24]
+    src = open(HEADER).read()
+    body = src[src.index("int32_t transpose_weight;"):src.index("} bra_fused_options;")]
+    decls = re.findall(r"^\s*(int32_t|void\*|int64_t)\s+(\w+)", body, flags=re.M)
+    assert decls == [("int32_t", "transpose_weight"), ("int32_t", "variant"),
+                     ("int32_t", "reserved"), ("void*", "workspace"),
+                     ("int64_t", "workspace_bytes")]
+
+
+def _ws_opts(ptr, nbytes, variant=None, transposed=False):
+    o = bra._options(transposed, variant)
+    o.workspace = ptr
+    o.workspace_bytes = nbytes
+    return o
+
+
+def _ws_size(lib, f, dtype=bra.FP16, transposed=False):
+    x, w, b, y = f.arrays()
+    return lib.bmm_rs_a2a_workspace_size(x, w, b, *f.args, dtype, y,
+                                         ctypes.byref(bra._options(transposed, None)))
+
+
+def _ws_expected(f, transposed=False):
+    """The documented layout restated: per rank, a copy of x when M/tp % 8 or
+    its pointer is not 16-byte aligned, of the weight when its row length
+    % 8 or its pointer is off; rows rounded up to 8 elements, each copy
+    rounded up to 256 bytes."""
+    ep, tp, E, C, M, H, t = f.args
+    P, El, Kp = ep * tp, E // ep, M // tp
+    if P > 1024 or any(a % 2 for a in f.x + f.w + f.y):
+        return 0
+    wlen = Kp if transposed else H
+    px = Kp % 8 != 0 or any(a % 16 for a in f.x)
+    pw = wlen % 8 != 0 or any(a % 16 for a in f.w)
+    if not px and not pw:
+        return 0
+    r8 = lambda v: (v + 7) // 8 * 8
+    r256 = lambda v: (v + 255) // 256 * 256
+    xb = r256(El * ep * C * r8(Kp) * 2)
+    wb = r256(El * (H if transposed else Kp) * r8(wlen) * 2)
+    return P * ((xb if px else 0) + (wb if pw else 0))
+
+
+@pytest.mark.parametrize("args", [(4, 2, 16, 12, 12, 4, 1), (2, 2, 4, 40, 130, 70, 0),
+                                  (2, 4, 4, 260, 1028, 516, 1), (8, 2, 16, 16, 2050, 1030, 0),
+                                  (2, 2, 8, 128, 128, 256, 0), (2, 2, 4, 40, 256, 70, 1),
+                                  (8, 4, 64, 512, 8192, 4096, 1)])
+@pytest.mark.parametrize("transposed", [False, True])
+def test_workspace_size_follows_the_layout(lib, args, transposed):
+    f = Fake(*args)
+    assert _ws_size(lib, f, transposed=transposed) == _ws_expected(f, transposed)
+    f.x[1] += 2                                   # element-aligned only: x copied
+    assert _ws_size(lib, f, transposed=transposed) == _ws_expected(f, transposed)
+    f.w[0] += 6
+    assert _ws_size(lib, f, transposed=transposed) == _ws_expected(f, transposed) > 0
+    f.y[0] += 1                                   # not element-aligned: no packed variant
+    assert _ws_size(lib, f, transposed=transposed) == 0
+
+
+def test_workspace_size_rejects_what_the_call_rejects(lib):
+    f = Fake(2, 2, 8, 4, 8, 8, 0)
+    x, w, b, y = f.arrays()
+    assert lib.bmm_rs_a2a_workspace_size(x, w, b, 2, 2, 8, 4, 8, 9, 0, bra.FP16, y, None) \
+        == -INVALID
+    assert lib.bmm_rs_a2a_workspace_size(None, w, b, 2, 2, 8, 4, 8, 8, 0, bra.FP16, y, None) \
+        == -NULLPTR
+    # the workspace fields of the options are ignored by the size query
+    assert lib.bmm_rs_a2a_workspace_size(x, w, b, 2, 2, 8, 4, 8, 8, 0, bra.FP16, y,
+                                         ctypes.byref(_ws_opts(3, -1))) == _ws_expected(f) > 0
+
+
+def test_workspace_selects_the_packed_variant(lib, monkeypatch):
+    monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
+    ws = 1 << 46
+    f = Fake(2, 2, 4, 40, 130, 70, 0)             # Kp = 65, H = 70: no TMA-ready rows
+    need = _ws_size(lib, f)
+    assert need > 0
+    assert _variant(lib, f) == bra.VARIANT_TCR                              # no workspace
+    assert _variant(lib, f, opts=_ws_opts(ws, need)) == bra.VARIANT_PACKED
+    assert _variant(lib, f, opts=_ws_opts(ws, need - 1)) == -INVALID        # too small
+    assert _variant(lib, f, opts=_ws_opts(ws + 16, need)) == -INVALID       # not 256-aligned
+    assert _variant(lib, f, opts=_ws_opts(None, need)) == -INVALID          # size without memory
+    assert _variant(lib, f, opts=_ws_opts(ws, -256)) == -INVALID
+    assert _variant(lib, f, opts=_ws_opts(None, 0, "packed")) == -UNSUPPORTED
+    assert _variant(lib, f, opts=_ws_opts(ws, need, "tcr")) == bra.VARIANT_TCR
+    monkeypatch.setenv("BRA_FORCE_VARIANT", "packed")
+    assert _variant(lib, f, opts=_ws_opts(ws, need)) == bra.VARIANT_PACKED
+    assert _variant(lib, f) == -UNSUPPORTED
+    monkeypatch.delenv("BRA_FORCE_VARIANT")
+    g = Fake(8, 4, 64, 512, 8192, 4096, 1)         # TMA-ready: the workspace is not used
+    assert _ws_size(lib, g) == 0
+    assert _variant(lib, g, opts=_ws_opts(ws, 1 << 30)) == bra.VARIANT_TC2
+    assert _variant(lib, g, opts=_ws_opts(ws, 0, "packed")) == bra.VARIANT_PACKED
+    h = Fake(2, 2, 4, 40, 130, 70, 0)
+    h.w[1] += 1                                   # not element-aligned: generic kernel
+    assert _variant(lib, h, opts=_ws_opts(ws, 1 << 40)) == bra.VARIANT_SIMT
+    assert _variant(lib, h, opts=_ws_opts(ws, 1 << 40, "packed")) == -UNSUPPORTED
+
+
+def test_transposed_weight_rows_decide_tma_readiness(lib):
+    """Transposed, the weight's rows are Kp long: H % 8 != 0 keeps the TMA
+    kernels (ragged N reads zeros), Kp % 8 != 0 does not."""
+    f = Fake(2, 2, 4, 40, 256, 70, 1)             # Kp = 128, H = 70
+    assert _variant(lib, f) == bra.VARIANT_TCR
+    assert _variant(lib, f, opts=bra._options(True, None)) in (bra.VARIANT_TC, bra.VARIANT_TC2)
+    g = Fake(2, 2, 4, 40, 130, 64, 1)             # Kp = 65, H = 64
+    assert _variant(lib, g, opts=bra._options(True, None)) == bra.VARIANT_TCR
+
+
+def test_overlapping_workspace_is_rejected_before_any_launch(lib):
+    f = Fake(2, 2, 4, 40, 130, 70, 0)
+    need = _ws_size(lib, f)
+    x, w, b, y = f.arrays()
+    for base in (f.x[2] // 256 * 256, f.y[0] // 256 * 256 - 256, f.b[3] // 256 * 256):
+        assert lib.bmm_rs_a2a_ex(x, w, b, *f.args, bra.FP16, y,
+                                 ctypes.byref(_ws_opts(base, need)), None) == INVALID

@@ -12,10 +12,15 @@ exhaustively over shape classes:
   below its first row (so inside the matrix's allocation), its rows all sit
   the same delta < 8 elements past that boundary, its pitch is a multiple of
   16 bytes, and it ends at the last row's end;
-* the even split of a send list over CTAs used by the exchange kernels.
+* the even split of a send list over CTAs used by the exchange kernels;
+* the repack kernel: every 32-bit word it loads holds a byte of the row being
+  copied (so it lies inside the row's 16-byte granules, inside the
+  allocation), every word it stores lies inside the destination row's pitch,
+  and the copied elements come out exactly, with a zero padding element for
+  odd lengths.
 
-The constants and formulas mirror fused_tcr.cu and ia2av.cu; a change there
-must be made here too.
+The constants and formulas mirror fused_tcr.cu, ia2av.cu and repack.cu; a
+change there must be made here too.
 """
 import itertools
 
@@ -135,3 +140,65 @@ def test_even_split_covers_the_send_list(n, parts):
         assert lo == prev and hi >= lo
         prev = hi
     assert prev == n
+
+
+def _repack_row(mem, sa, length, pitch, unroll=4):
+    """One warp's copy of one row, as repack.cu computes it (byte addresses
+    into `mem`, a bytes-like view of memory starting at address 0): returns
+    the destination words and the set of source word indices loaded."""
+    wa = sa & ~3
+    odd = (sa & 3) != 0
+    end = sa + 2 * length
+    nsrc = (end - wa + 3) >> 2
+    nout = (length + 1) >> 1
+    word = lambda k: int.from_bytes(mem[wa + 4 * k: wa + 4 * k + 4], "little")
+    loaded, out = set(), {}
+    for base in range(0, nout, 32 * unroll):
+        for u in range(unroll):
+            v, nb = [], []
+            for lane in range(32):
+                k = base + u * 32 + lane
+                if k < nsrc:
+                    loaded.add(k)
+                v.append(word(k) if k < nsrc else 0)
+            if odd:
+                for lane in range(32):
+                    k1 = base + u * 32 + lane + 1
+                    if lane < 31:
+                        nb.append(v[lane + 1])
+                    else:
+                        if k1 < nsrc:
+                            loaded.add(k1)
+                        nb.append(word(k1) if k1 < nsrc else 0)
+                v = [((a >> 16) | (b << 16)) & 0xFFFFFFFF for a, b in zip(v, nb)]
+            for lane in range(32):
+                k = base + u * 32 + lane
+                if k < nout:
+                    w = v[lane]
+                    if (length & 1) and k == nout - 1:
+                        w &= 0xFFFF
+                    out[k] = w
+    return out, loaded, nsrc, wa
+
+
+@pytest.mark.parametrize("length", [1, 2, 3, 7, 8, 9, 63, 64, 65, 255, 256, 257, 300])
+@pytest.mark.parametrize("off", [0, 2, 4, 6, 8, 10, 12, 14])
+def test_repack_reads_inside_the_row_and_copies_exactly(length, off):
+    rng = np.random.default_rng(length * 16 + off)
+    nrows = 3
+    base = 4096 + off                                     # element-aligned matrix start
+    mem = bytearray(rng.integers(0, 256, size=base + nrows * length * 2 + 64, dtype=np.uint8))
+    elems = np.frombuffer(bytes(mem[base:base + nrows * length * 2]), dtype="<u2").reshape(
+        nrows, length)
+    pitch = (length + 7) // 8 * 8
+    for row in range(nrows):
+        sa = base + row * length * 2
+        out, loaded, nsrc, wa = _repack_row(mem, sa, length, pitch)
+        for k in loaded:                                  # each loaded word holds a row byte
+            assert wa + 4 * k < sa + 2 * length and wa + 4 * k + 4 > sa
+        assert max(out) < pitch // 2 + (pitch % 2)        # stores stay inside the pitch
+        got = np.array([out[k] for k in sorted(out)], dtype=np.uint32)
+        halves = np.stack([got & 0xFFFF, got >> 16], axis=1).reshape(-1)
+        np.testing.assert_array_equal(halves[:length], elems[row])
+        if length & 1:
+            assert halves[length] == 0

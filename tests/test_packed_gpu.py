@@ -1,0 +1,183 @@
+"""The packed variant on the GPU: operands without a 16-byte row pitch are
+repacked into a caller-provided workspace (the two-phase workspace call of
+the CANN guide, 调用说明), then the TMA kernel reads the copies.
+
+* Unaligned shapes of several tiles with ragged row / column / K tails, both
+  shard types, bias or not, weight stored either way: against the oracle.
+* The workspace after a call holds each copied operand row for row, bit for
+  bit, at the documented offsets and pitch (odd lengths padded with a zero).
+* Element-aligned pointers (rows with a 16-byte pitch but starting 2..14
+  bytes past a boundary) and a large shape (4100-element rows) sampled.
+* A workspace filled with garbage beforehand changes nothing; a workspace
+  that is too small is rejected; forcing the variant without one is refused.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bmm_reducescatter_alltoall_gb300 as bra
+from oracle import fused as of
+from test_fused_gpu import (TOL, UNALIGNED_CASES, _oracle, _rel_err, _sampled_check, _shifted,
+                            _to_dev)
+from workloads import FUSED_CONFIGS, FusedConfig, fused_inputs_device, fused_inputs_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _workspace(nbytes, fill=0xA5):
+    return torch.full((max(int(nbytes), 1),), fill, dtype=torch.uint8, device="cuda")
+
+
+def _call(cfg, x, w, bias, transposed, ws, variant=None):
+    ys = bra.bmm_rs_a2a_infer_shape(cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H,
+                                    cfg.y_shard_type)["y"]
+    out = [torch.full(ys, float("nan"), dtype=x[0].dtype, device="cuda") for _ in range(cfg.P)]
+    bra.bmm_rs_a2a(x, w, bias, cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H, cfg.y_shard_type,
+                   out=out, transpose_weight=transposed, variant=variant, workspace=ws)
+    torch.cuda.synchronize()
+    assert bra.fault_status() == 0
+    return out
+
+
+def _need(cfg, x, w, bias, transposed):
+    ys = bra.bmm_rs_a2a_infer_shape(cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H,
+                                    cfg.y_shard_type)["y"]
+    probe = [torch.empty(ys, dtype=x[0].dtype, device="cuda") for _ in range(cfg.P)]
+    return bra.bmm_rs_a2a_workspace_size(x, w, bias, cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M,
+                                         cfg.H, cfg.y_shard_type, probe,
+                                         transpose_weight=transposed), probe
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+@pytest.mark.parametrize("case", UNALIGNED_CASES)
+@pytest.mark.parametrize("bias", [True, False])
+def test_packed_unaligned_shapes(case, bias, transposed):
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("pk", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=sum(case[:6]) + 23, has_bias=bias)
+    inp = fused_inputs_host(cfg)
+    ref = _oracle(cfg, inp)
+    d = _to_dev(inp)
+    w = [u.transpose(1, 2).contiguous() for u in d["w"]] if transposed else d["w"]
+    need, probe = _need(cfg, d["x"], w, d["bias"], transposed)
+    assert need > 0
+    ws = _workspace(need)
+    assert bra.bmm_rs_a2a_variant(d["x"], w, d["bias"], ep, tp, E, C, M, H, t, probe,
+                                  transpose_weight=transposed, workspace=ws) == \
+        bra.VARIANT_PACKED
+    out = _call(cfg, d["x"], w, d["bias"], transposed, ws)
+    err = _rel_err(out, ref)
+    assert err <= TOL[dt], f"{case} bias={bias} transposed={transposed}: rel err {err:.3e}"
+
+
+def _r8(v):
+    return (v + 7) // 8 * 8
+
+
+def _r256(v):
+    return (v + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+@pytest.mark.parametrize("case", [(2, 2, 4, 40, 130, 70, 0, "fp16"),
+                                  (4, 4, 8, 33 * 4, 36, 4, 1, "bf16"),
+                                  (2, 4, 4, 260, 1028, 516, 1, "fp16")])
+def test_workspace_holds_the_repacked_rows(case, transposed):
+    """x copies of every rank first, then weight copies; rows `pitch`
+    elements apart; each copy 256-byte aligned; bit-exact."""
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("pkw", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=sum(case[:6]))
+    d = _to_dev(fused_inputs_host(cfg))
+    w = [u.transpose(1, 2).contiguous() for u in d["w"]] if transposed else d["w"]
+    need, _ = _need(cfg, d["x"], w, d["bias"], transposed)
+    ws = _workspace(need)
+    _call(cfg, d["x"], w, d["bias"], transposed, ws)
+    P, El, Kp = cfg.P, E // ep, M // tp
+    wlen = Kp if transposed else H
+    wrows = El * (H if transposed else Kp)
+    xrows = El * ep * C
+    xb, wb = _r256(xrows * _r8(Kp) * 2), _r256(wrows * _r8(wlen) * 2)
+    px, pw = Kp % 8 != 0, wlen % 8 != 0
+    assert need == P * ((xb if px else 0) + (wb if pw else 0))
+    raw = ws.cpu()
+    off = 0
+    for copied, srcs, nb, rows, length in ((px, d["x"], xb, xrows, Kp), (pw, w, wb, wrows, wlen)):
+        if not copied:
+            continue
+        for r in range(P):
+            blk = raw[off:off + rows * _r8(length) * 2].view(torch.int16).view(rows, _r8(length))
+            want = srcs[r].reshape(rows, length).view(torch.int16).cpu()
+            assert torch.equal(blk[:, :length], want), f"rank {r}"
+            if length % 2:
+                assert (blk[:, length] == 0).all()
+            off += nb
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+def test_packed_element_aligned_pointers(transposed):
+    """Rows with a 16-byte pitch whose tensors start 1..7 elements past a
+    boundary: only the misplaced operands are copied."""
+    M, H = 272, 264
+    cfg = FusedConfig("pkp", ep=4, tp=2, E=8, C=96, M=M, H=H, y_shard_type=1, dtype="bf16",
+                      seed=M + H + 1)
+    inp = fused_inputs_host(cfg)
+    ref = _oracle(cfg, inp)
+    d = _to_dev(inp)
+    xs = [_shifted(x, 1 + r % 7) for r, x in enumerate(d["x"])]
+    w0 = [u.transpose(1, 2).contiguous() for u in d["w"]] if transposed else d["w"]
+    need_w_only, _ = _need(cfg, d["x"], [_shifted(u, 3) for u in w0], d["bias"], transposed)
+    need, _ = _need(cfg, xs, w0, d["bias"], transposed)
+    assert 0 < need and 0 < need_w_only
+    out = _call(cfg, xs, w0, d["bias"], transposed, _workspace(need))
+    err = _rel_err(out, ref)
+    assert err <= TOL["bf16"], f"transposed={transposed}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+def test_packed_large_sampled(transposed):
+    """4100-element token and weight rows (8200-byte pitch), 16 ranks, both
+    operands copied; sampled against the oracle."""
+    cfg = FUSED_CONFIGS["ep8tp2_E64_C256_M4096_H4096_t0_bf16"].replace(E=16, M=4100, H=4100)
+    dinp = fused_inputs_device(cfg)
+    w = [u.transpose(1, 2).contiguous() for u in dinp["w"]] if transposed else dinp["w"]
+    need, _ = _need(cfg, dinp["x"], w, dinp["bias"], transposed)
+    out = _call(cfg, dinp["x"], w, dinp["bias"], transposed, _workspace(need))
+    for y in out:
+        assert not torch.isnan(y).any().item()
+    err = _sampled_check(cfg, dinp, out, np.random.default_rng(13), per_rank=16)
+    assert err <= TOL["bf16"], f"sampled rel err {err:.3e}"
+
+
+def test_workspace_contents_do_not_matter_and_calls_repeat_bit_identically():
+    cfg = FusedConfig("pkr", ep=4, tp=2, E=8, C=160, M=1026, H=518, y_shard_type=0,
+                      dtype="bf16", seed=5)
+    d = _to_dev(fused_inputs_host(cfg))
+    need, _ = _need(cfg, d["x"], d["w"], d["bias"], False)
+    outs = [_call(cfg, d["x"], d["w"], d["bias"], False, _workspace(need, fill))
+            for fill in (0, 0xFF, 0x7C)]
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_small_workspace_and_forced_variant_are_refused(monkeypatch):
+    monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
+    cfg = FusedConfig("pks", ep=2, tp=2, E=4, C=40, M=130, H=70, y_shard_type=0, dtype="fp16",
+                      seed=3)
+    d = _to_dev(fused_inputs_host(cfg))
+    need, probe = _need(cfg, d["x"], d["w"], d["bias"], False)
+    with pytest.raises(bra.BraError) as e:
+        _call(cfg, d["x"], d["w"], d["bias"], False, _workspace(need - 256))
+    assert e.value.args[0].endswith(f"({bra.ERR_INVALID})")
+    with pytest.raises(bra.BraError) as e:
+        _call(cfg, d["x"], d["w"], d["bias"], False, None, variant="packed")
+    assert e.value.args[0].endswith(f"({bra.ERR_UNSUPPORTED})")
+    # an aligned shape ignores the workspace; forced, the packed variant
+    # copies nothing and runs the TMA kernel on the caller's tensors
+    cfg2 = cfg.replace(M=256, H=512)
+    inp2 = fused_inputs_host(cfg2)
+    d2 = _to_dev(inp2)
+    assert _need(cfg2, d2["x"], d2["w"], d2["bias"], False)[0] == 0
+    out = _call(cfg2, d2["x"], d2["w"], d2["bias"], False, None, variant="packed")
+    assert _rel_err(out, _oracle(cfg2, inp2)) <= TOL["fp16"]

@@ -123,8 +123,9 @@ void tensor_ranges(const bra::FusedProblem& p, std::vector<Range>* all) {
 
 // The copies the packed variant makes ([CANN] §调用说明 two-phase workspace):
 // an operand is copied when its rows lack a 16-byte pitch or a pointer is
-// not 16-byte aligned; copies have pitches rounded up to 8 elements and start
-// 256-byte aligned, x copies of all ranks first, then weight copies.
+// not 16-byte aligned; copies have pitches rounded up to 64 elements (rows
+// start on 128-byte L2 lines, so no TMA box row straddles two lines) and
+// start 256-byte aligned, x copies of all ranks first, then weight copies.
 struct PackPlan {
   bool ok = false;            // the packed variant can take the call
   bool px = false, pw = false;
@@ -154,8 +155,8 @@ PackPlan pack_plan(const bra::FusedProblem& p) {
     if (low(p.w[r], 15u)) q.pw = true;
   }
   q.ok = true;
-  q.xp = (p.Kp + 7) / 8 * 8;
-  q.wp = (wlen + 7) / 8 * 8;
+  q.xp = (p.Kp + 63) / 64 * 64;
+  q.wp = (wlen + 63) / 64 * 64;
   q.x_rows = (int64_t)p.El * p.ep * p.C;
   q.w_rows = (int64_t)p.El * (p.wt ? p.H : p.Kp);
   q.xbytes = round256(q.x_rows * q.xp * 2);

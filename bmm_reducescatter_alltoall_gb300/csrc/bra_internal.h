@@ -94,7 +94,7 @@ struct RepackJob {
   void* dst;         // 16-byte aligned; row k starts at dst + k * pitch * 2
   int64_t row0;      // index of this job's first row among all rows of the launch
   int32_t len;       // elements per row
-  int32_t pitch;     // destination row pitch in elements (>= len rounded up to 8)
+  int32_t pitch;     // destination row pitch in elements (a multiple of 8, > len if len is odd)
 };
 constexpr int kRepackJobs = 256;
 struct RepackArgs {

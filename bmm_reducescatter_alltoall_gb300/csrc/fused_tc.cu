@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_const
       tc_fence_after();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       if (p.y_elem)   // outputs or bias without 16-byte alignment: element stores
-        epilogue_rows_u<T>(p, t_base, tc.mt * BM + q * 32, sl, e, tc.nt * BN,
-                           bars + BAR_BYTES + q * kEpiStageBytes, lane);
+        epilogue_rows_u<T, true>(p, t_base, tc.mt * BM + q * 32, sl, e, tc.nt * BN,
+                                 bars + BAR_BYTES + q * kEpiStageBytes, lane);
       else
         epilogue_rows<T, BN>(p, t_base, tc.mt * BM + q * 32, sl, e, tc.nt * BN, epi_stage, lane);
       tc_fence_before();

@@ -234,8 +234,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         uint8_t* stg = bars + BAR_BYTES + q * kEpiStageBytes;
 #pragma unroll 1
         for (int sub = 0; sub < NSUB; ++sub)
-          epilogue_rows_u<T>(p, t_base + sub * 256, row0, sl, e, tc.nt * BN + sub * 256, stg,
-                             lane);
+          epilogue_rows_u<T, true>(p, t_base + sub * 256, row0, sl, e, tc.nt * BN + sub * 256,
+                                   stg, lane);
       } else {
         epilogue_rows<T, BN>(p, t_base, row0, sl, e, tc.nt * BN, epi_stage, lane);
       }

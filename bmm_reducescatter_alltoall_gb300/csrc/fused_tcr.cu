@@ -545,7 +545,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       const int row0 = tc.mt * BM + (int)rank * BM_CTA + q * 32;
-      epilogue_rows_u<T>(p, t_base, row0, sl, e, tc.nt * BN, stg, lane);
+      epilogue_rows_u<T, false>(p, t_base, row0, sl, e, tc.nt * BN, stg, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

@@ -70,6 +70,7 @@ constexpr int ALL_CHUNKS = A_CHUNKS + B_CHUNKS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + EPI_WARPS * kUStageBytes + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct UParams {
   const void* x[kChunkRanks];
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tcu_kernel(const __grid_cons
       if (!__all_sync(0xffffffffu, waited)) break;
       tc_fence_after();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      epilogue_rows_u<T>(p, t_base, tc.mt * BM + q * 32, sl, e, tc.nt * BN, stg, lane);
+      epilogue_rows_u<T, false>(p, t_base, tc.mt * BM + q * 32, sl, e, tc.nt * BN, stg, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));

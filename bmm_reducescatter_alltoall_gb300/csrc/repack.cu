@@ -1,7 +1,8 @@
 // Row repacking for the workspace path of bmm_rs_a2a: operands whose rows are
 // not 16-byte aligned (M/tp or H not a multiple of 8 elements, or a pointer
 // only element-aligned) are copied, row by row, into caller-provided
-// workspace with a pitch that is a multiple of 8 elements.  The tensor-core
+// workspace with a pitch that is a multiple of 64 elements (128 bytes, so
+// every row of a TMA box starts on an L2 line).  The tensor-core
 // kernels then read the copies through ordinary 128-byte-swizzle TMA maps
 // whose dimensions are the logical row lengths, so the padding is never
 // read (TMA fills coordinates past a row's end with zeros).
@@ -23,7 +24,7 @@ namespace bra {
 namespace {
 
 constexpr int kRThreads = 256;
-constexpr int kRUnroll = 4;   // 32-bit words per lane per pass (512 bytes per warp)
+constexpr int kRUnroll = 16;  // 32-bit words per lane per pass (2 KB per warp in flight)
 
 __global__ void __launch_bounds__(kRThreads) repack_rows_kernel(const __grid_constant__ RepackArgs a) {
   const int lane = threadIdx.x & 31;

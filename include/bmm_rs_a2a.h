@@ -184,7 +184,7 @@ typedef struct {
  * With a workspace of at least bmm_rs_a2a_workspace_size bytes, AUTO takes
  * BRA_VARIANT_PACKED for every shape whose x or weight rows lack a 16-byte
  * pitch (and whose pointers are element-aligned): the repack kernel copies
- * those operands' rows into the workspace at a pitch of a multiple of 8
+ * those operands' rows into the workspace at a pitch of a multiple of 64
  * elements, then the TMA kernel reads the copies (rows past the logical
  * length read as zeros, so the copies need no zero padding).
  */
@@ -213,8 +213,9 @@ BRA_API int bmm_rs_a2a_infer_shape(int64_t ep, int64_t tp, int64_t E, int64_t C,
  * [CANN] §调用说明, without the executor): for every rank, a copy of x[r]
  * when M/tp % 8 != 0 or x[r] is not 16-byte aligned, and of weight[r] when
  * its row length (H, or M/tp when transposed) % 8 != 0 or weight[r] is not
- * 16-byte aligned, each with rows rounded up to a multiple of 8 elements and
- * each copy starting 256-byte aligned.  0 when no operand needs a copy (the
+ * 16-byte aligned, each with rows rounded up to a multiple of 64 elements
+ * (128 bytes) and each copy starting 256-byte aligned (x copies of all ranks
+ * first, then weight copies).  0 when no operand needs a copy (the
  * TMA kernels read the caller's tensors) or when the packed variant cannot
  * take the call (a pointer not element-aligned, more than 1024 ranks).  The
  * workspace fields of opts are ignored.  Returns the size, or a negative

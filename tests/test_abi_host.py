@@ -444,7 +444,7 @@ def _ws_size(lib, f, dtype=bra.FP16, transposed=False):
 def _ws_expected(f, transposed=False):
     """The documented layout restated: per rank, a copy of x when M/tp % 8 or
     its pointer is not 16-byte aligned, of the weight when its row length
-    % 8 or its pointer is off; rows rounded up to 8 elements, each copy
+    % 8 or its pointer is off; rows rounded up to 64 elements, each copy
     rounded up to 256 bytes."""
     ep, tp, E, C, M, H, t = f.args
     P, El, Kp = ep * tp, E // ep, M // tp
@@ -455,10 +455,10 @@ def _ws_expected(f, transposed=False):
     pw = wlen % 8 != 0 or any(a % 16 for a in f.w)
     if not px and not pw:
         return 0
-    r8 = lambda v: (v + 7) // 8 * 8
+    r64 = lambda v: (v + 63) // 64 * 64
     r256 = lambda v: (v + 255) // 256 * 256
-    xb = r256(El * ep * C * r8(Kp) * 2)
-    wb = r256(El * (H if transposed else Kp) * r8(wlen) * 2)
+    xb = r256(El * ep * C * r64(Kp) * 2)
+    wb = r256(El * (H if transposed else Kp) * r64(wlen) * 2)
     return P * ((xb if px else 0) + (wb if pw else 0))
 
 

@@ -142,7 +142,7 @@ def test_even_split_covers_the_send_list(n, parts):
     assert prev == n
 
 
-def _repack_row(mem, sa, length, pitch, unroll=4):
+def _repack_row(mem, sa, length, pitch, unroll=16):
     """One warp's copy of one row, as repack.cu computes it (byte addresses
     into `mem`, a bytes-like view of memory starting at address 0): returns
     the destination words and the set of source word indices loaded."""
@@ -190,7 +190,7 @@ def test_repack_reads_inside_the_row_and_copies_exactly(length, off):
     mem = bytearray(rng.integers(0, 256, size=base + nrows * length * 2 + 64, dtype=np.uint8))
     elems = np.frombuffer(bytes(mem[base:base + nrows * length * 2]), dtype="<u2").reshape(
         nrows, length)
-    pitch = (length + 7) // 8 * 8
+    pitch = (length + 63) // 64 * 64
     for row in range(nrows):
         sa = base + row * length * 2
         out, loaded, nsrc, wa = _repack_row(mem, sa, length, pitch)

@@ -70,8 +70,8 @@ def test_packed_unaligned_shapes(case, bias, transposed):
     assert err <= TOL[dt], f"{case} bias={bias} transposed={transposed}: rel err {err:.3e}"
 
 
-def _r8(v):
-    return (v + 7) // 8 * 8
+def _r64(v):
+    return (v + 63) // 64 * 64
 
 
 def _r256(v):
@@ -97,7 +97,7 @@ def test_workspace_holds_the_repacked_rows(case, transposed):
     wlen = Kp if transposed else H
     wrows = El * (H if transposed else Kp)
     xrows = El * ep * C
-    xb, wb = _r256(xrows * _r8(Kp) * 2), _r256(wrows * _r8(wlen) * 2)
+    xb, wb = _r256(xrows * _r64(Kp) * 2), _r256(wrows * _r64(wlen) * 2)
     px, pw = Kp % 8 != 0, wlen % 8 != 0
     assert need == P * ((xb if px else 0) + (wb if pw else 0))
     raw = ws.cpu()
@@ -106,7 +106,7 @@ def test_workspace_holds_the_repacked_rows(case, transposed):
         if not copied:
             continue
         for r in range(P):
-            blk = raw[off:off + rows * _r8(length) * 2].view(torch.int16).view(rows, _r8(length))
+            blk = raw[off:off + rows * _r64(length) * 2].view(torch.int16).view(rows, _r64(length))
             want = srcs[r].reshape(rows, length).view(torch.int16).cpu()
             assert torch.equal(blk[:, :length], want), f"rank {r}"
             if length % 2:

@@ -2,7 +2,9 @@
 
 * Random shapes with rows of any alignment (both shard types, bias or not,
   weight stored either way, pointers offset by a few elements) run on the
-  automatic kernel choice and are compared with the oracle.
+  automatic kernel choice, half of them given a workspace (the packed
+  variant where the rows lack a 16-byte pitch), and are compared with the
+  oracle.
 * Every kernel runs the same inputs several times: each output element has
   one fixed accumulation order, so the results must be bit-identical call to
   call.  A synchronisation slip between the roles of a kernel (a stage read
@@ -61,8 +63,15 @@ def test_random_shapes_match_the_oracle(k):
     ys = bra.bmm_rs_a2a_infer_shape(cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H,
                                     cfg.y_shard_type)["y"]
     out = [torch.full(ys, float("nan"), dtype=xs[0].dtype, device="cuda") for _ in range(cfg.P)]
+    workspace = None
+    if rng.random() < 0.5:                        # the packed variant where it applies
+        n = bra.bmm_rs_a2a_workspace_size(xs, ws, bias, cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M,
+                                          cfg.H, cfg.y_shard_type, out,
+                                          transpose_weight=transposed)
+        if n > 0:
+            workspace = torch.full((n,), 0xA5, dtype=torch.uint8, device="cuda")
     bra.bmm_rs_a2a(xs, ws, bias, cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H, cfg.y_shard_type,
-                   out=out, transpose_weight=transposed)
+                   out=out, transpose_weight=transposed, workspace=workspace)
     torch.cuda.synchronize()
     assert bra.fault_status() == 0
     g = np.concatenate([o.float().cpu().numpy().ravel() for o in out]).astype(np.float64)
@@ -93,7 +102,8 @@ def _fused_repeat(variant, M, H, t, dt, monkeypatch, calls=5):
 
 
 @pytest.mark.parametrize("variant,M,H", [("tc2", 1024, 512), ("tc", 1024, 512),
-                                         ("tcr", 1026, 518), ("tcu", 1026, 518)])
+                                         ("tcr", 1026, 518), ("tcu", 1026, 518),
+                                         ("tc2", 1024, 520)])   # H/tp = 260: element stores
 @pytest.mark.parametrize("t", [0, 1])
 def test_repeated_fused_calls_are_bit_identical(variant, M, H, t, monkeypatch):
     _fused_repeat(variant, M, H, t, "bf16" if t == 0 else "fp16", monkeypatch)

@@ -397,19 +397,33 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base
   const int s = p.s0 + sl;
   const int Hp = p.H / p.tp;
   const int Cp = p.type == 1 ? p.C / p.tp : 1;
-  // yShardType 0: the bias depends on the column only, so the warp stages the
-  // tile's BN bias values (fp32) once and every row reads them by broadcast.
+  // this lane's own row (phase 1)
+  const int m_own = row0 + lane;
+  const bool own_ok = m_own < p.rows;
+  const int t_own = (own_ok && p.type == 1) ? (m_own % p.C) / Cp : 0;
+  // When the bias depends on the column only -- always for yShardType 0, and
+  // for yShardType 1 when the warp's 32 rows share a TP rank (row 0 of the
+  // warp is valid whenever any is) -- the warp stages the tile's BN bias
+  // values (fp32) once and every row reads them by broadcast.
+  const int t_first = __shfl_sync(0xffffffffu, t_own, 0);
   const uint32_t bias_stage = stage + 32 * kEpiRowStride;
-  const bool bias_staged = p.has_bias && p.type == 0;
+  const bool bias_staged =
+      p.has_bias && (p.type == 0 || __all_sync(0xffffffffu, !own_ok || t_own == t_first));
   if (bias_staged) {
     for (int g = lane; g < BN / 8; g += 32) {
       const int n = n0 + g * 8;
       float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if (n < p.H) {
-        const int t = n / Hp;
-        Out<T>::bias8(static_cast<const uint8_t*>(p.bias[sl * p.tp + t]) +
-                          ((int64_t)e * Hp + (n - t * Hp)) * Out<T>::kBiasBytes,
-                      b);
+        if (p.type == 0) {
+          const int t = n / Hp;
+          Out<T>::bias8(static_cast<const uint8_t*>(p.bias[sl * p.tp + t]) +
+                            ((int64_t)e * Hp + (n - t * Hp)) * Out<T>::kBiasBytes,
+                        b);
+        } else {
+          Out<T>::bias8(static_cast<const uint8_t*>(p.bias[sl * p.tp + t_first]) +
+                            ((int64_t)e * p.H + n) * Out<T>::kBiasBytes,
+                        b);
+        }
       }
       sts128(bias_stage + g * 32, make_uint4(__float_as_uint(b[0]), __float_as_uint(b[1]),
                                              __float_as_uint(b[2]), __float_as_uint(b[3])));
@@ -418,10 +432,6 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base
     }
     __syncwarp();
   }
-  // this lane's own row (phase 1)
-  const int m_own = row0 + lane;
-  const bool own_ok = m_own < p.rows;
-  const int t_own = (own_ok && p.type == 1) ? (m_own % p.C) / Cp : 0;
   // the 8 rows this lane stores (phase 2): r = 4q + lane/8
   const int kc = lane & 7;
   int64_t rbase[8];
@@ -464,7 +474,7 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base
         f[4] += __uint_as_float(b1.x); f[5] += __uint_as_float(b1.y);
         f[6] += __uint_as_float(b1.z); f[7] += __uint_as_float(b1.w);
       } else if (p.has_bias && own_ok && n < p.H) {
-        // yShardType 1: the row picks the TP rank, hence the bias row.
+        // yShardType 1, rows of several TP ranks: each row its own bias row.
         float b[8];
         Out<T>::bias8(static_cast<const uint8_t*>(p.bias[sl * p.tp + t_own]) +
                           ((int64_t)e * p.H + n) * Out<T>::kBiasBytes,

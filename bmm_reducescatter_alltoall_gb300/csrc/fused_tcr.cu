@@ -8,7 +8,7 @@
 // tcgen05.mma.cta_group::2; the K loop runs over the tp shards (the
 // reduce-scatter sum, fp32, in t order) and 64-wide K blocks; the epilogue
 // adds the sender's bias, rounds once and stores each element at its
-// all-to-all destination (2-byte stores, rows of any alignment).
+// all-to-all destination (tcu_epilogue.cuh: rows of any alignment).
 //
 // TMA needs row pitches that are multiples of 16 bytes.  A row-major matrix
 // whose pitch is not is split into row classes: with n = the least power of

@@ -22,11 +22,12 @@
 //   warp 4       allocates 512 TMEM columns (two 128 x 256 fp32
 //                accumulators); its lane 0 issues tcgen05.mma (M=128, N=256,
 //                K=16) and commits stages and accumulators.
-//   warps 0..3   epilogue: tcgen05.ld of the warp's TMEM lane quarter, bias
-//                (scalar loads), one rounding, rows staged in shared memory,
-//                then each row written element by element (2-byte stores,
-//                consecutive lanes on consecutive elements), so rows of any
-//                alignment and type-0 chunks that straddle a TP rank are fine.
+//   warps 0..3   epilogue (tcu_epilogue.cuh): tcgen05.ld of the warp's TMEM
+//                lane quarter, bias, one rounding; each row segment staged
+//                in shared memory shifted to its destination's 16-byte phase
+//                and written with aligned vector stores (partial end chunks
+//                and segments that straddle a TP rank's chunk piecewise), so
+//                rows of any alignment are fine.
 // Every wait is bounded (about 4 s); a wait that runs out records
 // BRA_ERR_TIMEOUT in a device word and every role leaves its loop.
 #include <cstring>

@@ -36,7 +36,7 @@ struct TcParams {
   uint32_t b_lbo, b_sbo;         // B operand strides (bytes), N-major weight
   int b_kmajor;                  // weight stored transposed: B is K-major
   int y_elem;                    // output rows / pointers or bias not 16-byte aligned:
-                                 // the epilogue stores element by element
+                                 // the element-wise epilogue (tcu_epilogue.cuh)
 };
 
 // ---------------------------------------------------------------------------

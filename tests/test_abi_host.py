@@ -535,3 +535,36 @@ def test_overlapping_workspace_is_rejected_before_any_launch(lib):
     for base in (f.x[2] // 256 * 256, f.y[0] // 256 * 256 - 256, f.b[3] // 256 * 256):
         assert lib.bmm_rs_a2a_ex(x, w, b, *f.args, bra.FP16, y,
                                  ctypes.byref(_ws_opts(base, need)), None) == INVALID
+
+
+def test_python_options_carry_the_workspace():
+    """The binding passes a workspace tensor's pointer and byte size, and
+    refuses one that is not a contiguous CUDA tensor."""
+    import torch
+
+    class FakeCuda:                               # stands in for a CUDA tensor on the CPU
+        is_cuda = True
+
+        def __init__(self, n, es, contiguous=True):
+            self.n, self.es, self.c = n, es, contiguous
+
+        def is_contiguous(self):
+            return self.c
+
+        def data_ptr(self):
+            return 1 << 44
+
+        def numel(self):
+            return self.n
+
+        def element_size(self):
+            return self.es
+
+    o = bra._options(True, "packed", FakeCuda(1000, 4))
+    assert (o.transpose_weight, o.variant, o.workspace, o.workspace_bytes) == \
+        (1, bra.VARIANT_PACKED, 1 << 44, 4000)
+    assert bra._options(False, None).workspace is None
+    with pytest.raises(ValueError):
+        bra._options(False, None, torch.zeros(16, dtype=torch.uint8))        # a CPU tensor
+    with pytest.raises(ValueError):
+        bra._options(False, None, FakeCuda(16, 1, contiguous=False))

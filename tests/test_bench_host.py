@@ -26,3 +26,16 @@ def test_unfused_reference_matches_oracle(cfg):
     err = max(float(np.max(np.abs(o.numpy() - r))) for o, r in zip(out, ref))
     err /= max(float(np.max(np.abs(r))) for r in ref)
     assert err <= (2e-3 if cfg.dtype == "fp16" else 1e-2)
+
+
+def test_arguments_and_defaults():
+    """The driver's contract: no flags give N = 1, K/W within minutes, the
+    headline workloads; --workspace and the profiling switches parse."""
+    a = bench._args([])
+    assert (a.gpus, a.warmup, a.impl, a.fused, a.a2av) == (1, 3, "ours", bench.FUSED_NAME,
+                                                          bench.A2AV_NAME)
+    assert a.steps >= 1 and a.warmup >= 3 and not a.workspace
+    b = bench._args(["--workspace", "--fused", "ep8tp2_E8_C256_M4100_H4100_t0_bf16",
+                     "--steps", "3", "--e2e-steps", "0", "--indexed-calls", "0"])
+    assert b.workspace and b.steps == 3 and b.e2e_steps == 0 and b.indexed_calls == 0
+    assert b.fused in FUSED_CONFIGS

@@ -18,20 +18,29 @@ def _bits(ts):
                    (torch.int32 if t.element_size() == 4 else torch.int8)).cpu() for t in ts]
 
 
-@pytest.mark.parametrize("M,H", [(512, 768), (514, 774)])     # TMA kernel, row-class kernel
-def test_fused_plan_matches_the_one_shot_call(M, H):
+# TMA kernel, row-class kernel, packed variant (workspace)
+@pytest.mark.parametrize("M,H,packed", [(512, 768, False), (514, 774, False), (514, 774, True)])
+def test_fused_plan_matches_the_one_shot_call(M, H, packed):
     cfg = FusedConfig("pl", ep=4, tp=2, E=8, C=128, M=M, H=H, y_shard_type=1, dtype="fp16",
                       seed=3)
     inp = fused_inputs_host(cfg)
     d = {k: [u.cuda() for u in v] for k, v in inp.items()}
     args = (cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M, cfg.H, cfg.y_shard_type)
-    plan = bra.bmm_rs_a2a_plan(d["x"], d["w"], d["bias"], *args)
+    ws = None
+    if packed:
+        ys = bra.bmm_rs_a2a_infer_shape(*args)["y"]
+        probe = [torch.empty(ys, dtype=torch.float16, device="cuda") for _ in range(cfg.P)]
+        n = bra.bmm_rs_a2a_workspace_size(d["x"], d["w"], d["bias"], *args, probe)
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        assert bra.bmm_rs_a2a_variant(d["x"], d["w"], d["bias"], *args, probe,
+                                      workspace=ws) == bra.VARIANT_PACKED
+    plan = bra.bmm_rs_a2a_plan(d["x"], d["w"], d["bias"], *args, workspace=ws)
     for step in range(3):
         if step == 2:
             for x in d["x"]:
                 x.mul_(-0.5)                       # new values, same buffers
         got = _bits(plan.run())
-        ref = _bits(bra.bmm_rs_a2a(d["x"], d["w"], d["bias"], *args))
+        ref = _bits(bra.bmm_rs_a2a(d["x"], d["w"], d["bias"], *args, workspace=ws))
         torch.cuda.synchronize()
         assert all(torch.equal(a, b) for a, b in zip(got, ref)), step
     assert bra.fault_status() == 0

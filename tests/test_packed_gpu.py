@@ -181,3 +181,24 @@ def test_small_workspace_and_forced_variant_are_refused(monkeypatch):
     assert _need(cfg2, d2["x"], d2["w"], d2["bias"], False)[0] == 0
     out = _call(cfg2, d2["x"], d2["w"], d2["bias"], False, None, variant="packed")
     assert _rel_err(out, _oracle(cfg2, inp2)) <= TOL["fp16"]
+
+
+@pytest.mark.parametrize("case", [
+    (32, 32, 32, 2, 32 * 6, 32 * 5, 0, "fp16"),   # P = 1024: 2048 copies, eight repack launches
+    (2, 1, 2, 2, 16, 65535, 0, "bf16"),           # weight rows of 65535 elements (pitch 65536)
+    (2, 1, 2, 2, 65535, 16, 1, "fp16"),           # x rows of 65535 elements, 1024 K blocks
+])
+def test_packed_at_the_limits(case):
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("pkl", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=ep + tp + E + C + 1)
+    inp = fused_inputs_host(cfg)
+    ref = _oracle(cfg, inp)
+    d = _to_dev(inp)
+    need, probe = _need(cfg, d["x"], d["w"], d["bias"], False)
+    ws = _workspace(need)
+    assert bra.bmm_rs_a2a_variant(d["x"], d["w"], d["bias"], ep, tp, E, C, M, H, t, probe,
+                                  workspace=ws) == bra.VARIANT_PACKED
+    out = _call(cfg, d["x"], d["w"], d["bias"], False, ws)
+    err = _rel_err(out, ref)
+    assert err <= TOL[dt], f"{case}: rel err {err:.3e}"

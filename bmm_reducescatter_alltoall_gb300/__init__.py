@@ -303,9 +303,19 @@ def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
                            transpose_weight, variant, workspace).run(stream)
 
 
-def bmm_rs_a2a_workspace_size(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
+def bmm_rs_a2a_workspace_size(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out=None,
                               transpose_weight: bool = False) -> int:
-    """Bytes of workspace the packed variant needs for these tensors (0: none)."""
+    """Bytes of workspace the packed variant needs for these tensors (0: none).
+
+    The size depends on x and weight (their shapes and whether each pointer
+    is 16-byte aligned); `out` only enters the check that the packed variant
+    can take the call (element-aligned outputs).  Without `out`, freshly
+    allocated outputs stand in for it.
+    """
+    if out is None:
+        torch = _torch()
+        ys = bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type)["y"]
+        out = [torch.empty(ys, dtype=x[0].dtype, device=x[0].device) for _ in range(ep * tp)]
     xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
                                      transpose_weight)
     opts = _options(transpose_weight, None)

@@ -20,8 +20,10 @@ _BF16_P = 8                                   # significant bits
 
 
 def round_fp16(v: np.ndarray) -> np.ndarray:
-    """float64 array of the fp16-nearest values (ties to even)."""
-    return np.asarray(v, dtype=np.float64).astype(np.float16).astype(np.float64)
+    """float64 array of the fp16-nearest values (ties to even); magnitudes past
+    the fp16 range become infinities, as IEEE rounding gives."""
+    with np.errstate(over="ignore"):
+        return np.asarray(v, dtype=np.float64).astype(np.float16).astype(np.float64)
 
 
 def round_bf16(v: np.ndarray) -> np.ndarray:

@@ -8,6 +8,7 @@ and with `bmm_rs_a2a_variant`, which runs the same validation without
 launching, for calls that would be accepted.
 """
 import ctypes
+import pathlib
 import itertools
 import os
 import re
@@ -31,7 +32,7 @@ def lib():
 
 
 def _declared_functions():
-    src = open(HEADER).read()
+    src = pathlib.Path(HEADER).read_text()
     return re.findall(r"^BRA_API\s+[\w\s\*]+?\b(\w+)\s*\(", src, flags=re.M)
 
 
@@ -420,7 +421,7 @@ def test_options_struct_layout():
     assert ctypes.sizeof(F) == 32 and ctypes.alignment(F) == 8
     assert [getattr(F, n).offset for n in ("transpose_weight", "variant", "reserved",
                                            "workspace", "workspace_bytes")] == [0, 4, 8, 16, 24]
-    src = open(HEADER).read()
+    src = pathlib.Path(HEADER).read_text()
     body = src[src.index("int32_t transpose_weight;"):src.index("} bra_fused_options;")]
     decls = re.findall(r"^\s*(int32_t|void\*|int64_t)\s+(\w+)", body, flags=re.M)
     assert decls == [("int32_t", "transpose_weight"), ("int32_t", "variant"),

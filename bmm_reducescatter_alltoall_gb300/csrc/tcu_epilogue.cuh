@@ -53,10 +53,11 @@ constexpr int kUStageBytes = 32 * kURowStride + 64 * 4;
 // kernel parameter block with bias[], y[], s0, El, C, H, tp, type, has_bias
 // and rows.  Per 64-column segment: phase 1, lane = row: bias in fp32, one
 // rounding, pairs packed and staged shifted by the run's delta; phase 2,
-// every lane a (row, 16-byte chunk) pair: aligned vector stores, and at most
-// three aligned 8/4/2-byte stores for each partial end chunk; phase 3:
-// segments that cross a boundary, lanes on consecutive columns.
-// kPrefetch: load the tile's bias up front and overlap three store passes
+// the runs' seven whole middle chunks with every lane a (row, chunk) pair,
+// then each lane its own run's two end chunks (at most three aligned
+// 8/4/2-byte stores each); phase 3: segments that cross a boundary, lanes on
+// consecutive columns.
+// kPrefetch: load the tile's bias up front and unroll the store passes
 // (faster where the epilogue warps have the SM sub-partitions' issue slots
 // and registers to themselves; the kernels whose loader warps share them
 // pass false).
@@ -156,7 +157,7 @@ __device__ __forceinline__ void epilogue_rows_u(const P& p, uint32_t t_base, int
       bool one_run = true;
       if (p.type == 0) {
         const int t0 = nc / Hp;
-        one_run = (nc + 63) / Hp == t0;
+        one_run = nc + 63 < (t0 + 1) * Hp;
         d = d_own + t0;
         off = off_own + (nc - t0 * Hp);
       }
@@ -191,59 +192,65 @@ __device__ __forceinline__ void epilogue_rows_u(const P& p, uint32_t t_base, int
       }
       w[i] = (uint32_t)Elt<T>::cvt(f0) | ((uint32_t)Elt<T>::cvt(f1) << 16);
     }
-    // stage: buffer element k holds column k - delta (delta = 0 off the fast path)
+    // stage: buffer element k holds column k - delta (delta = 0 off the fast
+    // path).  Word q + i of the row buffer (q = delta / 2) joins w[i-1] and
+    // w[i] by a funnel shift of 16 bits for an odd delta and of 32 (w[i]
+    // alone) for an even one, so every lane runs the same instructions.
     uint32_t* bw = reinterpret_cast<uint32_t*>(my_buf);
     const int q = delta >> 1;
-    if (delta & 1) {
-      bw[q] = w[0] << 16;
+    const uint32_t sh = (delta & 1) ? 16u : 32u;
+    bw[q] = __funnelshift_rc(0u, w[0], sh);
 #pragma unroll
-      for (int i = 1; i < 32; ++i) bw[q + i] = __funnelshift_r(w[i - 1], w[i], 16);
-      bw[q + 32] = w[31] >> 16;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) bw[q + i] = w[i];
-    }
+    for (int i = 1; i < 32; ++i) bw[q + i] = __funnelshift_rc(w[i - 1], w[i], sh);
+    bw[q + 32] = __funnelshift_rc(w[31], 0u, sh);
     __syncwarp();
-    // phase 2: runs; 32 rows x 9 chunks over nine passes of the warp.  A
-    // row's metadata travels as one word: its run's 16-byte aligned start
-    // with delta in the low bits (0: not on the fast path).
+    // phase 2a: a run covers buffer bytes [2 delta, 2 delta + 128), so its
+    // chunks 1..7 are always whole 16-byte vectors: 32 rows x 7 chunks, seven
+    // passes of the warp.  A row's metadata travels as one word: its run's
+    // 16-byte aligned start with delta in the low bits (0: off the fast path).
     const uint64_t meta = fast ? ((uint64_t)abase | (uint64_t)delta) : 0ull;
-#pragma unroll(kPrefetch ? 3 : 1)
-    for (int pass = 0; pass < 9; ++pass) {
+#pragma unroll(kPrefetch ? 7 : 1)
+    for (int pass = 0; pass < 7; ++pass) {
       const int idx = pass * 32 + lane;
-      const int rr = idx / 9, k = idx - 9 * rr;
+      const int rr = idx / 7, k = 1 + idx - 7 * rr;
       const uint32_t mlo = __shfl_sync(0xffffffffu, (uint32_t)meta, rr);
       const uint32_t mhi = __shfl_sync(0xffffffffu, (uint32_t)(meta >> 32), rr);
       const uint64_t m = ((uint64_t)mhi << 32) | mlo;
-      const int lo = 2 * (int)(m & 7);          // the run is buffer bytes [lo, lo + 128)
-      // chunk 8 only holds a tail
-      if (m == 0 || (k == 8 && lo == 0)) continue;
-      uint8_t* ab = reinterpret_cast<uint8_t*>(m & ~(uint64_t)15);
-      const uint4 val = *reinterpret_cast<const uint4*>(stage + rr * kURowStride + 16 * k);
-      uint8_t* dst = ab + 16 * k;
-      if (lo == 0 || (k > 0 && k < 8)) {
-        *reinterpret_cast<uint4*>(dst) = val;
-        continue;
+      if (m != 0) {
+        const uint4 val = *reinterpret_cast<const uint4*>(stage + rr * kURowStride + 16 * k);
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(m & ~(uint64_t)15) + 16 * k) = val;
       }
-      auto word = [&](int i) { return i == 0 ? val.x : i == 1 ? val.y : i == 2 ? val.z : val.w; };
-      if (k == 0) {                             // head: bytes [lo, 16)
-        int b = lo;
+    }
+    // phase 2b: the end chunks of the lane's own run: chunk 0 (whole when
+    // delta is 0, else its bytes [2 delta, 16)) and chunk 8 (its bytes
+    // [0, 2 delta) when delta > 0), with at most three aligned 8/4/2-byte
+    // stores each.
+    if (fast) {
+      uint8_t* ab = reinterpret_cast<uint8_t*>(abase);
+      const int lo = 2 * delta;
+      const uint4 v0 = *reinterpret_cast<const uint4*>(my_buf);
+      if (lo == 0) {
+        *reinterpret_cast<uint4*>(ab) = v0;
+      } else {
+        auto w0 = [&](int i) { return i == 0 ? v0.x : i == 1 ? v0.y : i == 2 ? v0.z : v0.w; };
+        int b = lo;                                 // head: bytes [lo, 16)
         if (b & 2) {
-          *reinterpret_cast<uint16_t*>(dst + b) = (uint16_t)(word(b >> 2) >> 16);
+          *reinterpret_cast<uint16_t*>(ab + b) = (uint16_t)(w0(b >> 2) >> 16);
           b += 2;
         }
         if (b & 4) {
-          *reinterpret_cast<uint32_t*>(dst + b) = word(b >> 2);
+          *reinterpret_cast<uint32_t*>(ab + b) = w0(b >> 2);
           b += 4;
         }
-        if (b & 8)
-          *reinterpret_cast<uint2*>(dst + b) = make_uint2(word(2), word(3));
-      } else {                                  // tail: bytes [0, lo)
-        if (lo & 8) *reinterpret_cast<uint2*>(dst) = make_uint2(word(0), word(1));
+        if (b & 8) *reinterpret_cast<uint2*>(ab + b) = make_uint2(v0.z, v0.w);
+        const uint4 v8 = *reinterpret_cast<const uint4*>(my_buf + 128);
+        auto w8 = [&](int i) { return i == 0 ? v8.x : i == 1 ? v8.y : i == 2 ? v8.z : v8.w; };
+        uint8_t* tl = ab + 128;                     // tail: bytes [0, lo)
+        if (lo & 8) *reinterpret_cast<uint2*>(tl) = make_uint2(v8.x, v8.y);
         const int b4 = lo & 8;
-        if (lo & 4) *reinterpret_cast<uint32_t*>(dst + b4) = word(b4 >> 2);
+        if (lo & 4) *reinterpret_cast<uint32_t*>(tl + b4) = w8(b4 >> 2);
         const int b2 = lo & 12;
-        if (lo & 2) *reinterpret_cast<uint16_t*>(dst + b2) = (uint16_t)word(b2 >> 2);
+        if (lo & 2) *reinterpret_cast<uint16_t*>(tl + b2) = (uint16_t)w8(b2 >> 2);
       }
     }
     // phase 3: valid rows off the fast path, element by element

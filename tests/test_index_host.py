@@ -202,3 +202,63 @@ def test_repack_reads_inside_the_row_and_copies_exactly(length, off):
         np.testing.assert_array_equal(halves[:length], elems[row])
         if length & 1:
             assert halves[length] == 0
+
+
+def _element_epilogue_stores(delta):
+    """(offset, size) of every global store the element-wise epilogue makes
+    for one run, in bytes from the run's 16-byte aligned start, as
+    tcu_epilogue.cuh computes them: chunks 1..7 whole, chunk 0 whole or its
+    head [2 delta, 16), chunk 8's tail [0, 2 delta) at offset 128."""
+    lo = 2 * delta
+    stores = [(16 * k, 16) for k in range(1, 8)]
+    if lo == 0:
+        stores.append((0, 16))
+        return stores
+    b = lo
+    if b & 2:
+        stores.append((b, 2))
+        b += 2
+    if b & 4:
+        stores.append((b, 4))
+        b += 4
+    if b & 8:
+        stores.append((b, 8))
+    if lo & 8:
+        stores.append((128, 8))
+    if lo & 4:
+        stores.append((128 + (lo & 8), 4))
+    if lo & 2:
+        stores.append((128 + (lo & 12), 2))
+    return stores
+
+
+@pytest.mark.parametrize("delta", range(8))
+def test_element_epilogue_writes_each_run_byte_once(delta):
+    lo = 2 * delta
+    written = np.zeros(160, dtype=np.int64)
+    for off, size in _element_epilogue_stores(delta):
+        assert off % size == 0                       # every store aligned to its size
+        assert off + size <= 144                     # inside the staged row buffer
+        written[off:off + size] += 1
+    want = np.zeros(160, dtype=np.int64)
+    want[lo:lo + 128] = 1                            # the run, and nothing else
+    np.testing.assert_array_equal(written, want)
+
+
+@pytest.mark.parametrize("delta", range(8))
+def test_element_epilogue_staging_shift(delta):
+    """Staged word q + i = funnel-shift of (w[i-1], w[i]) by 16 (odd delta)
+    or 32 (even): buffer element k holds column k - delta."""
+    w = [(2 * i) | ((2 * i + 1) << 16) for i in range(32)]      # columns 0..63, packed
+    sh = 16 if delta & 1 else 32
+    fsr = lambda lo_, hi_, s: (((hi_ << 32) | lo_) >> min(s, 32)) & 0xFFFFFFFF
+    q = delta >> 1
+    buf = [None] * 36
+    buf[q] = fsr(0, w[0], sh)
+    for i in range(1, 32):
+        buf[q + i] = fsr(w[i - 1], w[i], sh)
+    buf[q + 32] = fsr(w[31], 0, sh)
+    elems = []
+    for wd in buf:
+        elems += [None, None] if wd is None else [wd & 0xFFFF, wd >> 16]
+    assert elems[delta:delta + 64] == list(range(64))

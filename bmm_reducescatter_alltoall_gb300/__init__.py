@@ -196,6 +196,8 @@ def _options(transpose_weight: bool, variant, workspace=None) -> "FusedOptions":
     o = FusedOptions()
     o.transpose_weight = 1 if transpose_weight else 0
     o.variant = _VARIANTS[variant]
+    if isinstance(workspace, str):
+        raise ValueError('workspace="auto" is taken by bmm_rs_a2a and bmm_rs_a2a_plan only')
     if workspace is not None:
         if not (workspace.is_cuda and workspace.is_contiguous()):
             raise ValueError("workspace must be a contiguous CUDA tensor")
@@ -277,6 +279,18 @@ def bmm_rs_a2a_plan(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep:
         out = [torch.empty(ys, dtype=x[0].dtype, device=x[0].device) for _ in range(ep * tp)]
     xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
                                      transpose_weight)
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError('workspace must be a CUDA tensor, None or "auto"')
+        # torch's caching allocator provides the scratch memory the library
+        # asks for (the library itself allocates nothing); none when the
+        # operands are already TMA-ready
+        n = library().bmm_rs_a2a_workspace_size(
+            xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp,
+            ctypes.byref(_options(transpose_weight, None)))
+        if n < 0:
+            raise BraError(-n, "bmm_rs_a2a_workspace_size")
+        workspace = (torch.empty(n, dtype=torch.uint8, device=x[0].device) if n > 0 else None)
     opts = _options(transpose_weight, variant, workspace)
     args = (xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp, ctypes.byref(opts))
     return Plan(library().bmm_rs_a2a_ex, args, "bmm_rs_a2a", out,
@@ -294,9 +308,10 @@ def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
     transpose_weight: weight[r] is stored as (El, H, Kp) instead of
     (El, Kp, H).  variant: None/"auto", "tc", "tc2", "tcr", "tcu", "simt" or
     "packed".  workspace: an optional contiguous CUDA tensor of at least
-    bmm_rs_a2a_workspace_size(...) bytes; given one, shapes whose x or weight
-    rows lack a 16-byte pitch run the packed variant (operands repacked into
-    it, then the TMA kernel).  Returns out.  Asynchronous on `stream` (default: current stream).  For
+    bmm_rs_a2a_workspace_size(...) bytes, or "auto" to have one of that size
+    taken from torch's allocator; given one, shapes whose x or weight rows
+    lack a 16-byte pitch run the packed variant (operands repacked into it,
+    then the TMA kernel).  Returns out.  Asynchronous on `stream` (default: current stream).  For
     repeated calls on the same buffers, bmm_rs_a2a_plan skips the checks.
     """
     return bmm_rs_a2a_plan(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,

@@ -202,3 +202,29 @@ def test_packed_at_the_limits(case):
     out = _call(cfg, d["x"], d["w"], d["bias"], False, ws)
     err = _rel_err(out, ref)
     assert err <= TOL[dt], f"{case}: rel err {err:.3e}"
+
+
+def test_auto_workspace():
+    """workspace="auto": the binding takes the size the library asks for from
+    torch's allocator (none for TMA-ready operands) and the packed variant runs."""
+    cfg = FusedConfig("pka", ep=2, tp=2, E=4, C=40, M=130, H=70, y_shard_type=0, dtype="fp16",
+                      seed=9)
+    inp = fused_inputs_host(cfg)
+    d = _to_dev(inp)
+    plan = bra.bmm_rs_a2a_plan(d["x"], d["w"], d["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M,
+                               cfg.H, cfg.y_shard_type, workspace="auto")
+    ws = plan._keep[-1]
+    need, _ = _need(cfg, d["x"], d["w"], d["bias"], False)
+    assert ws is not None and ws.numel() == need
+    out = plan.run()
+    torch.cuda.synchronize()
+    assert bra.fault_status() == 0
+    assert _rel_err(out, _oracle(cfg, inp)) <= TOL["fp16"]
+    cfg2 = cfg.replace(M=256, H=512)
+    d2 = _to_dev(fused_inputs_host(cfg2))
+    plan2 = bra.bmm_rs_a2a_plan(d2["x"], d2["w"], d2["bias"], cfg2.ep, cfg2.tp, cfg2.E, cfg2.C,
+                                cfg2.M, cfg2.H, cfg2.y_shard_type, workspace="auto")
+    assert plan2._keep[-1] is None
+    with pytest.raises(ValueError):
+        bra.bmm_rs_a2a(d2["x"], d2["w"], d2["bias"], cfg2.ep, cfg2.tp, cfg2.E, cfg2.C, cfg2.M,
+                       cfg2.H, cfg2.y_shard_type, workspace="big")

@@ -125,11 +125,14 @@ typedef enum {
  *   BRA_ERR_CUDA     the launch failed (cudaGetLastError).
  * Variant: when the operands' rows and pointers are 16-byte aligned (Kp % 8
  * == 0, the weight's row length H -- Kp when transposed -- % 8 == 0, x and
- * weight 16-byte aligned) a TMA-fed tensor-core kernel runs: the CTA-pair kernel when the problem has at least 64 output
- * tiles of 256 x 256 and more than 128 token rows (ep*C) per expert group,
- * else the one-CTA kernel.  Its epilogue stores 16-byte vectors when the
+ * weight 16-byte aligned) a TMA-fed tensor-core kernel runs: the CTA-pair
+ * kernel when the problem has at least 64 output tiles of 256 x 256 and
+ * more than 128 token rows (ep*C) per expert group, else the one-CTA
+ * kernel.  Its epilogue stores 16-byte vectors from 16-byte rows when the
  * outputs and bias are 16-byte aligned (and Hp % 8 == 0 for yShardType 0),
- * else element by element (outputs and bias element-aligned).  Other shapes
+ * else it stages each row segment at its destination's 16-byte phase and
+ * stores the aligned part as vectors (outputs and bias element-aligned).
+ * Other shapes
  * with element-aligned pointers run, given a workspace (bmm_rs_a2a_ex), the
  * packed variant: those operands repacked, then the same TMA kernel.
  * Without a workspace they run the CTA-pair tensor-core kernel fed by
@@ -177,10 +180,12 @@ typedef struct {
  * bmm_rs_a2a_ex -- bmm_rs_a2a with options (NULL opts = all defaults, same
  * as bmm_rs_a2a).  Errors as bmm_rs_a2a, plus BRA_ERR_INVALID for an
  * unknown variant, a non-zero reserved field, a workspace that is not
- * 256-byte aligned, smaller than bmm_rs_a2a_workspace_size, negative in size
- * or overlapping an input or output (checked when a workspace is given and
+ * 256-byte aligned, a negative workspace_bytes or a non-zero one with a NULL
+ * workspace (always checked), a workspace smaller than
+ * bmm_rs_a2a_workspace_size or overlapping an input or output (checked when
  * the packed variant would use it), and BRA_ERR_UNSUPPORTED when a forced
- * tensor-core variant cannot take the shape or alignment.
+ * tensor-core variant cannot take the shape or alignment, or the packed
+ * variant is forced without a workspace where one is needed.
  * With a workspace of at least bmm_rs_a2a_workspace_size bytes, AUTO takes
  * BRA_VARIANT_PACKED for every shape whose x or weight rows lack a 16-byte
  * pitch (and whose pointers are element-aligned): the repack kernel copies

@@ -38,8 +38,8 @@ _lib = None
 class FusedOptions(ctypes.Structure):
     """bra_fused_options of the C header."""
     _fields_ = [("transpose_weight", ctypes.c_int32), ("variant", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("x_pitch", ctypes.c_int32), ("w_pitch", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64)]
 
 
 class BraError(RuntimeError):
@@ -157,6 +157,44 @@ def _checked_ptrs(ts, what: str, dtype, shape=None):
     return [t.data_ptr() for t in ts]
 
 
+def _pitched_ptrs(ts, what: str, dtype, shape):
+    """Data pointers and the shared row pitch (elements; 0 = dense) of 3-D
+    CUDA tensors of `shape` that are contiguous or row-pitched: strides
+    (shape[1] * pitch, pitch, 1) with pitch >= shape[2], the same pitch for
+    every entry (a (d0, d1, pitch) buffer viewed as (d0, d1, d2))."""
+    try:
+        if all(t.is_cuda and t.dtype is dtype and t.is_contiguous() and t.shape == shape
+               for t in ts):
+            return [t.data_ptr() for t in ts], 0
+    except AttributeError:
+        pass
+    torch = _torch()
+    pitch = None
+    for r, t in enumerate(ts):
+        name = f"{what}[{r}]"
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+        _shape_check(t, shape, name)
+        if t.is_contiguous():
+            p = shape[2]
+        else:
+            s0, s1, s2 = t.stride()
+            p = s1
+            if not (s2 == 1 and shape[1] > 1 and p >= shape[2] and
+                    (shape[0] == 1 or s0 == shape[1] * p)):
+                raise ValueError(f"{name} must be contiguous or row-pitched (strides "
+                                 f"(d1 * pitch, pitch, 1), pitch >= {shape[2]}); got {t.stride()}")
+        if pitch is None:
+            pitch = p
+        elif p != pitch:
+            raise ValueError(f"every {what} entry must have the same row pitch")
+    return [t.data_ptr() for t in ts], (0 if pitch == shape[2] else pitch)
+
+
 def _fused_dtype(dt) -> int:
     torch = _torch()
     if dt == torch.float16:
@@ -190,12 +228,13 @@ _VARIANTS = {None: 0, "auto": 0, "tc": VARIANT_TC, "tc2": VARIANT_TC2, "simt": V
              "tcu": VARIANT_TCU, "tcr": VARIANT_TCR, "packed": VARIANT_PACKED}
 
 
-def _options(transpose_weight: bool, variant, workspace=None) -> "FusedOptions":
+def _options(transpose_weight: bool, variant, workspace=None, pitches=(0, 0)) -> "FusedOptions":
     if variant not in _VARIANTS:
         raise ValueError(f"variant must be one of {sorted(k for k in _VARIANTS if k)}")
     o = FusedOptions()
     o.transpose_weight = 1 if transpose_weight else 0
     o.variant = _VARIANTS[variant]
+    o.x_pitch, o.w_pitch = pitches
     if isinstance(workspace, str):
         raise ValueError('workspace="auto" is taken by bmm_rs_a2a and bmm_rs_a2a_plan only')
     if workspace is not None:
@@ -216,8 +255,8 @@ def _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
     if transpose_weight:                      # stored as (El, H, Kp)
         wshape = (wshape[0], wshape[2], wshape[1])
     dt = x[0].dtype
-    xs = _checked_ptrs(x, "x", dt, shapes["x"])
-    ws = _checked_ptrs(weight, "weight", dt, wshape)
+    xs, xpitch = _pitched_ptrs(x, "x", dt, shapes["x"])
+    ws, wpitch = _pitched_ptrs(weight, "weight", dt, tuple(wshape))
     bptr = None
     if bias is not None:
         if len(bias) != P:
@@ -241,7 +280,8 @@ def _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
     if len(out) != P:
         raise ValueError(f"out needs ep*tp = {P} entries")
     ys = _checked_ptrs(out, "out", dt, shapes["y"])
-    return _ptr_array(xs), _ptr_array(ws), bptr, _ptr_array(ys), _fused_dtype(dt)
+    return (_ptr_array(xs), _ptr_array(ws), bptr, _ptr_array(ys), _fused_dtype(dt),
+            (xpitch, wpitch))
 
 
 class Plan:
@@ -277,8 +317,8 @@ def bmm_rs_a2a_plan(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep:
     if out is None:
         ys = bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type)["y"]
         out = [torch.empty(ys, dtype=x[0].dtype, device=x[0].device) for _ in range(ep * tp)]
-    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
-                                     transpose_weight)
+    xp, wp, bp, yp, dt, pitches = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type,
+                                              out, transpose_weight)
     if isinstance(workspace, str):
         if workspace != "auto":
             raise ValueError('workspace must be a CUDA tensor, None or "auto"')
@@ -287,11 +327,11 @@ def bmm_rs_a2a_plan(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep:
         # operands are already TMA-ready
         n = library().bmm_rs_a2a_workspace_size(
             xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp,
-            ctypes.byref(_options(transpose_weight, None)))
+            ctypes.byref(_options(transpose_weight, None, None, pitches)))
         if n < 0:
             raise BraError(-n, "bmm_rs_a2a_workspace_size")
         workspace = (torch.empty(n, dtype=torch.uint8, device=x[0].device) if n > 0 else None)
-    opts = _options(transpose_weight, variant, workspace)
+    opts = _options(transpose_weight, variant, workspace, pitches)
     args = (xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp, ctypes.byref(opts))
     return Plan(library().bmm_rs_a2a_ex, args, "bmm_rs_a2a", out,
                 (x, weight, bias, opts, xp, wp, bp, yp, workspace))
@@ -331,9 +371,9 @@ def bmm_rs_a2a_workspace_size(x, weight, bias, ep, tp, E, C, M, H, y_shard_type,
         torch = _torch()
         ys = bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, y_shard_type)["y"]
         out = [torch.empty(ys, dtype=x[0].dtype, device=x[0].device) for _ in range(ep * tp)]
-    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
-                                     transpose_weight)
-    opts = _options(transpose_weight, None)
+    xp, wp, bp, yp, dt, pitches = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type,
+                                              out, transpose_weight)
+    opts = _options(transpose_weight, None, None, pitches)
     n = library().bmm_rs_a2a_workspace_size(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt,
                                             yp, ctypes.byref(opts))
     if n < 0:
@@ -345,9 +385,9 @@ def bmm_rs_a2a_variant(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
                        transpose_weight: bool = False, variant: Optional[str] = None,
                        workspace=None) -> int:
     """The VARIANT_* constant bmm_rs_a2a would run; raises BraError if rejected."""
-    xp, wp, bp, yp, dt = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
-                                     transpose_weight)
-    opts = _options(transpose_weight, variant, workspace)
+    xp, wp, bp, yp, dt, pitches = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type,
+                                              out, transpose_weight)
+    opts = _options(transpose_weight, variant, workspace, pitches)
     v = library().bmm_rs_a2a_variant(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp,
                                      ctypes.byref(opts))
     if v < 0:

@@ -38,6 +38,7 @@ struct Range {
 };
 
 void tensor_ranges(const bra::FusedProblem& p, std::vector<Range>* all);
+int apply_pitches(const bra_fused_options* opts, bra::FusedProblem* p);
 
 // Validation in the order of CheckParams: null pointers, dtype, attributes,
 // shapes; then the aliasing rule.  On success fills `prob`.
@@ -49,8 +50,7 @@ int validate_fused(const void* const x[], const void* const weight[],
   if (!x || !weight || !out) return BRA_ERR_NULLPTR;
   if (dtype != BRA_FP16 && dtype != BRA_BF16) return BRA_ERR_INVALID;
   if (opts) {
-    for (int k = 0; k < 2; ++k)
-      if (opts->reserved[k] != 0) return BRA_ERR_INVALID;
+    if (opts->x_pitch < 0 || opts->w_pitch < 0) return BRA_ERR_INVALID;
     if (opts->variant != BRA_VARIANT_AUTO && opts->variant != BRA_VARIANT_TC &&
         opts->variant != BRA_VARIANT_TC2 && opts->variant != BRA_VARIANT_SIMT &&
         opts->variant != BRA_VARIANT_TCU && opts->variant != BRA_VARIANT_TCR &&
@@ -84,6 +84,11 @@ int validate_fused(const void* const x[], const void* const weight[],
   prob->H = (int)H;
   prob->type = (int)type;
   prob->dtype = dtype;
+  prob->wt = (opts && opts->transpose_weight) ? 1 : 0;
+  prob->xp = (int)Kp;
+  prob->wp = prob->wt ? (int)Kp : (int)H;
+  rc = apply_pitches(opts, prob);
+  if (rc != BRA_OK) return rc;
   // Outputs may overlap nothing.  Sorted by start, a pair (a before b)
   // overlaps iff b.lo < a.hi; track the largest end of every earlier range
   // and of every earlier output.
@@ -98,11 +103,26 @@ int validate_fused(const void* const x[], const void* const weight[],
     max_hi_all = std::max(max_hi_all, a.hi);
     if (a.out) max_hi_out = std::max(max_hi_out, a.hi);
   }
-
-  prob->wt = (opts && opts->transpose_weight) ? 1 : 0;
-  prob->xp = (int)Kp;
-  prob->wp = prob->wt ? (int)Kp : (int)H;
   return BRA_OK;
+}
+
+// Caller pitches (elements; 0 = dense): each at least its row length.
+int apply_pitches(const bra_fused_options* opts, bra::FusedProblem* p) {
+  if (!opts) return BRA_OK;
+  const int wlen = p->wt ? p->Kp : p->H;
+  if (opts->x_pitch != 0) {
+    if (opts->x_pitch < p->Kp) return BRA_ERR_INVALID;
+    p->xp = opts->x_pitch;
+  }
+  if (opts->w_pitch != 0) {
+    if (opts->w_pitch < wlen) return BRA_ERR_INVALID;
+    p->wp = opts->w_pitch;
+  }
+  return BRA_OK;
+}
+
+bool pitched(const bra::FusedProblem& p) {
+  return p.xp != p.Kp || p.wp != (p.wt ? p.Kp : p.H);
 }
 
 // Byte ranges of every input and output of a validated problem.
@@ -111,7 +131,12 @@ void tensor_ranges(const bra::FusedProblem& p, std::vector<Range>* all) {
   const int64_t El = p.El, Kp = p.Kp, H = p.H, C = p.C, E = El * p.ep;
   const int64_t bes = p.dtype == BRA_FP16 ? 2 : 4;
   const int64_t Hb = p.type == 0 ? H / p.tp : H;
-  const int64_t xb = El * p.ep * C * Kp * 2, wb = El * Kp * H * 2, bb = El * Hb * bes;
+  // pitched operands: El * rows rows `pitch` elements apart, the last one
+  // ending at its row length
+  const int64_t xrows = El * p.ep * C, wrows = El * (p.wt ? H : Kp);
+  const int64_t wlen = p.wt ? Kp : H;
+  const int64_t xb = ((xrows - 1) * p.xp + Kp) * 2, wb = ((wrows - 1) * p.wp + wlen) * 2;
+  const int64_t bb = El * Hb * bes;
   const int64_t yb = (p.type == 0 ? E * C * (H / p.tp) : E * (C / p.tp) * H) * 2;
   for (int64_t r = 0; r < P; ++r) {
     all->push_back({(uintptr_t)p.x[r], (uintptr_t)p.x[r] + (uintptr_t)xb, false});
@@ -205,6 +230,13 @@ int choose_variant(const bra::FusedProblem& p, const bra_fused_options* opts) {
   const bool tc_ok = bra::fused_tc_eligible(p);
   const bool tcu_ok = bra::fused_tcu_eligible(p);
   const bool tcr_ok = bra::fused_tcr_eligible(p);
+  // Caller-pitched operands: the TMA kernels only (the other kernels and the
+  // repack read dense rows).
+  if (pitched(p)) {
+    if (!tc_ok) return -BRA_ERR_UNSUPPORTED;
+    if (f == BRA_VARIANT_TC || f == BRA_VARIANT_TC2) return f;
+    return f == BRA_VARIANT_AUTO ? tma_kernel_for(p) : -BRA_ERR_UNSUPPORTED;
+  }
   if (f == BRA_VARIANT_SIMT) return BRA_VARIANT_SIMT;
   if (f == BRA_VARIANT_TC || f == BRA_VARIANT_TC2) return tc_ok ? f : -BRA_ERR_UNSUPPORTED;
   if (f == BRA_VARIANT_TCU) return tcu_ok ? f : -BRA_ERR_UNSUPPORTED;
@@ -468,7 +500,7 @@ int64_t bmm_rs_a2a_workspace_size(const void* const x[], const void* const weigh
   const int rc = validate_fused(x, weight, bias, ep, tp, E, C, M, H, yShardType, dtype, out, &o,
                                 &p);
   if (rc != BRA_OK) return -rc;
-  if (bra::fused_tc_eligible(p)) return 0;
+  if (bra::fused_tc_eligible(p) || pitched(p)) return 0;
   const PackPlan q = pack_plan(p);
   return q.ok ? q.total : 0;
 }

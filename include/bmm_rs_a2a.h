@@ -163,7 +163,16 @@ typedef struct {
   /* BRA_VARIANT_AUTO (0) or a bra_variant to force; takes precedence over
    * the BRA_FORCE_VARIANT environment variable. */
   int32_t variant;
-  int32_t reserved[2];
+  /* Row pitches, in elements, of x[r] (rows of Kp) and weight[r] (rows of
+   * H, or of Kp when transposed); 0 = dense (pitch = row length).  A pitch
+   * must be at least the row length; the tensor is then El * rows rows
+   * that many elements apart (the layout of a (El, rows, pitch) buffer
+   * viewed as (El, rows, length)), and the elements between a row's end and
+   * the next row are never read.  Pitched operands must be TMA-ready (pitch
+   * a multiple of 8 elements, pointers 16-byte aligned) and run on the TMA
+   * kernels with no copy; otherwise the call returns BRA_ERR_UNSUPPORTED. */
+  int32_t x_pitch;
+  int32_t w_pitch;
   /* Device memory the call may use as scratch, in the manner of the second
    * call of the two-phase aclnn interface ([CANN] §调用说明: the workspace
    * and its size).  NULL with workspace_bytes 0: no workspace.  Only
@@ -179,7 +188,8 @@ typedef struct {
 /*
  * bmm_rs_a2a_ex -- bmm_rs_a2a with options (NULL opts = all defaults, same
  * as bmm_rs_a2a).  Errors as bmm_rs_a2a, plus BRA_ERR_INVALID for an
- * unknown variant, a non-zero reserved field, a workspace that is not
+ * unknown variant, a negative pitch or one below its row length, a
+ * workspace that is not
  * 256-byte aligned, a negative workspace_bytes or a non-zero one with a NULL
  * workspace (always checked), a workspace smaller than
  * bmm_rs_a2a_workspace_size or overlapping an input or output (checked when

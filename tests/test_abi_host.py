@@ -279,7 +279,7 @@ def test_options_select_the_variant_and_are_checked(lib, monkeypatch):
     bad.variant = 9
     assert _variant(lib, g, opts=bad) == -INVALID
     bad = bra._options(False, None)
-    bad.reserved[1] = 1
+    bad.x_pitch = -8
     assert _variant(lib, g, opts=bad) == -INVALID
     x, w, b, y = g.arrays()
     assert lib.bmm_rs_a2a_ex(x, w, b, 8, 4, 64, 512, 8192, 4096, 1, bra.FP16, y,
@@ -415,17 +415,18 @@ def test_wait_selftest_argument_checks(lib):
 # --------------------------------------------------------------------------
 
 def test_options_struct_layout():
-    """bra_fused_options: two int32 fields, two reserved int32, then the
-    workspace pointer and its int64 size (32 bytes, 8-byte aligned)."""
+    """bra_fused_options: four int32 fields (layout, variant, the two row
+    pitches), then the workspace pointer and its int64 size (32 bytes,
+    8-byte aligned)."""
     F = bra.FusedOptions
     assert ctypes.sizeof(F) == 32 and ctypes.alignment(F) == 8
-    assert [getattr(F, n).offset for n in ("transpose_weight", "variant", "reserved",
-                                           "workspace", "workspace_bytes")] == [0, 4, 8, 16, 24]
+    assert [getattr(F, n).offset for n in ("transpose_weight", "variant", "x_pitch", "w_pitch",
+                                           "workspace", "workspace_bytes")] == [0, 4, 8, 12, 16, 24]
     src = pathlib.Path(HEADER).read_text()
     body = src[src.index("int32_t transpose_weight;"):src.index("} bra_fused_options;")]
     decls = re.findall(r"^\s*(int32_t|void\*|int64_t)\s+(\w+)", body, flags=re.M)
     assert decls == [("int32_t", "transpose_weight"), ("int32_t", "variant"),
-                     ("int32_t", "reserved"), ("void*", "workspace"),
+                     ("int32_t", "x_pitch"), ("int32_t", "w_pitch"), ("void*", "workspace"),
                      ("int64_t", "workspace_bytes")]
 
 
@@ -569,3 +570,48 @@ def test_python_options_carry_the_workspace():
         bra._options(False, None, torch.zeros(16, dtype=torch.uint8))        # a CPU tensor
     with pytest.raises(ValueError):
         bra._options(False, None, FakeCuda(16, 1, contiguous=False))
+
+
+def _pitch_opts(xp=0, wp=0, variant=None, transposed=False):
+    o = bra._options(transposed, variant)
+    o.x_pitch, o.w_pitch = xp, wp
+    return o
+
+
+def test_caller_pitches_select_the_tma_kernels_or_are_refused(lib, monkeypatch):
+    """Pitched operands run on the TMA kernels only: a 16-byte pitch and
+    16-byte pointers take them (with no workspace, H = 70 ragged), anything
+    else is BRA_ERR_UNSUPPORTED; a pitch below the row length is invalid."""
+    monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
+    f = Fake(2, 2, 4, 40, 256, 70, 1)             # Kp = 128, H = 70: weight rows unaligned
+    assert _variant(lib, f) == bra.VARIANT_TCR
+    assert _variant(lib, f, opts=_pitch_opts(wp=72)) in (bra.VARIANT_TC, bra.VARIANT_TC2)
+    assert _variant(lib, f, opts=_pitch_opts(xp=136, wp=80)) in (bra.VARIANT_TC, bra.VARIANT_TC2)
+    assert _variant(lib, f, opts=_pitch_opts(wp=71)) == -UNSUPPORTED      # not a 16-byte pitch
+    assert _variant(lib, f, opts=_pitch_opts(wp=69)) == -INVALID          # below the row length
+    assert _variant(lib, f, opts=_pitch_opts(xp=127)) == -INVALID
+    assert _variant(lib, f, opts=_pitch_opts(wp=72, variant="tcr")) == -UNSUPPORTED
+    assert _variant(lib, f, opts=_pitch_opts(wp=72, variant="packed")) == -UNSUPPORTED
+    assert _variant(lib, f, opts=_pitch_opts(wp=72, variant="tc")) == bra.VARIANT_TC
+    assert _ws_size(lib, f) > 0
+    x, w, b, y = f.arrays()
+    assert lib.bmm_rs_a2a_workspace_size(x, w, b, *f.args, bra.FP16, y,
+                                         ctypes.byref(_pitch_opts(wp=72))) == 0
+    f.w[1] += 2                                   # a pitched operand must be 16-byte aligned
+    assert _variant(lib, f, opts=_pitch_opts(wp=72)) == -UNSUPPORTED
+
+
+def test_pitched_extents_enter_the_aliasing_rule(lib):
+    """A pitched operand spans (rows - 1) * pitch + length elements: an
+    output placed inside that span is rejected, one just past it is not."""
+    f = Fake(2, 2, 4, 8, 16, 8, 0, base=1 << 41)  # x: (2, 16, 8) per rank, 32 rows of 8
+    ep, tp, E, C, M, H, t = f.args
+    pitch = 64
+    span = ((2 * 16 - 1) * pitch + 8) * 2
+    g = Fake(2, 2, 4, 8, 16, 8, 0, base=1 << 41)
+    g.y[0] = g.x[0] + span - 2                    # inside the pitched span of x[0]
+    assert _variant(lib, g, opts=_pitch_opts(xp=pitch)) == -INVALID
+    g.y[0] = g.x[0] + ((span + 15) // 16) * 16    # 16-byte aligned, just past it
+    for r in range(1, 4):                         # move the other ranks out of the way
+        g.x[r] += 1 << 30
+    assert _variant(lib, g, opts=_pitch_opts(xp=pitch)) > 0

@@ -228,3 +228,44 @@ def test_auto_workspace():
     with pytest.raises(ValueError):
         bra.bmm_rs_a2a(d2["x"], d2["w"], d2["bias"], cfg2.ep, cfg2.tp, cfg2.E, cfg2.C, cfg2.M,
                        cfg2.H, cfg2.y_shard_type, workspace="big")
+
+
+def _padded_view(t, pitch):
+    """A (d0, d1, pitch) buffer whose padding holds NaN, viewed as t's shape
+    and holding t's values: a row-pitched operand."""
+    d0, d1, d2 = t.shape
+    buf = torch.full((d0, d1, pitch), float("nan"), dtype=t.dtype, device=t.device)
+    buf[:, :, :d2].copy_(t)
+    return buf[:, :, :d2]
+
+
+@pytest.mark.parametrize("case,xpitch,wpitch,transposed", [
+    ((2, 2, 4, 40, 256, 70, 1, "fp16"), 0, 72, False),     # H = 70: only the weight pitched
+    ((2, 2, 4, 40, 130, 70, 0, "bf16"), 72, 80, False),    # Kp = 65 and H = 70 both pitched
+    ((4, 2, 8, 96, 200, 300, 1, "fp16"), 104, 0, True),    # transposed weight, rows of Kp = 100
+])
+def test_caller_pitched_operands(case, xpitch, wpitch, transposed):
+    """Operands kept in padded buffers run on the TMA kernels with no copy
+    and no workspace; the padding (NaN) is never read."""
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("pit", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=sum(case[:6]) + 31)
+    inp = fused_inputs_host(cfg)
+    ref = _oracle(cfg, inp)
+    d = _to_dev(inp)
+    w0 = [u.transpose(1, 2).contiguous() for u in d["w"]] if transposed else d["w"]
+    if transposed:
+        xs = [_padded_view(x, xpitch) for x in d["x"]]
+        ws = [_padded_view(u, xpitch) for u in w0]          # transposed rows are Kp long too
+    else:
+        xs = [_padded_view(x, xpitch) for x in d["x"]] if xpitch else d["x"]
+        ws = [_padded_view(u, wpitch) for u in w0] if wpitch else w0
+    ys = bra.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t)["y"]
+    probe = [torch.empty(ys, dtype=xs[0].dtype, device="cuda") for _ in range(cfg.P)]
+    assert bra.bmm_rs_a2a_variant(xs, ws, d["bias"], ep, tp, E, C, M, H, t, probe,
+                                  transpose_weight=transposed) in (bra.VARIANT_TC, bra.VARIANT_TC2)
+    assert bra.bmm_rs_a2a_workspace_size(xs, ws, d["bias"], ep, tp, E, C, M, H, t, probe,
+                                         transpose_weight=transposed) == 0
+    out = _call(cfg, xs, ws, d["bias"], transposed, None)
+    err = _rel_err(out, ref)
+    assert err <= TOL[dt], f"{case}: rel err {err:.3e}"

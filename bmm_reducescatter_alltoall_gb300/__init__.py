@@ -345,6 +345,9 @@ def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
 
     x[r], weight[r], bias[r] (or bias None) and out[r] are CUDA tensors of
     the shapes `bmm_rs_a2a_infer_shape` gives; out is allocated when None.
+    x and weight may also be row-pitched views of wider buffers (strides
+    (d1 * pitch, pitch, 1), one pitch per list): with a pitch that is a
+    multiple of 8 elements they run on the TMA kernels with no copy.
     transpose_weight: weight[r] is stored as (El, H, Kp) instead of
     (El, Kp, H).  variant: None/"auto", "tc", "tc2", "tcr", "tcu", "simt" or
     "packed".  workspace: an optional contiguous CUDA tensor of at least

@@ -230,12 +230,14 @@ int choose_variant(const bra::FusedProblem& p, const bra_fused_options* opts) {
   const bool tc_ok = bra::fused_tc_eligible(p);
   const bool tcu_ok = bra::fused_tcu_eligible(p);
   const bool tcr_ok = bra::fused_tcr_eligible(p);
-  // Caller-pitched operands: the TMA kernels only (the other kernels and the
-  // repack read dense rows).
+  // Caller-pitched operands: the TMA kernels, or the row-class kernel for
+  // other pitches (both address rows only through tensor maps); the
+  // load-staged and generic kernels and the repack read dense rows.
   if (pitched(p)) {
-    if (!tc_ok) return -BRA_ERR_UNSUPPORTED;
-    if (f == BRA_VARIANT_TC || f == BRA_VARIANT_TC2) return f;
-    return f == BRA_VARIANT_AUTO ? tma_kernel_for(p) : -BRA_ERR_UNSUPPORTED;
+    if (f == BRA_VARIANT_TC || f == BRA_VARIANT_TC2) return tc_ok ? f : -BRA_ERR_UNSUPPORTED;
+    if (f == BRA_VARIANT_TCR) return tcr_ok ? f : -BRA_ERR_UNSUPPORTED;
+    if (f != BRA_VARIANT_AUTO) return -BRA_ERR_UNSUPPORTED;
+    return tc_ok ? tma_kernel_for(p) : tcr_ok ? BRA_VARIANT_TCR : -BRA_ERR_UNSUPPORTED;
   }
   if (f == BRA_VARIANT_SIMT) return BRA_VARIANT_SIMT;
   if (f == BRA_VARIANT_TC || f == BRA_VARIANT_TC2) return tc_ok ? f : -BRA_ERR_UNSUPPORTED;

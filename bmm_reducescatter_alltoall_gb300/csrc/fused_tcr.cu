@@ -579,26 +579,40 @@ int ilog2(int n) {
   return l;
 }
 
-// Row classes of a row-major 16-bit matrix with rows of `rowlen` elements:
-// the least power of two n for which n rows span a multiple of 16 bytes, at
-// least 2 when a base pointer is not 16-byte aligned (a class map's rows then
-// start up to 7 elements before the row, and its pitch must exceed that).
-int row_classes(int64_t rowlen, const void* const* bases, int count) {
+// Largest delta (elements past a 16-byte boundary) of the first rows of n
+// classes, over all base pointers.
+int max_delta(int64_t pitch, int n, const void* const* bases, int count) {
+  int dmax = 0;
+  for (int i = 0; i < count; ++i)
+    for (int q = 0; q < n; ++q) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(bases[i]) + (uintptr_t)(q * pitch * 2);
+      const int d = (int)((a & 15u) >> 1);
+      dmax = d > dmax ? d : dmax;
+    }
+  return dmax;
+}
+
+// Row classes of a row-major 16-bit matrix with rows of `rowlen` elements
+// `pitch` elements apart (the row length, or a caller's larger pitch): the
+// least power of two n for which n rows span a multiple of 16 bytes and the
+// class map's rows (rowlen + delta elements, starting delta before the
+// row) do not overlap, n * pitch >= rowlen + delta for every class.  At most
+// 8, since 8 * pitch >= rowlen + 7.
+int row_classes(int64_t rowlen, int64_t pitch, const void* const* bases, int count) {
   int n = 1;
-  while ((rowlen * 2 * n) % 16 != 0) n *= 2;
-  if (n == 1)
-    for (int i = 0; i < count; ++i)
-      if (reinterpret_cast<uintptr_t>(bases[i]) & 15u) return 2;
+  while ((pitch * 2 * n) % 16 != 0) n *= 2;
+  while (n < 8 && n * pitch < rowlen + max_delta(pitch, n, bases, count)) n *= 2;
   return n;
 }
 
-// Class q of the nrows x rowlen matrix at `base` (rows q, q+n, ...): a 2-D
-// map starting at the 16-byte boundary at or below row q; *delta = the
-// row's offset from it in elements, or -1 when the class has no row.  The
-// boundary lies in the same allocation as the matrix (allocations start
-// 16-byte aligned), and the map ends at the last row's end.
-bool encode_class(CUtensorMap* m, int8_t* delta, const void* base, int64_t rowlen, int64_t nrows,
-                  int n, int q, uint32_t box0, uint32_t box1) {
+// Class q of the nrows x rowlen matrix at `base`, rows `pitch` elements
+// apart (rows q, q+n, ...): a 2-D map starting at the 16-byte boundary at or
+// below row q; *delta = the row's offset from it in elements, or -1 when the
+// class has no row.  The boundary lies in the same allocation as the matrix
+// (allocations start 16-byte aligned), and the map ends at the last row's
+// end, so elements between a row's end and the next row are never read.
+bool encode_class(CUtensorMap* m, int8_t* delta, const void* base, int64_t rowlen, int64_t pitch,
+                  int64_t nrows, int n, int q, uint32_t box0, uint32_t box1) {
   std::memset(m, 0, sizeof(*m));
   if (q >= nrows) {
     *delta = -1;
@@ -606,11 +620,11 @@ bool encode_class(CUtensorMap* m, int8_t* delta, const void* base, int64_t rowle
   }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const uintptr_t a = reinterpret_cast<uintptr_t>(base) + (uintptr_t)(q * rowlen * 2);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(base) + (uintptr_t)(q * pitch * 2);
   const uintptr_t a16 = a & ~(uintptr_t)15;
   const int d = (int)((a - a16) / 2);
   const cuuint64_t dims[2] = {(cuuint64_t)(rowlen + d), (cuuint64_t)((nrows - q + n - 1) / n)};
-  const cuuint64_t strides[1] = {(cuuint64_t)(rowlen * 2 * n)};
+  const cuuint64_t strides[1] = {(cuuint64_t)(pitch * 2 * n)};
   const cuuint32_t box[2] = {box0, box1};
   const cuuint32_t estr[2] = {1, 1};
   *delta = (int8_t)d;
@@ -626,8 +640,8 @@ struct Classes {
 Classes classes_of(const FusedProblem& f) {
   const int P = f.ep * f.tp;
   Classes c;
-  c.ncx = row_classes(f.Kp, f.x, P);
-  c.ncw = row_classes(f.wt ? f.Kp : f.H, f.w, P);
+  c.ncx = row_classes(f.Kp, f.xp, f.x, P);
+  c.ncw = row_classes(f.wt ? f.Kp : f.H, f.wp, f.w, P);
   return c;
 }
 
@@ -740,12 +754,12 @@ cudaError_t launch_fused_tcr(const FusedProblem& f, cudaStream_t st) {
       CUtensorMap* xm = &p->maps[rl * mpr];
       int8_t* xd = &p->delta[rl * mpr];
       for (int q = 0; q < cl.ncx; ++q)
-        if (!encode_class(&xm[q], &xd[q], f.x[gr], f.Kp, x_rows, cl.ncx, q, BK + 8,
+        if (!encode_class(&xm[q], &xd[q], f.x[gr], f.Kp, f.xp, x_rows, cl.ncx, q, BK + 8,
                           BM_CTA / cl.ncx))
           return cudaErrorInvalidValue;
       for (int q = 0; q < cl.ncw; ++q)
-        if (!encode_class(&xm[cl.ncx + q], &xd[cl.ncx + q], f.w[gr], w_len, w_rows, cl.ncw, q,
-                          wbox0, wbox1))
+        if (!encode_class(&xm[cl.ncx + q], &xd[cl.ncx + q], f.w[gr], w_len, f.wp, w_rows,
+                          cl.ncw, q, wbox0, wbox1))
           return cudaErrorInvalidValue;
     }
     p->num_tiles = (s1 - s0) * f.El * p->m_tiles * p->n_tiles;

@@ -168,9 +168,12 @@ typedef struct {
    * must be at least the row length; the tensor is then El * rows rows
    * that many elements apart (the layout of a (El, rows, pitch) buffer
    * viewed as (El, rows, length)), and the elements between a row's end and
-   * the next row are never read.  Pitched operands must be TMA-ready (pitch
-   * a multiple of 8 elements, pointers 16-byte aligned) and run on the TMA
-   * kernels with no copy; otherwise the call returns BRA_ERR_UNSUPPORTED. */
+   * the next row are never read.  Pitched operands run with no copy: on the
+   * TMA kernels when TMA-ready (pitch a multiple of 8 elements, pointers
+   * 16-byte aligned), else on the row-class kernel (element-aligned
+   * pointers, its map limit); otherwise the call returns
+   * BRA_ERR_UNSUPPORTED (the load-staged and generic kernels and the packed
+   * variant take dense rows only). */
   int32_t x_pitch;
   int32_t w_pitch;
   /* Device memory the call may use as scratch, in the manner of the second

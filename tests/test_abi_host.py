@@ -578,27 +578,35 @@ def _pitch_opts(xp=0, wp=0, variant=None, transposed=False):
     return o
 
 
-def test_caller_pitches_select_the_tma_kernels_or_are_refused(lib, monkeypatch):
-    """Pitched operands run on the TMA kernels only: a 16-byte pitch and
-    16-byte pointers take them (with no workspace, H = 70 ragged), anything
-    else is BRA_ERR_UNSUPPORTED; a pitch below the row length is invalid."""
+def test_caller_pitches_select_the_kernel_or_are_refused(lib, monkeypatch):
+    """Pitched operands: a 16-byte pitch with 16-byte pointers takes the TMA
+    kernels (with no workspace, H = 70 ragged); other pitches or pointers take
+    the row-class kernel; what only the load-staged, generic or packed paths
+    could take is BRA_ERR_UNSUPPORTED; a pitch below the row length is
+    invalid."""
     monkeypatch.delenv("BRA_FORCE_VARIANT", raising=False)
     f = Fake(2, 2, 4, 40, 256, 70, 1)             # Kp = 128, H = 70: weight rows unaligned
     assert _variant(lib, f) == bra.VARIANT_TCR
     assert _variant(lib, f, opts=_pitch_opts(wp=72)) in (bra.VARIANT_TC, bra.VARIANT_TC2)
     assert _variant(lib, f, opts=_pitch_opts(xp=136, wp=80)) in (bra.VARIANT_TC, bra.VARIANT_TC2)
-    assert _variant(lib, f, opts=_pitch_opts(wp=71)) == -UNSUPPORTED      # not a 16-byte pitch
+    assert _variant(lib, f, opts=_pitch_opts(wp=71)) == bra.VARIANT_TCR    # not a 16-byte pitch
     assert _variant(lib, f, opts=_pitch_opts(wp=69)) == -INVALID          # below the row length
     assert _variant(lib, f, opts=_pitch_opts(xp=127)) == -INVALID
-    assert _variant(lib, f, opts=_pitch_opts(wp=72, variant="tcr")) == -UNSUPPORTED
+    assert _variant(lib, f, opts=_pitch_opts(wp=72, variant="tcr")) == bra.VARIANT_TCR
     assert _variant(lib, f, opts=_pitch_opts(wp=72, variant="packed")) == -UNSUPPORTED
+    assert _variant(lib, f, opts=_pitch_opts(wp=72, variant="tcu")) == -UNSUPPORTED
+    assert _variant(lib, f, opts=_pitch_opts(wp=72, variant="simt")) == -UNSUPPORTED
+    assert _variant(lib, f, opts=_pitch_opts(wp=71, variant="tc")) == -UNSUPPORTED
     assert _variant(lib, f, opts=_pitch_opts(wp=72, variant="tc")) == bra.VARIANT_TC
     assert _ws_size(lib, f) > 0
     x, w, b, y = f.arrays()
     assert lib.bmm_rs_a2a_workspace_size(x, w, b, *f.args, bra.FP16, y,
                                          ctypes.byref(_pitch_opts(wp=72))) == 0
-    f.w[1] += 2                                   # a pitched operand must be 16-byte aligned
-    assert _variant(lib, f, opts=_pitch_opts(wp=72)) == -UNSUPPORTED
+    f.w[1] += 2                                   # element-aligned only: the row-class kernel
+    assert _variant(lib, f, opts=_pitch_opts(wp=72)) == bra.VARIANT_TCR
+    g = Fake(2, 16, 4, 16, 16 * 3, 5, 1)          # 8 + 8 classes x tp = 16: maps do not fit
+    assert _variant(lib, g) == bra.VARIANT_TCU
+    assert _variant(lib, g, opts=_pitch_opts(xp=3, wp=7)) == -UNSUPPORTED
 
 
 def test_pitched_extents_enter_the_aliasing_rule(lib):

@@ -33,12 +33,17 @@ RAW_B = BN_CTA * KROW
 SW_A, SW_B, B_BOX = 16384, 16384, 8192
 
 
-def _classes(rowlen, aligned=True):
+def _classes(rowlen, aligned=True, pitch=None, base_off=None):
+    """Row classes as fused_tcr.cu's row_classes counts them: n rows span a
+    multiple of 16 bytes and n * pitch covers the row plus the largest delta."""
+    pitch = rowlen if pitch is None else pitch
+    base_off = (0 if aligned else 2) if base_off is None else base_off
     n = 1
-    while (rowlen * 2 * n) % 16:
+    while (pitch * 2 * n) % 16:
         n *= 2
-    if n == 1 and not aligned:
-        n = 2
+    while n < 8 and n * pitch < rowlen + max(((base_off + q * pitch * 2) % 16) // 2
+                                             for q in range(n)):
+        n *= 2
     return n
 
 
@@ -101,32 +106,37 @@ def test_row_class_stage_addressing(wt, ncx, ncw):
     assert len(written) == (SW_A + SW_B) // 16 and set(written.values()) == {1}
 
 
-def _class_map(base, rowlen, nrows, n, q):
-    """(map base address, delta, inner extent, outer extent, pitch) of class q."""
-    a = base + q * rowlen * 2
+def _class_map(base, rowlen, nrows, n, q, rpitch=None):
+    """(map base address, delta, inner extent, outer extent, pitch) of class q
+    of a matrix whose rows are `rpitch` elements apart (default: dense)."""
+    rpitch = rowlen if rpitch is None else rpitch
+    a = base + q * rpitch * 2
     a16 = a & ~15
     d = (a - a16) // 2
-    return a16, d, rowlen + d, (nrows - q + n - 1) // n, rowlen * 2 * n
+    return a16, d, rowlen + d, (nrows - q + n - 1) // n, rpitch * 2 * n
 
 
-@pytest.mark.parametrize("rowlen", [1, 3, 6, 7, 8, 9, 65, 100, 257, 1025, 2050, 4100, 65535])
-@pytest.mark.parametrize("base_off", [0, 2, 6, 14])
-def test_row_class_maps_stay_inside_the_matrix(rowlen, base_off):
+@pytest.mark.parametrize("rowlen", [1, 2, 3, 4, 5, 6, 7, 8, 9, 65, 100, 257, 1025, 2050, 4100,
+                                    65535])
+@pytest.mark.parametrize("base_off", [0, 2, 4, 6, 8, 10, 12, 14])
+@pytest.mark.parametrize("extra", [0, 1, 3, 8])            # caller pitch = rowlen + extra
+def test_row_class_maps_stay_inside_the_matrix(rowlen, base_off, extra):
     base = (1 << 20) + base_off                           # an element-aligned pointer
     alloc_start = base & ~15                              # allocations start 16-byte aligned
     nrows = 37
-    end = base + nrows * rowlen * 2
-    n = _classes(rowlen, aligned=base_off == 0)
+    rpitch = rowlen + extra
+    end = base + ((nrows - 1) * rpitch + rowlen) * 2      # the pitched matrix's last byte + 1
+    n = _classes(rowlen, pitch=rpitch, base_off=base_off)
     for q in range(min(n, nrows)):
-        a16, d, inner, outer, pitch = _class_map(base, rowlen, nrows, n, q)
+        a16, d, inner, outer, pitch = _class_map(base, rowlen, nrows, n, q, rpitch)
         assert a16 >= alloc_start and 0 <= d < 8 and pitch % 16 == 0
         assert pitch >= inner * 2                          # rows do not overlap in the map
         for j in range(outer):
             row = q + j * n
-            start = base + row * rowlen * 2
+            start = base + row * rpitch * 2
             assert start - (a16 + j * pitch) == 2 * d      # every row sits delta past its boundary
         last = q + (outer - 1) * n
-        assert a16 + (outer - 1) * pitch + inner * 2 == base + (last + 1) * rowlen * 2 <= end
+        assert a16 + (outer - 1) * pitch + inner * 2 == base + (last * rpitch + rowlen) * 2 <= end
 
 
 @pytest.mark.parametrize("n", [0, 1, 5, 17, 1000, 2 ** 40 + 7])

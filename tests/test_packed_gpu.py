@@ -243,10 +243,14 @@ def _padded_view(t, pitch):
     ((2, 2, 4, 40, 256, 70, 1, "fp16"), 0, 72, False),     # H = 70: only the weight pitched
     ((2, 2, 4, 40, 130, 70, 0, "bf16"), 72, 80, False),    # Kp = 65 and H = 70 both pitched
     ((4, 2, 8, 96, 200, 300, 1, "fp16"), 104, 0, True),    # transposed weight, rows of Kp = 100
+    ((2, 2, 4, 40, 130, 70, 0, "bf16"), 67, 73, False),    # odd pitches: the row-class kernel
+    ((2, 2, 4, 6, 12, 4, 1, "fp16"), 7, 5, False),         # rows of 6 and 4 elements, pitches 7, 5
+    ((4, 2, 8, 96, 200, 300, 1, "bf16"), 103, 0, True),    # transposed, odd pitch
 ])
 def test_caller_pitched_operands(case, xpitch, wpitch, transposed):
-    """Operands kept in padded buffers run on the TMA kernels with no copy
-    and no workspace; the padding (NaN) is never read."""
+    """Operands kept in padded buffers run with no copy and no workspace:
+    16-byte pitches on the TMA kernels, other pitches on the row-class
+    kernel; the padding (NaN) is never read."""
     ep, tp, E, C, M, H, t, dt = case
     cfg = FusedConfig("pit", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
                       seed=sum(case[:6]) + 31)
@@ -262,8 +266,11 @@ def test_caller_pitched_operands(case, xpitch, wpitch, transposed):
         ws = [_padded_view(u, wpitch) for u in w0] if wpitch else w0
     ys = bra.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t)["y"]
     probe = [torch.empty(ys, dtype=xs[0].dtype, device="cuda") for _ in range(cfg.P)]
+    pitches = [p for p in (xpitch, wpitch) if p]
+    want = ((bra.VARIANT_TC, bra.VARIANT_TC2) if all(p % 8 == 0 for p in pitches)
+            else (bra.VARIANT_TCR,))
     assert bra.bmm_rs_a2a_variant(xs, ws, d["bias"], ep, tp, E, C, M, H, t, probe,
-                                  transpose_weight=transposed) in (bra.VARIANT_TC, bra.VARIANT_TC2)
+                                  transpose_weight=transposed) in want
     assert bra.bmm_rs_a2a_workspace_size(xs, ws, d["bias"], ep, tp, E, C, M, H, t, probe,
                                          transpose_weight=transposed) == 0
     out = _call(cfg, xs, ws, d["bias"], transposed, None)

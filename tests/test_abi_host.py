@@ -623,3 +623,40 @@ def test_pitched_extents_enter_the_aliasing_rule(lib):
     for r in range(1, 4):                         # move the other ranks out of the way
         g.x[r] += 1 << 30
     assert _variant(lib, g, opts=_pitch_opts(xp=pitch)) > 0
+
+
+def test_binding_detects_row_pitches():
+    """The binding passes the shared row pitch of row-pitched x / weight
+    views (0 for dense ones) and refuses other strides or mixed pitches.
+    CPU tensors stand in for CUDA ones through a subclass that reports a
+    CUDA device."""
+    import torch
+
+    class FakeCuda(torch.Tensor):
+        @property
+        def device(self):
+            return torch.device("cuda", 0)
+
+        @property
+        def is_cuda(self):
+            return True
+
+    def fake(shape, pitch=None):
+        d0, d1, d2 = shape
+        buf = torch.zeros((d0, d1, pitch or d2), dtype=torch.float16).as_subclass(FakeCuda)
+        return buf[:, :, :d2]
+
+    shape = (2, 5, 7)
+    _, p = bra._pitched_ptrs([fake(shape), fake(shape)], "x", torch.float16, shape)
+    assert p == 0
+    _, p = bra._pitched_ptrs([fake(shape, 9), fake(shape, 9)], "x", torch.float16, shape)
+    assert p == 9
+    with pytest.raises(ValueError, match="same row pitch"):
+        bra._pitched_ptrs([fake(shape, 9), fake(shape, 16)], "x", torch.float16, shape)
+    _, p = bra._pitched_ptrs([fake(shape), fake(shape, 7)], "x", torch.float16, shape)
+    assert p == 0                                 # pitch equal to the length is dense
+    odd = torch.zeros((2, 7, 5), dtype=torch.float16).as_subclass(FakeCuda).transpose(1, 2)
+    with pytest.raises(ValueError, match="row-pitched"):
+        bra._pitched_ptrs([odd], "x", torch.float16, shape)
+    with pytest.raises(TypeError):
+        bra._pitched_ptrs([fake(shape).float()], "x", torch.float16, shape)

@@ -11,7 +11,9 @@ or evicted by the fused call's 10 GB of traffic between all_to_all_v calls.
 Prints one JSON line (rank 0).  Besides the step it reports all_to_all_v and
 the indexed exchange (each sender's list a permutation of its input) timed
 alone, the same op unfused from torch ops as context, and an end-to-end figure
-with host buffers.  `--impl reference` times the CPU oracle on a bounded
+with host buffers.  `--fused NAME` picks another fused workload and
+`--workspace` gives the fused call a workspace (unaligned shapes then time the
+packed variant).  `--impl reference` times the CPU oracle on a bounded
 sample of the same workload instead.  With torchrun (N > 1) every
 rank runs an independent replica of the step on its own GPU.
 """

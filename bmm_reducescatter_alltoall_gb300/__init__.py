@@ -18,7 +18,7 @@ from typing import List, Optional, Sequence
 __all__ = [
     "BraError", "FP16", "BF16", "FP32", "INT8", "VARIANT_TC", "VARIANT_TC2", "VARIANT_SIMT",
     "VARIANT_TCU", "VARIANT_TCR", "VARIANT_PACKED", "wait_selftest", "indexed_all_to_all_v",
-    "bmm_rs_a2a_workspace_size",
+    "bmm_rs_a2a_workspace_size", "bmm_rs_a2a_noalloc", "NOALLOC_SCRATCH_BYTES",
     "FusedOptions", "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
     "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked", "Plan", "bmm_rs_a2a_plan",
     "all_to_all_v_plan", "indexed_all_to_all_v_plan",
@@ -71,6 +71,9 @@ def library() -> ctypes.CDLL:
     lib.bmm_rs_a2a_variant.restype = c_int
     lib.bmm_rs_a2a_workspace_size.argtypes = lib.bmm_rs_a2a_variant.argtypes
     lib.bmm_rs_a2a_workspace_size.restype = i64
+    lib.bmm_rs_a2a_noalloc.argtypes = [pp, pp, pp, i64, i64, i64, i64, i64, i64, i64, c_int, pp,
+                                       c_int, vp]
+    lib.bmm_rs_a2a_noalloc.restype = c_int
     lib.bmm_rs_a2a_infer_shape.argtypes = [i64] * 7 + [i64p] * 4
     lib.bmm_rs_a2a_infer_shape.restype = c_int
     lib.cal_all_to_all_v_blocks.argtypes = [i64, i64]
@@ -359,6 +362,29 @@ def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
     """
     return bmm_rs_a2a_plan(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
                            transpose_weight, variant, workspace).run(stream)
+
+
+# Size of the library's own scratch array used by bmm_rs_a2a_noalloc
+# (BRA_NOALLOC_SCRATCH_BYTES of the C header).
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def bmm_rs_a2a_noalloc(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
+                       tp: int, E: int, C: int, M: int, H: int, y_shard_type: int,
+                       out: Sequence, stream=None, transpose_weight: bool = False) -> List:
+    """The packed variant with the library's own scratch array instead of a
+    workspace (bmm_rs_a2a_noalloc of the C header): for callers that cannot
+    allocate device memory.  Allocates nothing, so `out` is required.  The
+    copies must fit NOALLOC_SCRATCH_BYTES; calls that overlap on the GPU
+    share the array and race.  Returns out."""
+    xp, wp, bp, yp, dt, pitches = _fused_args(x, weight, bias, ep, tp, E, C, M, H, y_shard_type,
+                                              out, transpose_weight)
+    if pitches != (0, 0):
+        raise ValueError("bmm_rs_a2a_noalloc takes dense x and weight")
+    _check(library().bmm_rs_a2a_noalloc(xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp,
+                                        1 if transpose_weight else 0, _stream_handle(stream)),
+           "bmm_rs_a2a_noalloc")
+    return out
 
 
 def bmm_rs_a2a_workspace_size(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out=None,

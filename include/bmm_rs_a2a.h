@@ -246,6 +246,46 @@ BRA_API int64_t bmm_rs_a2a_workspace_size(const void* const x[], const void* con
                                           const bra_fused_options* opts);
 
 /*
+ * bmm_rs_a2a_noalloc -- bmm_rs_a2a_ex forced to BRA_VARIANT_PACKED, with
+ * scratch memory the library holds itself instead of a caller workspace.
+ * The pages have no counterpart: the CANN op always takes its workspace
+ * from the caller.
+ *
+ * Who it is for: callers that cannot allocate device memory for a
+ * workspace -- a plugin inside a host program that owns all device memory
+ * and hands its plugins only their inputs and outputs, or a path that must
+ * not call cudaMalloc because cudaMalloc may synchronise the device.  The
+ * call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine runs on its path.  The caller still passes every input and output.
+ *
+ * Scratch: one file-scope device array of BRA_NOALLOC_SCRATCH_BYTES
+ * (32 MiB), loaded with the library on every device that uses it and held
+ * there until the process exits.  The first call on a device, with that
+ * device current, looks up the array's address (cudaGetSymbolAddress) and
+ * keeps it; make that first call before any stream capture.  Every call on
+ * a device shares the array, and the array keeps the last call's contents
+ * (nothing in it has to start at zero: the repack writes every byte the
+ * TMA kernel reads).  Calls whose work overlaps on the GPU (different
+ * streams, no ordering between them) race on the array and give wrong
+ * results: order them on one stream or with events.
+ *
+ * Arguments: as bmm_rs_a2a; transpose_weight non-zero means weight[r] is
+ * stored as (El, H, Kp) (the bra_fused_options field of that name).
+ * Operands must be dense (no pitch).  Operands whose rows have a 16-byte
+ * pitch and 16-byte aligned pointers are not copied and use no scratch.
+ * Errors: as bmm_rs_a2a_ex with BRA_VARIANT_PACKED forced; plus
+ * BRA_ERR_UNSUPPORTED when the copies need more than
+ * BRA_NOALLOC_SCRATCH_BYTES (bmm_rs_a2a_workspace_size gives the need) or
+ * the current device's ordinal is 64 or more, and BRA_ERR_CUDA when the
+ * array's address cannot be obtained.
+ */
+#define BRA_NOALLOC_SCRATCH_BYTES (32u << 20)
+BRA_API int bmm_rs_a2a_noalloc(const void* const x[], const void* const weight[],
+                               const void* const bias[], int64_t ep, int64_t tp, int64_t E,
+                               int64_t C, int64_t M, int64_t H, int64_t yShardType, int dtype,
+                               void* const out[], int transpose_weight, bra_stream_t stream);
+
+/*
  * bmm_rs_a2a_variant -- which kernel bmm_rs_a2a_ex would launch for these
  * arguments and options (BRA_VARIANT_TC, BRA_VARIANT_TC2, BRA_VARIANT_TCR,
  * BRA_VARIANT_TCU, BRA_VARIANT_SIMT or BRA_VARIANT_PACKED), honouring

@@ -160,6 +160,38 @@ def bmm_rs_a2a(x: Sequence, w: Sequence, bias: Optional[Sequence],
     return [round_to(a, dtype) for a in y]
 
 
+def group_outputs(x_group: Sequence, w_group: Sequence, bias_group: Optional[Sequence],
+                  ep: int, tp: int, C: int, H: int, y_shard_type: int, dtype: str,
+                  type1_layout: str = "blocked") -> dict:
+    """Sender view for one TP group s and one local expert e: the four steps
+    of [CANN] §功能说明与计算流程 restricted to that (s, e), so that a whole
+    expert block of a large problem can be evaluated without the others.
+
+    x_group[t], w_group[t]: expert e of rank s*tp+t, shapes (ep*C, M/tp) and
+    (M/tp, H); bias_group: None, or tp rows (length H/tp for yShardType 0, H
+    for 1) holding expert e's bias of rank s*tp+t.  Returns {(j, t): block},
+    the block receiver j*tp+t stores at dim-0 index s*E/ep + e (shape (C,
+    H/tp) for yShardType 0, (C/tp, H) for 1), as float64 arrays of values
+    exactly representable in `dtype`.
+    """
+    assert len(x_group) == tp and len(w_group) == tp
+    # 1. BatchMatMul on every rank of the group, 2. summed in t order.
+    total = None
+    for t in range(tp):
+        prod = np.matmul(_f64(x_group[t]), _f64(w_group[t]))   # (ep*C, H)
+        total = prod if total is None else total + prod
+    chunk_rows = C if y_shard_type == 0 else C // tp
+    out = {}
+    for t in range(tp):
+        temp2 = _rs_chunk(total[None], t, ep, tp, C, H, y_shard_type, type1_layout)[0]
+        # 3. this rank's bias, broadcast over the rows
+        temp3 = temp2 if bias_group is None else temp2 + _f64(bias_group[t]).reshape(1, -1)
+        # 4. chunk j of the rows goes to EP rank j
+        for j in range(ep):
+            out[(j, t)] = round_to(temp3[j * chunk_rows:(j + 1) * chunk_rows], dtype)
+    return out
+
+
 def y_source(ep, tp, E, C, H, y_shard_type, d, i, c, h,
              type1_layout: str = "blocked") -> dict:
     """Receiver view: where output element y[d][i, c, h] comes from.

@@ -1,8 +1,10 @@
 """Fused BMM -> ReduceScatter -> Add -> AllToAll on the GPU against the oracle.
 
 Tolerance: max|gpu - oracle| / max|oracle| <= 2e-3 for fp16 and 1e-2 for
-bf16, over every output element (small shapes) or over sampled elements
-computed one by one by the oracle (the full-size workloads).  Every case is
+bf16, over every output element (small shapes); at the full-size workloads
+over every output element of six whole sender groups (s, e), and over a
+point in every 128 x 256 output tile of every group, computed one by one by
+the oracle.  Every case is
 also run without bias, so the bias (N(0,1), the largest term at the full
 sizes) cannot hide an error in the contraction.
 """
@@ -197,7 +199,7 @@ def test_tc_and_generic_agree(variant, monkeypatch):
 
 
 # --------------------------------------------------------------------------
-# Full-size workloads, sampled outputs
+# Full-size workloads: whole expert blocks, and a point in every tile
 # --------------------------------------------------------------------------
 
 def _sample_points(cfg, rng, per_rank=24):
@@ -214,28 +216,78 @@ def _sample_points(cfg, rng, per_rank=24):
     return pts
 
 
-def _sampled_check(cfg, dinp, out, rng, per_rank):
+def _tile_points(cfg, rng, tile_m=128, tile_n=256):
+    """One random point inside every tile_m x tile_n tile of every sender
+    group's tp-summed product Z_{s,e} (ep*C x H), as output coordinates
+    (d, i, c, h).  128 x 256 tiles refine both kernels' tilings (128 x 256
+    one-CTA tiles, 256 x 256 pair tiles), so a tile computed from the wrong
+    group, band or shard, or stored to the wrong place, shows at a point."""
+    El, rows = cfg.E // cfg.ep, cfg.ep * cfg.C
+    mts, nts = -(-rows // tile_m), -(-cfg.H // tile_n)
+    g, mt, nt = np.meshgrid(np.arange(cfg.ep * El), np.arange(mts), np.arange(nts),
+                            indexing="ij")
+    g, mt, nt = g.ravel(), mt.ravel(), nt.ravel()
+    zrow = mt * tile_m + rng.integers(0, np.minimum(tile_m, rows - mt * tile_m))
+    zcol = nt * tile_n + rng.integers(0, np.minimum(tile_n, cfg.H - nt * tile_n))
+    s, e = g // El, g % El
+    j = zrow // cfg.C
+    if cfg.y_shard_type == 0:
+        Hp = cfg.H // cfg.tp
+        t, c, h = zcol // Hp, zrow % cfg.C, zcol % Hp
+    else:
+        Cp = cfg.C // cfg.tp
+        t, c, h = (zrow % cfg.C) // Cp, (zrow % cfg.C) % Cp, zcol
+    return list(zip((j * cfg.tp + t).tolist(), (s * El + e).tolist(), c.tolist(), h.tolist(),
+                    zrow.tolist(), zcol.tolist()))
+
+
+def _points_check(cfg, dinp, out, pts, w_transposed=False):
+    """max|gpu - oracle| / max|oracle| over output points (d, i, c, h, ...),
+    each evaluated by the oracle's receiver view: its source found by
+    y_source, then the tp dot products of one x row and one weight column
+    plus the sender's bias, rounded once."""
     El = cfg.E // cfg.ep
-    pts = _sample_points(cfg, rng, per_rank)
-    got, want = [], []
-    for (d, i, c, h) in pts:
-        src = of.y_source(cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.H, cfg.y_shard_type, d, i, c, h)
-        ranks = [src["s"] * cfg.tp + u for u in range(cfg.tp)]
-        rows = torch.stack([dinp["x"][r][src["e"], src["zrow"], :] for r in ranks]).float().cpu()
-        cols = torch.stack([dinp["w"][r][src["e"], :, src["zcol"]] for r in ranks]).float().cpu()
-        b = None
-        if dinp["bias"] is not None:
-            b = float(dinp["bias"][src["bias_rank"]].reshape(El, -1)[src["e"], src["bias_col"]])
-        want.append(of.bmm_rs_a2a_point(rows.numpy(), cols.numpy(), b, cfg.dtype))
-        got.append(float(out[d][i, c, h]))
-    got, want = np.array(got), np.array(want)
+    src = [of.y_source(cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.H, cfg.y_shard_type, *p[:4])
+           for p in pts]
+    for p, q in zip(pts, src):                 # the points were aimed at these Z entries
+        if len(p) > 4:
+            assert (q["zrow"], q["zcol"]) == (p[4], p[5]), (p, q)
+    dev = dinp["x"][0].device
+    got = np.empty(len(pts))
+    want = np.empty(len(pts))
+    by_d, by_s = {}, {}
+    for k, (p, q) in enumerate(zip(pts, src)):
+        by_d.setdefault(p[0], []).append(k)
+        by_s.setdefault(q["s"], []).append(k)
+    for d, ks in by_d.items():
+        idx = [torch.tensor([pts[k][a] for k in ks], device=dev) for a in (1, 2, 3)]
+        got[ks] = out[d][idx[0], idx[1], idx[2]].double().cpu().numpy()
+    for s, ks in by_s.items():
+        e = torch.tensor([src[k]["e"] for k in ks], device=dev)
+        zr = torch.tensor([src[k]["zrow"] for k in ks], device=dev)
+        zc = torch.tensor([src[k]["zcol"] for k in ks], device=dev)
+        ranks = [s * cfg.tp + u for u in range(cfg.tp)]
+        rows = torch.stack([dinp["x"][r][e, zr, :] for r in ranks], 1).double().cpu().numpy()
+        cols = torch.stack([(dinp["w"][r][e, zc, :] if w_transposed else dinp["w"][r][e, :, zc])
+                            for r in ranks], 1).double().cpu().numpy()
+        for n, k in enumerate(ks):
+            b = None
+            if dinp["bias"] is not None:
+                q = src[k]
+                b = float(dinp["bias"][q["bias_rank"]].reshape(El, -1)[q["e"], q["bias_col"]])
+            want[k] = of.bmm_rs_a2a_point(rows[n], cols[n], b, cfg.dtype)
+    assert np.isfinite(got).all(), "an output element was not written"
     return float(np.max(np.abs(got - want)) / np.max(np.abs(want)))
 
 
+FULL_SIZE = ["ep8tp2_E64_C256_M4096_H4096_t0_bf16", "ep8tp4_E64_C512_M8192_H4096_t1_fp16"]
+
+
 @pytest.mark.parametrize("variant", [None, "tc", "tc2"])
-@pytest.mark.parametrize("name", ["ep8tp2_E64_C256_M4096_H4096_t0_bf16",
-                                  "ep8tp4_E64_C512_M8192_H4096_t1_fp16"])
-def test_full_size_workloads_sampled(name, variant, monkeypatch):
+@pytest.mark.parametrize("name", FULL_SIZE)
+def test_full_size_workloads_every_tile(name, variant, monkeypatch):
+    """A point in every 128 x 256 output tile of every (rank, expert) group,
+    plus the tile-seam points of every receiver, against the oracle."""
     cfg = FUSED_CONFIGS[name]
     rng = np.random.default_rng(99)
     for bias in (True, False):
@@ -244,8 +296,46 @@ def test_full_size_workloads_sampled(name, variant, monkeypatch):
         out = _run(c, dinp, variant, monkeypatch)
         for y in out:                                  # every element written
             assert not torch.isnan(y).any().item()
-        err = _sampled_check(c, dinp, out, rng, per_rank=12 if cfg.P > 16 else 24)
-        assert err <= TOL[cfg.dtype], f"{name} bias={bias}: sampled rel err {err:.3e}"
+        pts = _tile_points(c, rng) + _sample_points(c, rng, per_rank=4)
+        err = _points_check(c, dinp, out, pts)
+        assert err <= TOL[cfg.dtype], f"{name} bias={bias}: rel err {err:.3e} at {len(pts)} points"
+        del dinp, out
+        torch.cuda.empty_cache()
+
+
+# Sender groups (s, e) compared whole: the first and the last group of the
+# launch (the last one ends in a partial wave of CTA pairs), and groups whose
+# tiles start at different offsets into a wave.
+WHOLE_GROUPS = [(0, 0), (1, 3), (3, 7), (5, 1), (6, 6), (7, 7)]
+
+
+@pytest.mark.parametrize("name", FULL_SIZE)
+def test_full_size_whole_expert_blocks(name, monkeypatch):
+    """Every output element that six whole sender groups (s, e) produce --
+    their blocks at all ep*tp receivers -- against the oracle's evaluation of
+    those groups, with and without bias, on the kernel the bench times."""
+    cfg = FUSED_CONFIGS[name]
+    El, tp = cfg.E // cfg.ep, cfg.tp
+    for bias in (True, False):
+        c = cfg.replace(has_bias=bias)
+        dinp = fused_inputs_device(c)
+        out = _run(c, dinp, None, monkeypatch)
+        num = den = 0.0
+        n = 0
+        for s, e in WHOLE_GROUPS:
+            ranks = [s * tp + u for u in range(tp)]
+            bg = None if not bias else [dinp["bias"][r].reshape(El, -1)[e].cpu() for r in ranks]
+            blocks = of.group_outputs([dinp["x"][r][e].cpu() for r in ranks],
+                                      [dinp["w"][r][e].cpu() for r in ranks], bg,
+                                      c.ep, tp, c.C, c.H, c.y_shard_type, c.dtype)
+            for (j, u), ref in blocks.items():
+                got = out[j * tp + u][s * El + e].double().cpu().numpy()
+                assert np.isfinite(got).all(), "an output element was not written"
+                num = max(num, float(np.max(np.abs(got - ref))))
+                den = max(den, float(np.max(np.abs(ref))))
+                n += ref.size
+        err = num / den
+        assert err <= TOL[cfg.dtype], f"{name} bias={bias}: rel err {err:.3e} over {n} outputs"
         del dinp, out
         torch.cuda.empty_cache()
 
@@ -291,7 +381,7 @@ def test_transposed_weight(case, variant):
     assert err <= TOL[dt], f"{case} {variant} transposed: rel err {err:.3e}"
 
 
-def test_transposed_weight_full_size_sampled():
+def test_transposed_weight_full_size_every_tile():
     cfg = FUSED_CONFIGS["ep8tp2_E64_C256_M4096_H4096_t0_bf16"]
     dinp = fused_inputs_device(cfg)
     wt = [w.transpose(1, 2).contiguous() for w in dinp["w"]]
@@ -304,16 +394,19 @@ def test_transposed_weight_full_size_sampled():
     assert bra.fault_status() == 0
     for y in out:
         assert not torch.isnan(y).any().item()
-    err = _sampled_check(cfg, dinp, out, np.random.default_rng(7), per_rank=16)
-    assert err <= TOL["bf16"], f"sampled rel err {err:.3e}"
+    rng = np.random.default_rng(7)
+    err = _points_check(cfg, {"x": dinp["x"], "w": wt, "bias": dinp["bias"]}, out,
+                        _tile_points(cfg, rng) + _sample_points(cfg, rng, per_rank=4),
+                        w_transposed=True)
+    assert err <= TOL["bf16"], f"rel err {err:.3e}"
 
 
 @pytest.mark.parametrize("variant", [None, "tcu"])
 @pytest.mark.parametrize("transposed", [False, True])
-def test_unaligned_large_sampled(transposed, variant, monkeypatch):
+def test_unaligned_large_every_tile(transposed, variant, monkeypatch):
     """A large shape with 4100-byte token rows and 8200-byte weight rows: the
     row-class TMA kernel (the automatic choice) and the load-staged kernel,
-    sampled against the oracle."""
+    against the oracle at a point in every output tile."""
     cfg = FUSED_CONFIGS["ep8tp2_E64_C256_M4096_H4096_t0_bf16"].replace(E=16, M=4100, H=4100)
     dinp = fused_inputs_device(cfg)
     w = [u.transpose(1, 2).contiguous() for u in dinp["w"]] if transposed else dinp["w"]
@@ -330,8 +423,9 @@ def test_unaligned_large_sampled(transposed, variant, monkeypatch):
     assert bra.fault_status() == 0
     for y in out:
         assert not torch.isnan(y).any().item()
-    err = _sampled_check(cfg, dinp, out, np.random.default_rng(11), per_rank=16)
-    assert err <= TOL["bf16"], f"sampled rel err {err:.3e}"
+    rng = np.random.default_rng(11)
+    err = _points_check(cfg, dinp, out, _tile_points(cfg, rng) + _sample_points(cfg, rng, 4))
+    assert err <= TOL["bf16"], f"rel err {err:.3e}"
 
 
 @pytest.mark.parametrize("variant", [None, "tc", "tc2"])

@@ -381,6 +381,49 @@ def test_sender_view_equals_receiver_view_brute_force(ep, tp, t, bias_ndim):
         np.testing.assert_array_equal(u, v)
 
 
+@pytest.mark.parametrize("ep,tp", [(1, 1), (2, 2), (4, 2), (2, 4)])
+@pytest.mark.parametrize("t", [0, 1])
+@pytest.mark.parametrize("bias", [True, False])
+@pytest.mark.parametrize("layout", ["blocked", "contiguous"])
+def test_group_outputs_are_the_full_oracles_blocks(ep, tp, t, bias, layout):
+    """One (s, e) evaluated alone gives exactly the blocks the whole-problem
+    oracle writes for it, at every receiver (both type-1 readings)."""
+    E, C, M, H = 3 * ep, 3 * tp, 5 * tp, 2 * tp
+    cfg = _cfg(ep, tp, E, C, M, H, t, dtype="bf16" if t else "fp16", seed=ep + 3 * tp,
+               bias=bias)
+    inp = fused_inputs_host(cfg)
+    y = _run(cfg, inp, type1_layout=layout)
+    El = E // ep
+    for s in range(ep):
+        for e in range(El):
+            rs = [s * tp + u for u in range(tp)]
+            bg = None if not bias else [inp["bias"][r].reshape(El, -1)[e] for r in rs]
+            blocks = of.group_outputs([inp["x"][r][e] for r in rs], [inp["w"][r][e] for r in rs],
+                                      bg, ep, tp, C, H, t, cfg.dtype, type1_layout=layout)
+            assert sorted(blocks) == [(j, u) for j in range(ep) for u in range(tp)]
+            for (j, u), blk in blocks.items():
+                np.testing.assert_array_equal(blk, y[j * tp + u][s * El + e])
+
+
+def test_group_outputs_brute_force():
+    """Against the receiver-view scalar loops on a tiny problem."""
+    ep, tp, E, C, M, H = 2, 2, 4, 4, 6, 4
+    for t in (0, 1):
+        cfg = _cfg(ep, tp, E, C, M, H, t, seed=11 + t)
+        inp = fused_inputs_host(cfg)
+        ref = of.naive_bmm_rs_a2a(inp["x"], inp["w"], inp["bias"], ep, tp, E, C, M, H, t,
+                                  "fp16")
+        for s in range(ep):
+            for e in range(E // ep):
+                rs = [s * tp + u for u in range(tp)]
+                blocks = of.group_outputs([inp["x"][r][e] for r in rs],
+                                          [inp["w"][r][e] for r in rs],
+                                          [inp["bias"][r][e, 0] for r in rs],
+                                          ep, tp, C, H, t, "fp16")
+                for (j, u), blk in blocks.items():
+                    np.testing.assert_array_equal(blk, ref[j * tp + u][s * (E // ep) + e])
+
+
 def test_point_evaluation_matches_full_oracle():
     cfg = _cfg(4, 2, 16, 12, 12, 4, 1)
     inp = fused_inputs_host(cfg)

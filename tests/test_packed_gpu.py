@@ -17,7 +17,8 @@ import torch
 
 import bmm_reducescatter_alltoall_gb300 as bra
 from oracle import fused as of
-from test_fused_gpu import (TOL, UNALIGNED_CASES, _oracle, _rel_err, _sampled_check, _shifted,
+from test_fused_gpu import (TOL, UNALIGNED_CASES, _oracle, _points_check, _rel_err,
+                            _sample_points, _shifted, _tile_points,
                             _to_dev)
 from workloads import FUSED_CONFIGS, FusedConfig, fused_inputs_device, fused_inputs_host
 
@@ -135,9 +136,9 @@ def test_packed_element_aligned_pointers(transposed):
 
 
 @pytest.mark.parametrize("transposed", [False, True])
-def test_packed_large_sampled(transposed):
+def test_packed_large_every_tile(transposed):
     """4100-element token and weight rows (8200-byte pitch), 16 ranks, both
-    operands copied; sampled against the oracle."""
+    operands copied; a point in every output tile against the oracle."""
     cfg = FUSED_CONFIGS["ep8tp2_E64_C256_M4096_H4096_t0_bf16"].replace(E=16, M=4100, H=4100)
     dinp = fused_inputs_device(cfg)
     w = [u.transpose(1, 2).contiguous() for u in dinp["w"]] if transposed else dinp["w"]
@@ -145,8 +146,9 @@ def test_packed_large_sampled(transposed):
     out = _call(cfg, dinp["x"], w, dinp["bias"], transposed, _workspace(need))
     for y in out:
         assert not torch.isnan(y).any().item()
-    err = _sampled_check(cfg, dinp, out, np.random.default_rng(13), per_rank=16)
-    assert err <= TOL["bf16"], f"sampled rel err {err:.3e}"
+    rng = np.random.default_rng(13)
+    err = _points_check(cfg, dinp, out, _tile_points(cfg, rng) + _sample_points(cfg, rng, 4))
+    assert err <= TOL["bf16"], f"rel err {err:.3e}"
 
 
 def test_workspace_contents_do_not_matter_and_calls_repeat_bit_identically():

@@ -61,6 +61,11 @@ def _args(argv=None):
                     help="instead of the step: all_to_all_v alone over a range of sizes "
                          "(L2 swept before every timed call), plus a CUDA graph of 100 "
                          "back-to-back calls per size; one JSON line per size")
+    ap.add_argument("--mma-peak", action="store_true",
+                    help="instead of the step: the tensor-core rate probe on every SM (dense "
+                         "kind::f16 FLOP per SM clock) and the peak it implies")
+    ap.add_argument("--sweep-core-num", type=int, nargs="*", default=None,
+                    help="core_num values for --a2av-sweep (default: each workload's L)")
     return ap.parse_args(argv)
 
 
@@ -192,9 +197,9 @@ def _peaks():
             d = json.load(f)
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
-                "source": "measured"}
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
-            "source": "fallback"}
+            "sm_max_mhz": 2070.0, "source": "fallback"}
 
 
 def _traffic_record(kernel: str):
@@ -495,6 +500,7 @@ def run_ours(a):
         "traffic": None if a_traffic is None else a_traffic["dram_bytes_per_launch"],
         "algorithmic_bytes_per_launch": a_bytes, "mean_ms": a_ms, "min_ms": min(a2av_ms),
         "B": bra.cal_all_to_all_v_blocks(acfg.P, acfg.L),
+        "blocks": bra.all_to_all_v_launch_blocks(acfg.P, acfg.L),
     }
 
     # ---- context: the same op unfused from torch ops (after the timed region) ----
@@ -592,6 +598,18 @@ def run_ours(a):
         del ix
         if bra.fault_status() != 0:
             raise RuntimeError("watchdog word set by the indexed exchange")
+
+    # ---- the tensor-core rate probe: dense FLOP per SM clock, measured, and
+    # the peak it gives at the maximum SM clock (after the timed region) ----
+    mma = mma_rate(bra, torch, dev, 1 << 12, torch.float16)
+    spec = mma["sms"] * (peaks.get("sm_max_mhz") or 2070.0) * 1e6 * mma["flop_per_sm_clk"] / 1e12
+    roofline["spec_peak"] = {
+        "tflops": spec, "frac": f_tflops / spec,
+        "derivation": f"{mma['sms']} SMs x {peaks.get('sm_max_mhz') or 2070.0:.0f} MHz x "
+                      f"{mma['flop_per_sm_clk']:.0f} FLOP per SM clock (tcgen05 kind::f16 "
+                      "probe, fp16, all SMs)",
+        "probe_mhz": mma["probe_mhz"],
+    }
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -789,91 +807,165 @@ def run_a2av_sweep(a):
     sweep = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     timed = max(a.steps, 20)
-    for base, field, values in SWEEP:
-        for v in values:
-            cfg = A2AV_CONFIGS[base].replace(**{field: v})
-            sc = a2av_counts(cfg)
-            dt = torch.int8 if cfg.dtype == "int8" else torch.float32
-            g = torch.Generator(device=dev)
-            g.manual_seed(cfg.seed)
-            ins = []
-            for i in range(cfg.P):
-                n = int(sc[i].sum())
-                if dt == torch.int8:
-                    ins.append(torch.randint(-128, 128, (n,), generator=g, device=dev,
-                                             dtype=torch.int8))
-                else:
-                    ins.append(torch.randn(n, generator=g, device=dev))
-            outs = [torch.empty(int(c), dtype=dt, device=dev) for c in sc.sum(axis=0)]
-            sc_d = torch.from_numpy(sc).to(dev)
-            book = [torch.empty((cfg.P, cfg.P), dtype=torch.int64, device=dev)
-                    for _ in range(3)]
+    cases = [(base, field, v, L) for base, field, values in SWEEP for v in values
+             for L in (a.sweep_core_num or [A2AV_CONFIGS[base].L])]
+    for base, field, v, L in cases:
+        cfg = A2AV_CONFIGS[base].replace(**{field: v, "L": L})
+        sc = a2av_counts(cfg)
+        dt = torch.int8 if cfg.dtype == "int8" else torch.float32
+        g = torch.Generator(device=dev)
+        g.manual_seed(cfg.seed)
+        ins = []
+        for i in range(cfg.P):
+            n = int(sc[i].sum())
+            if dt == torch.int8:
+                ins.append(torch.randint(-128, 128, (n,), generator=g, device=dev,
+                                         dtype=torch.int8))
+            else:
+                ins.append(torch.randn(n, generator=g, device=dev))
+        outs = [torch.empty(int(c), dtype=dt, device=dev) for c in sc.sum(axis=0)]
+        sc_d = torch.from_numpy(sc).to(dev)
+        book = [torch.empty((cfg.P, cfg.P), dtype=torch.int64, device=dev)
+                for _ in range(3)]
 
-            def call():
-                bra.all_to_all_v(ins, sc_d, outs, cfg.L, send_displs=book[0],
-                                 recv_counts=book[1], recv_displs=book[2])
+        def call():
+            bra.all_to_all_v(ins, sc_d, outs, cfg.L, send_displs=book[0],
+                             recv_counts=book[1], recv_displs=book[2])
 
-            for _ in range(max(a.warmup, 3)):
-                bra.l2_flush(sweep, stream=stream)
-                call()
-            torch.cuda.synchronize(dev)
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(timed)]
-            for e0, e1 in ev:
-                torch.cuda._sleep(20_000_000)   # keeps the GPU busy so the host runs ahead
-                bra.l2_flush(sweep, stream=stream)
-                e0.record(stream)
-                call()
-                e1.record(stream)
-            torch.cuda.synchronize(dev)
-            us = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
-            med = statistics.median(us)
+        for _ in range(max(a.warmup, 3)):
+            bra.l2_flush(sweep, stream=stream)
+            call()
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(timed)]
+        for e0, e1 in ev:
+            torch.cuda._sleep(20_000_000)   # keeps the GPU busy so the host runs ahead
+            bra.l2_flush(sweep, stream=stream)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
+        med = statistics.median(us)
 
-            # 100 back-to-back calls in one CUDA graph: launch cost amortised,
-            # inputs warm in L2 where they fit
-            graph = torch.cuda.CUDAGraph()
-            side = torch.cuda.Stream(dev)
-            side.wait_stream(stream)
-            with torch.cuda.stream(side):
+        # 100 back-to-back calls in one CUDA graph: launch cost amortised,
+        # inputs warm in L2 where they fit
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            call()
+        stream.wait_stream(side)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(graph):
+            for _ in range(100):
                 call()
-            stream.wait_stream(side)
-            torch.cuda.synchronize(dev)
-            with torch.cuda.graph(graph):
-                for _ in range(100):
-                    call()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(3):
             graph.replay()
-            torch.cuda.synchronize(dev)
-            g0 = torch.cuda.Event(enable_timing=True)
-            g1 = torch.cuda.Event(enable_timing=True)
-            g0.record(stream)
-            for _ in range(3):
-                graph.replay()
-            g1.record(stream)
-            torch.cuda.synchronize(dev)
-            graph_us = g0.elapsed_time(g1) * 1e3 / 300
-            if bra.fault_status() != 0:
-                raise RuntimeError("watchdog word set during the sweep")
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_us = g0.elapsed_time(g1) * 1e3 / 300
+        if bra.fault_status() != 0:
+            raise RuntimeError("watchdog word set during the sweep")
 
-            nbytes = 2 * int(sc.sum()) * ins[0].element_size() + 4 * sc.size * 8
-            gbs = nbytes / (med * 1e-6) / 1e9
-            print(json.dumps({
-                "sweep": "all_to_all_v", "workload": base, field: v, "P": cfg.P, "L": cfg.L,
-                "dtype": cfg.dtype, "bytes_moved": nbytes, "calls": timed,
-                "median_us": med, "min_us": us[0], "GB/s": gbs,
-                "frac_of_hbm": gbs / peaks["hbm_gbs"],
-                "graph_us_per_call": graph_us,
-                "graph_GB/s": nbytes / (graph_us * 1e-6) / 1e9,
-                "l2": "256 MiB read-only sweep before every timed call (not in the time); "
-                      "the graph replays run back to back without it",
-            }), flush=True)
-            del ins, outs, sc_d, book, graph
-            torch.cuda.empty_cache()
+        nbytes = 2 * int(sc.sum()) * ins[0].element_size() + 4 * sc.size * 8
+        gbs = nbytes / (med * 1e-6) / 1e9
+        print(json.dumps({
+            "sweep": "all_to_all_v", "workload": base, field: v, "P": cfg.P, "L": cfg.L,
+            "blocks": bra.all_to_all_v_launch_blocks(cfg.P, cfg.L),
+            "dtype": cfg.dtype, "bytes_moved": nbytes, "calls": timed,
+            "median_us": med, "min_us": us[0], "GB/s": gbs,
+            "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "graph_us_per_call": graph_us,
+            "graph_GB/s": nbytes / (graph_us * 1e-6) / 1e9,
+            "l2": "256 MiB read-only sweep before every timed call (not in the time); "
+                  "the graph replays run back to back without it",
+        }), flush=True)
+        del ins, outs, sc_d, book, graph
+        torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------
+# tensor-core rate probe (not the step: the per-SM dense f16 / bf16 rate)
+# --------------------------------------------------------------------------
+
+MMA_FLOP = 2 * 128 * 256 * 16      # one M=128 N=256 K=16 MMA
+
+
+def mma_rate(bra, torch, dev, iters, dtype, ctas=None):
+    """Run the probe on `ctas` SMs (default: all); per-SM FLOP per clock
+    (median over CTAs), the clock the probe ran at, and the whole launch's
+    TFLOP/s by CUDA events."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ctas = ctas or sms
+    bra.mma_rate_probe(ctas, 64, dtype)                    # warm-up
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    rec = bra.mma_rate_probe(ctas, iters, dtype)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    r = rec.cpu().numpy()
+    if (r[:, 2] != 0).any():
+        raise RuntimeError("tensor-core rate probe: a bounded wait ran out")
+    flop = iters * 4 * MMA_FLOP
+    per_clk = flop / r[:, 0]
+    mhz = r[:, 0] / r[:, 1] * 1e3
+    return {"ctas": int(ctas), "sms": int(sms), "distinct_sms": int(len(set(r[:, 3].tolist()))),
+            "iters": iters, "flop_per_sm_clk": float(statistics.median(per_clk)),
+            "flop_per_sm_clk_min": float(per_clk.min()), "probe_mhz": float(statistics.median(mhz)),
+            "tflops_events": ctas * flop / (e0.elapsed_time(e1) / 1e3) / 1e12}
+
+
+def run_mma_peak(a):
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from bmm_reducescatter_alltoall_gb300 import _build
+    _build.build()
+    import bmm_reducescatter_alltoall_gb300 as bra
+
+    peaks = _peaks()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    out = {}
+    wall0 = time.monotonic()
+    for name, dt in (("bf16", torch.bfloat16), ("fp16", torch.float16)):
+        out[name] = {"one_sm": mma_rate(bra, torch, dev, 1 << 14, dt, ctas=1),
+                     "all_sms": mma_rate(bra, torch, dev, 1 << 14, dt)}
+    wall1 = time.monotonic()
+    time.sleep(0.25)
+    sampler.mark(wall0, wall1)
+    clocks = sampler.stop()
+    rate = out["bf16"]["all_sms"]["flop_per_sm_clk"]
+    sms = out["bf16"]["all_sms"]["sms"]
+    max_mhz = peaks.get("sm_max_mhz") or 2070.0
+    print(json.dumps({
+        "probe": "tcgen05.mma.cta_group::1.kind::f16 M=128 N=256 K=16, operands resident in "
+                 "shared memory, one CTA per SM",
+        **out,
+        "spec_peak_tflops": sms * max_mhz * 1e6 * rate / 1e12,
+        "derivation": f"{sms} SMs x {max_mhz:.0f} MHz (maximum SM clock) x {rate:.0f} dense "
+                      "FLOP per SM clock (measured, bf16)",
+        "measured_peaks": {"bf16_tflops": peaks["bf16_tflops"],
+                           "bf16_tflops_sustained": peaks["bf16_tflops_sustained"]},
+        "clocks": clocks,
+    }), flush=True)
 
 
 def main(argv=None):
     a = _args(argv)
     if a.impl == "reference":
         run_reference(a)
+    elif a.mma_peak:
+        run_mma_peak(a)
     elif a.a2av_sweep:
         run_a2av_sweep(a)
     else:

@@ -22,7 +22,7 @@ __all__ = [
     "FusedOptions", "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
     "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked", "Plan", "bmm_rs_a2a_plan",
     "all_to_all_v_plan", "indexed_all_to_all_v_plan",
-    "cal_all_to_all_v_blocks", "l2_flush", "fault_status", "status_str", "version",
+    "cal_all_to_all_v_blocks", "all_to_all_v_launch_blocks", "l2_flush", "mma_rate_probe", "fault_status", "status_str", "version",
 ]
 
 FP16, BF16, FP32, INT8 = 0, 1, 2, 3
@@ -39,7 +39,8 @@ class FusedOptions(ctypes.Structure):
     """bra_fused_options of the C header."""
     _fields_ = [("transpose_weight", ctypes.c_int32), ("variant", ctypes.c_int32),
                 ("x_pitch", ctypes.c_int32), ("w_pitch", ctypes.c_int32),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64),
+                ("status", ctypes.c_void_p)]
 
 
 class BraError(RuntimeError):
@@ -78,6 +79,8 @@ def library() -> ctypes.CDLL:
     lib.bmm_rs_a2a_infer_shape.restype = c_int
     lib.cal_all_to_all_v_blocks.argtypes = [i64, i64]
     lib.cal_all_to_all_v_blocks.restype = i64
+    lib.all_to_all_v_launch_blocks.argtypes = [i64, i64]
+    lib.all_to_all_v_launch_blocks.restype = i64
     lib.all_to_all_v.argtypes = [pp, vp, vp, vp, vp, pp, i64, i64, c_int, vp]
     lib.all_to_all_v.restype = c_int
     lib.all_to_all_v_checked.argtypes = [pp, vp, vp, vp, vp, pp, i64, i64, c_int, i64p, vp, vp]
@@ -91,6 +94,8 @@ def library() -> ctypes.CDLL:
     lib.bra_l2_flush.restype = c_int
     lib.bra_fault_status.argtypes = [ctypes.POINTER(i32), c_int]
     lib.bra_fault_status.restype = c_int
+    lib.bra_mma_rate_probe.argtypes = [c_int, c_int, c_int, vp, vp]
+    lib.bra_mma_rate_probe.restype = c_int
     lib.bra_wait_selftest.argtypes = [c_int, vp, vp]
     lib.bra_wait_selftest.restype = c_int
     lib.bra_version.argtypes = []
@@ -185,12 +190,18 @@ def _pitched_ptrs(ts, what: str, dtype, shape):
         if t.is_contiguous():
             p = shape[2]
         else:
+            # Strides of unit dimensions do not address anything: with d1 = 1
+            # the pitch is the step between d0 entries.
+            d0, d1, d2 = shape
             s0, s1, s2 = t.stride()
-            p = s1
-            if not (s2 == 1 and shape[1] > 1 and p >= shape[2] and
-                    (shape[0] == 1 or s0 == shape[1] * p)):
+            p = s1 if d1 > 1 else s0
+            if not ((d2 == 1 or s2 == 1) and p >= d2 and
+                    (d0 == 1 or s0 == d1 * p) and (d1 == 1 or s1 == p)):
                 raise ValueError(f"{name} must be contiguous or row-pitched (strides "
                                  f"(d1 * pitch, pitch, 1), pitch >= {shape[2]}); got {t.stride()}")
+            if p > 2**31 - 1:
+                raise ValueError(f"{name}: row pitch {p} elements exceeds the library's "
+                                 f"32-bit pitch field")
         if pitch is None:
             pitch = p
         elif p != pitch:
@@ -231,7 +242,8 @@ _VARIANTS = {None: 0, "auto": 0, "tc": VARIANT_TC, "tc2": VARIANT_TC2, "simt": V
              "tcu": VARIANT_TCU, "tcr": VARIANT_TCR, "packed": VARIANT_PACKED}
 
 
-def _options(transpose_weight: bool, variant, workspace=None, pitches=(0, 0)) -> "FusedOptions":
+def _options(transpose_weight: bool, variant, workspace=None, pitches=(0, 0),
+             status=None) -> "FusedOptions":
     if variant not in _VARIANTS:
         raise ValueError(f"variant must be one of {sorted(k for k in _VARIANTS if k)}")
     o = FusedOptions()
@@ -245,6 +257,12 @@ def _options(transpose_weight: bool, variant, workspace=None, pitches=(0, 0)) ->
             raise ValueError("workspace must be a contiguous CUDA tensor")
         o.workspace = workspace.data_ptr()
         o.workspace_bytes = workspace.numel() * workspace.element_size()
+    if status is not None:
+        torch = _torch()
+        if not (isinstance(status, torch.Tensor) and status.is_cuda and
+                status.dtype == torch.int32 and status.numel() >= 1):
+            raise ValueError("status must be a CUDA int32 tensor of at least one element")
+        o.status = status.data_ptr()
     return o
 
 
@@ -314,7 +332,7 @@ class Plan:
 def bmm_rs_a2a_plan(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int, tp: int,
                     E: int, C: int, M: int, H: int, y_shard_type: int,
                     out: Optional[Sequence] = None, transpose_weight: bool = False,
-                    variant: Optional[str] = None, workspace=None) -> Plan:
+                    variant: Optional[str] = None, workspace=None, status=None) -> Plan:
     """bmm_rs_a2a prepared once (see Plan); plan.run() returns out."""
     torch = _torch()
     if out is None:
@@ -334,16 +352,16 @@ def bmm_rs_a2a_plan(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep:
         if n < 0:
             raise BraError(-n, "bmm_rs_a2a_workspace_size")
         workspace = (torch.empty(n, dtype=torch.uint8, device=x[0].device) if n > 0 else None)
-    opts = _options(transpose_weight, variant, workspace, pitches)
+    opts = _options(transpose_weight, variant, workspace, pitches, status)
     args = (xp, wp, bp, ep, tp, E, C, M, H, y_shard_type, dt, yp, ctypes.byref(opts))
     return Plan(library().bmm_rs_a2a_ex, args, "bmm_rs_a2a", out,
-                (x, weight, bias, opts, xp, wp, bp, yp, workspace))
+                (x, weight, bias, opts, xp, wp, bp, yp, status, workspace))
 
 
 def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int, tp: int,
                E: int, C: int, M: int, H: int, y_shard_type: int,
                out: Optional[Sequence] = None, stream=None, transpose_weight: bool = False,
-               variant: Optional[str] = None, workspace=None) -> List:
+               variant: Optional[str] = None, workspace=None, status=None) -> List:
     """Fused BMM -> ReduceScatter -> Add -> AllToAll over P = ep*tp ranks.
 
     x[r], weight[r], bias[r] (or bias None) and out[r] are CUDA tensors of
@@ -357,11 +375,15 @@ def bmm_rs_a2a(x: Sequence, weight: Sequence, bias: Optional[Sequence], ep: int,
     bmm_rs_a2a_workspace_size(...) bytes, or "auto" to have one of that size
     taken from torch's allocator; given one, shapes whose x or weight rows
     lack a 16-byte pitch run the packed variant (operands repacked into it,
-    then the TMA kernel).  Returns out.  Asynchronous on `stream` (default: current stream).  For
-    repeated calls on the same buffers, bmm_rs_a2a_plan skips the checks.
+    then the TMA kernel).  status: an optional CUDA int32 tensor, this
+    call's own timeout word (0 before the kernels; ERR_TIMEOUT if a bounded
+    wait of this call gave up), unlike fault_status(), which every call on
+    the device shares.  Returns out.  Asynchronous on `stream` (default:
+    current stream).  For repeated calls on the same buffers,
+    bmm_rs_a2a_plan skips the checks.
     """
     return bmm_rs_a2a_plan(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
-                           transpose_weight, variant, workspace).run(stream)
+                           transpose_weight, variant, workspace, status).run(stream)
 
 
 # Size of the library's own scratch array used by bmm_rs_a2a_noalloc
@@ -426,6 +448,16 @@ def bmm_rs_a2a_variant(x, weight, bias, ep, tp, E, C, M, H, y_shard_type, out,
 
 def cal_all_to_all_v_blocks(P: int, L: int) -> int:
     return int(library().cal_all_to_all_v_blocks(int(P), int(L)))
+
+
+def all_to_all_v_launch_blocks(P: int, L: int) -> int:
+    """Thread blocks (one per SM) all_to_all_v launches on the current device
+    for P ranks and core_num L: CalAllToAllVBlocks(P, L), at most the SM
+    count."""
+    n = int(library().all_to_all_v_launch_blocks(int(P), int(L)))
+    if n < 0:
+        _check(-n, "all_to_all_v_launch_blocks")
+    return n
 
 
 def _a2av_args(inputs, send_counts, out, send_displs, recv_counts, recv_displs):
@@ -567,6 +599,19 @@ def wait_selftest(which: str, status, stream=None) -> None:
     _dev_tensor(status, "status", torch.int32)
     _check(library().bra_wait_selftest(code, status.data_ptr(), _stream_handle(stream)),
            "bra_wait_selftest")
+
+
+def mma_rate_probe(ctas: int, iters: int, dtype=None, stream=None):
+    """Tensor-core rate probe (bra_mma_rate_probe of the C header): `ctas`
+    CTAs, one per SM, each issuing iters x 4 back-to-back M=128 N=256 K=16
+    kind::f16 MMAs.  Returns a CUDA int64 tensor (ctas, 4): cycles, ns,
+    status, SM id per CTA (asynchronous on `stream`)."""
+    torch = _torch()
+    dt = BF16 if dtype is None or dtype == torch.bfloat16 else FP16
+    rec = torch.zeros((int(ctas), 4), dtype=torch.int64, device="cuda")
+    _check(library().bra_mma_rate_probe(int(ctas), int(iters), dt, rec.data_ptr(),
+                                        _stream_handle(stream)), "bra_mma_rate_probe")
+    return rec
 
 
 def fault_status(clear: bool = False) -> int:

@@ -65,6 +65,7 @@ KERNEL_SOURCES = {
     "a2av_kernel": "a2av.cu",
     "ia2av_kernel": "ia2av.cu",
     "repack_rows_kernel": "repack.cu",
+    "mma_probe_kernel": "mma_probe.cu",
 }
 
 

@@ -85,6 +85,7 @@ int validate_fused(const void* const x[], const void* const weight[],
   prob->type = (int)type;
   prob->dtype = dtype;
   prob->wt = (opts && opts->transpose_weight) ? 1 : 0;
+  prob->status = opts ? opts->status : nullptr;
   prob->xp = (int)Kp;
   prob->wp = prob->wt ? (int)Kp : (int)H;
   rc = apply_pitches(opts, prob);
@@ -373,11 +374,12 @@ int a2av_common(const void* const input[], const int64_t* send_counts,
   a.P = (int)P;
   a.esize = dtype == BRA_FP32 ? 4 : 1;
   a.check_cap = checked ? 1 : 0;
-  const int ctas = bra::a2av_ctas_per_rank((int)P);
+  const int blocks = bra::a2av_launch_blocks(B);
+  if (blocks < 1) return BRA_ERR_CUDA;
   if (log_enabled())
-    std::fprintf(stderr, "[bra] all_to_all_v P=%lld L=%lld B=%lld ctas/rank=%d grid=(%d,%lld)\n",
-                 (long long)P, (long long)core_num, (long long)B, ctas, ctas, (long long)P);
-  cudaError_t e = bra::launch_a2av(a, ctas, stream);
+    std::fprintf(stderr, "[bra] all_to_all_v P=%lld L=%lld B=%lld blocks=%d\n", (long long)P,
+                 (long long)core_num, (long long)B, blocks);
+  cudaError_t e = bra::launch_a2av(a, blocks, stream);
   return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
 }
 
@@ -460,6 +462,9 @@ int bmm_rs_a2a_ex(const void* const x[], const void* const weight[],
     std::fprintf(stderr, "[bra] bmm_rs_a2a ep=%lld tp=%lld E=%lld C=%lld M=%lld H=%lld type=%lld -> %s\n",
                  (long long)ep, (long long)tp, (long long)E, (long long)C, (long long)M,
                  (long long)H, (long long)yShardType, variant_name(v));
+  if (p.status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), (cudaStream_t)stream) !=
+                      cudaSuccess)
+    return BRA_ERR_CUDA;
   if (v == BRA_VARIANT_PACKED) return run_packed(p, opts, (cudaStream_t)stream);
   cudaError_t e = v == BRA_VARIANT_TC2   ? bra::launch_fused_tc2(p, (cudaStream_t)stream)
                   : v == BRA_VARIANT_TC  ? bra::launch_fused_tc(p, (cudaStream_t)stream)
@@ -543,6 +548,15 @@ int64_t cal_all_to_all_v_blocks(int64_t P, int64_t L) {
   return (L / P) * P;
 }
 
+int64_t all_to_all_v_launch_blocks(int64_t P, int64_t L) {
+  if (P < 1 || L < 1 || L > kInt32Max) return -BRA_ERR_INVALID;
+  if (P > bra::kA2avMaxP) return -BRA_ERR_UNSUPPORTED;
+  const int64_t B = cal_all_to_all_v_blocks(P, L);
+  if (B < 1 || B * P > kInt32Max) return -BRA_ERR_INVALID;
+  const int n = bra::a2av_launch_blocks(B);
+  return n < 1 ? -BRA_ERR_CUDA : n;
+}
+
 int all_to_all_v(const void* const input[], const int64_t* send_counts,
                  int64_t* send_displs, int64_t* recv_counts,
                  int64_t* recv_displs, void* const out[], int64_t P,
@@ -605,6 +619,20 @@ int bra_wait_selftest(int which, int32_t* status_dev, bra_stream_t stream) {
     e = bra::launch_tcr_wait_probe(status_dev, (cudaStream_t)stream);
   else
     return BRA_ERR_INVALID;
+  return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
+}
+
+int bra_mma_rate_probe(int ctas, int iters, int dtype, int64_t* rec_dev, bra_stream_t stream) {
+  if (!rec_dev) return BRA_ERR_NULLPTR;
+  if (dtype != BRA_FP16 && dtype != BRA_BF16) return BRA_ERR_INVALID;
+  if (iters < 1 || iters > (1 << 22)) return BRA_ERR_INVALID;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  if (ctas < 1 || ctas > sms) return BRA_ERR_INVALID;
+  const cudaError_t e =
+      bra::launch_mma_probe(ctas, iters, dtype == BRA_BF16, rec_dev, (cudaStream_t)stream);
   return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
 }
 

@@ -30,10 +30,15 @@ struct A2avArgs {
   int P;
   int esize;                // element size in bytes (4 or 1)
   int check_cap;            // compare received totals against cap[]
+  int stages;               // ring depth (set by launch_a2av)
 };
 
-// Launch the exchange with `ctas_per_rank` CTAs per source rank.
-cudaError_t launch_a2av(const A2avArgs& a, int ctas_per_rank, cudaStream_t st);
+// Blocks the exchange launches for an admitted block count B on the current
+// device: B, at most the SM count (one block per SM); -1 if the device
+// cannot be queried.
+int a2av_launch_blocks(int64_t B);
+// Launch the exchange on `blocks` blocks.
+cudaError_t launch_a2av(const A2avArgs& a, int blocks, cudaStream_t st);
 
 // Indexed exchange: rank i's send list is input[i] gathered through idx[i].
 struct IA2avArgs {
@@ -51,8 +56,6 @@ struct IA2avArgs {
 };
 cudaError_t launch_ia2av(const IA2avArgs& a, int ctas_per_rank, cudaStream_t st);
 int ia2av_ctas_per_rank(int P);
-// CTAs per rank that fill the GPU once.
-int a2av_ctas_per_rank(int P);
 
 // Problem description shared by the fused kernels.
 struct FusedProblem {
@@ -69,6 +72,7 @@ struct FusedProblem {
   // tensors; larger for repacked copies, whose rows start 16-byte aligned.
   // Only the TMA kernels (fused_tc*) accept pitches other than the lengths.
   int xp, wp;
+  int32_t* status;           // per-call timeout word (optional)
 };
 
 cudaError_t launch_fused_simt(const FusedProblem& f, cudaStream_t st);
@@ -86,6 +90,8 @@ cudaError_t launch_fused_tcr(const FusedProblem& f, cudaStream_t st);
 bool fused_tcr_eligible(const FusedProblem& f);
 
 cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t st);
+// Tensor-core rate probe: `ctas` CTAs, one per SM, each iters x 4 MMAs.
+cudaError_t launch_mma_probe(int ctas, int iters, bool bf16, int64_t* rec, cudaStream_t st);
 
 // Row repacking: copies rows of 16-bit elements that start at any even byte
 // address to rows that start 16-byte aligned, `pitch` elements apart.

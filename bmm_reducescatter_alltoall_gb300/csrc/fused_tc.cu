@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tc_kernel(const __grid_const
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && p.status && *abort_flag) atomicExch(p.status, (int32_t)BRA_ERR_TIMEOUT);
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc<1>(tmem_base, TMEM_COLS);

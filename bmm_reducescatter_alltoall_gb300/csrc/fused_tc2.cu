@@ -261,6 +261,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();   // no remote arrive or MMA of the pair still pending
+  if (threadIdx.x == 0 && p.status && *abort_flag) atomicExch(p.status, (int32_t)BRA_ERR_TIMEOUT);
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc<2>(tmem_base, TMEM_COLS);

@@ -124,6 +124,7 @@ struct RParams {
   int b_kmajor;                // weight stored transposed: B rows are N rows
   int lgx, lgw;                // log2 of the class counts of x rows and weight rows
   uint32_t idesc;
+  int32_t* status;             // per-call timeout word (optional)
 };
 static_assert(sizeof(RParams) <= 32764, "kernel parameter space");
 
@@ -564,6 +565,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();   // no remote arrive or MMA of the pair still pending
+  if (threadIdx.x == 0 && p.status && *abort_flag) atomicExch(p.status, (int32_t)BRA_ERR_TIMEOUT);
   if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc<2>(tmem_base, TMEM_COLS);
@@ -727,6 +729,7 @@ cudaError_t launch_fused_tcr(const FusedProblem& f, cudaStream_t st) {
   p->H = f.H;
   p->type = f.type;
   p->has_bias = f.bias != nullptr;
+  p->status = f.status;
   p->b_kmajor = f.wt;
   p->rows = f.ep * f.C;
   p->m_tiles = (p->rows + BM - 1) / BM;

@@ -82,6 +82,7 @@ struct UParams {
   int s0, rows, m_tiles, n_tiles, k_blocks, num_tiles;
   int b_kmajor;
   uint32_t idesc;
+  int32_t* status;   // per-call timeout word (optional)
 };
 
 __device__ __forceinline__ uint4 ldg128(uintptr_t a) {
@@ -331,6 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1) fused_tcu_kernel(const __grid_cons
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && p.status && *abort_flag) atomicExch(p.status, (int32_t)BRA_ERR_TIMEOUT);
   if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc<1>(tmem_base, TMEM_COLS);
@@ -374,6 +376,7 @@ cudaError_t launch_fused_tcu(const FusedProblem& f, cudaStream_t st) {
   p->H = f.H;
   p->type = f.type;
   p->has_bias = f.bias != nullptr;
+  p->status = f.status;
   p->b_kmajor = f.wt;
   p->rows = f.ep * f.C;
   p->m_tiles = (p->rows + BM - 1) / BM;

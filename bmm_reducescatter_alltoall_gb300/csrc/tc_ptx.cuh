@@ -37,6 +37,7 @@ struct TcParams {
   int b_kmajor;                  // weight stored transposed: B is K-major
   int y_elem;                    // output rows / pointers or bias not 16-byte aligned:
                                  // the element-wise epilogue (tcu_epilogue.cuh)
+  int32_t* status;               // per-call timeout word (optional)
 };
 
 // ---------------------------------------------------------------------------
@@ -568,6 +569,7 @@ inline void fill_common(TcParams* p, const FusedProblem& f, int bm, int bn, int 
   p->type = f.type;
   p->has_bias = f.bias != nullptr;
   p->b_kmajor = f.wt;
+  p->status = f.status;
   p->rows = f.ep * f.C;
   // 16-byte vector stores need 16-byte output rows and pointers, and the
   // vector bias loads 16-byte bias rows and pointers.

@@ -23,8 +23,13 @@
  *     asynchronously.  The return value reports argument validation and the
  *     launch itself, not completion; on any error nothing is launched unless
  *     the code is BRA_ERR_CUDA from the launch.
- *   - Calls are stateless: calls whose outputs are disjoint may run
- *     concurrently on different streams.
+ *   - Calls keep no state from one call to the next, so calls whose outputs
+ *     are disjoint may run concurrently on different streams.  Two things
+ *     are shared: the watchdog words that bra_fault_status reads (one set
+ *     per device, written by any call whose bounded wait gave up, on any
+ *     stream; for a word of one call's own, use the status of
+ *     all_to_all_v_checked, indexed_all_to_all_v or bra_fused_options), and
+ *     the scratch array of bmm_rs_a2a_noalloc.
  *   - Functions are thread-safe.
  */
 #ifndef BMM_RS_A2A_H
@@ -186,6 +191,12 @@ typedef struct {
    * work on `stream` completes. */
   void* workspace;
   int64_t workspace_bytes;
+  /* Optional device int32 of this call alone (NULL: none).  Set to BRA_OK on
+   * `stream` before the call's kernels; a kernel whose bounded wait gives up
+   * then writes BRA_ERR_TIMEOUT to it (its output is then incomplete).
+   * Unlike the per-device words bra_fault_status reads, which every call on
+   * the device shares, a timeout in another call never reaches it. */
+  int32_t* status;
 } bra_fused_options;
 
 /*
@@ -312,6 +323,20 @@ BRA_API int bmm_rs_a2a_variant(const void* const x[], const void* const weight[]
 BRA_API int64_t cal_all_to_all_v_blocks(int64_t P, int64_t L);
 
 /*
+ * all_to_all_v_launch_blocks -- thread blocks all_to_all_v and
+ * all_to_all_v_checked launch on the current device for P ranks and
+ * core_num L: B = cal_all_to_all_v_blocks(P, L), at most the device's SM
+ * count.  Each block takes a whole SM (its shared memory leaves room for no
+ * other block), so the exchange occupies that many SMs and no more; B above
+ * the SM count is clamped because blocks beyond it could not all be resident
+ * at once, which [PTO] §启动宽度 requires of the admitted blocks.
+ * Returns the count, -BRA_ERR_INVALID for arguments all_to_all_v rejects
+ * (P outside [1, 64] gives -BRA_ERR_UNSUPPORTED above 64), or -BRA_ERR_CUDA
+ * when the device cannot be queried.  Host function; queries the device.
+ */
+BRA_API int64_t all_to_all_v_launch_blocks(int64_t P, int64_t L);
+
+/*
  * all_to_all_v -- variable-count exchange among P virtual ranks ([PTO] §行为
  * and §ABI; addressing as in [VCCL] §5 ref): rank i sends send_counts[i][j]
  * elements to rank j, for every pair including i == j:
@@ -333,11 +358,13 @@ BRA_API int64_t cal_all_to_all_v_blocks(int64_t P, int64_t L);
  *                (the caller's obligation here; see all_to_all_v_checked);
  *                may be NULL when that sum is 0.
  *   P            number of ranks, 1 <= P <= 64.
- *   core_num     requested block count L per rank, in [1, INT32_MAX],
- *                validated with B = cal_all_to_all_v_blocks(P, L).  B is an
- *                Ascend launch width; here each rank's send buffer is split
- *                into as many equal ranges as fill the GPU once, which the
- *                results do not depend on.
+ *   core_num     requested block count L, in [1, INT32_MAX].  The call
+ *                launches B = cal_all_to_all_v_blocks(P, L) thread blocks,
+ *                one per SM, at most the SM count
+ *                (all_to_all_v_launch_blocks): the exchange occupies B SMs
+ *                and leaves the others to concurrent work.  The blocks split
+ *                the concatenated send buffers of ranks 0..P-1 into equal
+ *                element ranges; results do not depend on B.
  *   dtype        BRA_FP32 or BRA_INT8 ([PTO] §约束与诊断 allowlist).
  * Errors (nothing launched):
  *   BRA_ERR_NULLPTR  input, out, send_counts or a bookkeeping array is NULL.
@@ -442,7 +469,9 @@ BRA_API int bra_l2_flush(void* buf, size_t bytes, bra_stream_t stream);
  * bra_fault_status -- the watchdog words of the current device: 0, or the
  * BRA_ERR_TIMEOUT code a kernel (a tensor-core fused kernel or all_to_all_v) recorded
  * when one of its bounded waits gave up (the kernel then stops early and its
- * output is incomplete).
+ * output is incomplete).  The words belong to the device, not to a call:
+ * every call on the device, on any stream, writes the same words, so a set
+ * word says that some call timed out since the last clear, not which.
  * Synchronous (reads device memory after prior work on the legacy stream).
  * With clear != 0 the word is reset to 0.  Returns BRA_OK or BRA_ERR_CUDA.
  */
@@ -465,6 +494,25 @@ BRA_API int bra_fault_status(int32_t* code, int clear);
  */
 enum { BRA_WAIT_A2AV = 0, BRA_WAIT_TC = 1, BRA_WAIT_TC_CLUSTER = 2 };
 BRA_API int bra_wait_selftest(int which, int32_t* status_dev, bra_stream_t stream);
+
+/*
+ * bra_mma_rate_probe -- measurement aid for the tensor-core roofline: the
+ * dense kind::f16 rate of an SM, measured.  Launches `ctas` CTAs, one per SM
+ * (at most the SM count); each issues iters x 4 back-to-back
+ * tcgen05.mma.cta_group::1.kind::f16 of M = 128, N = 256, K = 16 (2^20 FLOP
+ * each) on zero-filled operands already in shared memory, staged like the
+ * fused kernels' (128-byte swizzle, K-major A, N-major B), into one TMEM
+ * accumulator, and writes its record to rec_dev[4 * c .. 4 * c + 3] (device
+ * int64): SM clock cycles and %globaltimer nanoseconds from the first issue
+ * to the completion of the last, BRA_OK or BRA_ERR_TIMEOUT (its bounded
+ * wait, about 4 s, ran out), and the SM id.  FLOP per SM clock =
+ * iters * 4 * 2^20 / cycles.  dtype: BRA_FP16 or BRA_BF16.  Asynchronous on
+ * `stream`.  Returns BRA_ERR_NULLPTR, BRA_ERR_INVALID (ctas outside
+ * [1, SM count], iters outside [1, 2^22], other dtype), BRA_ERR_CUDA or
+ * BRA_OK.
+ */
+BRA_API int bra_mma_rate_probe(int ctas, int iters, int dtype, int64_t* rec_dev,
+                               bra_stream_t stream);
 
 /* Library version, "major.minor.patch". */
 BRA_API const char* bra_version(void);

@@ -142,6 +142,29 @@ def test_rank_counts_and_launch_widths(P, dt):
         check_exact(sc, inputs, dt, L)
 
 
+@pytest.mark.parametrize("P,L", [(8, 1), (8, 3), (8, 8), (8, 19), (32, 64), (32, 10**6),
+                                 (64, 200), (3, 2)])
+def test_launch_blocks_follow_core_num(P, L, capfd, monkeypatch):
+    """The exchange launches B = CalAllToAllVBlocks(P, L) blocks, one per SM,
+    at most the SM count, and stays bit-exact at every width."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B = bra.cal_all_to_all_v_blocks(P, L)
+    want = min(B, sms)
+    assert bra.all_to_all_v_launch_blocks(P, L) == want
+    monkeypatch.setenv("BRA_LOG", "1")
+    sc, inputs = _random_case(P, "int8", seed=7 * P + L % 1009, hi=5000 if P <= 8 else 600)
+    check_exact(sc, inputs, "int8", L, in_off=[k % 16 for k in range(P)])
+    assert f"B={B} blocks={want}" in capfd.readouterr().err
+
+
+@pytest.mark.parametrize("L", [1, 5, 64, 152])
+def test_sixty_four_ranks_many_chunks(L):
+    """P = 64 (the largest count matrix, the shortest ring) with pieces that
+    span many ring wraps per block, from one block up to one per SM."""
+    sc, inputs = _random_case(64, "int8", seed=640 + L, hi=12000, zero_frac=0.3)
+    check_exact(sc, inputs, "int8", L, in_off=[(3 * k) % 16 for k in range(64)])
+
+
 @pytest.mark.parametrize("dt", ["fp32", "int8"])
 def test_every_byte_misalignment(dt):
     P = 4

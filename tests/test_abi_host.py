@@ -61,6 +61,21 @@ def test_cal_blocks_matches_oracle(lib):
     assert bra.cal_all_to_all_v_blocks(0, 4) == -1
 
 
+def test_launch_blocks_rejects_what_the_exchange_rejects(lib):
+    """all_to_all_v_launch_blocks refuses the arguments all_to_all_v refuses
+    (without a device, valid arguments fail only at the device query)."""
+    import torch
+    for P, L, code in ((0, 4, INVALID), (8, 0, INVALID), (8, 2**31, INVALID),
+                       (65, 65, bra.ERR_UNSUPPORTED), (64, 2**31 - 1, INVALID)):
+        with pytest.raises(bra.BraError) as e:
+            bra.all_to_all_v_launch_blocks(P, L)
+        assert e.value.code == code, (P, L)
+    if not torch.cuda.is_available():
+        with pytest.raises(bra.BraError) as e:
+            bra.all_to_all_v_launch_blocks(8, 10)
+        assert e.value.code == bra.ERR_CUDA
+
+
 def test_infer_shape_matches_oracle_and_rules(lib):
     rng = np.random.default_rng(0)
     seen_ok = seen_bad = 0
@@ -416,18 +431,19 @@ def test_wait_selftest_argument_checks(lib):
 
 def test_options_struct_layout():
     """bra_fused_options: four int32 fields (layout, variant, the two row
-    pitches), then the workspace pointer and its int64 size (32 bytes,
-    8-byte aligned)."""
+    pitches), the workspace pointer and its int64 size, then the per-call
+    status pointer (40 bytes, 8-byte aligned)."""
     F = bra.FusedOptions
-    assert ctypes.sizeof(F) == 32 and ctypes.alignment(F) == 8
+    assert ctypes.sizeof(F) == 40 and ctypes.alignment(F) == 8
     assert [getattr(F, n).offset for n in ("transpose_weight", "variant", "x_pitch", "w_pitch",
-                                           "workspace", "workspace_bytes")] == [0, 4, 8, 12, 16, 24]
+                                           "workspace", "workspace_bytes", "status")] == \
+        [0, 4, 8, 12, 16, 24, 32]
     src = pathlib.Path(HEADER).read_text()
     body = src[src.index("int32_t transpose_weight;"):src.index("} bra_fused_options;")]
-    decls = re.findall(r"^\s*(int32_t|void\*|int64_t)\s+(\w+)", body, flags=re.M)
+    decls = re.findall(r"^\s*(int32_t\*|int32_t|void\*|int64_t)\s+(\w+)", body, flags=re.M)
     assert decls == [("int32_t", "transpose_weight"), ("int32_t", "variant"),
                      ("int32_t", "x_pitch"), ("int32_t", "w_pitch"), ("void*", "workspace"),
-                     ("int64_t", "workspace_bytes")]
+                     ("int64_t", "workspace_bytes"), ("int32_t*", "status")]
 
 
 def _ws_opts(ptr, nbytes, variant=None, transposed=False):
@@ -660,3 +676,13 @@ def test_binding_detects_row_pitches():
         bra._pitched_ptrs([odd], "x", torch.float16, shape)
     with pytest.raises(TypeError):
         bra._pitched_ptrs([fake(shape).float()], "x", torch.float16, shape)
+    # d1 = 1 (ep*C = 1 rows per expert): the pitch is the step between experts.
+    one = (4, 1, 6)
+    _, p = bra._pitched_ptrs([fake(one, 11), fake(one, 11)], "x", torch.float16, one)
+    assert p == 11
+    # A pitch beyond the library's 32-bit field is refused, not wrapped.
+    big = 2**31
+    huge = torch.empty_strided((2, 2, 4), (2 * big, big, 1), dtype=torch.float16,
+                               device="meta").as_subclass(FakeCuda)
+    with pytest.raises(ValueError, match="32-bit pitch"):
+        bra._pitched_ptrs([huge], "x", torch.float16, (2, 2, 4))

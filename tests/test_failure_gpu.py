@@ -43,3 +43,37 @@ def test_bounded_wait_runs_out_and_reports(which):
     assert bra.fault_status() == 0
     assert _exchange_is_exact()
     assert bra.fault_status() == 0
+
+
+def test_fused_status_word_is_the_calls_own():
+    """A bounded wait that runs out on one stream sets the device's watchdog
+    word, which every call shares, but not the status word of a fused call
+    running meanwhile on another stream: that word is set to 0 before the
+    call's kernels and stays 0, and the call's output matches the oracle."""
+    from oracle import fused as of
+    from workloads import FUSED_CONFIGS, fused_inputs_host
+
+    bra.fault_status(clear=True)
+    cfg = FUSED_CONFIGS["ep4tp2_E16_C12_M12_H4_t1_fp16"].replace(name="st", C=128, M=256, H=256)
+    inp = fused_inputs_host(cfg)
+    dev = {k: [t.cuda() for t in v] for k, v in inp.items()}
+    probe_status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    call_status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    bra.wait_selftest("tc", probe_status, stream=s1)
+    out = bra.bmm_rs_a2a(dev["x"], dev["w"], dev["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M,
+                         cfg.H, cfg.y_shard_type, stream=s2, status=call_status)
+    s2.synchronize()
+    assert int(call_status.item()) == 0      # done while the probe still waits
+    torch.cuda.synchronize()
+    assert int(probe_status.item()) == bra.ERR_TIMEOUT
+    assert bra.fault_status() == bra.ERR_TIMEOUT
+    assert int(call_status.item()) == 0
+    ref = of.bmm_rs_a2a(inp["x"], inp["w"], inp["bias"], cfg.ep, cfg.tp, cfg.E, cfg.C, cfg.M,
+                        cfg.H, cfg.y_shard_type, cfg.dtype)
+    g = np.concatenate([o.float().cpu().numpy().ravel() for o in out]).astype(np.float64)
+    r = np.concatenate([a.ravel() for a in ref])
+    assert np.max(np.abs(g - r)) / np.max(np.abs(r)) <= 2e-3
+    bra.fault_status(clear=True)
+    assert bra.fault_status() == 0

@@ -272,3 +272,220 @@ def test_element_epilogue_staging_shift(delta):
     for wd in buf:
         elems += [None, None] if wd is None else [wd & 0xFFFF, wd >> 16]
     assert elems[delta:delta + 64] == list(range(64))
+
+
+# ---------------------------------------------------------------------------
+# all_to_all_v kernel (a2av.cu): block ranges, segments, staged chunks, the
+# consumer groups' chunk shares and the piece writes.
+A2AV_CHUNK, A2AV_STRIDE, A2AV_GROUPS, A2AV_MAXSEG = 16384, 16384 + 128, 4, 4
+
+
+def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_mem, written):
+    """Run the kernel's addressing for every block: `mem` maps a source
+    address to its byte value, `out_mem` / `written` receive the stores.
+    Checks every staged read and every store against the buffers."""
+    P = sc.shape[0]
+    rowtot = sc.sum(axis=1)
+    T = int(rowtot.sum())
+    rowoff = np.concatenate([[0], np.cumsum(rowtot)[:-1]])
+    sd = np.concatenate([np.zeros((P, 1), np.int64), np.cumsum(sc, axis=1)[:, :-1]], axis=1)
+    rd = np.concatenate([np.zeros((1, P), np.int64), np.cumsum(sc, axis=0)[:-1, :]], axis=0)
+    for b in range(nb):
+        q_, rem = divmod(T, nb)
+        lo, hi = q_ * b + min(b, rem), q_ * (b + 1) + min(b + 1, rem)
+        segs = []
+        for r in range(P):
+            off, tot = int(rowoff[r]), int(rowtot[r])
+            if tot > 0 and off < hi and off + tot > lo:
+                slo, shi = max(lo - off, 0), min(hi - off, tot)
+                g0 = (in_base[r] + slo * es) & ~15
+                g1 = (in_base[r] + shi * es + 15) & ~15
+                segs.append((r, slo, shi, g0, g1, -(-(g1 - g0) // A2AV_CHUNK)))
+        chbase = np.concatenate([[0], np.cumsum([s[5] for s in segs])]).astype(np.int64)
+        # Producer: chunk t of the block staged from [c0, ce).
+        staged = {}
+        t = 0
+        for (r, slo, shi, g0, g1, nch) in segs:
+            lo_g, hi_g = in_base[r] & ~15, (in_base[r] + in_len_b[r] + 15) & ~15
+            for c0 in range(g0, g1, A2AV_CHUNK):
+                ce = min(c0 + A2AV_CHUNK + 16, g1)
+                assert lo_g <= c0 < ce <= hi_g and (ce - c0) % 16 == 0 and c0 % 16 == 0
+                assert ce - c0 <= A2AV_STRIDE
+                staged[t] = (c0, ce)
+                t += 1
+        assert t == chbase[-1]
+        # Consumers, batch by batch.
+        for b0 in range(0, len(segs), A2AV_MAXSEG):
+            batch = segs[b0:b0 + A2AV_MAXSEG]
+            tables = []
+            for (i, slo, shi, g0, g1, nch) in batch:
+                pieces = []
+                for j in range(P):
+                    c = int(sc[i, j])
+                    c0e, c1e = max(slo, sd[i, j]), min(shi, sd[i, j] + c)
+                    n = (c1e - c0e) * es if c1e > c0e else 0
+                    if n == 0:
+                        continue
+                    src = in_base[i] + c0e * es
+                    dst = out_base[j] + (rd[i, j] + (c0e - sd[i, j])) * es
+                    head = min((16 - dst % 16) % 16, n)
+                    pieces.append((src, dst, (n - head) >> 4, head, (n - head) & 15, j))
+                tables.append(pieces)
+            tb, te = chbase[b0], chbase[b0 + len(batch)]
+            for g in range(A2AV_GROUPS):
+                t = tb + ((g - tb % A2AV_GROUPS) + A2AV_GROUPS) % A2AV_GROUPS
+                sg, q = b0, 0
+                while t < te:
+                    while chbase[sg + 1] <= t:
+                        sg, q = sg + 1, 0
+                    c0s, ce = staged[t]
+                    G1 = segs[sg][4]
+                    c0 = segs[sg][3] + (t - chbase[sg]) * A2AV_CHUNK
+                    assert c0 == c0s
+                    c1 = min(c0 + A2AV_CHUNK, G1)
+                    stage = mem[c0:ce]
+                    pcs = tables[sg - b0]
+                    qq = q
+                    while qq < len(pcs):
+                        src, dst, nvec, head, tail, j = pcs[qq]
+                        if src >= c1:
+                            break
+                        base = src + head
+                        pe = base + nvec * 16 + tail
+                        if pe <= c0:
+                            q = qq + 1
+                            qq += 1
+                            continue
+                        vlo = 0 if base >= c0 else (c0 - base + 15) >> 4
+                        vhi = 0 if base >= c1 else (c1 - base + 15) >> 4
+                        vhi = min(vhi, nvec)
+                        if vhi > vlo:
+                            o = base + vlo * 16 - c0
+                            k = np.arange(vhi - vlo)
+                            rd0 = (o & ~15) + 16 * k          # first staged word read
+                            assert rd0.min() >= 0 and (rd0 + 32).max() <= A2AV_STRIDE
+                            first = o + 16 * k                # the vector's bytes in the stage
+                            assert (first + 16).max() <= ce - c0
+                            d = dst + head + 16 * (vlo + k)
+                            assert (d % 16 == 0).all()
+                            idx = (first[:, None] + np.arange(16)).ravel()
+                            dd = (d[:, None] + np.arange(16)).ravel()
+                            out_mem[dd] = stage[idx]
+                            written[dd] += 1
+                        for off in list(range(head)) + [head + nvec * 16 + x for x in range(tail)]:
+                            sb = src + off
+                            if c0 <= sb < c1:
+                                out_mem[dst + off] = stage[sb - c0]
+                                written[dst + off] += 1
+                        if pe > c1:
+                            break
+                        q = qq + 1
+                        qq += 1
+                    t += A2AV_GROUPS
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("es", [1, 4])
+def test_exchange_block_addressing(seed, es):
+    """Every byte each rank receives is written exactly once with the right
+    source byte, staged reads stay inside the staged chunk (and its ring
+    slot), bulk loads stay inside the send buffer's 16-byte granules, and no
+    byte outside the received ranges is stored -- for launch widths below,
+    at and above P, unaligned bases and pieces spanning chunks."""
+    rng = np.random.default_rng(seed)
+    P = int(rng.choice([1, 2, 3, 5, 8]))
+    small = rng.integers(0, 40, size=(P, P))
+    big = rng.integers(0, 3 * A2AV_CHUNK // es, size=(P, P))
+    sc = np.where(rng.random((P, P)) < 0.4, big, small).astype(np.int64)
+    sc[rng.random((P, P)) < 0.2] = 0
+    in_len = sc.sum(axis=1) * es
+    out_len = sc.sum(axis=0) * es
+    # Buffers at 4096-byte-spaced slots plus an offset of whole elements.
+    addr = 4096
+    in_base, out_base = [], []
+    for n in in_len:
+        addr += int(rng.integers(0, 16 // es)) * es
+        in_base.append(addr)
+        addr = (addr + int(n) + 4096 + 4095) // 4096 * 4096
+    for n in out_len:
+        addr += int(rng.integers(0, 16 // es)) * es
+        out_base.append(addr)
+        addr = (addr + int(n) + 4096 + 4095) // 4096 * 4096
+    mem = rng.integers(0, 256, size=addr + 64).astype(np.uint8)
+    out_mem = np.zeros(addr + 64, np.uint8)
+    written = np.zeros(addr + 64, np.int32)
+    for nb in sorted({1, 3, max(1, P - 1), P, 2 * P + 1, 64}):
+        out_mem[:] = 0
+        written[:] = 0
+        _a2av_block_copy(sc, es, in_base, in_len, out_base, nb, 12, mem, out_mem, written)
+        expect_w = np.zeros_like(written)
+        for j in range(P):
+            expect_w[out_base[j]:out_base[j] + out_len[j]] = 1
+        assert np.array_equal(written, expect_w), nb
+        for i in range(P):
+            for j in range(P):
+                sdb = int(sc[i, :j].sum()) * es
+                rdb = int(sc[:i, j].sum()) * es
+                n = int(sc[i, j]) * es
+                assert np.array_equal(out_mem[out_base[j] + rdb:out_base[j] + rdb + n],
+                                      mem[in_base[i] + sdb:in_base[i] + sdb + n]), (nb, i, j)
+
+
+def _ring_schedule(stages, groups, nchunks, rng):
+    """One random interleaving of the exchange's ring protocol: a producer
+    loading chunk t into stage t % stages after a parity wait on the stage's
+    empty barrier, loads landing at random later times (completing a phase
+    of the stage's full barrier), and consumer group t % groups taking chunk
+    t after a parity wait on the full barrier, then arriving on the empty
+    barrier.  A parity wait on phase u passes when the number of completed
+    phases has the other parity (mbarrier try_wait.parity).  Returns False
+    when a group passed its wait while its stage held another chunk or had a
+    load in flight."""
+    full_c = [0] * stages
+    empty_c = [0] * stages
+    content = [-1] * stages
+    in_flight = {}                       # stage -> chunk
+    nxt = 0                              # producer's next chunk
+    todo = [list(range(g, nchunks, groups)) for g in range(groups)]
+    while nxt < nchunks or in_flight or any(todo):
+        moves = []
+        if nxt < nchunks:
+            s, u = nxt % stages, nxt // stages
+            if (empty_c[s] & 1) != ((u & 1) ^ 1):
+                moves.append(("issue", None))
+        moves += [("land", s) for s in in_flight]
+        for g in range(groups):
+            if todo[g]:
+                t = todo[g][0]
+                s, u = t % stages, t // stages
+                if (full_c[s] & 1) != (u & 1):
+                    moves.append(("take", g))
+        kind, arg = moves[rng.integers(len(moves))]
+        if kind == "issue":
+            s = nxt % stages
+            assert s not in in_flight
+            in_flight[s] = nxt
+            nxt += 1
+        elif kind == "land":
+            content[arg] = in_flight.pop(arg)
+            full_c[arg] += 1
+        else:
+            t = todo[arg].pop(0)
+            s = t % stages
+            if content[s] != t or s in in_flight:
+                return False
+            empty_c[s] += 1
+    return True
+
+
+def test_exchange_ring_protocol_under_random_schedules():
+    """With the stage count a multiple of the consumer groups (what the
+    launch enforces), no group ever reads a stage before its own chunk has
+    landed there, under any interleaving; with other stage counts some
+    interleaving makes a parity wait pass on an older phase."""
+    rng = np.random.default_rng(0)
+    for stages in (4, 8, 12):
+        for _ in range(300):
+            assert _ring_schedule(stages, A2AV_GROUPS, int(rng.integers(1, 80)), rng)
+    for stages in (6, 11):
+        assert not all(_ring_schedule(stages, A2AV_GROUPS, 60, rng) for _ in range(300))

@@ -232,13 +232,16 @@ def test_auto_workspace():
                        cfg2.H, cfg2.y_shard_type, workspace="big")
 
 
-def _padded_view(t, pitch):
+def _padded_view(t, pitch, offset=0):
     """A (d0, d1, pitch) buffer whose padding holds NaN, viewed as t's shape
-    and holding t's values: a row-pitched operand."""
+    and holding t's values: a row-pitched operand.  With an offset the view
+    starts that many elements into its buffer (a base address without
+    16-byte alignment)."""
     d0, d1, d2 = t.shape
-    buf = torch.full((d0, d1, pitch), float("nan"), dtype=t.dtype, device=t.device)
-    buf[:, :, :d2].copy_(t)
-    return buf[:, :, :d2]
+    buf = torch.full((offset + d0 * d1 * pitch,), float("nan"), dtype=t.dtype, device=t.device)
+    v = buf.as_strided((d0, d1, d2), (d1 * pitch, pitch, 1), offset)
+    v.copy_(t)
+    return v
 
 
 @pytest.mark.parametrize("case,xpitch,wpitch,transposed", [
@@ -250,6 +253,23 @@ def _padded_view(t, pitch):
     ((4, 2, 8, 96, 200, 300, 1, "bf16"), 103, 0, True),    # transposed, odd pitch
 ])
 def test_caller_pitched_operands(case, xpitch, wpitch, transposed):
+    _pitched_case(case, xpitch, wpitch, transposed, 0, 0)
+
+
+@pytest.mark.parametrize("case,xpitch,wpitch,xoff,woff", [
+    ((2, 2, 4, 6, 12, 4, 1, "fp16"), 7, 5, 1, 3),          # rows of 6 and 4, odd pitches
+    ((2, 2, 4, 6, 12, 4, 0, "bf16"), 7, 5, 5, 7),
+    ((2, 2, 4, 40, 130, 70, 0, "bf16"), 67, 73, 2, 6),     # Kp = 65 and H = 70
+    ((2, 2, 4, 40, 256, 70, 1, "fp16"), 0, 71, 0, 1),      # only the weight pitched
+])
+def test_caller_pitched_operands_unaligned_base(case, xpitch, wpitch, xoff, woff):
+    """Row-pitched views that start 1..7 elements into their buffers: base
+    addresses without 16-byte alignment reach the row-class kernel (short
+    rows included) and match the oracle; the padding is never read."""
+    _pitched_case(case, xpitch, wpitch, False, xoff, woff)
+
+
+def _pitched_case(case, xpitch, wpitch, transposed, xoff, woff):
     """Operands kept in padded buffers run with no copy and no workspace:
     16-byte pitches on the TMA kernels, other pitches on the row-class
     kernel; the padding (NaN) is never read."""
@@ -264,13 +284,13 @@ def test_caller_pitched_operands(case, xpitch, wpitch, transposed):
         xs = [_padded_view(x, xpitch) for x in d["x"]]
         ws = [_padded_view(u, xpitch) for u in w0]          # transposed rows are Kp long too
     else:
-        xs = [_padded_view(x, xpitch) for x in d["x"]] if xpitch else d["x"]
-        ws = [_padded_view(u, wpitch) for u in w0] if wpitch else w0
+        xs = [_padded_view(x, xpitch, xoff) for x in d["x"]] if xpitch else d["x"]
+        ws = [_padded_view(u, wpitch, woff) for u in w0] if wpitch else w0
     ys = bra.bmm_rs_a2a_infer_shape(ep, tp, E, C, M, H, t)["y"]
     probe = [torch.empty(ys, dtype=xs[0].dtype, device="cuda") for _ in range(cfg.P)]
     pitches = [p for p in (xpitch, wpitch) if p]
-    want = ((bra.VARIANT_TC, bra.VARIANT_TC2) if all(p % 8 == 0 for p in pitches)
-            else (bra.VARIANT_TCR,))
+    aligned = all(p % 8 == 0 for p in pitches) and xoff % 8 == 0 and woff % 8 == 0
+    want = (bra.VARIANT_TC, bra.VARIANT_TC2) if aligned else (bra.VARIANT_TCR,)
     assert bra.bmm_rs_a2a_variant(xs, ws, d["bias"], ep, tp, E, C, M, H, t, probe,
                                   transpose_weight=transposed) in want
     assert bra.bmm_rs_a2a_workspace_size(xs, ws, d["bias"], ep, tp, E, C, M, H, t, probe,

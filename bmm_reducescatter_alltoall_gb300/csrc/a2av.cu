@@ -24,25 +24,30 @@
 // the segments follow from them.  Every block sees the same matrix, so all
 // take the same verdict without a grid sync; a rejected call copies
 // nothing.
-// Roles after set-up:
-//   warp 0, lane 0   producer: streams the segments' source bytes through a
-//                    ring of `stages` chunks of kChunk bytes (16-byte
-//                    granules, each chunk staged with one granule more) with
-//                    cp.async.bulk (completion on an mbarrier);
-//   warps 1..        kGroups consumer groups of kGroupWarps warps; group g
-//                    takes chunks g, g + kGroups, ... and writes every vector
-//                    whose first source byte lies in the chunk, shifting the
-//                    words into destination alignment (int8 can be off by any
-//                    byte, fp32 by whole words), while the group's first warp
-//                    writes the head and tail bytes that lie in it.  Piece
-//                    tables are built kMaxSeg segments at a time.
-//   Afterwards the consumers write the bookkeeping (send displacements,
-//   receive counts, receive displacements), entries spread over all blocks.
+// Copy: the block's source bytes are cut into chunks of kChunk bytes
+// (16-byte granules; each chunk is staged with one granule more, so every
+// destination vector whose first byte lies in a chunk is whole in its
+// stage).  Chunk t belongs to warp t mod kWarps, and each warp is its own
+// pipeline: lane 0 streams the warp's chunks into the warp's private ring of
+// `stages` slots with cp.async.bulk (completion on the slot's mbarrier),
+// the warp writes every destination vector of the chunk, shifting the
+// staged words into destination alignment (int8 can be off by any byte,
+// fp32 by whole words), and lane 0 refills the slot with the warp's chunk
+// `stages` later.  One issuing thread per warp: a thread's bulk copies
+// complete at about one chunk per load latency, and a warp's own chunk work
+// is a chain of dependent steps, so many independent warp pipelines keep an
+// SM's loads and stores in flight.  Piece tables are built by all threads,
+// kMaxSeg segments at a time; the head and tail bytes of each piece (before
+// its first and after its last 16-byte-aligned destination vector) are
+// copied straight from the send buffer after the batch's chunks.
+// Afterwards the bookkeeping (send displacements, receive counts, receive
+// displacements) is written, its entries spread over all blocks.
 // A granule holding a byte of a buffer never crosses a page the buffer does
 // not touch, so granule-wide loads stay in bounds.  Every wait is bounded
 // (about 2 s by %globaltimer); a wait that runs out records BRA_ERR_TIMEOUT
-// in this file's device word, flags the CTA, and all roles leave their
-// loops (the consumers still meet their named barriers).
+// in this file's device word and flags the CTA; every warp then skips its
+// remaining chunks (still meeting the CTA barriers) and gives the copies it
+// issued time to land before the CTA ends.
 #include <cstdint>
 #include <mutex>
 
@@ -55,41 +60,36 @@ __device__ int32_t g_a2av_fault_word = 0;
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-#ifndef BRA_A2AV_GROUPS
-#define BRA_A2AV_GROUPS 4
-#endif
-#ifndef BRA_A2AV_GROUP_WARPS
-#define BRA_A2AV_GROUP_WARPS 4
+#ifndef BRA_A2AV_WARPS
+#define BRA_A2AV_WARPS 16
 #endif
 #ifndef BRA_A2AV_MAX_STAGES
-#define BRA_A2AV_MAX_STAGES 12
+#define BRA_A2AV_MAX_STAGES 3
 #endif
-constexpr int kGroups = BRA_A2AV_GROUPS;
-constexpr int kGroupWarps = BRA_A2AV_GROUP_WARPS;
-constexpr int kGroupThreads = 32 * kGroupWarps;
-constexpr int kConsumers = kGroups * kGroupThreads;
-constexpr int kThreads = 32 + kConsumers;
-constexpr int kWarps = kThreads / 32;
-constexpr int kMaxStages = BRA_A2AV_MAX_STAGES;
+#ifndef BRA_A2AV_CHUNK
+#define BRA_A2AV_CHUNK 4096
+#endif
+constexpr int kWarps = BRA_A2AV_WARPS;           // copy warps = pipelines per block
+constexpr int kThreads = 32 * kWarps;
+constexpr int kRowsPerWarp = (kA2avMaxP + kWarps - 1) / kWarps;   // count rows per warp at set-up
+constexpr int kMaxStages = BRA_A2AV_MAX_STAGES;  // ring slots per warp
 constexpr int kMaxSeg = 4;                       // segments whose pieces are tabled at once
-constexpr uint32_t kChunk = 16384;               // source bytes a chunk writes out
+constexpr uint32_t kChunk = BRA_A2AV_CHUNK;      // source bytes a chunk writes out
 constexpr int kStageStride = kChunk + 128;       // staged with one granule more
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
-static_assert(kConsumers >= kMaxSeg * kA2avMaxP, "one consumer thread per tabled piece");
-static_assert(kGroups * kGroupWarps >= kMaxSeg, "one compacting warp per tabled segment");
-// Chunk t goes to ring stage t % stages and to group t % kGroups.  With the
-// stage count a multiple of kGroups every stage belongs to one group, whose
-// uses of it are its own consecutive chunks; otherwise a group could wait on
-// a stage's full barrier two uses ahead of the load in flight, and the
-// parity wait would pass on the older phase.
-static_assert(kMaxStages % kGroups == 0, "stages come in whole multiples of the groups");
+static_assert(kThreads >= kMaxSeg * kA2avMaxP, "one thread per tabled piece");
+static_assert(kWarps >= kMaxSeg, "one compacting warp per tabled segment");
+static_assert((kChunk & (kChunk - 1)) == 0 && kChunk >= 512, "chunk: a power of two");
 
-struct Piece {
-  const char* src;   // first source byte
-  char* dst;         // first destination byte
-  int64_t nvec;      // 16-byte destination vectors
-  int head;          // bytes before the first vector
-  int tail;          // bytes after the last vector
+// One piece of a segment: its 16-byte-aligned destination vectors, and the
+// head and tail bytes before the first and after the last of them.
+struct Run {
+  uintptr_t vb;      // source address of the first vector's first byte
+  char* d;           // destination of the first vector (16-byte aligned)
+  int64_t nvec;      // vectors (the piece is listed for the chunk loop when > 0)
+  uint8_t delta;     // vb % 16: offset of the staged words from destination alignment
+  uint8_t head;      // bytes before the first vector
+  uint8_t tail;      // bytes after the last vector
 };
 
 __device__ __forceinline__ int64_t warp_sum64(int64_t v) {
@@ -148,9 +148,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -170,7 +167,8 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // Bounded wait for the phase with the given parity.  False when the CTA was
 // flagged by another role or the wait ran out (then this call flags the CTA
 // and records BRA_ERR_TIMEOUT in the device word).
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                            volatile int* abort_flag) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
@@ -185,9 +183,8 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
     }
   }
 }
-// Barrier among the consumer warps only (named barrier 1).
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort_flag);
 }
 // Bulk copy of `bytes` (a multiple of 16) from a 16-byte-aligned global
 // address into shared memory, completing on `bar`.
@@ -205,97 +202,96 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "r"(addr));
   return v;
 }
-__device__ __forceinline__ uint32_t lds8(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
 
 #ifndef BRA_A2AV_UNROLL
 #define BRA_A2AV_UNROLL 4
 #endif
 // Copy n destination vectors from a staged tile whose words start Q words +
 // r bits before the destination alignment (SHIFT false: the tile is in
-// destination alignment).  Each thread issues the shared-memory loads of
-// kUnroll vectors before the first store, so their latencies overlap.
+// destination alignment), by one warp: lane l takes vectors l, l + 32, ...
+// A lane loads its vector's first staged granule and takes the words it
+// needs of the next granule from the next lane (lane 31 loads that granule
+// itself): one shared-memory granule per vector.  Each lane issues the
+// loads of kUnroll vectors before the first store, so their latencies
+// overlap.
 constexpr int kUnroll = BRA_A2AV_UNROLL;
 template <int Q, bool SHIFT>
-__device__ __forceinline__ void vec_copy(uint4* d4, uint32_t buf, int n, int t, uint32_t r) {
-  int k = t;
+__device__ __forceinline__ void vec_copy(uint4* d4, uint32_t buf, int n, int lane, uint32_t r) {
+  if constexpr (!SHIFT) {
+    int k = lane;
 #pragma unroll 1
-  for (; k + (kUnroll - 1) * kGroupThreads < n; k += kUnroll * kGroupThreads) {
-    uint4 a[kUnroll], b[kUnroll];
+    for (; k + (kUnroll - 1) * 32 < n; k += kUnroll * 32) {
+      uint4 a[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t ad = buf + 16u * (uint32_t)(k + u * kGroupThreads);
-      a[u] = lds128(ad);
-      if (SHIFT) b[u] = lds128(ad + 16u);
+      for (int u = 0; u < kUnroll; ++u) a[u] = lds128(buf + 16u * (uint32_t)(k + u * 32));
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) d4[k + u * 32] = a[u];
     }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      d4[k + u * kGroupThreads] = SHIFT ? realign<Q>(a[u], b[u], r) : a[u];
-  }
 #pragma unroll 1
-  for (; k < n; k += kGroupThreads) {
-    const uint32_t ad = buf + 16u * (uint32_t)k;
-    d4[k] = SHIFT ? realign<Q>(lds128(ad), lds128(ad + 16u), r) : lds128(ad);
+    for (; k < n; k += 32) d4[k] = lds128(buf + 16u * (uint32_t)k);
+  } else {
+#pragma unroll 1
+    for (int base = 0; base < n; base += kUnroll * 32) {
+      uint4 a[kUnroll], nx[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int k = base + u * 32 + lane;
+        const uint32_t ad = buf + 16u * (uint32_t)k;
+        // Granule k: vector k's first, and the second of vector k - 1 (k <= n).
+        a[u] = k <= n ? lds128(ad) : make_uint4(0u, 0u, 0u, 0u);
+        nx[u] = (lane == 31 && k < n) ? lds128(ad + 16u) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int k = base + u * 32 + lane;
+        uint4 b;
+        b.x = __shfl_down_sync(kFull, a[u].x, 1);
+        b.y = Q >= 1 ? __shfl_down_sync(kFull, a[u].y, 1) : 0u;
+        b.z = Q >= 2 ? __shfl_down_sync(kFull, a[u].z, 1) : 0u;
+        b.w = Q >= 3 ? __shfl_down_sync(kFull, a[u].w, 1) : 0u;
+        if (lane == 31) b = nx[u];
+        if (k < n) d4[k] = realign<Q>(a[u], b, r);
+      }
+    }
   }
 }
 
-// Write the vectors and the head / tail bytes of the pieces of one staged
-// chunk: source bytes [c0, c1) held at buf (source byte c0 + o at buf + o,
-// plus one granule past c1).  q is the group's first unfinished piece of the
-// segment; pieces are in source order.
-__device__ __forceinline__ void copy_chunk(const Piece* pc, const int* list, int np, int& q,
-                                           uintptr_t c0, uintptr_t c1, uint32_t buf, int gt,
-                                           bool head_warp, int lane) {
+// Write the vectors of the runs of one staged chunk: vectors whose first
+// source byte lies in [c0, c1), held at buf (source byte c0 + o at buf + o,
+// plus one granule past c1), by one warp.  q is the warp's first unfinished
+// run of the segment; runs are in source order.
+__device__ __forceinline__ void copy_runs(const Run* runs, const int* list, int nr, int& q,
+                                          uintptr_t c0, uintptr_t c1, uint32_t buf, int lane) {
 #pragma unroll 1
-  for (int qq = q; qq < np; ++qq) {
-    const Piece& p = pc[list[qq]];
-    const uintptr_t ps = reinterpret_cast<uintptr_t>(p.src);
-    if (ps >= c1) break;   // starts in a later chunk
-    const int64_t head = p.head, nvec = p.nvec;
-    const int tail = p.tail;
-    const uintptr_t base = ps + (uintptr_t)head;
-    const uintptr_t pe = base + (uintptr_t)(nvec * 16) + (uintptr_t)tail;
-    if (pe <= c0) {        // ended in a chunk another group took
+  for (int qq = q; qq < nr; ++qq) {
+    const Run& rr = runs[list[qq]];
+    const uintptr_t vb = rr.vb;
+    if (vb >= c1) break;   // starts in a later chunk
+    const int64_t nvec = rr.nvec;
+    const uintptr_t last = vb + (uintptr_t)((nvec - 1) * 16);   // last vector's first byte
+    if (last < c0) {       // ended in a chunk another warp took
       q = qq + 1;
       continue;
     }
-    char* const dj = p.dst;
-    // Vectors v whose first source byte base + 16 v lies in [c0, c1).
-    const int64_t vlo = base >= c0 ? 0 : (int64_t)((c0 - base + 15) >> 4);
-    int64_t vhi = base >= c1 ? 0 : (int64_t)((c1 - base + 15) >> 4);
+    const int64_t vlo = vb >= c0 ? 0 : (int64_t)((c0 - vb + 15) >> 4);
+    int64_t vhi = (int64_t)((c1 - vb + 15) >> 4);
     if (vhi > nvec) vhi = nvec;
-    if (vhi > vlo) {
-      const uint32_t o = (uint32_t)(base + (uintptr_t)(vlo * 16) - c0);
-      const uint32_t vbuf = buf + (o & ~15u), delta = o & 15u, r = (delta & 3u) * 8u;
-      uint4* d4 = reinterpret_cast<uint4*>(dj + head) + vlo;
-      const int n = (int)(vhi - vlo);
-      switch (delta >> 2) {
-        case 0:
-          if (r == 0)
-            vec_copy<0, false>(d4, vbuf, n, gt, 0u);
-          else
-            vec_copy<0, true>(d4, vbuf, n, gt, r);
-          break;
-        case 1: vec_copy<1, true>(d4, vbuf, n, gt, r); break;
-        case 2: vec_copy<2, true>(d4, vbuf, n, gt, r); break;
-        default: vec_copy<3, true>(d4, vbuf, n, gt, r); break;
-      }
+    const uint32_t o = (uint32_t)(vb + (uintptr_t)(vlo * 16) - c0);
+    const uint32_t vbuf = buf + (o & ~15u), delta = rr.delta, r = (delta & 3u) * 8u;
+    uint4* d4 = reinterpret_cast<uint4*>(rr.d) + vlo;
+    const int n = (int)(vhi - vlo);
+    switch (delta >> 2) {
+      case 0:
+        if (r == 0)
+          vec_copy<0, false>(d4, vbuf, n, lane, 0u);
+        else
+          vec_copy<0, true>(d4, vbuf, n, lane, r);
+        break;
+      case 1: vec_copy<1, true>(d4, vbuf, n, lane, r); break;
+      case 2: vec_copy<2, true>(d4, vbuf, n, lane, r); break;
+      default: vec_copy<3, true>(d4, vbuf, n, lane, r); break;
     }
-    // Head bytes (lanes 0-15) and tail bytes (lanes 16-31) of the group's
-    // first warp, each written by the chunk holding its source byte.
-    if (head_warp) {
-      const int bb = lane & 15;
-      const int64_t off = lane < 16 ? (bb < head ? bb : -1)
-                                    : (bb < tail ? head + nvec * 16 + bb : -1);
-      if (off >= 0) {
-        const uintptr_t sb = ps + (uintptr_t)off;
-        if (sb >= c0 && sb < c1) dj[off] = (char)lds8(buf + (uint32_t)(sb - c0));
-      }
-    }
-    if (pe > c1) break;   // continues in a later chunk
+    if (last >= c1) break;   // continues in a later chunk
     q = qq + 1;
   }
 }
@@ -312,65 +308,74 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   __shared__ int64_t s_seg_lo[kA2avMaxP], s_seg_hi[kA2avMaxP];
   __shared__ uintptr_t s_seg_g0[kA2avMaxP], s_seg_g1[kA2avMaxP];
   __shared__ int64_t s_chbase[kA2avMaxP + 1];
-  __shared__ Piece s_piece[kMaxSeg][kA2avMaxP];
-  __shared__ int s_list[kMaxSeg][kA2avMaxP];   // non-empty pieces, in source order
+  __shared__ Run s_run[kMaxSeg][kA2avMaxP];
+  __shared__ int s_list[kMaxSeg][kA2avMaxP];   // runs with vectors, in source order
   __shared__ uint8_t s_has[kMaxSeg][kA2avMaxP];
   __shared__ int s_np[kMaxSeg];
-  __shared__ __align__(8) uint64_t s_full[kMaxStages];
-  __shared__ __align__(8) uint64_t s_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t s_full[kWarps][kMaxStages];   // each warp's ring slots
   __shared__ int s_nseg;
-  __shared__ int s_bad;
   __shared__ int s_abort;   // a bounded wait ran out
 
   const int P = a.P, stages = a.stages;
   const int nb = gridDim.x, b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t es = a.esize;
-  int64_t* cnt = reinterpret_cast<int64_t*>(dyn + stages * kStageStride);
+  int64_t* cnt = reinterpret_cast<int64_t*>(dyn + kWarps * stages * kStageStride);
   const uint32_t ring_base = smem_u32(dyn);
 
   // ---------------- set-up (all warps) ----------------
-#pragma unroll 4
-  for (int k = tid; k < P * P; k += kThreads) cnt[k] = __ldg(a.sc + k);
   if (tid < P) {
     s_in[tid] = static_cast<const char*>(a.in[tid]);
     s_out[tid] = static_cast<char*>(a.out[tid]);
   }
-  if (tid == 0) {
-    s_bad = 0;
-    s_abort = 0;
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(smem_u32(&s_full[s]), 1);
-      mbar_init(smem_u32(&s_empty[s]), kGroupWarps);   // the warps of the consuming group
+  if (tid == 0) s_abort = 0;
+  if (lane < stages) mbar_init(smem_u32(&s_full[warp][lane]), 1);   // the warp's own slots
+  __syncwarp();
+  if (lane == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  // Rows warp, warp + kWarps, ... of the counts, all loaded before any is
+  // used: to shared memory, their totals, and the checks (a negative count,
+  // a non-zero count that would touch a NULL buffer; the host marks NULL
+  // buffers in two bit masks).
+  int bad = 0;
+  {
+    int64_t v[kRowsPerWarp][2];
+#pragma unroll
+    for (int m = 0; m < kRowsPerWarp; ++m) {
+      const int r = warp + m * kWarps;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = lane + 32 * h;
+        v[m][h] = (r < P && j < P) ? __ldg(a.sc + r * P + j) : 0;
+      }
     }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  // Row totals and the checks, a warp per row.
-  for (int r = warp; r < P; r += kWarps) {
-    const bool in_nul = s_in[r] == nullptr;
-    int64_t s = 0;
-    bool bad = false;
-    for (int j = lane; j < P; j += 32) {
-      const int64_t c = cnt[r * P + j];
-      s += c;
-      bad |= c < 0 || (c > 0 && (in_nul || s_out[j] == nullptr));
+#pragma unroll
+    for (int m = 0; m < kRowsPerWarp; ++m) {
+      const int r = warp + m * kWarps;
+      if (r >= P) break;
+      const bool in_nul = (a.in_null >> r) & 1u;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = lane + 32 * h;
+        if (j < P) {
+          const int64_t c = v[m][h];
+          cnt[r * P + j] = c;
+          bad |= c < 0 || (c > 0 && (in_nul || ((a.out_null >> j) & 1u)));
+        }
+      }
+      const int64_t s = warp_sum64(v[m][0] + v[m][1]);
+      if (lane == 0) s_rowtot[r] = s;
     }
-    s = warp_sum64(s);
-    if (__any_sync(kFull, bad) && lane == 0) s_bad = 1;
-    if (lane == 0) s_rowtot[r] = s;
   }
-  // Checked variant: a receive total over capacity (every block decides alike).
-  if (a.check_cap && tid < P) {
+  bad = __syncthreads_or(bad);
+  // Checked variant: receive totals over capacity (every block decides
+  // alike), by warps 2 and 3 while warp 0 lays out the segments.
+  int over = 0;
+  if (a.check_cap && tid >= 64 && tid < 64 + P) {
+    const int j = tid - 64;
     int64_t s = 0;
-    for (int k = 0; k < P; ++k) s += cnt[k * P + tid];
-    if (s > a.cap[tid]) s_bad = 1;
+    for (int k = 0; k < P; ++k) s += cnt[k * P + j];
+    over = s > a.cap[j];
   }
-  __syncthreads();
-  const bool bad = s_bad != 0;
-  if (a.status && b == 0 && tid == 0) *a.status = bad ? BRA_ERR_INVALID : BRA_OK;
-  if (bad) return;   // nothing issued yet: no copy in flight
-
   if (warp == 0) {
     // Rank offsets in the concatenated send buffers, this block's range and
     // its segments (compacted, in rank order), and their chunk counts.
@@ -420,86 +425,82 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
       s_nseg = nseg;
     }
   }
-  __syncthreads();   // the last CTA-wide barrier: roles split from here
+  // The last CTA-wide barrier: roles split from here.
+  over = __syncthreads_or(over);
+  if (a.status && b == 0 && tid == 0) *a.status = (bad || over) ? BRA_ERR_INVALID : BRA_OK;
+  if (bad || over) return;   // nothing issued yet: no copy in flight
   volatile int* abort_flag = &s_abort;
   const int nseg = s_nseg;
+  const int64_t nch = s_chbase[nseg];
 
-  if (warp == 0) {
-    if (lane != 0) return;
-    // ---------------- producer ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-#pragma unroll 1
-    for (int sg = 0; sg < nseg && ok; ++sg) {
-      const uintptr_t G0 = s_seg_g0[sg], G1 = s_seg_g1[sg];
-#pragma unroll 1
-      for (uintptr_t c0 = G0; c0 < G1; c0 += kChunk) {
-        if (!mbar_wait(smem_u32(&s_empty[stage]), phase ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uintptr_t ce = c0 + kChunk + 16 < G1 ? c0 + kChunk + 16 : G1;
-        const uint32_t fb = smem_u32(&s_full[stage]);
-        mbar_expect_tx(fb, (uint32_t)(ce - c0));
-        bulk_load(ring_base + stage * kStageStride, reinterpret_cast<const void*>(c0),
-                  (uint32_t)(ce - c0), fb);
-        if (++stage == stages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    if (!ok) {   // a wait ran out: give copies already issued time to land
-      const unsigned long long t0 = global_ns();
-      while (global_ns() - t0 < 2000000ull) {
-      }
-    }
-    return;
-  }
+  // ---------------- the warp's pipeline ----------------
+  // Lane 0 loads the warp's chunks t = warp, warp + kWarps, ... in order,
+  // chunk number i of the warp into slot i % stages; `stages` are loaded
+  // up front and each one consumed frees its slot for the next.
+  const uint32_t ring = ring_base + (uint32_t)(warp * stages * kStageStride);
+  int64_t t_load = warp;
+  int sg_load = 0;
+  auto load_next = [&](int slot) {
+    if (t_load >= nch) return;
+    while (s_chbase[sg_load + 1] <= t_load) ++sg_load;
+    const uintptr_t c0 = s_seg_g0[sg_load] + (uintptr_t)(t_load - s_chbase[sg_load]) * kChunk;
+    const uintptr_t G1 = s_seg_g1[sg_load];
+    const uintptr_t ce = c0 + kChunk + 16 < G1 ? c0 + kChunk + 16 : G1;
+    const uint32_t fb = smem_u32(&s_full[warp][slot]);
+    mbar_expect_tx(fb, (uint32_t)(ce - c0));
+    bulk_load(ring + slot * kStageStride, reinterpret_cast<const void*>(c0), (uint32_t)(ce - c0),
+              fb);
+    t_load += kWarps;
+  };
+  if (lane == 0)
+    for (int k = 0; k < stages; ++k) load_next(k);
 
-  // ---------------- consumers (warps 1..) ----------------
-  const int ct = tid - 32;                       // consumer thread
-  const int g = ct / kGroupThreads;              // group
-  const int gt = ct - g * kGroupThreads;         // thread within the group
-  const bool head_warp = gt < 32;
   bool live = true;
+  int slot = 0;
+  uint32_t ph = 0;
+  int64_t t = warp;   // the warp's next chunk to write
+  int sg = 0, q = 0;  // its segment and first unfinished run there
 #pragma unroll 1
   for (int b0 = 0; b0 < nseg; b0 += kMaxSeg) {
     const int nbatch = nseg - b0 < kMaxSeg ? nseg - b0 : kMaxSeg;
-    if (b0 > 0) consumer_sync();   // every group is done with the previous tables
-    // Piece (s, j) of segment b0 + s by consumer thread s * 64 + j.
-    if (ct < nbatch * kA2avMaxP) {
-      const int s = ct / kA2avMaxP, j = ct % kA2avMaxP;
-      bool has = false;
+    if (b0 > 0) __syncthreads();   // every warp is done with the previous tables
+    // Piece (s, j) of segment b0 + s by thread s * 64 + j.
+    if (tid < nbatch * kA2avMaxP) {
+      const int s = tid / kA2avMaxP, j = tid % kA2avMaxP;
+      Run& rr = s_run[s][j];
+      rr.nvec = 0;
+      rr.head = 0;
+      rr.tail = 0;
       if (j < P) {
-        const int sg = b0 + s, i = s_seg_rank[sg];
+        const int sgi = b0 + s, i = s_seg_rank[sgi];
         int64_t sd = 0, rd = 0;
 #pragma unroll 8
         for (int k = 0; k < j; ++k) sd += cnt[i * P + k];
 #pragma unroll 8
         for (int k = 0; k < i; ++k) rd += cnt[k * P + j];
-        const int64_t c = cnt[i * P + j], lo = s_seg_lo[sg], hi = s_seg_hi[sg];
+        const int64_t c = cnt[i * P + j], lo = s_seg_lo[sgi], hi = s_seg_hi[sgi];
         const int64_t c0 = lo > sd ? lo : sd;
         const int64_t c1 = hi < sd + c ? hi : sd + c;
         const int64_t n = c1 > c0 ? (c1 - c0) * es : 0;
-        Piece& p = s_piece[s][j];
-        p.src = s_in[i] + (n ? c0 * es : 0);
-        char* dst = s_out[j] + (n ? (rd + (c0 - sd)) * es : 0);
-        int64_t head = (16 - (int64_t)((uintptr_t)dst & 15)) & 15;
-        if (head > n) head = n;
-        p.dst = dst;
-        p.head = (int)head;
-        p.nvec = (n - head) >> 4;
-        p.tail = (int)((n - head) & 15);
-        has = n > 0;
+        if (n > 0) {
+          const char* src = s_in[i] + c0 * es;
+          char* dst = s_out[j] + (rd + (c0 - sd)) * es;
+          int64_t head = (16 - (int64_t)((uintptr_t)dst & 15)) & 15;
+          if (head > n) head = n;
+          rr.vb = reinterpret_cast<uintptr_t>(src) + (uintptr_t)head;
+          rr.d = dst + head;
+          rr.nvec = (n - head) >> 4;
+          rr.delta = (uint8_t)(rr.vb & 15u);
+          rr.head = (uint8_t)head;
+          rr.tail = (uint8_t)((n - head) & 15);
+        }
       }
-      s_has[s][j] = has ? 1 : 0;
+      s_has[s][j] = rr.nvec > 0 ? 1 : 0;
     }
-    consumer_sync();
-    // Compact list of each segment's non-empty pieces (consumer warp s).
-    if (ct / 32 < nbatch) {
-      const int s = ct / 32;
+    __syncthreads();
+    // Compact list of each segment's pieces with vectors (warp s).
+    if (warp < nbatch) {
+      const int s = warp;
       const bool h0 = lane < P && s_has[s][lane];
       const bool h1 = lane + 32 < P && s_has[s][lane + 32];
       const unsigned m0 = __ballot_sync(kFull, h0);
@@ -509,39 +510,68 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
       if (h1) s_list[s][__popc(m0) + __popc(m1 & below)] = lane + 32;
       if (lane == 0) s_np[s] = __popc(m0) + __popc(m1);
     }
-    consumer_sync();
+    __syncthreads();
 
-    // This group's chunks of the batch: global chunk indices t = g mod kGroups.
-    const int64_t tb = s_chbase[b0], te = s_chbase[b0 + nbatch];
-    int64_t t = tb + (((int64_t)g - tb % kGroups) + kGroups) % kGroups;
-    int sg = b0, q = 0;
+    // The warp's chunks of this batch.
+    const int64_t te = s_chbase[b0 + nbatch];
 #pragma unroll 1
-    for (; t < te && live; t += kGroups) {
+    for (; t < te && live; t += kWarps) {
       while (s_chbase[sg + 1] <= t) {
         ++sg;
         q = 0;
       }
-      const int stage = (int)(t % stages);
-      const uint32_t ph = (uint32_t)((t / stages) & 1);
-      const bool waited = mbar_wait(smem_u32(&s_full[stage]), ph, abort_flag);
+      const bool waited = mbar_wait(smem_u32(&s_full[warp][slot]), ph, abort_flag);
       live = __all_sync(kFull, waited);
       if (!live) break;
       const uintptr_t c0 = s_seg_g0[sg] + (uintptr_t)(t - s_chbase[sg]) * kChunk;
       const uintptr_t G1 = s_seg_g1[sg];
       const uintptr_t c1 = c0 + kChunk < G1 ? c0 + kChunk : G1;   // bytes this chunk writes
       const int s = sg - b0;
-      copy_chunk(s_piece[s], s_list[s], s_np[s], q, c0, c1, ring_base + stage * kStageStride,
-                 gt, head_warp, lane);
+      copy_runs(s_run[s], s_list[s], s_np[s], q, c0, c1, ring + slot * kStageStride, lane);
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s_empty[stage]));
+      if (lane == 0) load_next(slot);   // the warp's chunk `stages` later
+      if (++slot == stages) {
+        slot = 0;
+        ph ^= 1u;
+      }
+    }
+    // Head and tail bytes of the batch's pieces, straight from the send
+    // buffer (loads first, then stores).
+    if (live && tid < nbatch * kA2avMaxP) {
+      const Run& rr = s_run[tid / kA2avMaxP][tid % kA2avMaxP];
+      const int head = rr.head, tail = rr.tail;
+      if (head + tail > 0) {
+        const char* src = reinterpret_cast<const char*>(rr.vb);
+        const char* ts = src + rr.nvec * 16;
+        char hb[15], tb[15];
+#pragma unroll
+        for (int k = 0; k < 15; ++k) {
+          hb[k] = k < head ? __ldg(src - head + k) : 0;
+          tb[k] = k < tail ? __ldg(ts + k) : 0;
+        }
+        char* td = rr.d + rr.nvec * 16;
+#pragma unroll
+        for (int k = 0; k < 15; ++k) {
+          if (k < head) rr.d[k - head] = hb[k];
+          if (k < tail) td[k] = tb[k];
+        }
+      }
     }
   }
-  if (!live) return;
+  if (!live) {   // a wait ran out: give copies already issued time to land
+    if (lane == 0) {
+      const unsigned long long t0 = global_ns();
+      while (global_ns() - t0 < 2000000ull) {
+      }
+    }
+    return;
+  }
 
-  // Bookkeeping, entries (i, j) spread over every consumer thread of the grid.
+  // Bookkeeping, entries (i, j) dealt round-robin over the blocks, then over
+  // each block's threads.
   const int64_t PP = (int64_t)P * P;
 #pragma unroll 1
-  for (int64_t e = (int64_t)b * kConsumers + ct; e < PP; e += (int64_t)nb * kConsumers) {
+  for (int64_t e = b + (int64_t)nb * tid; e < PP; e += (int64_t)nb * kThreads) {
     const int i = (int)(e / P), j = (int)(e % P);
     int64_t sd = 0, rd = 0;
     for (int k = 0; k < j; ++k) sd += cnt[i * P + k];
@@ -606,13 +636,12 @@ cudaError_t a2av_device_info(A2avDeviceInfo* out) {
   return cudaSuccess;
 }
 
-// Ring stages that fit beside a P x P count matrix: a multiple of kGroups
-// (each stage then belongs to one consumer group), at most kMaxStages.
+// Ring slots per warp that fit beside a P x P count matrix, at most
+// kMaxStages.
 int stages_for(const A2avDeviceInfo& di, int P) {
   const int cnt_bytes = (P * P * 8 + 127) / 128 * 128;
-  int s = (di.dyn_max - cnt_bytes) / kStageStride;
-  s = s > kMaxStages ? kMaxStages : s;
-  return s / kGroups * kGroups;
+  const int s = (di.dyn_max - cnt_bytes) / (kWarps * kStageStride);
+  return s > kMaxStages ? kMaxStages : s;
 }
 
 }  // namespace
@@ -629,9 +658,10 @@ cudaError_t launch_a2av(const A2avArgs& args, int blocks, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   A2avArgs a = args;
   a.stages = stages_for(di, a.P);
-  if (a.stages < kGroups || a.stages % kGroups != 0 || blocks < 1)
-    return cudaErrorInvalidConfiguration;
-  const size_t dyn = (size_t)a.stages * kStageStride + (size_t)a.P * a.P * 8;
+  if (a.stages < 2 || blocks < 1) return cudaErrorInvalidConfiguration;
+  // The whole shared memory a block may take, whatever the ring uses: two
+  // blocks never share an SM, and the exchange occupies `blocks` SMs.
+  const size_t dyn = (size_t)di.dyn_max;
   a2av_kernel<<<blocks, kThreads, dyn, st>>>(a);
   return cudaGetLastError();
 }

@@ -365,6 +365,8 @@ int a2av_common(const void* const input[], const int64_t* send_counts,
     a.in[r] = input[r];
     a.out[r] = out[r];
     a.cap[r] = checked ? out_capacity[r] : 0;
+    if (!input[r]) a.in_null |= uint64_t(1) << r;
+    if (!out[r]) a.out_null |= uint64_t(1) << r;
   }
   a.sc = send_counts;
   a.sd = send_displs;

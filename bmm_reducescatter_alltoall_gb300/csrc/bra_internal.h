@@ -27,6 +27,8 @@ struct A2avArgs {
   int64_t* rc;              // recv_counts [P][P]
   int64_t* rd;              // recv_displs [P][P]
   int32_t* status;          // optional device status word
+  uint64_t in_null;         // bit r: in[r] is NULL
+  uint64_t out_null;        // bit r: out[r] is NULL
   int P;
   int esize;                // element size in bytes (4 or 1)
   int check_cap;            // compare received totals against cap[]

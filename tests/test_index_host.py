@@ -276,20 +276,22 @@ def test_element_epilogue_staging_shift(delta):
 
 # ---------------------------------------------------------------------------
 # all_to_all_v kernel (a2av.cu): block ranges, segments, staged chunks, the
-# consumer groups' chunk shares and the piece writes.
-A2AV_CHUNK, A2AV_STRIDE, A2AV_GROUPS, A2AV_MAXSEG = 16384, 16384 + 128, 4, 4
+# warps' chunk shares and the piece writes.
+A2AV_CHUNK, A2AV_STRIDE, A2AV_WARPS, A2AV_MAXSEG = 4096, 4096 + 128, 16, 4
 
 
 def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_mem, written):
     """Run the kernel's addressing for every block: `mem` maps a source
     address to its byte value, `out_mem` / `written` receive the stores.
-    Checks every staged read and every store against the buffers."""
+    Checks every staged read, every direct read and every store against the
+    buffers."""
     P = sc.shape[0]
     rowtot = sc.sum(axis=1)
     T = int(rowtot.sum())
     rowoff = np.concatenate([[0], np.cumsum(rowtot)[:-1]])
     sd = np.concatenate([np.zeros((P, 1), np.int64), np.cumsum(sc, axis=1)[:, :-1]], axis=1)
     rd = np.concatenate([np.zeros((1, P), np.int64), np.cumsum(sc, axis=0)[:-1, :]], axis=0)
+    span = [(in_base[r], in_base[r] + int(in_len_b[r])) for r in range(P)]
     for b in range(nb):
         q_, rem = divmod(T, nb)
         lo, hi = q_ * b + min(b, rem), q_ * (b + 1) + min(b + 1, rem)
@@ -302,7 +304,7 @@ def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_m
                 g1 = (in_base[r] + shi * es + 15) & ~15
                 segs.append((r, slo, shi, g0, g1, -(-(g1 - g0) // A2AV_CHUNK)))
         chbase = np.concatenate([[0], np.cumsum([s[5] for s in segs])]).astype(np.int64)
-        # Producer: chunk t of the block staged from [c0, ce).
+        # Loads: chunk t of the block staged from [c0, ce).
         staged = {}
         t = 0
         for (r, slo, shi, g0, g1, nch) in segs:
@@ -314,12 +316,13 @@ def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_m
                 staged[t] = (c0, ce)
                 t += 1
         assert t == chbase[-1]
-        # Consumers, batch by batch.
+        # Batch by batch: tables (head and tail bytes copied from the send
+        # buffer), then each warp's chunks t = w, w + A2AV_WARPS, ...
         for b0 in range(0, len(segs), A2AV_MAXSEG):
             batch = segs[b0:b0 + A2AV_MAXSEG]
             tables = []
             for (i, slo, shi, g0, g1, nch) in batch:
-                pieces = []
+                runs = []
                 for j in range(P):
                     c = int(sc[i, j])
                     c0e, c1e = max(slo, sd[i, j]), min(shi, sd[i, j] + c)
@@ -329,11 +332,17 @@ def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_m
                     src = in_base[i] + c0e * es
                     dst = out_base[j] + (rd[i, j] + (c0e - sd[i, j])) * es
                     head = min((16 - dst % 16) % 16, n)
-                    pieces.append((src, dst, (n - head) >> 4, head, (n - head) & 15, j))
-                tables.append(pieces)
+                    nvec, tail = (n - head) >> 4, (n - head) & 15
+                    for off in list(range(head)) + [head + nvec * 16 + x for x in range(tail)]:
+                        assert span[i][0] <= src + off < span[i][1]
+                        out_mem[dst + off] = mem[src + off]
+                        written[dst + off] += 1
+                    if nvec > 0:
+                        runs.append((src + head, dst + head, nvec))
+                tables.append(runs)
             tb, te = chbase[b0], chbase[b0 + len(batch)]
-            for g in range(A2AV_GROUPS):
-                t = tb + ((g - tb % A2AV_GROUPS) + A2AV_GROUPS) % A2AV_GROUPS
+            for g in range(A2AV_WARPS):
+                t = tb + ((g - tb % A2AV_WARPS) + A2AV_WARPS) % A2AV_WARPS
                 sg, q = b0, 0
                 while t < te:
                     while chbase[sg + 1] <= t:
@@ -344,44 +353,36 @@ def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_m
                     assert c0 == c0s
                     c1 = min(c0 + A2AV_CHUNK, G1)
                     stage = mem[c0:ce]
-                    pcs = tables[sg - b0]
+                    runs = tables[sg - b0]
                     qq = q
-                    while qq < len(pcs):
-                        src, dst, nvec, head, tail, j = pcs[qq]
-                        if src >= c1:
+                    while qq < len(runs):
+                        vb, d, nvec = runs[qq]
+                        if vb >= c1:
                             break
-                        base = src + head
-                        pe = base + nvec * 16 + tail
-                        if pe <= c0:
+                        last = vb + (nvec - 1) * 16
+                        if last < c0:
                             q = qq + 1
                             qq += 1
                             continue
-                        vlo = 0 if base >= c0 else (c0 - base + 15) >> 4
-                        vhi = 0 if base >= c1 else (c1 - base + 15) >> 4
-                        vhi = min(vhi, nvec)
-                        if vhi > vlo:
-                            o = base + vlo * 16 - c0
-                            k = np.arange(vhi - vlo)
-                            rd0 = (o & ~15) + 16 * k          # first staged word read
-                            assert rd0.min() >= 0 and (rd0 + 32).max() <= A2AV_STRIDE
-                            first = o + 16 * k                # the vector's bytes in the stage
-                            assert (first + 16).max() <= ce - c0
-                            d = dst + head + 16 * (vlo + k)
-                            assert (d % 16 == 0).all()
-                            idx = (first[:, None] + np.arange(16)).ravel()
-                            dd = (d[:, None] + np.arange(16)).ravel()
-                            out_mem[dd] = stage[idx]
-                            written[dd] += 1
-                        for off in list(range(head)) + [head + nvec * 16 + x for x in range(tail)]:
-                            sb = src + off
-                            if c0 <= sb < c1:
-                                out_mem[dst + off] = stage[sb - c0]
-                                written[dst + off] += 1
-                        if pe > c1:
+                        vlo = 0 if vb >= c0 else (c0 - vb + 15) >> 4
+                        vhi = min((c1 - vb + 15) >> 4, nvec)
+                        o = vb + vlo * 16 - c0
+                        k = np.arange(vhi - vlo)
+                        rd0 = (o & ~15) + 16 * k          # first staged word read
+                        assert rd0.min() >= 0 and (rd0 + 32).max() <= A2AV_STRIDE
+                        first = o + 16 * k                # the vector's bytes in the stage
+                        assert (first + 16).max() <= ce - c0
+                        dv = d + 16 * (vlo + k)
+                        assert (dv % 16 == 0).all()
+                        idx = (first[:, None] + np.arange(16)).ravel()
+                        dd = (dv[:, None] + np.arange(16)).ravel()
+                        out_mem[dd] = stage[idx]
+                        written[dd] += 1
+                        if last >= c1:
                             break
                         q = qq + 1
                         qq += 1
-                    t += A2AV_GROUPS
+                    t += A2AV_WARPS
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -395,7 +396,7 @@ def test_exchange_block_addressing(seed, es):
     rng = np.random.default_rng(seed)
     P = int(rng.choice([1, 2, 3, 5, 8]))
     small = rng.integers(0, 40, size=(P, P))
-    big = rng.integers(0, 3 * A2AV_CHUNK // es, size=(P, P))
+    big = rng.integers(0, 12 * A2AV_CHUNK // es, size=(P, P))
     sc = np.where(rng.random((P, P)) < 0.4, big, small).astype(np.int64)
     sc[rng.random((P, P)) < 0.2] = 0
     in_len = sc.sum(axis=1) * es
@@ -432,27 +433,30 @@ def test_exchange_block_addressing(seed, es):
 
 
 def _ring_schedule(stages, groups, nchunks, rng):
-    """One random interleaving of the exchange's ring protocol: a producer
-    loading chunk t into stage t % stages after a parity wait on the stage's
-    empty barrier, loads landing at random later times (completing a phase
-    of the stage's full barrier), and consumer group t % groups taking chunk
-    t after a parity wait on the full barrier, then arriving on the empty
-    barrier.  A parity wait on phase u passes when the number of completed
-    phases has the other parity (mbarrier try_wait.parity).  Returns False
-    when a group passed its wait while its stage held another chunk or had a
-    load in flight."""
+    """One random interleaving of the exchange's ring protocol: producer g
+    loading chunks t = g, g + groups, ... in order into stage t % stages
+    after a parity wait on the stage's empty barrier, loads landing at
+    random later times (completing a phase of the stage's full barrier),
+    and consumer group t % groups taking chunk t after a parity wait on the
+    full barrier, then arriving on the empty barrier.  A parity wait on
+    phase u passes when the number of completed phases has the other parity
+    (mbarrier try_wait.parity).  Returns False when a group passed its wait
+    while its stage held another chunk or had a load in flight, or a
+    producer loaded into a stage with a load still in flight."""
     full_c = [0] * stages
     empty_c = [0] * stages
     content = [-1] * stages
     in_flight = {}                       # stage -> chunk
-    nxt = 0                              # producer's next chunk
+    issue = [list(range(g, nchunks, groups)) for g in range(groups)]
     todo = [list(range(g, nchunks, groups)) for g in range(groups)]
-    while nxt < nchunks or in_flight or any(todo):
+    while any(issue) or in_flight or any(todo):
         moves = []
-        if nxt < nchunks:
-            s, u = nxt % stages, nxt // stages
-            if (empty_c[s] & 1) != ((u & 1) ^ 1):
-                moves.append(("issue", None))
+        for g in range(groups):
+            if issue[g]:
+                t = issue[g][0]
+                s, u = t % stages, t // stages
+                if (empty_c[s] & 1) != ((u & 1) ^ 1):
+                    moves.append(("issue", g))
         moves += [("land", s) for s in in_flight]
         for g in range(groups):
             if todo[g]:
@@ -460,12 +464,15 @@ def _ring_schedule(stages, groups, nchunks, rng):
                 s, u = t % stages, t // stages
                 if (full_c[s] & 1) != (u & 1):
                     moves.append(("take", g))
+        if not moves:
+            return False                 # nobody can move: a deadlock
         kind, arg = moves[rng.integers(len(moves))]
         if kind == "issue":
-            s = nxt % stages
-            assert s not in in_flight
-            in_flight[s] = nxt
-            nxt += 1
+            t = issue[arg].pop(0)
+            s = t % stages
+            if s in in_flight:
+                return False
+            in_flight[s] = t
         elif kind == "land":
             content[arg] = in_flight.pop(arg)
             full_c[arg] += 1
@@ -479,13 +486,19 @@ def _ring_schedule(stages, groups, nchunks, rng):
 
 
 def test_exchange_ring_protocol_under_random_schedules():
-    """With the stage count a multiple of the consumer groups (what the
-    launch enforces), no group ever reads a stage before its own chunk has
-    landed there, under any interleaving; with other stage counts some
-    interleaving makes a parity wait pass on an older phase."""
+    """The kernel's slots: warp w's i-th chunk goes to its slot i % S, so
+    chunk t sits in slot t % (W * S) of the block when slots are numbered
+    warp-major.  With the slot count a multiple of the pipelines (W * S),
+    every slot has one loader and one consumer, and no pipeline ever reads a
+    slot before its own chunk has landed there, under any interleaving; with
+    other slot counts some interleaving breaks the protocol."""
     rng = np.random.default_rng(0)
-    for stages in (4, 8, 12):
-        for _ in range(300):
-            assert _ring_schedule(stages, A2AV_GROUPS, int(rng.integers(1, 80)), rng)
-    for stages in (6, 11):
-        assert not all(_ring_schedule(stages, A2AV_GROUPS, 60, rng) for _ in range(300))
+    for stages in (A2AV_WARPS * 2, A2AV_WARPS * 3):
+        for _ in range(100):
+            assert _ring_schedule(stages, A2AV_WARPS, int(rng.integers(1, 200)), rng)
+    for stages in (6, 12):
+        for _ in range(100):
+            assert _ring_schedule(stages, 3, int(rng.integers(1, 60)), rng)
+    for stages in (A2AV_WARPS * 2 + 1, 11):
+        assert not all(_ring_schedule(stages, 4 if stages == 11 else A2AV_WARPS, 200, rng)
+                       for _ in range(100))

@@ -532,27 +532,46 @@ def run_ours(a):
 
     # ---- all_to_all_v timed alone: each call after the L2 sweep, with the GPU
     # idle between calls (not following the fused kernel's power draw) ----
-    a_alone = []
-    for _ in range(a.a2av_alone_calls):
-        torch.cuda._sleep(20_000_000)     # keeps the GPU busy so the host runs ahead
-        flush()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        a2av()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        a_alone.append(e0.elapsed_time(e1))
-    # the mean, not the median: event times come in ~2 us steps at this size
-    a_alone_ms = statistics.mean(a_alone) if a_alone else float("nan")
+    def time_alone(fn):
+        ms = []
+        for _ in range(a.a2av_alone_calls):
+            torch.cuda._sleep(20_000_000)     # keeps the GPU busy so the host runs ahead
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(e0.elapsed_time(e1))
+        return ms
+
+    def alone_record(ms, blocks):
+        # the mean, not the median: event times come in ~2 us steps at this size
+        m = statistics.mean(ms)
+        return {"achieved": a_bytes / (m / 1e3) / 1e9, "unit": "GB/s",
+                "frac": a_bytes / (m / 1e3) / 1e9 / peaks["hbm_gbs"], "mean_ms": m,
+                "min_ms": min(ms), "calls": len(ms), "blocks": blocks}
+
+    a_alone = time_alone(a2av)
     a2av_line["alone"] = None if not a_alone else {
-        "achieved": a_bytes / (a_alone_ms / 1e3) / 1e9, "unit": "GB/s",
-        "frac": a_bytes / (a_alone_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
-        "mean_ms": a_alone_ms, "min_ms": min(a_alone), "calls": len(a_alone),
+        **alone_record(a_alone, a2av_line["blocks"]),
         "note": "each call after the read-only L2 sweep, timed alone (CUDA events, ~2 us "
                 "resolution); the in-step figure above follows the fused kernel at its "
                 "power-capped clock, which also slows L2",
     }
+    # The same exchange with core_num = the SM count: as many blocks as the
+    # launch-width rule admits on the whole GPU (context for the B above).
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if a_alone:
+        full_plan = bra.all_to_all_v_plan(a_in, sc_d, a_out, sms, send_displs=book[0],
+                                          recv_counts=book[1], recv_displs=book[2])
+        full_plan.run(stream)
+        a2av_line["alone_whole_gpu"] = {
+            **alone_record(time_alone(lambda: full_plan.run(stream)),
+                           bra.all_to_all_v_launch_blocks(acfg.P, sms)),
+            "core_num": sms,
+        }
 
     # ---- indexed all_to_all_v timed alone: the same counts and payload, each
     # sender's list gathered through a permutation of its input ----

@@ -428,13 +428,14 @@ int ia2av_common(const void* const input[], const int64_t in_len[],
   a.status = status_dev;
   a.P = (int)P;
   a.esize = dtype == BRA_FP32 ? 4 : 1;
-  const int ctas = bra::ia2av_ctas_per_rank((int)P);
+  const int blocks = bra::ia2av_launch_blocks(core_num);
+  if (blocks < 1) return BRA_ERR_CUDA;
   if (log_enabled())
-    std::fprintf(stderr, "[bra] indexed_all_to_all_v P=%lld L=%lld B=%lld grid=(%d,%lld)\n",
-                 (long long)P, (long long)core_num, (long long)B, ctas, (long long)P);
+    std::fprintf(stderr, "[bra] indexed_all_to_all_v P=%lld L=%lld blocks=%d\n", (long long)P,
+                 (long long)core_num, blocks);
   cudaError_t e = cudaSuccess;
   if (status_dev) e = cudaMemsetAsync(status_dev, 0, sizeof(int32_t), stream);
-  if (e == cudaSuccess) e = bra::launch_ia2av(a, ctas, stream);
+  if (e == cudaSuccess) e = bra::launch_ia2av(a, blocks, stream);
   return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
 }
 

@@ -56,8 +56,10 @@ struct IA2avArgs {
   int P;
   int esize;                  // element size in bytes (4 or 1)
 };
-cudaError_t launch_ia2av(const IA2avArgs& a, int ctas_per_rank, cudaStream_t st);
-int ia2av_ctas_per_rank(int P);
+// Blocks the indexed exchange launches for core_num L: L, at most the SM
+// count (one block per SM); -1 if the device cannot be queried.
+int ia2av_launch_blocks(int64_t L);
+cudaError_t launch_ia2av(const IA2avArgs& a, int blocks, cudaStream_t st);
 
 // Problem description shared by the fused kernels.
 struct FusedProblem {

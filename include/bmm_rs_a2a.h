@@ -420,8 +420,14 @@ BRA_API int all_to_all_v_checked(const void* const input[], const int64_t* send_
  *   in_len[P]    host; element counts of the inputs (copied at the call).
  *   index[P]     device int64; index[i] holds at least n_i entries (may be
  *                NULL when n_i is 0).
- *   send_counts, send_displs, recv_counts, recv_displs, out, P, core_num,
- *   dtype        as for all_to_all_v.
+ *   send_counts, send_displs, recv_counts, recv_displs, out, P, dtype
+ *                as for all_to_all_v.
+ *   core_num     L, in [1, INT32_MAX]: the exact number of blocks the call
+ *                launches ([PTO] §A5 URMA 索引交换: L is the exact core
+ *                count, not folded by cal_all_to_all_v_blocks), one per SM,
+ *                at most the SM count.  The blocks split the send lists of
+ *                ranks 0..P-1, taken one after another, into equal position
+ *                ranges; results do not depend on L.
  *   status_dev   optional device int32: set to BRA_OK on the stream before
  *                the kernel, then to BRA_ERR_INVALID if the call was rejected
  *                on the device or an index value was out of range.

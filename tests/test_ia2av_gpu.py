@@ -90,6 +90,18 @@ def test_small_cases_bit_exact(P, dt, kind):
     _check_against_oracle(sc, inputs, index, dt, L=max(P, 1))
 
 
+@pytest.mark.parametrize("P,L", [(8, 1), (8, 3), (8, 8), (32, 64), (32, 152), (5, 1000)])
+def test_launch_width_is_exactly_core_num(P, L, capfd, monkeypatch):
+    """The indexed exchange launches exactly L blocks (one per SM, at most
+    the SM count) and stays bit-exact at every width."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    monkeypatch.setenv("BRA_LOG", "1")
+    sc, inputs, lens = _case(P, seed=900 + P + L, dt="int8", hi=4000 if P <= 8 else 400)
+    index = a2av_index(sc, lens, "perm", seed=L)
+    _check_against_oracle(sc, inputs, index, "int8", L=L)
+    assert f"L={L} blocks={min(L, sms)}" in capfd.readouterr().err
+
+
 def test_identity_index_equals_all_to_all_v():
     cfg = A2AV_CONFIGS["P8_L10_fp32_uniform4096"]
     sc, inputs = a2av_inputs(cfg)

@@ -580,36 +580,44 @@ def run_ours(a):
         perm = a2av_index(sc, [len(v) for v in a_inputs], "perm", seed=acfg.seed)
         ix = [torch.from_numpy(v).to(dev) for v in perm]
 
-        ia_plan = bra.indexed_all_to_all_v_plan(a_in, ix, sc_d, a_out, acfg.L,
-                                                send_displs=book[0], recv_counts=book[1],
-                                                recv_displs=book[2])
+        def ia_time(L):
+            plan = bra.indexed_all_to_all_v_plan(a_in, ix, sc_d, a_out, L,
+                                                 send_displs=book[0], recv_counts=book[1],
+                                                 recv_displs=book[2])
+            for _ in range(3):
+                plan.run(stream)
+            ms = []
+            for _ in range(a.indexed_calls):
+                torch.cuda._sleep(20_000_000)
+                flush()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                plan.run(stream)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ms.append(e0.elapsed_time(e1))
+            return ms
 
-        def ia2av():
-            ia_plan.run(stream)
-
-        for _ in range(3):
-            ia2av()
-        ia_ms = []
-        for _ in range(a.indexed_calls):
-            torch.cuda._sleep(20_000_000)
-            flush()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            ia2av()
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            ia_ms.append(e0.elapsed_time(e1))
+        ia_ms = ia_time(acfg.L)
         n_el = int(sc.sum())
         ia_bytes = 2 * n_el * a_in[0].element_size() + 8 * n_el + 4 * sc.size * 8
         m = statistics.mean(ia_ms)
+        # core_num L is the exact block count of this call (one block per
+        # SM); the same call on every SM for context
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        w_ms = ia_time(sms)
+        wm = statistics.mean(w_ms)
         indexed = {
             "kernel": "ia2av_kernel", "workload": f"{a.a2av}, index = a permutation of each "
                                                   "sender's input (seeded)",
             "achieved": ia_bytes / (m / 1e3) / 1e9, "unit": "GB/s",
             "frac": ia_bytes / (m / 1e3) / 1e9 / peaks["hbm_gbs"], "peak": peaks["hbm_gbs"],
             "algorithmic_bytes_per_launch": ia_bytes, "mean_ms": m, "min_ms": min(ia_ms),
-            "calls": len(ia_ms),
+            "calls": len(ia_ms), "blocks": min(acfg.L, sms),
+            "whole_gpu": {"core_num": sms, "blocks": sms, "mean_ms": wm,
+                          "achieved": ia_bytes / (wm / 1e3) / 1e9,
+                          "frac": ia_bytes / (wm / 1e3) / 1e9 / peaks["hbm_gbs"]},
             "note": "bytes = payload read + write + 8-byte index per element + bookkeeping; "
                     "each call after the read-only L2 sweep, timed alone; the gathers are "
                     "random, one 32-byte sector per element",

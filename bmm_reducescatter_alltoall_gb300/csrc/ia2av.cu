@@ -11,10 +11,12 @@
 // k of a send list is gathered and stored straight at its destination.
 //
 // Launch width: the page makes core_num L the exact number of cores a launch
-// uses.  Here that is L blocks, one per SM (a block's shared-memory request
-// leaves room for no other), at most the SM count.  The blocks split the
-// send lists of ranks 0..P-1, taken one after another, into equal position
-// ranges; a block walks its range rank by rank and, inside a rank, by
+// uses.  Here that is L blocks, one per SM (a block of 1024 threads at more
+// than 32 registers each holds over half an SM's register file, so no two
+// share an SM), at most the SM count.  The block keeps its shared memory
+// small: random gathers need the L1 for the lines they have in flight.  The
+// blocks split the send lists of ranks 0..P-1, taken one after another, into
+// equal position ranges; a block walks its range rank by rank and, inside a rank, by
 // destination.  Every block reads the whole count matrix first and rejects
 // the call (nothing written) on a negative count or a NULL buffer that would
 // be touched, so all blocks take the same decision without talking to each
@@ -241,9 +243,7 @@ cudaError_t launch_ia2av(const IA2avArgs& a, int blocks, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (blocks < 1 || (size_t)a.P * a.P * sizeof(int64_t) > (size_t)di.dyn_max)
     return cudaErrorInvalidConfiguration;
-  // The whole shared memory a block may take (the count matrix uses at most
-  // 32 KiB of it): two blocks never share an SM.
-  const size_t smem = (size_t)di.dyn_max;
+  const size_t smem = (size_t)a.P * a.P * sizeof(int64_t);   // at most 32 KiB
   if (a.esize == 4)
     ia2av_kernel<uint32_t><<<blocks, kThreads, smem, st>>>(a);
   else

@@ -57,6 +57,9 @@ def _args(argv=None):
                          "shapes whose x or weight rows lack a 16-byte pitch then run the "
                          "packed variant (operands repacked, then the TMA kernel)")
     ap.add_argument("--a2av", default=A2AV_NAME)
+    ap.add_argument("--a2av-scale", type=int, default=None,
+                    help="counts scale of the Dirichlet exchange workload (its counts are "
+                         "rint(scale * w_ij); the default 2^21 sends ~2 MiB per rank)")
     ap.add_argument("--a2av-sweep", action="store_true",
                     help="instead of the step: all_to_all_v alone over a range of sizes "
                          "(L2 swept before every timed call), plus a CUDA graph of 100 "
@@ -190,6 +193,21 @@ class ClockSampler:
 # helpers
 # --------------------------------------------------------------------------
 
+def _a2av_config(a):
+    from workloads import A2AV_CONFIGS
+    cfg = A2AV_CONFIGS[a.a2av]
+    if a.a2av_scale is not None:
+        if cfg.counts != "dirichlet":
+            raise SystemExit("--a2av-scale applies to a Dirichlet exchange workload")
+        cfg = cfg.replace(scale=a.a2av_scale)
+    return cfg
+
+
+def _a2av_name(a):
+    """The exchange workload's name, with its counts scale when it was changed."""
+    return a.a2av if a.a2av_scale is None else f"{a.a2av}_scale{a.a2av_scale}"
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -281,7 +299,7 @@ def run_reference(a):
         return
     from workloads import A2AV_CONFIGS, FUSED_CONFIGS, a2av_inputs
     cfg = FUSED_CONFIGS[a.fused]
-    acfg = A2AV_CONFIGS[a.a2av]
+    acfg = _a2av_config(a)
     sc, inputs = a2av_inputs(acfg)
     # calibrate on a small C', then size C' for the run
     c_small = max(cfg.tp, 64 - 64 % cfg.tp)
@@ -305,13 +323,13 @@ def run_reference(a):
     value = flops / step_s / 1e12
     sample = (f"fused oracle (fp64 numpy) on one local expert per rank and C'={C1} tokens per "
               f"EP block ({flops / 1e12:.3f} TFLOP) of {a.fused}, plus the full all_to_all_v "
-              f"{a.a2av}")
+              f"{_a2av_name(a)}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup, "ms_per_step": step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{a.fused} + {a.a2av}", "sample": sample},
+        "config": {"workload": f"{a.fused} + {_a2av_name(a)}", "sample": sample},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _cores(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -368,7 +386,7 @@ def run_ours(a):
     from workloads import A2AV_CONFIGS, FUSED_CONFIGS, a2av_index, a2av_inputs, fused_inputs_device
 
     cfg = FUSED_CONFIGS[a.fused]
-    acfg = A2AV_CONFIGS[a.a2av]
+    acfg = _a2av_config(a)
     P = cfg.P
     stream = torch.cuda.current_stream(dev)
 
@@ -609,7 +627,7 @@ def run_ours(a):
         w_ms = ia_time(sms)
         wm = statistics.mean(w_ms)
         indexed = {
-            "kernel": "ia2av_kernel", "workload": f"{a.a2av}, index = a permutation of each "
+            "kernel": "ia2av_kernel", "workload": f"{_a2av_name(a)}, index = a permutation of each "
                                                   "sender's input (seeded)",
             "achieved": ia_bytes / (m / 1e3) / 1e9, "unit": "GB/s",
             "frac": ia_bytes / (m / 1e3) / 1e9 / peaks["hbm_gbs"], "peak": peaks["hbm_gbs"],
@@ -772,7 +790,7 @@ def run_ours(a):
         }
         nb, sa = oracle_a2av(sc, a_inputs)
         cpu_baseline["all_to_all_v"] = {"value": nb / sa / 1e9, "unit": "GB/s",
-                                        "sample": f"full {a.a2av} exchange in {sa:.3f} s"}
+                                        "sample": f"full {_a2av_name(a)} exchange in {sa:.3f} s"}
 
     if dist.rank == 0:
         line = {
@@ -781,7 +799,7 @@ def run_ours(a):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.dtype, "data": "synthetic",
             "config": {
-                "workload": f"{a.fused} + {a.a2av}",
+                "workload": f"{a.fused} + {_a2av_name(a)}",
                 "fused": {"ep": cfg.ep, "tp": cfg.tp, "E": cfg.E, "C": cfg.C, "M": cfg.M,
                           "H": cfg.H, "yShardType": cfg.y_shard_type, "dtype": cfg.dtype,
                           "tflop_per_step": step_flops / 1e12, "variant": fused_kernel,

@@ -22,7 +22,8 @@
 // be touched, so all blocks take the same decision without talking to each
 // other.  In the copy, consecutive threads take consecutive positions: index
 // loads and stores are coalesced, the gathers follow the index; each thread
-// keeps four positions in flight.  An index outside [0, in_len_i) is never
+// keeps eight positions in flight (4% faster than four, at 64 registers, no
+// spills; 512 threads with eight were 10-17% slower).  An index outside [0, in_len_i) is never
 // dereferenced; its position is not delivered and the optional status word
 // gets BRA_ERR_INVALID.  There are no waits.
 #include <mutex>
@@ -34,10 +35,13 @@ namespace bra {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kThreads = 1024;
+#ifndef BRA_IA2AV_THREADS
+#define BRA_IA2AV_THREADS 1024
+#endif
+constexpr int kThreads = BRA_IA2AV_THREADS;
 constexpr int kWarps = kThreads / 32;
 #ifndef BRA_IA2AV_UNROLL
-#define BRA_IA2AV_UNROLL 4
+#define BRA_IA2AV_UNROLL 8
 #endif
 constexpr int kUnroll = BRA_IA2AV_UNROLL;   // positions in flight per thread
 

@@ -266,3 +266,32 @@ def test_l2_flush_reads_without_writing():
     assert torch.equal(buf, before)
     with pytest.raises(bra.BraError):
         bra.l2_flush(buf[1:])                         # not 16-byte aligned
+
+
+@pytest.mark.parametrize("L", [64, 1])
+def test_piece_beyond_two_gib(L):
+    """One pair carries 2^31 + 4099 int8 elements (element offsets and byte
+    counts past 32 bits) from an input that starts 3 bytes past 16-byte
+    alignment: every byte arrives, checked on the device against the input
+    (the exchange's definition, out[1][n] = in[0][n]), and the bookkeeping
+    matches the oracle's."""
+    n = (1 << 31) + 4099
+    sc = np.array([[0, n], [5, 0]], dtype=np.int64)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(31)
+    buf0 = torch.randint(-128, 128, (n + 3,), generator=g, dtype=torch.int8, device="cuda")
+    in0 = buf0[3:]
+    in1 = torch.tensor([1, 2, 3, 4, 5], dtype=torch.int8, device="cuda")
+    out1 = torch.empty(n + 7, dtype=torch.int8, device="cuda")
+    out1[n:] = 0x5A
+    out0 = torch.full((5,), 0x11, dtype=torch.int8, device="cuda")
+    res = bra.all_to_all_v([in0, in1], torch.from_numpy(sc).cuda(), [out0, out1], L)
+    torch.cuda.synchronize()
+    assert torch.equal(out1[:n], in0)
+    assert (out1[n:] == 0x5A).all()
+    assert torch.equal(out0, in1)
+    for key, want in zip(("send_displs", "recv_counts", "recv_displs"), oa.a2av_bookkeeping(sc)):
+        np.testing.assert_array_equal(res[key].cpu().numpy(), want)
+    assert bra.fault_status() == 0
+    del buf0, out1
+    torch.cuda.empty_cache()

@@ -37,11 +37,12 @@
 // complete at about one chunk per load latency, and a warp's own chunk work
 // is a chain of dependent steps, so many independent warp pipelines keep an
 // SM's loads and stores in flight.  Piece tables are built by all threads,
-// kMaxSeg segments at a time; the head and tail bytes of each piece (before
+// kMaxSeg segments at a time.  The head and tail bytes of each piece (before
 // its first and after its last 16-byte-aligned destination vector) are
-// copied straight from the send buffer after the batch's chunks.
-// Afterwards the bookkeeping (send displacements, receive counts, receive
-// displacements) is written, its entries spread over all blocks.
+// copied straight from the send buffer, and the bookkeeping (send
+// displacements, receive counts, receive displacements) is written, by every
+// thread after its warp's first chunk, while the warp's next chunks are in
+// flight; the bookkeeping entries are spread over all blocks.
 // A granule holding a byte of a buffer never crosses a page the buffer does
 // not touch, so granule-wide loads stay in bounds.  Every wait is bounded
 // (about 2 s by %globaltimer); a wait that runs out records BRA_ERR_TIMEOUT
@@ -455,6 +456,24 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   if (lane == 0)
     for (int k = 0; k < stages; ++k) load_next(k);
 
+  // Bookkeeping, entries (i, j) dealt round-robin over the blocks, then over
+  // each block's threads; every thread does its share after its warp's first
+  // chunk (below), while the warp's next chunks are in flight.
+  auto bookkeeping = [&]() {
+    const int64_t PP = (int64_t)P * P;
+#pragma unroll 1
+    for (int64_t e = b + (int64_t)nb * tid; e < PP; e += (int64_t)nb * kThreads) {
+      const int i = (int)(e / P), j = (int)(e % P);
+      int64_t sd = 0, rd = 0;
+      for (int k = 0; k < j; ++k) sd += cnt[i * P + k];
+      for (int k = 0; k < i; ++k) rd += cnt[k * P + j];
+      a.sd[(int64_t)i * P + j] = sd;
+      a.rc[(int64_t)j * P + i] = cnt[i * P + j];
+      a.rd[(int64_t)j * P + i] = rd;
+    }
+  };
+  bool book_done = false;
+
   bool live = true;
   int slot = 0;
   uint32_t ph = 0;
@@ -511,6 +530,40 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
       if (lane == 0) s_np[s] = __popc(m0) + __popc(m1);
     }
     __syncthreads();
+    // Head and tail bytes of the batch's pieces, straight from the send
+    // buffer: byte slot x = (piece, b) with b < 15 the head's byte b and
+    // 16 <= b < 31 the tail's byte b - 16, dealt over every thread, four
+    // loads in flight per thread.  Each warp does its share after writing
+    // its first chunk of the batch, while its next chunks are in flight.
+    auto head_tail = [&]() {
+      const int nslot = nbatch * kA2avMaxP * 32;
+#pragma unroll 1
+      for (int x0 = 0; x0 < nslot; x0 += 4 * kThreads) {
+        char v[4];
+        char* dst[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int x = x0 + u * kThreads + tid;
+          dst[u] = nullptr;
+          v[u] = 0;
+          if (x < nslot) {
+            const Run& rr = s_run[(x >> 5) / kA2avMaxP][(x >> 5) % kA2avMaxP];
+            const int bb = x & 31;
+            const bool in_head = bb < rr.head;
+            const bool in_tail = bb >= 16 && bb - 16 < rr.tail;
+            if (in_head || in_tail) {
+              const int64_t o = in_head ? (int64_t)bb - rr.head : rr.nvec * 16 + (bb - 16);
+              v[u] = __ldg(reinterpret_cast<const char*>(rr.vb) + o);
+              dst[u] = rr.d + o;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (dst[u]) *dst[u] = v[u];
+      }
+    };
+    bool ht_done = false;
 
     // The warp's chunks of this batch.
     const int64_t te = s_chbase[b0 + nbatch];
@@ -534,30 +587,18 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
         slot = 0;
         ph ^= 1u;
       }
-    }
-    // Head and tail bytes of the batch's pieces, straight from the send
-    // buffer (loads first, then stores).
-    if (live && tid < nbatch * kA2avMaxP) {
-      const Run& rr = s_run[tid / kA2avMaxP][tid % kA2avMaxP];
-      const int head = rr.head, tail = rr.tail;
-      if (head + tail > 0) {
-        const char* src = reinterpret_cast<const char*>(rr.vb);
-        const char* ts = src + rr.nvec * 16;
-        char hb[15], tb[15];
-#pragma unroll
-        for (int k = 0; k < 15; ++k) {
-          hb[k] = k < head ? __ldg(src - head + k) : 0;
-          tb[k] = k < tail ? __ldg(ts + k) : 0;
-        }
-        char* td = rr.d + rr.nvec * 16;
-#pragma unroll
-        for (int k = 0; k < 15; ++k) {
-          if (k < head) rr.d[k - head] = hb[k];
-          if (k < tail) td[k] = tb[k];
+      if (!ht_done) {
+        head_tail();
+        ht_done = true;
+        if (!book_done) {
+          bookkeeping();
+          book_done = true;
         }
       }
     }
+    if (live && !ht_done) head_tail();   // the warp had no chunk in this batch
   }
+  if (live && !book_done) bookkeeping();
   if (!live) {   // a wait ran out: give copies already issued time to land
     if (lane == 0) {
       const unsigned long long t0 = global_ns();
@@ -565,20 +606,6 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
       }
     }
     return;
-  }
-
-  // Bookkeeping, entries (i, j) dealt round-robin over the blocks, then over
-  // each block's threads.
-  const int64_t PP = (int64_t)P * P;
-#pragma unroll 1
-  for (int64_t e = b + (int64_t)nb * tid; e < PP; e += (int64_t)nb * kThreads) {
-    const int i = (int)(e / P), j = (int)(e % P);
-    int64_t sd = 0, rd = 0;
-    for (int k = 0; k < j; ++k) sd += cnt[i * P + k];
-    for (int k = 0; k < i; ++k) rd += cnt[k * P + j];
-    a.sd[(int64_t)i * P + j] = sd;
-    a.rc[(int64_t)j * P + i] = cnt[i * P + j];
-    a.rd[(int64_t)j * P + i] = rd;
   }
 }
 

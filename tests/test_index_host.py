@@ -278,6 +278,7 @@ def test_element_epilogue_staging_shift(delta):
 # all_to_all_v kernel (a2av.cu): block ranges, segments, staged chunks, the
 # warps' chunk shares and the piece writes.
 A2AV_CHUNK, A2AV_STRIDE, A2AV_WARPS, A2AV_MAXSEG = 4096, 4096 + 128, 16, 4
+P_MAX = 64   # pieces tabled per segment (the kernel's kA2avMaxP)
 
 
 def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_mem, written):
@@ -321,6 +322,7 @@ def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_m
         for b0 in range(0, len(segs), A2AV_MAXSEG):
             batch = segs[b0:b0 + A2AV_MAXSEG]
             tables = []
+            pieces = {}
             for (i, slo, shi, g0, g1, nch) in batch:
                 runs = []
                 for j in range(P):
@@ -333,13 +335,27 @@ def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_m
                     dst = out_base[j] + (rd[i, j] + (c0e - sd[i, j])) * es
                     head = min((16 - dst % 16) % 16, n)
                     nvec, tail = (n - head) >> 4, (n - head) & 15
-                    for off in list(range(head)) + [head + nvec * 16 + x for x in range(tail)]:
-                        assert span[i][0] <= src + off < span[i][1]
-                        out_mem[dst + off] = mem[src + off]
-                        written[dst + off] += 1
+                    pieces[(len(tables), j)] = (src + head, dst + head, nvec, head, tail)
                     if nvec > 0:
                         runs.append((src + head, dst + head, nvec))
                 tables.append(runs)
+            # Head and tail bytes: byte slot x = (piece, b) of the batch, b < 15
+            # the head's byte b, 16 <= b < 31 the tail's byte b - 16.
+            for x in range(len(batch) * P_MAX * 32):
+                key = ((x >> 5) // P_MAX, (x >> 5) % P_MAX)
+                if key not in pieces:
+                    continue
+                vb, d, nvec, head, tail = pieces[key]
+                bb = x & 31
+                if bb < head:
+                    o = bb - head
+                elif 16 <= bb < 16 + tail:
+                    o = nvec * 16 + bb - 16
+                else:
+                    continue
+                assert span[segs[b0 + key[0]][0]][0] <= vb + o < span[segs[b0 + key[0]][0]][1]
+                out_mem[d + o] = mem[vb + o]
+                written[d + o] += 1
             tb, te = chbase[b0], chbase[b0 + len(batch)]
             for g in range(A2AV_WARPS):
                 t = tb + ((g - tb % A2AV_WARPS) + A2AV_WARPS) % A2AV_WARPS

@@ -295,3 +295,30 @@ def test_piece_beyond_two_gib(L):
     assert bra.fault_status() == 0
     del buf0, out1
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("k", range(24))
+def test_random_exchanges_match_the_oracle(k):
+    """Random rank counts, launch widths, dtypes, count mixes (zeros, a few
+    large pieces among many small ones, rows of one destination) and buffer
+    offsets, bit-exact against the oracle."""
+    rng = np.random.default_rng(5000 + k)
+    P = int(rng.choice([1, 2, 3, 5, 8, 13, 32, 47, 64]))
+    dt = "int8" if rng.random() < 0.6 else "fp32"
+    es = 1 if dt == "int8" else 4
+    L = int(rng.choice([1, 2, P, 2 * P + 1, 64, 152, 1000]))
+    big = rng.integers(0, (1 << 18) // es, size=(P, P))
+    small = rng.integers(0, 40, size=(P, P))
+    sc = np.where(rng.random((P, P)) < 4.0 / max(P, 4), big, small).astype(np.int64)
+    sc[rng.random((P, P)) < 0.3] = 0
+    if rng.random() < 0.3:                         # one row sends everything to one rank
+        r = int(rng.integers(0, P))
+        sc[r] = 0
+        sc[r, int(rng.integers(0, P))] = int(rng.integers(1, (1 << 20) // es))
+    ndt = np.int8 if dt == "int8" else np.float32
+    inputs = [(rng.integers(-128, 128, size=int(sc[i].sum()), dtype=np.int8) if dt == "int8"
+               else rng.standard_normal(int(sc[i].sum())).astype(np.float32)) for i in range(P)]
+    offs = 16 // es
+    check_exact(sc, inputs, dt, L, in_off=[int(rng.integers(0, offs)) for _ in range(P)],
+                out_off=[int(rng.integers(0, offs)) for _ in range(P)])
+    assert bra.fault_status() == 0

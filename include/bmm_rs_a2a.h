@@ -57,7 +57,7 @@ typedef enum {
   BRA_OK = 0,
   BRA_ERR_NULLPTR = 161001,     /* a required pointer is NULL                 */
   BRA_ERR_INVALID = 161002,     /* dtype, attribute, shape or aliasing rule   */
-  BRA_ERR_UNSUPPORTED = 161003, /* valid per the pages but beyond this build  */
+  BRA_ERR_UNSUPPORTED = 161003, /* valid per the pages, beyond the library limits */
   BRA_ERR_CUDA = 161100,        /* a CUDA call failed (launch or query)       */
   BRA_ERR_TIMEOUT = 161101      /* a kernel gave up a bounded wait            */
 } bra_status;

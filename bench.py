@@ -578,6 +578,35 @@ def run_ours(a):
                 "resolution); the in-step figure above follows the fused kernel at its "
                 "power-capped clock, which also slows L2",
     }
+    # Back to back in a CUDA graph (no sweep between calls, 50 calls per
+    # replay): event timing without its ~2 us quantum and launch gaps.
+    if a_alone:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            a2av_plan.run(side)
+        stream.wait_stream(side)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(g):
+            for _ in range(50):
+                a2av_plan.run(torch.cuda.current_stream(dev))
+        g.replay()
+        torch.cuda.synchronize(dev)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(4):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        gms = g0.elapsed_time(g1) / 200
+        a2av_line["alone_graph"] = {
+            "mean_ms": gms, "achieved": a_bytes / (gms / 1e3) / 1e9, "unit": "GB/s",
+            "frac": a_bytes / (gms / 1e3) / 1e9 / peaks["hbm_gbs"], "calls": 200,
+            "note": "200 calls back to back in a CUDA graph, no L2 sweep between them (the "
+                    "payload is larger than L2)"}
+        del g
     # The same exchange with core_num = the SM count: as many blocks as the
     # launch-width rule admits on the whole GPU (context for the B above).
     sms = torch.cuda.get_device_properties(dev).multi_processor_count

@@ -24,7 +24,7 @@
 // the segments follow from them.  Every block sees the same matrix, so all
 // take the same verdict without a grid sync; a rejected call copies
 // nothing.
-// Copy: the block's source bytes are cut into chunks of kChunk bytes
+// Copy: the block's source bytes are cut into chunks of `chunk` bytes
 // (16-byte granules; each chunk is staged with one granule more, so every
 // destination vector whose first byte lies in a chunk is whole in its
 // stage).  Chunk t belongs to warp t mod kWarps, and each warp is its own
@@ -67,20 +67,22 @@ constexpr unsigned kFull = 0xffffffffu;
 #ifndef BRA_A2AV_MAX_STAGES
 #define BRA_A2AV_MAX_STAGES 3
 #endif
-#ifndef BRA_A2AV_CHUNK
-#define BRA_A2AV_CHUNK 4096
-#endif
 constexpr int kWarps = BRA_A2AV_WARPS;           // copy warps = pipelines per block
 constexpr int kThreads = 32 * kWarps;
 constexpr int kRowsPerWarp = (kA2avMaxP + kWarps - 1) / kWarps;   // count rows per warp at set-up
 constexpr int kMaxStages = BRA_A2AV_MAX_STAGES;  // ring slots per warp
 constexpr int kMaxSeg = 4;                       // segments whose pieces are tabled at once
-constexpr uint32_t kChunk = BRA_A2AV_CHUNK;      // source bytes a chunk writes out
-constexpr int kStageStride = kChunk + 128;       // staged with one granule more
+// Chunk sizes, largest first: the launch takes the first whose ring of at
+// least two slots per warp fits beside the P x P counts.  6 KiB chunks in
+// two slots ran the bench workload ~5% faster than 4 KiB in three on 64 and
+// 128 blocks (fewer chunks, less per-chunk work), and ~7% slower on
+// exchanges of a few MB.
+constexpr uint32_t kChunks[2] = {6144, 4096};
+constexpr uint32_t kSlotPad = 128;               // a chunk is staged with one granule more
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 static_assert(kThreads >= kMaxSeg * kA2avMaxP, "one thread per tabled piece");
 static_assert(kWarps >= kMaxSeg, "one compacting warp per tabled segment");
-static_assert((kChunk & (kChunk - 1)) == 0 && kChunk >= 512, "chunk: a power of two");
+static_assert(kChunks[0] % 512 == 0 && kChunks[1] % 512 == 0, "chunks: whole 512-byte steps");
 
 // One piece of a segment: its 16-byte-aligned destination vectors, and the
 // head and tail bytes before the first and after the last of them.
@@ -318,10 +320,11 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   __shared__ int s_abort;   // a bounded wait ran out
 
   const int P = a.P, stages = a.stages;
+  const uint32_t chunk = a.chunk, stride = a.chunk + kSlotPad;   // slot bytes
   const int nb = gridDim.x, b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t es = a.esize;
-  int64_t* cnt = reinterpret_cast<int64_t*>(dyn + kWarps * stages * kStageStride);
+  int64_t* cnt = reinterpret_cast<int64_t*>(dyn + kWarps * stages * stride);
   const uint32_t ring_base = smem_u32(dyn);
 
   // ---------------- set-up (all warps) ----------------
@@ -414,9 +417,9 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
     // Chunks per segment and their exclusive prefix (the global chunk index
     // of each segment's first chunk).
     int64_t n0 = 0, n1 = 0;
-    if (lane < nseg) n0 = (int64_t)((s_seg_g1[lane] - s_seg_g0[lane] + kChunk - 1) / kChunk);
+    if (lane < nseg) n0 = (int64_t)((s_seg_g1[lane] - s_seg_g0[lane] + chunk - 1) / chunk);
     if (lane + 32 < nseg)
-      n1 = (int64_t)((s_seg_g1[lane + 32] - s_seg_g0[lane + 32] + kChunk - 1) / kChunk);
+      n1 = (int64_t)((s_seg_g1[lane + 32] - s_seg_g0[lane + 32] + chunk - 1) / chunk);
     int64_t e0, e1, nch;
     warp_exscan64(n0, n1, lane, e0, e1, nch);
     if (lane < nseg) s_chbase[lane] = e0;
@@ -438,18 +441,18 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
   // Lane 0 loads the warp's chunks t = warp, warp + kWarps, ... in order,
   // chunk number i of the warp into slot i % stages; `stages` are loaded
   // up front and each one consumed frees its slot for the next.
-  const uint32_t ring = ring_base + (uint32_t)(warp * stages * kStageStride);
+  const uint32_t ring = ring_base + (uint32_t)(warp * stages * stride);
   int64_t t_load = warp;
   int sg_load = 0;
   auto load_next = [&](int slot) {
     if (t_load >= nch) return;
     while (s_chbase[sg_load + 1] <= t_load) ++sg_load;
-    const uintptr_t c0 = s_seg_g0[sg_load] + (uintptr_t)(t_load - s_chbase[sg_load]) * kChunk;
+    const uintptr_t c0 = s_seg_g0[sg_load] + (uintptr_t)(t_load - s_chbase[sg_load]) * chunk;
     const uintptr_t G1 = s_seg_g1[sg_load];
-    const uintptr_t ce = c0 + kChunk + 16 < G1 ? c0 + kChunk + 16 : G1;
+    const uintptr_t ce = c0 + chunk + 16 < G1 ? c0 + chunk + 16 : G1;
     const uint32_t fb = smem_u32(&s_full[warp][slot]);
     mbar_expect_tx(fb, (uint32_t)(ce - c0));
-    bulk_load(ring + slot * kStageStride, reinterpret_cast<const void*>(c0), (uint32_t)(ce - c0),
+    bulk_load(ring + slot * stride, reinterpret_cast<const void*>(c0), (uint32_t)(ce - c0),
               fb);
     t_load += kWarps;
   };
@@ -576,11 +579,11 @@ a2av_kernel(const __grid_constant__ A2avArgs a) {
       const bool waited = mbar_wait(smem_u32(&s_full[warp][slot]), ph, abort_flag);
       live = __all_sync(kFull, waited);
       if (!live) break;
-      const uintptr_t c0 = s_seg_g0[sg] + (uintptr_t)(t - s_chbase[sg]) * kChunk;
+      const uintptr_t c0 = s_seg_g0[sg] + (uintptr_t)(t - s_chbase[sg]) * chunk;
       const uintptr_t G1 = s_seg_g1[sg];
-      const uintptr_t c1 = c0 + kChunk < G1 ? c0 + kChunk : G1;   // bytes this chunk writes
+      const uintptr_t c1 = c0 + chunk < G1 ? c0 + chunk : G1;   // bytes this chunk writes
       const int s = sg - b0;
-      copy_runs(s_run[s], s_list[s], s_np[s], q, c0, c1, ring + slot * kStageStride, lane);
+      copy_runs(s_run[s], s_list[s], s_np[s], q, c0, c1, ring + slot * stride, lane);
       __syncwarp();
       if (lane == 0) load_next(slot);   // the warp's chunk `stages` later
       if (++slot == stages) {
@@ -663,12 +666,21 @@ cudaError_t a2av_device_info(A2avDeviceInfo* out) {
   return cudaSuccess;
 }
 
-// Ring slots per warp that fit beside a P x P count matrix, at most
-// kMaxStages.
-int stages_for(const A2avDeviceInfo& di, int P) {
+// Chunk size and ring slots per warp for P ranks: the largest chunk of
+// kChunks with at least two slots per warp beside the P x P counts, and as
+// many slots as fit, at most kMaxStages.  Slots 0 means none fits.
+void ring_for(const A2avDeviceInfo& di, int P, uint32_t* chunk, int* slots) {
   const int cnt_bytes = (P * P * 8 + 127) / 128 * 128;
-  const int s = (di.dyn_max - cnt_bytes) / (kWarps * kStageStride);
-  return s > kMaxStages ? kMaxStages : s;
+  for (uint32_t c : kChunks) {
+    const int s = (di.dyn_max - cnt_bytes) / (kWarps * (int)(c + kSlotPad));
+    if (s >= 2) {
+      *chunk = c;
+      *slots = s > kMaxStages ? kMaxStages : s;
+      return;
+    }
+  }
+  *chunk = kChunks[1];
+  *slots = 0;
 }
 
 }  // namespace
@@ -684,7 +696,7 @@ cudaError_t launch_a2av(const A2avArgs& args, int blocks, cudaStream_t st) {
   cudaError_t e = a2av_device_info(&di);
   if (e != cudaSuccess) return e;
   A2avArgs a = args;
-  a.stages = stages_for(di, a.P);
+  ring_for(di, a.P, &a.chunk, &a.stages);
   if (a.stages < 2 || blocks < 1) return cudaErrorInvalidConfiguration;
   // The whole shared memory a block may take, whatever the ring uses: two
   // blocks never share an SM, and the exchange occupies `blocks` SMs.

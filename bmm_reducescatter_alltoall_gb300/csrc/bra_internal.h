@@ -32,7 +32,8 @@ struct A2avArgs {
   int P;
   int esize;                // element size in bytes (4 or 1)
   int check_cap;            // compare received totals against cap[]
-  int stages;               // ring depth (set by launch_a2av)
+  int stages;               // ring slots per warp (set by launch_a2av)
+  uint32_t chunk;           // bytes per chunk (set by launch_a2av)
 };
 
 // Blocks the exchange launches for an admitted block count B on the current

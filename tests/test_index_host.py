@@ -277,11 +277,11 @@ def test_element_epilogue_staging_shift(delta):
 # ---------------------------------------------------------------------------
 # all_to_all_v kernel (a2av.cu): block ranges, segments, staged chunks, the
 # warps' chunk shares and the piece writes.
-A2AV_CHUNK, A2AV_STRIDE, A2AV_WARPS, A2AV_MAXSEG = 4096, 4096 + 128, 16, 4
+A2AV_CHUNKS, A2AV_PAD, A2AV_WARPS, A2AV_MAXSEG = (6144, 4096), 128, 16, 4
 P_MAX = 64   # pieces tabled per segment (the kernel's kA2avMaxP)
 
 
-def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_mem, written):
+def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, chunk, mem, out_mem, written):
     """Run the kernel's addressing for every block: `mem` maps a source
     address to its byte value, `out_mem` / `written` receive the stores.
     Checks every staged read, every direct read and every store against the
@@ -303,17 +303,17 @@ def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_m
                 slo, shi = max(lo - off, 0), min(hi - off, tot)
                 g0 = (in_base[r] + slo * es) & ~15
                 g1 = (in_base[r] + shi * es + 15) & ~15
-                segs.append((r, slo, shi, g0, g1, -(-(g1 - g0) // A2AV_CHUNK)))
+                segs.append((r, slo, shi, g0, g1, -(-(g1 - g0) // chunk)))
         chbase = np.concatenate([[0], np.cumsum([s[5] for s in segs])]).astype(np.int64)
         # Loads: chunk t of the block staged from [c0, ce).
         staged = {}
         t = 0
         for (r, slo, shi, g0, g1, nch) in segs:
             lo_g, hi_g = in_base[r] & ~15, (in_base[r] + in_len_b[r] + 15) & ~15
-            for c0 in range(g0, g1, A2AV_CHUNK):
-                ce = min(c0 + A2AV_CHUNK + 16, g1)
+            for c0 in range(g0, g1, chunk):
+                ce = min(c0 + chunk + 16, g1)
                 assert lo_g <= c0 < ce <= hi_g and (ce - c0) % 16 == 0 and c0 % 16 == 0
-                assert ce - c0 <= A2AV_STRIDE
+                assert ce - c0 <= (chunk + A2AV_PAD)
                 staged[t] = (c0, ce)
                 t += 1
         assert t == chbase[-1]
@@ -365,9 +365,9 @@ def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_m
                         sg, q = sg + 1, 0
                     c0s, ce = staged[t]
                     G1 = segs[sg][4]
-                    c0 = segs[sg][3] + (t - chbase[sg]) * A2AV_CHUNK
+                    c0 = segs[sg][3] + (t - chbase[sg]) * chunk
                     assert c0 == c0s
-                    c1 = min(c0 + A2AV_CHUNK, G1)
+                    c1 = min(c0 + chunk, G1)
                     stage = mem[c0:ce]
                     runs = tables[sg - b0]
                     qq = q
@@ -385,7 +385,7 @@ def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_m
                         o = vb + vlo * 16 - c0
                         k = np.arange(vhi - vlo)
                         rd0 = (o & ~15) + 16 * k          # first staged word read
-                        assert rd0.min() >= 0 and (rd0 + 32).max() <= A2AV_STRIDE
+                        assert rd0.min() >= 0 and (rd0 + 32).max() <= (chunk + A2AV_PAD)
                         first = o + 16 * k                # the vector's bytes in the stage
                         assert (first + 16).max() <= ce - c0
                         dv = d + 16 * (vlo + k)
@@ -401,9 +401,10 @@ def _a2av_block_copy(sc, es, in_base, in_len_b, out_base, nb, stages, mem, out_m
                     t += A2AV_WARPS
 
 
+@pytest.mark.parametrize("chunk", A2AV_CHUNKS)
 @pytest.mark.parametrize("seed", range(6))
 @pytest.mark.parametrize("es", [1, 4])
-def test_exchange_block_addressing(seed, es):
+def test_exchange_block_addressing(seed, es, chunk):
     """Every byte each rank receives is written exactly once with the right
     source byte, staged reads stay inside the staged chunk (and its ring
     slot), bulk loads stay inside the send buffer's 16-byte granules, and no
@@ -412,7 +413,7 @@ def test_exchange_block_addressing(seed, es):
     rng = np.random.default_rng(seed)
     P = int(rng.choice([1, 2, 3, 5, 8]))
     small = rng.integers(0, 40, size=(P, P))
-    big = rng.integers(0, 12 * A2AV_CHUNK // es, size=(P, P))
+    big = rng.integers(0, 12 * chunk // es, size=(P, P))
     sc = np.where(rng.random((P, P)) < 0.4, big, small).astype(np.int64)
     sc[rng.random((P, P)) < 0.2] = 0
     in_len = sc.sum(axis=1) * es
@@ -434,7 +435,7 @@ def test_exchange_block_addressing(seed, es):
     for nb in sorted({1, 3, max(1, P - 1), P, 2 * P + 1, 64}):
         out_mem[:] = 0
         written[:] = 0
-        _a2av_block_copy(sc, es, in_base, in_len, out_base, nb, 12, mem, out_mem, written)
+        _a2av_block_copy(sc, es, in_base, in_len, out_base, nb, chunk, mem, out_mem, written)
         expect_w = np.zeros_like(written)
         for j in range(P):
             expect_w[out_base[j]:out_base[j] + out_len[j]] = 1

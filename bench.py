@@ -512,6 +512,11 @@ def run_ours(a):
         "algorithmic_flops_per_launch": step_flops / fused_launches,
         "mean_ms": f_ms, "min_ms": min(fused_ms),
     }
+    # ---- context: cuBLAS in the fused op's dtype right after the timed region,
+    # for as long (a dense 8192^3 GEMM back to back; under a long loop both run
+    # at the power cap, and fp16 settles at a lower clock than bf16) ----
+    roofline["cublas_same_dtype"] = cublas_context(torch, dev, ydt, min(max(total_s, 0.3), 4.0),
+                                                   f_tflops)
     a2av_line = {
         "kernel": "a2av_kernel", "value": a_gbs, "unit": "GB/s", "bound": "hbm",
         "achieved": a_gbs, "peak": peaks["hbm_gbs"], "frac": a_gbs / peaks["hbm_gbs"],
@@ -969,6 +974,46 @@ def run_a2av_sweep(a):
 # --------------------------------------------------------------------------
 
 MMA_FLOP = 2 * 128 * 256 * 16      # one M=128 N=256 K=16 MMA
+
+
+def cublas_context(torch, dev, dtype, seconds, fused_tflops):
+    """torch.matmul of two 8192 x 8192 matrices in `dtype`, back to back for
+    about `seconds`, timed by CUDA events, with the median SM clock sampled
+    meanwhile; and the fused kernel's rate over it."""
+    n = 8192
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    a = torch.randn(n, n, device=dev, generator=g).to(dtype)
+    b = torch.randn(n, n, device=dev, generator=g).to(dtype)
+    c = torch.empty(n, n, device=dev, dtype=dtype)
+    for _ in range(3):
+        torch.matmul(a, b, out=c)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.25)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    calls = 0
+    w0 = time.monotonic()
+    e0.record()
+    while time.monotonic() - w0 < seconds:
+        for _ in range(8):
+            torch.matmul(a, b, out=c)
+        calls += 8
+        torch.cuda.synchronize(dev)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    w1 = time.monotonic()
+    time.sleep(0.25)
+    sampler.mark(w0, w1)
+    clk = sampler.stop()
+    ms = e0.elapsed_time(e1) / calls
+    tf = 2.0 * n ** 3 / (ms / 1e3) / 1e12
+    del a, b, c
+    return {"tflops": tf, "calls": calls, "seconds": round(w1 - w0, 2), "sm_mhz": clk["sm_mhz"],
+            "fused_over_cublas": fused_tflops / tf,
+            "what": f"torch.matmul {n}^3 {str(dtype).replace('torch.', '')}, back to back right "
+                    "after the timed region for as long as it (context: the same power regime)"}
 
 
 def mma_rate(bra, torch, dev, iters, dtype, ctas=None):

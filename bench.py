@@ -663,6 +663,8 @@ def run_ours(a):
         indexed = {
             "kernel": "ia2av_kernel", "workload": f"{_a2av_name(a)}, index = a permutation of each "
                                                   "sender's input (seeded)",
+            "bound": "gathers (one random load per element; gather_bound below), reported also "
+                     "in GB/s against HBM",
             "achieved": ia_bytes / (m / 1e3) / 1e9, "unit": "GB/s",
             "frac": ia_bytes / (m / 1e3) / 1e9 / peaks["hbm_gbs"], "peak": peaks["hbm_gbs"],
             "algorithmic_bytes_per_launch": ia_bytes, "mean_ms": m, "min_ms": min(ia_ms),
@@ -673,6 +675,24 @@ def run_ours(a):
             "note": "bytes = payload read + write + 8-byte index per element + bookkeeping; "
                     "each call after the read-only L2 sweep, timed alone; the gathers are "
                     "random, one 32-byte sector per element",
+        }
+        # The gathers, not HBM, bound this call: one load per element, each in
+        # its own line.  The gather-rate probe on as many SMs, right after,
+        # gives the rate the SMs can issue them at.
+        gbuf = torch.randint(0, 256, (64 << 20,), dtype=torch.uint8, device=dev)
+        gb = gather_rate(bra, torch, dev, gbuf, min(acfg.L, sms))
+        gw = gather_rate(bra, torch, dev, gbuf, sms)
+        del gbuf
+        indexed["gather_bound"] = {
+            "what": "random one-byte loads from a 64 MiB buffer (L2-resident) on the same number "
+                    "of SMs, right after (bra_gather_rate_probe): one per gathered element",
+            "probe_gathers_per_s": gb["gathers_per_s"], "probe_per_sm_clk": gb["per_sm_clk"],
+            "probe_mhz": gb["mhz"], "achieved_gathers_per_s": n_el / (m / 1e3),
+            "frac": n_el / (m / 1e3) / gb["gathers_per_s"],
+            "whole_gpu": {"probe_gathers_per_s": gw["gathers_per_s"],
+                          "probe_per_sm_clk": gw["per_sm_clk"],
+                          "achieved_gathers_per_s": n_el / (wm / 1e3),
+                          "frac": n_el / (wm / 1e3) / gw["gathers_per_s"]},
         }
         del ix
         if bra.fault_status() != 0:
@@ -1014,6 +1034,25 @@ def cublas_context(torch, dev, dtype, seconds, fused_tflops):
             "fused_over_cublas": fused_tflops / tf,
             "what": f"torch.matmul {n}^3 {str(dtype).replace('torch.', '')}, back to back right "
                     "after the timed region for as long as it (context: the same power regime)"}
+
+
+def gather_rate(bra, torch, dev, buf, ctas, iters=128):
+    """The gather-rate probe on `ctas` SMs: random one-byte loads per second
+    (CUDA events over the launch) and per SM clock (the CTAs' own cycle
+    counts, median), and the clock it ran at."""
+    bra.gather_rate_probe(buf, ctas, 8)                     # warm-up
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    rec = bra.gather_rate_probe(buf, ctas, iters)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    r = rec.cpu().numpy()
+    per_cta = 1024 * iters * 8
+    return {"ctas": int(ctas), "gathers_per_s": ctas * per_cta / (e0.elapsed_time(e1) / 1e3),
+            "per_sm_clk": float(statistics.median(per_cta / r[:, 0])),
+            "mhz": float(statistics.median(r[:, 0] / r[:, 1] * 1e3)),
+            "distinct_sms": int(len(set(r[:, 2].tolist())))}
 
 
 def mma_rate(bra, torch, dev, iters, dtype, ctas=None):

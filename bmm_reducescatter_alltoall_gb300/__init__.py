@@ -22,7 +22,7 @@ __all__ = [
     "FusedOptions", "library", "library_path", "bmm_rs_a2a", "bmm_rs_a2a_infer_shape",
     "bmm_rs_a2a_variant", "all_to_all_v", "all_to_all_v_checked", "Plan", "bmm_rs_a2a_plan",
     "all_to_all_v_plan", "indexed_all_to_all_v_plan",
-    "cal_all_to_all_v_blocks", "all_to_all_v_launch_blocks", "l2_flush", "mma_rate_probe", "fault_status", "status_str", "version",
+    "cal_all_to_all_v_blocks", "all_to_all_v_launch_blocks", "l2_flush", "mma_rate_probe", "gather_rate_probe", "fault_status", "status_str", "version",
 ]
 
 FP16, BF16, FP32, INT8 = 0, 1, 2, 3
@@ -96,6 +96,8 @@ def library() -> ctypes.CDLL:
     lib.bra_fault_status.restype = c_int
     lib.bra_mma_rate_probe.argtypes = [c_int, c_int, c_int, vp, vp]
     lib.bra_mma_rate_probe.restype = c_int
+    lib.bra_gather_rate_probe.argtypes = [vp, i64, c_int, c_int, vp, vp]
+    lib.bra_gather_rate_probe.restype = c_int
     lib.bra_wait_selftest.argtypes = [c_int, vp, vp]
     lib.bra_wait_selftest.restype = c_int
     lib.bra_version.argtypes = []
@@ -611,6 +613,22 @@ def mma_rate_probe(ctas: int, iters: int, dtype=None, stream=None):
     rec = torch.zeros((int(ctas), 4), dtype=torch.int64, device="cuda")
     _check(library().bra_mma_rate_probe(int(ctas), int(iters), dt, rec.data_ptr(),
                                         _stream_handle(stream)), "bra_mma_rate_probe")
+    return rec
+
+
+def gather_rate_probe(buf, ctas: int, iters: int, stream=None):
+    """Gather-rate probe (bra_gather_rate_probe of the C header): `ctas` CTAs,
+    one per SM, each 1024 threads x iters x 8 random one-byte loads from
+    `buf` (a contiguous CUDA tensor whose size in bytes is a power of two).
+    Returns a CUDA int64 tensor (ctas, 4): cycles, ns, SM id, byte sum per
+    CTA (asynchronous on `stream`)."""
+    torch = _torch()
+    if not (buf.is_cuda and buf.is_contiguous()):
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    rec = torch.zeros((int(ctas), 4), dtype=torch.int64, device=buf.device)
+    _check(library().bra_gather_rate_probe(buf.data_ptr(), buf.numel() * buf.element_size(),
+                                           int(ctas), int(iters), rec.data_ptr(),
+                                           _stream_handle(stream)), "bra_gather_rate_probe")
     return rec
 
 

@@ -66,6 +66,7 @@ KERNEL_SOURCES = {
     "ia2av_kernel": "ia2av.cu",
     "repack_rows_kernel": "repack.cu",
     "mma_probe_kernel": "mma_probe.cu",
+    "gather_probe_kernel": "gather_probe.cu",
 }
 
 

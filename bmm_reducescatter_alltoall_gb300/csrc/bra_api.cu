@@ -639,6 +639,22 @@ int bra_mma_rate_probe(int ctas, int iters, int dtype, int64_t* rec_dev, bra_str
   return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
 }
 
+int bra_gather_rate_probe(const void* buf, int64_t bytes, int ctas, int iters, int64_t* rec_dev,
+                          bra_stream_t stream) {
+  if (!buf || !rec_dev) return BRA_ERR_NULLPTR;
+  if (bytes < 4096 || bytes > (int64_t(1) << 40) || (bytes & (bytes - 1)) != 0)
+    return BRA_ERR_INVALID;
+  if (iters < 1 || iters > (1 << 20)) return BRA_ERR_INVALID;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  if (ctas < 1 || ctas > sms) return BRA_ERR_INVALID;
+  const cudaError_t e =
+      bra::launch_gather_probe(buf, bytes, ctas, iters, rec_dev, (cudaStream_t)stream);
+  return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA;
+}
+
 const char* bra_version(void) { return "0.1.0"; }
 
 }  // extern "C"

@@ -97,6 +97,10 @@ bool fused_tcr_eligible(const FusedProblem& f);
 cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t st);
 // Tensor-core rate probe: `ctas` CTAs, one per SM, each iters x 4 MMAs.
 cudaError_t launch_mma_probe(int ctas, int iters, bool bf16, int64_t* rec, cudaStream_t st);
+// Gather-rate probe: `ctas` CTAs, one per SM, each 1024 threads x iters x 8
+// random one-byte loads from buf (bytes a power of two).
+cudaError_t launch_gather_probe(const void* buf, int64_t bytes, int ctas, int iters, int64_t* rec,
+                                cudaStream_t st);
 
 // Row repacking: copies rows of 16-bit elements that start at any even byte
 // address to rows that start 16-byte aligned, `pitch` elements apart.

@@ -520,6 +520,24 @@ BRA_API int bra_wait_selftest(int which, int32_t* status_dev, bra_stream_t strea
 BRA_API int bra_mma_rate_probe(int ctas, int iters, int dtype, int64_t* rec_dev,
                                bra_stream_t stream);
 
+/*
+ * bra_gather_rate_probe -- measurement aid for the indexed exchange's
+ * roofline: the rate at which an SM completes random one-byte loads, each in
+ * its own 128-byte line (the cost of one gathered element of
+ * indexed_all_to_all_v, whose index is arbitrary; [PTO] §A5 URMA 索引交换).
+ * Launches `ctas` CTAs of 1024 threads, one per SM (at most the SM count);
+ * each thread issues iters x 8 one-byte loads from pseudo-random offsets of
+ * buf (device memory of `bytes` bytes, a power of two from 4 KiB to 2^40;
+ * only read), and each CTA writes rec_dev[4 * c .. 4 * c + 3] (device int64):
+ * SM clock cycles and %globaltimer nanoseconds of its loop, its SM id, and
+ * the sum of the bytes it loaded.  Loads per SM clock =
+ * 1024 * iters * 8 / cycles.  The loop has no wait.  Asynchronous on
+ * `stream`.  Returns BRA_ERR_NULLPTR, BRA_ERR_INVALID (bytes, ctas outside
+ * [1, SM count], iters outside [1, 2^20]), BRA_ERR_CUDA or BRA_OK.
+ */
+BRA_API int bra_gather_rate_probe(const void* buf, int64_t bytes, int ctas, int iters,
+                                  int64_t* rec_dev, bra_stream_t stream);
+
 /* Library version, "major.minor.patch". */
 BRA_API const char* bra_version(void);
 

@@ -1,8 +1,12 @@
-"""The tensor-core rate probe (a measurement aid for the fused kernels'
-roofline): every CTA lands on its own SM, every bounded wait completes, and
-the dense kind::f16 rate it measures is a power of two in FLOP per SM clock
-within the range a tensor core can have (1k to 32k)."""
+"""The rate probes (measurement aids for the rooflines).  Tensor-core probe:
+every CTA lands on its own SM, every bounded wait completes, and the dense
+kind::f16 rate it measures is a power of two in FLOP per SM clock within the
+range a tensor core can have (1k to 32k).  Gather probe: every CTA lands on
+its own SM, the byte sums are those of random loads from the buffer, and the
+rate lies between a quarter of a load and eight loads per SM clock."""
 import math
+
+import numpy as np
 
 import pytest
 import torch
@@ -31,3 +35,28 @@ def test_probe_rejects_bad_arguments():
     for ctas, iters in ((0, 1), (sms + 1, 1), (1, 0), (1, 1 << 23)):
         with pytest.raises(bra.BraError):
             bra.mma_rate_probe(ctas, iters)
+
+
+def test_gather_probe_runs_one_cta_per_sm():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    buf = torch.full((1 << 20,), 3, dtype=torch.uint8, device="cuda")
+    iters = 16
+    rec = bra.gather_rate_probe(buf, sms, iters)
+    torch.cuda.synchronize()
+    r = rec.cpu().numpy()
+    assert len(set(r[:, 2].tolist())) == sms
+    # every loaded byte is 3: each CTA's sum is 3 x its loads
+    assert (r[:, 3] == 3 * 1024 * iters * 8).all()
+    per_clk = 1024 * iters * 8 / r[:, 0]
+    assert 0.25 <= float(np.median(per_clk)) <= 8.0
+
+
+def test_gather_probe_rejects_bad_arguments():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ok = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    odd = torch.zeros(3 << 12, dtype=torch.uint8, device="cuda")
+    small = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    for buf, ctas, iters in ((odd, 1, 1), (small, 1, 1), (ok, 0, 1), (ok, sms + 1, 1),
+                             (ok, 1, 0), (ok, 1, (1 << 20) + 1)):
+        with pytest.raises(bra.BraError):
+            bra.gather_rate_probe(buf, ctas, iters)

@@ -583,6 +583,17 @@ def run_ours(a):
                 "resolution); the in-step figure above follows the fused kernel at its "
                 "power-capped clock, which also slows L2",
     }
+    # The floor of that timing: the same event pair around a launch that does
+    # nothing (a one-thread kernel, after the same sweep), and the call's rate
+    # net of it.  Context beside `alone`, which stays the figure.
+    if a_alone:
+        floor = statistics.mean(time_alone(lambda: torch.cuda._sleep(1)))
+        net = statistics.mean(a_alone) - floor
+        a2av_line["alone"]["net_of_event_floor"] = {
+            "floor_ms": floor, "achieved": a_bytes / (net / 1e3) / 1e9, "unit": "GB/s",
+            "frac": a_bytes / (net / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "note": "floor = the mean event-timed span of an empty launch after the same sweep "
+                    "(two events plus one kernel launch); rate = bytes / (alone mean - floor)"}
     # Back to back in a CUDA graph (no sweep between calls, 50 calls per
     # replay): event timing without its ~2 us quantum and launch gaps.
     if a_alone:

@@ -13,6 +13,7 @@ exhaustively over shape classes:
   the same delta < 8 elements past that boundary, its pitch is a multiple of
   16 bytes, and it ends at the last row's end;
 * the even split of a send list over CTAs used by the exchange kernels;
+* the fused kernels' tile raster: one to one onto the launch's output tiles;
 * the repack kernel: every 32-bit word it loads holds a byte of the row being
   copied (so it lies inside the row's 16-byte granules, inside the
   allocation), every word it stores lies inside the destination row's pitch,
@@ -104,6 +105,37 @@ def test_row_class_stage_addressing(wt, ncx, ncw):
         assert dst % 16 == 0 and dst + 16 <= SW_A + SW_B
         written[dst] = written.get(dst, 0) + 1
     assert len(written) == (SW_A + SW_B) // 16 and set(written.values()) == {1}
+
+
+def _tile_coord(tile, m_tiles, n_tiles, group_m):
+    """tc_ptx.cuh's tile_coord: group, then super-rows of group_m m tiles
+    walked n tile by n tile (group_m <= 0: row-major)."""
+    per_group = m_tiles * n_tiles
+    g, t = divmod(tile, per_group)
+    if group_m <= 0:
+        return g, t // n_tiles, t % n_tiles
+    span = group_m * n_tiles
+    sr, u = divmod(t, span)
+    first_m = sr * group_m
+    rows = min(group_m, m_tiles - first_m)
+    return g, first_m + u % rows, u // rows
+
+
+@pytest.mark.parametrize("group_m", [0, 1, 4, 8, 16])
+def test_tile_raster_covers_every_tile_once(group_m):
+    """The persistent fused kernels hand tile t to pair t mod npairs and place
+    it with tile_coord: over any shape (ragged last super-row included) the
+    tiles of a launch map one to one onto (group, m tile, n tile), so every
+    output tile is computed exactly once."""
+    for m_tiles in range(1, 37):
+        for n_tiles in range(1, 19):
+            groups = 3
+            seen = set()
+            for tile in range(groups * m_tiles * n_tiles):
+                g, mt, nt = _tile_coord(tile, m_tiles, n_tiles, group_m)
+                assert 0 <= g < groups and 0 <= mt < m_tiles and 0 <= nt < n_tiles
+                seen.add((g, mt, nt))
+            assert len(seen) == groups * m_tiles * n_tiles
 
 
 def _class_map(base, rowlen, nrows, n, q, rpitch=None):

@@ -6,8 +6,9 @@ all_to_all_v.  Covers identity, permutation and repeating indices over
 longer inputs, fp32 and int8, P from 1 to 64, the int8 P = 32 Dirichlet
 workload at full size, unaligned input and output views, out-of-range index
 values (not delivered, reported), the device-side rejections (negative
-count, a NULL buffer that would be used: nothing written) and untouched
-sentinels beyond what each rank receives.
+count, a NULL buffer that would be used: nothing written), untouched
+sentinels beyond what each rank receives, and seeded random cases mixing all
+of these.
 """
 import numpy as np
 import pytest
@@ -215,3 +216,42 @@ def test_null_output_that_would_receive_rejects_the_whole_call():
         assert (o == -1.0).all().item()
     for b in book:
         assert (b == BOOK_SENT).all().item()
+
+
+@pytest.mark.parametrize("k", range(16))
+def test_random_indexed_exchanges_match_the_oracle(k):
+    """Random rank counts, launch widths, dtypes, count mixes (zeros, a few
+    large pieces among many small ones), index kinds (identity, permutation,
+    repeats with unused input), a sprinkling of out-of-range index values and
+    buffer offsets, bit-exact against the oracle, with the out-of-range
+    elements reported and left undelivered."""
+    rng = np.random.default_rng(7000 + k)
+    P = int(rng.choice([1, 2, 3, 5, 8, 13, 32, 47, 64]))
+    dt = "int8" if rng.random() < 0.6 else "fp32"
+    L = int(rng.choice([1, 2, P, 2 * P + 1, 64, 152, 1000]))
+    big = rng.integers(0, 1 << 15, size=(P, P))
+    small = rng.integers(0, 40, size=(P, P))
+    sc = np.where(rng.random((P, P)) < 4.0 / max(P, 4), big, small).astype(np.int64)
+    sc[rng.random((P, P)) < 0.3] = 0
+    kind = str(rng.choice(["identity", "perm", "random"]))
+    extra = int(rng.integers(1, 200)) if kind == "random" else 0
+    lens = [int(sc[i].sum()) + extra for i in range(P)]
+    inputs = [(rng.integers(-128, 128, size=n, dtype=np.int8) if dt == "int8"
+               else rng.standard_normal(n).astype(np.float32)) for n in lens]
+    index = a2av_index(sc, lens, kind, seed=int(rng.integers(0, 1 << 30)))
+    bad = 0
+    if rng.random() < 0.5:
+        for i in range(P):
+            n = int(sc[i].sum())
+            if n == 0:
+                continue
+            at = rng.choice(n, size=min(n, int(rng.integers(1, 6))), replace=False)
+            index[i][at] = np.where(rng.random(len(at)) < 0.5,
+                                    -1 - rng.integers(0, 1 << 40, size=len(at)),
+                                    lens[i] + rng.integers(0, 1 << 40, size=len(at)))
+            bad += len(at)
+    offs = 4 if dt == "int8" else 2
+    ref = _check_against_oracle(sc, inputs, index, dt, L=L, in_off=int(rng.integers(0, offs)),
+                                out_off=int(rng.integers(0, offs)))
+    assert ref["invalid"] == bad
+    assert bra.fault_status() == 0

@@ -84,6 +84,8 @@ cudaError_t launch_fused_simt(const FusedProblem& f, cudaStream_t st);
 // Both return cudaErrorInvalidValue if a TMA descriptor cannot be encoded.
 cudaError_t launch_fused_tc(const FusedProblem& f, cudaStream_t st);    // one CTA per tile
 cudaError_t launch_fused_tc2(const FusedProblem& f, cudaStream_t st);   // CTA pair per tile
+// Width of that kernel's pair tiles for this problem: 256 or 512.
+int fused_tc2_tile_n(const FusedProblem& f);
 // Shape / alignment predicate of the tensor-core variant.
 bool fused_tc_eligible(const FusedProblem& f);
 // Tensor-core variant for rows of any alignment (operands staged by loads).

@@ -29,6 +29,7 @@
 // Every wait is bounded (about 4 s by %globaltimer) and reports through the
 // device fault word; both CTAs always reach the closing cluster barrier and
 // free their tensor memory.
+#include <cstdlib>
 #include <cstring>
 #include <memory>
 #include <mutex>
@@ -57,8 +58,12 @@ constexpr int kGroupM = BRA_TC2_GROUP_M;
 constexpr int A_BYTES = BM_CTA * BK * 2;          // 16 KiB
 constexpr int B_BOX_BYTES = 64 * BK * 2;          // 8 KiB: 64 N-major columns
 constexpr int B_SUB_BYTES = 128 * BK * 2;         // 16 KiB: one CTA's half of N = 256
-constexpr int THREADS = 256;
 constexpr int EPI_WARP0 = 4;
+// Epilogue warps of the 512-wide tile: 8 (two per TMEM lane quarter, each
+// draining half of the columns) or 4.
+#ifndef BRA_TC2_EPI_WARPS2
+#define BRA_TC2_EPI_WARPS2 8
+#endif
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
 
@@ -74,16 +79,24 @@ struct Shape {
   static constexpr int BN = 256 * NSUB;
   static constexpr int B_BYTES = NSUB * B_SUB_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = NSUB == 1 ? 6 : 4;
   static constexpr int NACC = NSUB == 1 ? 2 : 1;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 4 * kEpiStageBytes + 1024;
+  static constexpr int EPI_WARPS = NSUB == 1 ? 4 : BRA_TC2_EPI_WARPS2;
+  static constexpr int EPI_SPLIT = EPI_WARPS / 4;             // column parts of a lane quarter
+  static constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
+  // stages: as many as fit beside the epilogue warps' staging tiles
+  static constexpr int STAGES = NSUB == 1 ? 6 : (EPI_WARPS == 8 ? 3 : 4);
+  static constexpr int SMEM_BYTES =
+      STAGES * STAGE_BYTES + BAR_BYTES + EPI_WARPS * kEpiStageBytes + 1024;
+  static_assert(EPI_WARPS == 4 || (EPI_WARPS == 8 && NSUB == 2), "epilogue warps");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 template <typename T, int NSUB>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS, 1)
     fused_tc2_kernel(const __grid_constant__ TcParams p) {
   using S = Shape<NSUB>;
   constexpr int STAGES = S::STAGES, STAGE_BYTES = S::STAGE_BYTES, BN = S::BN, NACC = S::NACC;
+  constexpr int EPI_SPLIT = S::EPI_SPLIT, BN_EPI = BN / EPI_SPLIT;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -113,7 +126,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(tfull_bar(a), 1);    // one multicast commit per tile
-      mbar_init(tempty_bar(a), 8);   // leader: 4 epilogue warps of each CTA
+      mbar_init(tempty_bar(a), 2 * S::EPI_WARPS);   // leader: the epilogue warps of each CTA
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -221,8 +234,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (!ok) spin_ns(2000000ull);   // let MMAs already issued complete
   } else if (warp >= EPI_WARP0) {
     // ---------------- epilogue (both CTAs) ----------------
-    const int q = warp & 3;
-    const uint32_t epi_stage = epi_stage_base + (uint32_t)q * kEpiStageBytes;
+    // lane quarter q of TMEM (warp % 4), column part h of EPI_SPLIT
+    const int q = warp & 3, h = (warp - EPI_WARP0) >> 2;
+    const uint32_t epi_stage = epi_stage_base + (uint32_t)(warp - EPI_WARP0) * kEpiStageBytes;
     const uint32_t leader_tempty0 = map_to_rank(tempty_bar(0), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -232,16 +246,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const bool waited = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, fault);
       if (!__all_sync(0xffffffffu, waited)) break;
       tc_fence_after();
-      const uint32_t t_base = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      const uint32_t t_base = tmem_base + (uint32_t)(acc * BN + h * BN_EPI) +
+                              ((uint32_t)(q * 32) << 16);
       const int row0 = tc.mt * BM + (int)rank * BM_CTA + q * 32;
+      const int n0 = tc.nt * BN + h * BN_EPI;
       if (p.y_elem) {   // outputs or bias without 16-byte alignment: element stores
-        uint8_t* stg = bars + BAR_BYTES + q * kEpiStageBytes;
+        uint8_t* stg = bars + BAR_BYTES + (warp - EPI_WARP0) * kEpiStageBytes;
 #pragma unroll 1
-        for (int sub = 0; sub < NSUB; ++sub)
-          epilogue_rows_u<T, true>(p, t_base + sub * 256, row0, sl, e, tc.nt * BN + sub * 256,
-                                   stg, lane);
+        for (int sub = 0; sub < BN_EPI / 256; ++sub)
+          epilogue_rows_u<T, true>(p, t_base + sub * 256, row0, sl, e, n0 + sub * 256, stg, lane);
       } else {
-        epilogue_rows<T, BN>(p, t_base, row0, sl, e, tc.nt * BN, epi_stage, lane);
+        epilogue_rows<T, BN_EPI>(p, t_base, row0, sl, e, n0, epi_stage, lane);
       }
       tc_fence_before();
       __syncwarp();
@@ -282,7 +297,7 @@ cudaError_t setup_kernel(int* pairs) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.blockDim = dim3(Shape<NSUB>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -298,14 +313,26 @@ cudaError_t setup_kernel(int* pairs) {
   return cudaSuccess;
 }
 
-// Pair tiles 256 wide by default: with the MMA issue loop down to one add per
-// MMA, the double-buffered accumulator of the 256-wide tile beats the single
-// 512-wide accumulator on both workloads measured (M = 4096 and 8192).
-// BRA_TC2_NSUB=2 selects the 512-wide tile.
-#ifndef BRA_TC2_NSUB
-#define BRA_TC2_NSUB 1
-#endif
-int choose_nsub(const FusedProblem&) { return BRA_TC2_NSUB == 2 ? 2 : 1; }
+}  // namespace
+
+// Pair tile width.  The 512-wide tile moves a quarter less operand traffic
+// per FLOP from L2 and into shared memory, which at the power cap buys a
+// higher SM clock (1537 against 1290 MHz on the fp16 M = 8192 workload), but
+// its single accumulator leaves the tensor core idle while the epilogue
+// drains it.  With a long K loop the clock wins: K = tp * Kp = 8192 ran 5%
+// faster sustained and 3-5% in short runs; at K = 4096 (the bf16 M = 4096
+// workload) the 256-wide tile with its overlapped epilogue stayed 4-7% ahead.
+// BRA_TC2_WIDE=0|1, read at every call, forces the 256- or 512-wide tile.
+int fused_tc2_tile_n(const FusedProblem& f) {
+  const char* v = std::getenv("BRA_TC2_WIDE");
+  if (v && *v) return *v == '1' ? 512 : 256;
+  const int64_t K = (int64_t)f.tp * f.Kp;
+  const int64_t rows = (int64_t)f.ep * f.C;
+  const int64_t tiles = (int64_t)f.ep * f.El * ((rows + 255) / 256) * (((int64_t)f.H + 511) / 512);
+  return K >= 8192 && f.H >= 1024 && tiles >= 38 ? 512 : 256;
+}
+
+namespace {
 
 template <int NSUB>
 cudaError_t launch_nsub(const FusedProblem& f, int pairs, cudaStream_t st) {
@@ -324,9 +351,9 @@ cudaError_t launch_nsub(const FusedProblem& f, int pairs, cudaStream_t st) {
     p->num_tiles = (s1 - s0) * f.El * p->m_tiles * p->n_tiles;
     const int np = p->num_tiles < pairs ? p->num_tiles : pairs;
     if (bf16)
-      fused_tc2_kernel<__nv_bfloat16, NSUB><<<2 * np, THREADS, S::SMEM_BYTES, st>>>(*p);
+      fused_tc2_kernel<__nv_bfloat16, NSUB><<<2 * np, S::THREADS, S::SMEM_BYTES, st>>>(*p);
     else
-      fused_tc2_kernel<__half, NSUB><<<2 * np, THREADS, S::SMEM_BYTES, st>>>(*p);
+      fused_tc2_kernel<__half, NSUB><<<2 * np, S::THREADS, S::SMEM_BYTES, st>>>(*p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -360,7 +387,7 @@ cudaError_t launch_fused_tc2(const FusedProblem& f, cudaStream_t st) {
     pairs1 = di.pairs;
     pairs2 = di.pairs2;
   }
-  return choose_nsub(f) == 2 ? launch_nsub<2>(f, pairs2, st) : launch_nsub<1>(f, pairs1, st);
+  return fused_tc2_tile_n(f) == 512 ? launch_nsub<2>(f, pairs2, st) : launch_nsub<1>(f, pairs1, st);
 }
 
 cudaError_t read_fault_word2(int32_t* code, int clear) {

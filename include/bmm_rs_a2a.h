@@ -69,7 +69,7 @@ typedef enum {
   BRA_VARIANT_AUTO = 0,
   BRA_VARIANT_TC = 1,    /* tcgen05 / TMEM / TMA kernel, one CTA per tile  */
   BRA_VARIANT_SIMT = 2,  /* generic kernel: any alignment, any size        */
-  BRA_VARIANT_TC2 = 3,   /* tcgen05 kernel, a CTA pair per 256x256 tile    */
+  BRA_VARIANT_TC2 = 3,   /* tcgen05 kernel, a CTA pair per 256x256 or 256x512 tile */
   BRA_VARIANT_TCU = 4,   /* tcgen05 kernel for rows of any alignment:
                             operands staged by loads, not TMA             */
   BRA_VARIANT_TCR = 5,   /* tcgen05 CTA-pair kernel for rows of any
@@ -133,7 +133,10 @@ typedef enum {
  * weight 16-byte aligned) a TMA-fed tensor-core kernel runs: the CTA-pair
  * kernel when the problem has at least 64 output tiles of 256 x 256 and
  * more than 128 token rows (ep*C) per expert group, else the one-CTA
- * kernel.  Its epilogue stores 16-byte vectors from 16-byte rows when the
+ * kernel.  The CTA pair computes 256 x 512 tiles when the K loop is long
+ * (tp * Kp >= 8192), H >= 1024 and there are at least 38 such tiles, else
+ * 256 x 256 tiles (the environment variable BRA_TC2_WIDE=1 or 0, read at
+ * every call, forces one).  Its epilogue stores 16-byte vectors from 16-byte rows when the
  * outputs and bias are 16-byte aligned (and Hp % 8 == 0 for yShardType 0),
  * else it stages each row segment at its destination's 16-byte phase and
  * stores the aligned part as vectors (outputs and bias element-aligned).

@@ -117,6 +117,49 @@ def test_tensor_core_kernels(case, bias, variant, monkeypatch):
     assert err <= TOL[dt], f"{case} bias={bias} {variant}: rel err {err:.3e}"
 
 
+@pytest.mark.parametrize("case", TC_CASES)
+@pytest.mark.parametrize("bias", [True, False])
+def test_pair_kernel_wide_tiles(case, bias, monkeypatch, capfd):
+    """The CTA-pair kernel with 256 x 512 tiles forced (eight epilogue warps,
+    one accumulator per CTA) on every shape of the table, against the oracle."""
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("tcw", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=sum(case[:6]) + 41, has_bias=bias)
+    inp = fused_inputs_host(cfg)
+    ref = _oracle(cfg, inp)
+    monkeypatch.setenv("BRA_TC2_WIDE", "1")
+    monkeypatch.setenv("BRA_LOG", "1")
+    capfd.readouterr()
+    out = _run(cfg, _to_dev(inp), "tc2", monkeypatch)
+    assert "-> tc2 (256x512 tiles)" in capfd.readouterr().err
+    err = _rel_err(out, ref)
+    assert err <= TOL[dt], f"{case} bias={bias}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("case,wide", [
+    ((4, 4, 8, 256, 8192, 1024, 1, "fp16"), True),    # K = 8192, H = 1024: 64 wide tiles
+    ((4, 4, 8, 264, 8192, 1104, 0, "bf16"), True),    # ragged m and n tiles, H/tp = 276
+    ((4, 2, 8, 256, 4096, 1024, 0, "bf16"), False),   # K = 4096: 256-wide
+    ((4, 4, 8, 256, 8192, 512, 1, "fp16"), False),    # H < 1024: 256-wide
+])
+def test_pair_kernel_tile_width_choice(case, wide, monkeypatch, capfd):
+    """The automatic choice of the pair tile's width follows the K loop's
+    length, H and the tile count, and both widths match the oracle."""
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("tcx", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=sum(case[:6]) + 43)
+    inp = fused_inputs_host(cfg)
+    ref = _oracle(cfg, inp)
+    monkeypatch.delenv("BRA_TC2_WIDE", raising=False)
+    monkeypatch.setenv("BRA_LOG", "1")
+    capfd.readouterr()
+    out = _run(cfg, _to_dev(inp), None, monkeypatch)
+    log = capfd.readouterr().err
+    assert ("-> tc2 (256x512 tiles)" if wide else "-> tc2 (256x256 tiles)") in log, log
+    err = _rel_err(out, ref)
+    assert err <= TOL[dt], f"{case}: rel err {err:.3e}"
+
+
 @pytest.mark.parametrize("case", TC_CASES[:5])
 def test_generic_kernel_on_the_same_shapes(case, monkeypatch):
     ep, tp, E, C, M, H, t, dt = case

@@ -243,20 +243,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS
     for (int tile = pair; tile < p.num_tiles; tile += npairs) {
       const TileCoord tc = tile_coord(tile, p.m_tiles, p.n_tiles, kGroupM);
       const int sl = tc.g / p.El, e = tc.g % p.El;
+      const int row0 = tc.mt * BM + (int)rank * BM_CTA + q * 32;
+      const int n0 = tc.nt * BN + h * BN_EPI;
+      // the tile's bias, staged while its accumulator is still being computed
+      const bool bias_staged =
+          !p.y_elem && epilogue_bias<T, BN_EPI>(p, row0, sl, e, n0, epi_stage, lane);
       const bool waited = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, fault);
       if (!__all_sync(0xffffffffu, waited)) break;
       tc_fence_after();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * BN + h * BN_EPI) +
                               ((uint32_t)(q * 32) << 16);
-      const int row0 = tc.mt * BM + (int)rank * BM_CTA + q * 32;
-      const int n0 = tc.nt * BN + h * BN_EPI;
       if (p.y_elem) {   // outputs or bias without 16-byte alignment: element stores
         uint8_t* stg = bars + BAR_BYTES + (warp - EPI_WARP0) * kEpiStageBytes;
 #pragma unroll 1
         for (int sub = 0; sub < BN_EPI / 256; ++sub)
           epilogue_rows_u<T, true>(p, t_base + sub * 256, row0, sl, e, n0 + sub * 256, stg, lane);
       } else {
-        epilogue_rows<T, BN_EPI>(p, t_base, row0, sl, e, n0, epi_stage, lane);
+        epilogue_body<T, BN_EPI>(p, t_base, row0, sl, e, n0, epi_stage, lane, bias_staged);
       }
       tc_fence_before();
       __syncwarp();

@@ -378,9 +378,10 @@ __device__ __forceinline__ uint4 lds128e(uint32_t addr) {
   return v;
 }
 
-// One epilogue warp drains its 32 TMEM lanes (accumulator rows row0 ..
-// row0+31 of Z_{s,e}, the global row index in ep*C) of a BN-column
-// accumulator, columns n0 .. n0+BN-1, 64 columns at a time:
+// The epilogue of one warp (epilogue_rows below: epilogue_bias, then
+// epilogue_body) drains its 32 TMEM lanes (accumulator rows row0 .. row0+31
+// of Z_{s,e}, the global row index in ep*C) of a BN-column accumulator,
+// columns n0 .. n0+BN-1, 64 columns at a time:
 //   1. lane l holds row row0+l: tcgen05.ld two 32-column slices, add the
 //      sender's bias in fp32, round once, write the 128-byte row segment to
 //      the warp's staging tile;
@@ -391,21 +392,22 @@ __device__ __forceinline__ uint4 lds128e(uint32_t addr) {
 //        yShardType 1: y[j*tp + (m%C)/Cp][s*El+e, (m%C)%Cp, n]   (j = m / C).
 // Every lane runs the warp-wide tcgen05.ld; stores are masked per row and
 // per 8 columns (H is a multiple of 8).
+// Bias staging of the tile (step 0 of the epilogue, which the caller may run
+// before the accumulator is ready: it depends on the tile's coordinates
+// only).  When the bias depends on the column only -- always for
+// yShardType 0, and for yShardType 1 when the warp's 32 rows share a TP rank
+// (row 0 of the warp is valid whenever any is) -- the warp stages the tile's
+// BN bias values (fp32) once in its staging tile and every row reads them
+// by broadcast; returns whether it did (warp-uniform).
 template <typename T, int BN>
-__device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base, int row0, int sl,
-                                              int e, int n0, uint32_t stage, int lane) {
+__device__ __forceinline__ bool epilogue_bias(const TcParams& p, int row0, int sl, int e, int n0,
+                                              uint32_t stage, int lane) {
   static_assert(BN * 4 <= kEpiBiasBytes, "bias staging");
-  const int s = p.s0 + sl;
   const int Hp = p.H / p.tp;
   const int Cp = p.type == 1 ? p.C / p.tp : 1;
-  // this lane's own row (phase 1)
   const int m_own = row0 + lane;
   const bool own_ok = m_own < p.rows;
   const int t_own = (own_ok && p.type == 1) ? (m_own % p.C) / Cp : 0;
-  // When the bias depends on the column only -- always for yShardType 0, and
-  // for yShardType 1 when the warp's 32 rows share a TP rank (row 0 of the
-  // warp is valid whenever any is) -- the warp stages the tile's BN bias
-  // values (fp32) once and every row reads them by broadcast.
   const int t_first = __shfl_sync(0xffffffffu, t_own, 0);
   const uint32_t bias_stage = stage + 32 * kEpiRowStride;
   const bool bias_staged =
@@ -431,8 +433,27 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base
       sts128(bias_stage + g * 32 + 16, make_uint4(__float_as_uint(b[4]), __float_as_uint(b[5]),
                                                   __float_as_uint(b[6]), __float_as_uint(b[7])));
     }
-    __syncwarp();
   }
+  __syncwarp();
+  return bias_staged;
+}
+
+// The rest of the epilogue, once the accumulator is ready (bias_staged: what
+// epilogue_bias returned for this tile).  The next 64 columns' TMEM loads are
+// issued as soon as a chunk is staged, so they land while the chunk's stores
+// go out.
+template <typename T, int BN>
+__device__ __forceinline__ void epilogue_body(const TcParams& p, uint32_t t_base, int row0, int sl,
+                                              int e, int n0, uint32_t stage, int lane,
+                                              bool bias_staged) {
+  const int s = p.s0 + sl;
+  const int Hp = p.H / p.tp;
+  const int Cp = p.type == 1 ? p.C / p.tp : 1;
+  // this lane's own row (phase 1)
+  const int m_own = row0 + lane;
+  const bool own_ok = m_own < p.rows;
+  const int t_own = (own_ok && p.type == 1) ? (m_own % p.C) / Cp : 0;
+  const uint32_t bias_stage = stage + 32 * kEpiRowStride;
   // the 8 rows this lane stores (phase 2): r = 4q + lane/8
   const int kc = lane & 7;
   int64_t rbase[8];
@@ -454,53 +475,72 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base
     }
   }
   const uint32_t my_row = stage + (uint32_t)lane * kEpiRowStride;
+  uint32_t v[64];
+  tmem_ld32(t_base, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+  tmem_ld32(t_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
 #pragma unroll 1
   for (int ch = 0; ch < BN / 64; ++ch) {
-    uint32_t v[64];
-    tmem_ld32(t_base + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-    tmem_ld32(t_base + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
     tmem_ld_wait();
-    // phase 1: bias, convert, stage the row segment
+    // phase 1: bias, convert, stage the row segment.  Loads are issued in
+    // batches ahead of their use (shared-memory accesses here are ordered
+    // asm statements, so a load placed after a store would wait for it).
+    if (bias_staged) {
 #pragma unroll
-    for (int g8 = 0; g8 < 8; ++g8) {
-      const int n = n0 + ch * 64 + g8 * 8;
-      float f[8];
+      for (int bq = 0; bq < 4; ++bq) {          // 16 columns per batch
+        uint4 b[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(v[g8 * 8 + k]);
-      if (bias_staged) {
-        const uint32_t ba = bias_stage + (uint32_t)(ch * 64 + g8 * 8) * 4;
-        const uint4 b0 = lds128e(ba), b1 = lds128e(ba + 16);
-        f[0] += __uint_as_float(b0.x); f[1] += __uint_as_float(b0.y);
-        f[2] += __uint_as_float(b0.z); f[3] += __uint_as_float(b0.w);
-        f[4] += __uint_as_float(b1.x); f[5] += __uint_as_float(b1.y);
-        f[6] += __uint_as_float(b1.z); f[7] += __uint_as_float(b1.w);
-      } else if (p.has_bias && own_ok && n < p.H) {
-        // yShardType 1, rows of several TP ranks: each row its own bias row.
-        float b[8];
-        Out<T>::bias8(static_cast<const uint8_t*>(p.bias[sl * p.tp + t_own]) +
-                          ((int64_t)e * p.H + n) * Out<T>::kBiasBytes,
-                      b);
+        for (int i = 0; i < 4; ++i)
+          b[i] = lds128e(bias_stage + (uint32_t)(ch * 64 + bq * 16 + i * 4) * 4);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) f[k] += b[k];
+        for (int i = 0; i < 4; ++i) {
+          uint32_t* w = &v[bq * 16 + i * 4];
+          w[0] = __float_as_uint(__uint_as_float(w[0]) + __uint_as_float(b[i].x));
+          w[1] = __float_as_uint(__uint_as_float(w[1]) + __uint_as_float(b[i].y));
+          w[2] = __float_as_uint(__uint_as_float(w[2]) + __uint_as_float(b[i].z));
+          w[3] = __float_as_uint(__uint_as_float(w[3]) + __uint_as_float(b[i].w));
+        }
       }
-      uint4 o;
-      o.x = Out<T>::pack(f[0], f[1]);
-      o.y = Out<T>::pack(f[2], f[3]);
-      o.z = Out<T>::pack(f[4], f[5]);
-      o.w = Out<T>::pack(f[6], f[7]);
-      sts128(my_row + g8 * 16, o);
+    } else if (p.has_bias && own_ok) {
+      // yShardType 1, rows of several TP ranks: each row its own bias row.
+#pragma unroll
+      for (int g8 = 0; g8 < 8; ++g8) {
+        const int n = n0 + ch * 64 + g8 * 8;
+        if (n < p.H) {
+          float b[8];
+          Out<T>::bias8(static_cast<const uint8_t*>(p.bias[sl * p.tp + t_own]) +
+                            ((int64_t)e * p.H + n) * Out<T>::kBiasBytes,
+                        b);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            v[g8 * 8 + k] = __float_as_uint(__uint_as_float(v[g8 * 8 + k]) + b[k]);
+        }
+      }
+    }
+    uint32_t o[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      o[k] = Out<T>::pack(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8)
+      sts128(my_row + g8 * 16, make_uint4(o[4 * g8], o[4 * g8 + 1], o[4 * g8 + 2], o[4 * g8 + 3]));
+    // the next chunk's accumulator columns, into the registers just consumed
+    if (ch + 1 < BN / 64) {
+      tmem_ld32(t_base + (ch + 1) * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(t_base + (ch + 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
     }
     __syncwarp();
-    // phase 2: row segments to their destinations
+    // phase 2: row segments to their destinations, all eight loaded first
     const int n = n0 + ch * 64 + kc * 8;
     if (n < p.H) {
       const int t0 = p.type == 0 ? n / Hp : 0;
       const int h0 = n - t0 * Hp;
+      uint4 val[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        val[q] = lds128e(stage + (uint32_t)(4 * q + (lane >> 3)) * kEpiRowStride + kc * 16);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         if (rdest[q] < 0) continue;
-        const int r = 4 * q + (lane >> 3);
-        const uint4 val = lds128e(stage + (uint32_t)r * kEpiRowStride + kc * 16);
         int d;
         int64_t off;
         if (p.type == 0) {
@@ -511,11 +551,19 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base
           off = rbase[q] + n;
         }
         T* yd = static_cast<T*>(p.y[d]);
-        *reinterpret_cast<uint4*>(yd + off) = val;
+        *reinterpret_cast<uint4*>(yd + off) = val[q];
       }
     }
     __syncwarp();
   }
+}
+
+// The whole epilogue of one warp (bias staging, then the body).
+template <typename T, int BN>
+__device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base, int row0, int sl,
+                                              int e, int n0, uint32_t stage, int lane) {
+  const bool bias_staged = epilogue_bias<T, BN>(p, row0, sl, e, n0, stage, lane);
+  epilogue_body<T, BN>(p, t_base, row0, sl, e, n0, stage, lane, bias_staged);
 }
 
 // ---------------------------------------------------------------------------

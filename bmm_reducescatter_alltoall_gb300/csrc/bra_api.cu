@@ -466,8 +466,12 @@ int bmm_rs_a2a_ex(const void* const x[], const void* const weight[],
                  "[bra] bmm_rs_a2a ep=%lld tp=%lld E=%lld C=%lld M=%lld H=%lld type=%lld -> %s%s\n",
                  (long long)ep, (long long)tp, (long long)E, (long long)C, (long long)M,
                  (long long)H, (long long)yShardType, variant_name(v),
-                 v != BRA_VARIANT_TC2 ? "" : bra::fused_tc2_tile_n(p) == 512 ? " (256x512 tiles)"
-                                                                            : " (256x256 tiles)");
+                 v != BRA_VARIANT_TC2                ? ""
+                 : bra::fused_tc2_tile_n(p) == 512 ? (bra::fused_tc2_share(p)
+                                                          ? " (256x512 tiles, weight boxes shared)"
+                                                          : " (256x512 tiles)")
+                 : bra::fused_tc2_share(p)         ? " (256x256 tiles, weight boxes shared)"
+                                                   : " (256x256 tiles)");
   if (p.status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), (cudaStream_t)stream) !=
                       cudaSuccess)
     return BRA_ERR_CUDA;

@@ -86,6 +86,8 @@ cudaError_t launch_fused_tc(const FusedProblem& f, cudaStream_t st);    // one C
 cudaError_t launch_fused_tc2(const FusedProblem& f, cudaStream_t st);   // CTA pair per tile
 // Width of that kernel's pair tiles for this problem: 256 or 512.
 int fused_tc2_tile_n(const FusedProblem& f);
+// Whether that kernel runs two pairs per cluster sharing each weight box.
+int fused_tc2_share(const FusedProblem& f);
 // Shape / alignment predicate of the tensor-core variant.
 bool fused_tc_eligible(const FusedProblem& f);
 // Tensor-core variant for rows of any alignment (operands staged by loads).

@@ -91,9 +91,14 @@ struct Shape {
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-template <typename T, int NSUB>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS, 1)
+// CL pairs per cluster.  CL = 2: the two pairs compute m tiles 2i and 2i+1
+// of the same n tile and load each weight box once, multicast to the CTA of
+// either pair that holds it (half of the weight's L2 reads); a stage is free
+// again once both pairs' MMAs have read it.
+template <typename T, int NSUB, int CL>
+__global__ void __cluster_dims__(2 * CL, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS, 1)
     fused_tc2_kernel(const __grid_constant__ TcParams p) {
+  static_assert(CL == 1 || CL == 2, "pairs per cluster");
   using S = Shape<NSUB>;
   constexpr int STAGES = S::STAGES, STAGE_BYTES = S::STAGE_BYTES, BN = S::BN, NACC = S::NACC;
   constexpr int EPI_SPLIT = S::EPI_SPLIT, BN_EPI = BN / EPI_SPLIT;
@@ -116,13 +121,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS
   static_assert(8 * (2 * STAGES + 4) + 16 <= BAR_BYTES, "barrier area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const uint32_t rank = cluster_rank();      // 0 .. 2 CL - 1
+  const uint32_t r2 = rank & 1u;             // CTA within its pair
+  const uint32_t lead = rank & ~1u;          // its pair's leader
+  const int pc = (int)(rank >> 1);           // pair within the cluster
+  // super-tiles: CL m tiles (one per pair) of one n tile, handed out per cluster
+  const int cl = blockIdx.x / (2 * CL), ncl = gridDim.x / (2 * CL);
+  const int m_super = (p.m_tiles + CL - 1) / CL;
+  const int num_super = p.num_tiles / (p.m_tiles * p.n_tiles) * m_super * p.n_tiles;
+  constexpr int kGroupS = kGroupM / CL > 0 ? kGroupM / CL : 1;
+  constexpr uint16_t kAllCtas = (uint16_t)((1u << (2 * CL)) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);     // leader: its expect_tx; both halves' bytes
-      mbar_init(empty_bar(s), 1);    // one multicast commit per use
+      mbar_init(empty_bar(s), CL);   // one multicast commit per pair and use
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(tfull_bar(a), 1);    // one multicast commit per tile
@@ -149,14 +162,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
-    const uint32_t leader_full0 = map_to_rank(full_bar(0), 0);
+    const uint32_t leader_full0 = map_to_rank(full_bar(0), lead);
+    const uint16_t share = (uint16_t)((1u << rank) | (1u << (rank ^ 2u)));   // CL = 2
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
-      const TileCoord tc = tile_coord(tile, p.m_tiles, p.n_tiles, kGroupM);
+    for (int st = cl; ok && st < num_super; st += ncl) {
+      TileCoord tc = tile_coord(st, m_super, p.n_tiles, kGroupS);
+      tc.mt = tc.mt * CL + pc;
       const int sl = tc.g / p.El, e = tc.g % p.El;
-      const int a_row = tc.mt * BM + (int)rank * BM_CTA;
+      const int a_row = tc.mt * BM + (int)r2 * BM_CTA;
       for (int t = 0; ok && t < p.tp; ++t) {
         const int r = sl * p.tp + t;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -164,7 +179,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS
             ok = false;
             break;
           }
-          if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+          if (r2 == 0) mbar_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
           const uint32_t fb = leader_full0 + 8u * stage;
           const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
@@ -172,14 +187,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS
 #pragma unroll
           for (int sub = 0; sub < NSUB; ++sub) {
             // this CTA's 128 columns of N=256 sub-tile `sub`
-            const int b_col = tc.nt * BN + sub * 256 + (int)rank * 128;
+            const int b_col = tc.nt * BN + sub * 256 + (int)r2 * 128;
             const uint32_t bs = b_dst + sub * B_SUB_BYTES;
             if (p.b_kmajor) {
-              tma_load_3d_pair(bs, &p.tw[r], fb, kb * BK, b_col, e);   // 128 rows x 128 B
+              // 128 rows x 128 B; shared: the pair whose index is sub % 2 loads it
+              if (CL == 1)
+                tma_load_3d_pair(bs, &p.tw[r], fb, kb * BK, b_col, e);
+              else if (sub % 2 == pc)
+                tma_load_3d_pair_mc(bs, &p.tw[r], fb, kb * BK, b_col, e, share);
             } else {
 #pragma unroll
-              for (int c = 0; c < 2; ++c)
-                tma_load_3d_pair(bs + c * B_BOX_BYTES, &p.tw[r], fb, b_col + c * 64, kb * BK, e);
+              for (int c = 0; c < 2; ++c) {
+                if (CL == 1)
+                  tma_load_3d_pair(bs + c * B_BOX_BYTES, &p.tw[r], fb, b_col + c * 64, kb * BK, e);
+                else if ((sub * 2 + c) % 2 == pc)   // boxes dealt over the two pairs
+                  tma_load_3d_pair_mc(bs + c * B_BOX_BYTES, &p.tw[r], fb, b_col + c * 64,
+                                      kb * BK, e, share);
+              }
             }
           }
           if (++stage == STAGES) {
@@ -190,7 +214,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS
       }
     }
     if (!ok) spin_ns(2000000ull);   // let copies already issued land
-  } else if (warp == 1 && lane == 0 && rank == 0) {
+  } else if (warp == 1 && lane == 0 && r2 == 0) {
     // ---------------- MMA issuer (leader only) ----------------
     const RingDescs rd = ring_descs(p, smem_base, smem_base + A_BYTES);
     int stage = 0;
@@ -198,7 +222,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+    for (int st = cl; ok && st < num_super; st += ncl) {
       if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, fault)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);   // acc = 0 when NACC = 1
@@ -218,14 +242,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS
                       rd.b0 + so + (uint64_t)((sub * B_SUB_BYTES) >> 4) + rd.b_kstep * k, p.idesc,
                       (kk > 0 || k > 0) ? 1u : 0u);
         }
-        tc_commit_pair(empty_bar(stage), 0x3);
+        tc_commit_pair(empty_bar(stage), kAllCtas);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      tc_commit_pair(tfull_bar(acc), 0x3);
+      tc_commit_pair(tfull_bar(acc), (uint16_t)(0x3u << (2 * pc)));
       if (++acc == NACC) {
         acc = 0;
         acc_phase ^= 1u;
@@ -237,13 +261,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS
     // lane quarter q of TMEM (warp % 4), column part h of EPI_SPLIT
     const int q = warp & 3, h = (warp - EPI_WARP0) >> 2;
     const uint32_t epi_stage = epi_stage_base + (uint32_t)(warp - EPI_WARP0) * kEpiStageBytes;
-    const uint32_t leader_tempty0 = map_to_rank(tempty_bar(0), 0);
+    const uint32_t leader_tempty0 = map_to_rank(tempty_bar(0), lead);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = pair; tile < p.num_tiles; tile += npairs) {
-      const TileCoord tc = tile_coord(tile, p.m_tiles, p.n_tiles, kGroupM);
+    for (int st = cl; st < num_super; st += ncl) {
+      TileCoord tc = tile_coord(st, m_super, p.n_tiles, kGroupS);
+      tc.mt = tc.mt * CL + pc;
       const int sl = tc.g / p.El, e = tc.g % p.El;
-      const int row0 = tc.mt * BM + (int)rank * BM_CTA + q * 32;
+      const int row0 = tc.mt * BM + (int)r2 * BM_CTA + q * 32;
       const int n0 = tc.nt * BN + h * BN_EPI;
       // the tile's bias, staged while its accumulator is still being computed
       const bool bias_staged =
@@ -264,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (rank == 0)
+        if (r2 == 0)
           mbar_arrive(tempty_bar(acc));
         else
           mbar_arrive_cluster(leader_tempty0 + 8u * acc);
@@ -287,32 +312,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<NSUB>::THREADS
 }
 
 struct DeviceInfo2 {
-  int pairs = 0;    // co-resident clusters, N = 256 pair tiles
-  int pairs2 = 0;   // co-resident clusters, N = 512 pair tiles
+  int clusters[2][2] = {};   // co-resident clusters: [N = 512 tiles][two pairs a cluster]
   bool ready = false;
 };
 
-template <typename T, int NSUB>
-cudaError_t setup_kernel(int* pairs) {
+template <typename T, int NSUB, int CL>
+cudaError_t setup_kernel(int* clusters) {
   constexpr int smem = Shape<NSUB>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(fused_tc2_kernel<T, NSUB>,
+  cudaError_t e = cudaFuncSetAttribute(fused_tc2_kernel<T, NSUB, CL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2, 1, 1);
+  cfg.gridDim = dim3(2 * CL, 1, 1);
   cfg.blockDim = dim3(Shape<NSUB>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.x = 2 * CL;
   attr.val.clusterDim.y = 1;
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, fused_tc2_kernel<T, NSUB>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, fused_tc2_kernel<T, NSUB, CL>, &cfg);
   if (e != cudaSuccess) return e;
-  *pairs = n;
+  *clusters = n;
   return cudaSuccess;
 }
 
@@ -335,10 +359,21 @@ int fused_tc2_tile_n(const FusedProblem& f) {
   return K >= 8192 && f.H >= 1024 && tiles >= 38 ? 512 : 256;
 }
 
+// Whether two pairs share each weight box (clusters of four CTAs).
+// BRA_TC2_SHARE=0|1, read at every call, forces the choice.
+#ifndef BRA_TC2_SHARE_DEFAULT
+#define BRA_TC2_SHARE_DEFAULT 0
+#endif
+int fused_tc2_share(const FusedProblem&) {
+  const char* v = std::getenv("BRA_TC2_SHARE");
+  if (v && *v) return *v == '1' ? 1 : 0;
+  return BRA_TC2_SHARE_DEFAULT;
+}
+
 namespace {
 
-template <int NSUB>
-cudaError_t launch_nsub(const FusedProblem& f, int pairs, cudaStream_t st) {
+template <int NSUB, int CL>
+cudaError_t launch_nsub(const FusedProblem& f, int clusters, cudaStream_t st) {
   using S = Shape<NSUB>;
   std::unique_ptr<TcParams> p(new TcParams);
   std::memset(p.get(), 0, sizeof(TcParams));
@@ -352,11 +387,12 @@ cudaError_t launch_nsub(const FusedProblem& f, int pairs, cudaStream_t st) {
     const int s1 = s0 + s_per_launch < f.ep ? s0 + s_per_launch : f.ep;
     if (!fill_chunk(p.get(), f, s0, s1, BM_CTA, 64, BK, 128)) return cudaErrorInvalidValue;
     p->num_tiles = (s1 - s0) * f.El * p->m_tiles * p->n_tiles;
-    const int np = p->num_tiles < pairs ? p->num_tiles : pairs;
+    const int num_super = (s1 - s0) * f.El * ((p->m_tiles + CL - 1) / CL) * p->n_tiles;
+    const int nc = num_super < clusters ? num_super : clusters;
     if (bf16)
-      fused_tc2_kernel<__nv_bfloat16, NSUB><<<2 * np, S::THREADS, S::SMEM_BYTES, st>>>(*p);
+      fused_tc2_kernel<__nv_bfloat16, NSUB, CL><<<2 * CL * nc, S::THREADS, S::SMEM_BYTES, st>>>(*p);
     else
-      fused_tc2_kernel<__half, NSUB><<<2 * np, S::THREADS, S::SMEM_BYTES, st>>>(*p);
+      fused_tc2_kernel<__half, NSUB, CL><<<2 * CL * nc, S::THREADS, S::SMEM_BYTES, st>>>(*p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -371,26 +407,33 @@ cudaError_t launch_fused_tc2(const FusedProblem& f, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   static std::mutex mu;
   static DeviceInfo2 info[64];
-  int pairs1 = 1, pairs2 = 1;
+  int cl[2][2];
   {
     std::lock_guard<std::mutex> lk(mu);
     DeviceInfo2& di = info[dev & 63];
     if (!di.ready) {
-      int a = 0, b = 0, c = 0, d = 0;
-      if ((e = setup_kernel<__half, 1>(&a)) != cudaSuccess) return e;
-      if ((e = setup_kernel<__nv_bfloat16, 1>(&b)) != cudaSuccess) return e;
-      if ((e = setup_kernel<__half, 2>(&c)) != cudaSuccess) return e;
-      if ((e = setup_kernel<__nv_bfloat16, 2>(&d)) != cudaSuccess) return e;
-      di.pairs = a < b ? a : b;
-      di.pairs2 = c < d ? c : d;
-      if (di.pairs < 1) di.pairs = 1;
-      if (di.pairs2 < 1) di.pairs2 = 1;
+      int a[8] = {};
+      if ((e = setup_kernel<__half, 1, 1>(&a[0])) != cudaSuccess) return e;
+      if ((e = setup_kernel<__nv_bfloat16, 1, 1>(&a[1])) != cudaSuccess) return e;
+      if ((e = setup_kernel<__half, 2, 1>(&a[2])) != cudaSuccess) return e;
+      if ((e = setup_kernel<__nv_bfloat16, 2, 1>(&a[3])) != cudaSuccess) return e;
+      if ((e = setup_kernel<__half, 1, 2>(&a[4])) != cudaSuccess) return e;
+      if ((e = setup_kernel<__nv_bfloat16, 1, 2>(&a[5])) != cudaSuccess) return e;
+      if ((e = setup_kernel<__half, 2, 2>(&a[6])) != cudaSuccess) return e;
+      if ((e = setup_kernel<__nv_bfloat16, 2, 2>(&a[7])) != cudaSuccess) return e;
+      // a[2k], a[2k+1]: the fp16 and bf16 kernels of tile width k % 2, k / 2 + 1 pairs
+      for (int k = 0; k < 4; ++k) {
+        const int m = a[2 * k] < a[2 * k + 1] ? a[2 * k] : a[2 * k + 1];
+        di.clusters[k % 2][k / 2] = m < 1 ? 1 : m;
+      }
       di.ready = true;
     }
-    pairs1 = di.pairs;
-    pairs2 = di.pairs2;
+    for (int k = 0; k < 4; ++k) cl[k % 2][k / 2] = di.clusters[k % 2][k / 2];
   }
-  return fused_tc2_tile_n(f) == 512 ? launch_nsub<2>(f, pairs2, st) : launch_nsub<1>(f, pairs1, st);
+  const bool wide = fused_tc2_tile_n(f) == 512;
+  if (fused_tc2_share(f))
+    return wide ? launch_nsub<2, 2>(f, cl[1][1], st) : launch_nsub<1, 2>(f, cl[0][1], st);
+  return wide ? launch_nsub<2, 1>(f, cl[1][0], st) : launch_nsub<1, 1>(f, cl[0][0], st);
 }
 
 cudaError_t read_fault_word2(int32_t* code, int clear) {

@@ -136,6 +136,29 @@ def test_pair_kernel_wide_tiles(case, bias, monkeypatch, capfd):
     assert err <= TOL[dt], f"{case} bias={bias}: rel err {err:.3e}"
 
 
+@pytest.mark.parametrize("wide", ["0", "1"])
+@pytest.mark.parametrize("case", TC_CASES + [(4, 4, 8, 264, 8192, 1104, 0, "bf16"),
+                                             (2, 2, 4, 300, 512, 1024, 1, "fp16")])
+def test_pair_kernel_shared_weight_boxes(case, wide, monkeypatch, capfd):
+    """Two CTA pairs per cluster computing m tiles 2i and 2i+1 of one n tile,
+    each weight box loaded once and multicast to both pairs (odd m-tile counts
+    leave the second pair a tile past the rows), both tile widths, against the
+    oracle."""
+    ep, tp, E, C, M, H, t, dt = case
+    cfg = FusedConfig("tcs", ep=ep, tp=tp, E=E, C=C, M=M, H=H, y_shard_type=t, dtype=dt,
+                      seed=sum(case[:6]) + 47)
+    inp = fused_inputs_host(cfg)
+    ref = _oracle(cfg, inp)
+    monkeypatch.setenv("BRA_TC2_SHARE", "1")
+    monkeypatch.setenv("BRA_TC2_WIDE", wide)
+    monkeypatch.setenv("BRA_LOG", "1")
+    capfd.readouterr()
+    out = _run(cfg, _to_dev(inp), "tc2", monkeypatch)
+    assert "weight boxes shared)" in capfd.readouterr().err
+    err = _rel_err(out, ref)
+    assert err <= TOL[dt], f"{case} wide={wide}: rel err {err:.3e}"
+
+
 @pytest.mark.parametrize("case,wide", [
     ((4, 4, 8, 256, 8192, 1024, 1, "fp16"), True),    # K = 8192, H = 1024: 64 wide tiles
     ((4, 4, 8, 264, 8192, 1104, 0, "bf16"), True),    # ragged m and n tiles, H/tp = 276

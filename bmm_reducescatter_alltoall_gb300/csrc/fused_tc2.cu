@@ -20,12 +20,14 @@
 //     the leader posts the expected bytes of both halves.
 //   * Only the leader issues MMAs; its commits multicast to the empty and
 //     accumulator-full barriers of both CTAs.
-//   * Each CTA's epilogue drains its own TMEM (its 128 rows x 256 columns)
-//     and arrives on the leader's accumulator-empty barrier (remote arrive
-//     for the peer).
+//   * Each CTA's epilogue drains its own TMEM (its 128 rows) and arrives on
+//     the leader's accumulator-empty barrier (remote arrive for the peer):
+//     four warps, one per TMEM lane quarter, or for the wide tile eight, two
+//     per quarter with half of the columns each.
 //   * TMEM: 512 columns allocated by the pair (tcgen05.alloc.cta_group::2 in
 //     both CTAs; both get the same column range): two 256-column
 //     accumulators, or one 512-column accumulator for the wide tile.
+//   * Optionally two pairs per cluster share each weight box (see CL below).
 // Every wait is bounded (about 4 s by %globaltimer) and reports through the
 // device fault word; both CTAs always reach the closing cluster barrier and
 // free their tensor memory.

@@ -136,7 +136,9 @@ typedef enum {
  * kernel.  The CTA pair computes 256 x 512 tiles when the K loop is long
  * (tp * Kp >= 8192), H >= 1024 and there are at least 38 such tiles, else
  * 256 x 256 tiles (the environment variable BRA_TC2_WIDE=1 or 0, read at
- * every call, forces one).  Its epilogue stores 16-byte vectors from 16-byte rows when the
+ * every call, forces one; BRA_TC2_SHARE=1 runs it as clusters of two pairs
+ * that share each weight box by TMA multicast, an option measured no faster
+ * and off by default).  Its epilogue stores 16-byte vectors from 16-byte rows when the
  * outputs and bias are 16-byte aligned (and Hp % 8 == 0 for yShardType 0),
  * else it stages each row segment at its destination's 16-byte phase and
  * stores the aligned part as vectors (outputs and bias element-aligned).

@@ -280,21 +280,26 @@ __global__ void __cluster_dims__(2 * CL, 1, 1) __launch_bounds__(Shape<NSUB>::TH
       tc_fence_after();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * BN + h * BN_EPI) +
                               ((uint32_t)(q * 32) << 16);
+      // hand the accumulator back to the leader's MMA issuer (remote arrive
+      // for the peer) once this warp's TMEM reads are done
+      auto release = [&] {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (r2 == 0)
+            mbar_arrive(tempty_bar(acc));
+          else
+            mbar_arrive_cluster(leader_tempty0 + 8u * acc);
+        }
+      };
       if (p.y_elem) {   // outputs or bias without 16-byte alignment: element stores
         uint8_t* stg = bars + BAR_BYTES + (warp - EPI_WARP0) * kEpiStageBytes;
 #pragma unroll 1
         for (int sub = 0; sub < BN_EPI / 256; ++sub)
           epilogue_rows_u<T, true>(p, t_base + sub * 256, row0, sl, e, n0 + sub * 256, stg, lane);
+        release();
       } else {
-        epilogue_body<T, BN_EPI>(p, t_base, row0, sl, e, n0, epi_stage, lane, bias_staged);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (r2 == 0)
-          mbar_arrive(tempty_bar(acc));
-        else
-          mbar_arrive_cluster(leader_tempty0 + 8u * acc);
+        epilogue_body<T, BN_EPI>(p, t_base, row0, sl, e, n0, epi_stage, lane, bias_staged, release);
       }
       if (++acc == NACC) {
         acc = 0;

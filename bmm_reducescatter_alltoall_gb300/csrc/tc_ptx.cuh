@@ -454,11 +454,13 @@ __device__ __forceinline__ bool epilogue_bias(const TcParams& p, int row0, int s
 // The rest of the epilogue, once the accumulator is ready (bias_staged: what
 // epilogue_bias returned for this tile).  The next 64 columns' TMEM loads are
 // issued as soon as a chunk is staged, so they land while the chunk's stores
-// go out.
-template <typename T, int BN>
+// go out.  tmem_done() runs on every lane right after the last TMEM load has
+// landed: the accumulator may be handed back there, before the last chunk's
+// conversion and stores.
+template <typename T, int BN, typename TmemDone>
 __device__ __forceinline__ void epilogue_body(const TcParams& p, uint32_t t_base, int row0, int sl,
                                               int e, int n0, uint32_t stage, int lane,
-                                              bool bias_staged) {
+                                              bool bias_staged, TmemDone&& tmem_done) {
   const int s = p.s0 + sl;
   const int Hp = p.H / p.tp;
   const int Cp = p.type == 1 ? p.C / p.tp : 1;
@@ -494,6 +496,7 @@ __device__ __forceinline__ void epilogue_body(const TcParams& p, uint32_t t_base
 #pragma unroll 1
   for (int ch = 0; ch < BN / 64; ++ch) {
     tmem_ld_wait();
+    if (ch + 1 == BN / 64) tmem_done();
     // phase 1: bias, convert, stage the row segment.  Loads are issued in
     // batches ahead of their use (shared-memory accesses here are ordered
     // asm statements, so a load placed after a store would wait for it).
@@ -576,7 +579,7 @@ template <typename T, int BN>
 __device__ __forceinline__ void epilogue_rows(const TcParams& p, uint32_t t_base, int row0, int sl,
                                               int e, int n0, uint32_t stage, int lane) {
   const bool bias_staged = epilogue_bias<T, BN>(p, row0, sl, e, n0, stage, lane);
-  epilogue_body<T, BN>(p, t_base, row0, sl, e, n0, stage, lane, bias_staged);
+  epilogue_body<T, BN>(p, t_base, row0, sl, e, n0, stage, lane, bias_staged, [] {});
 }
 
 // ---------------------------------------------------------------------------

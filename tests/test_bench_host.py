@@ -39,3 +39,40 @@ def test_arguments_and_defaults():
                      "--steps", "3", "--e2e-steps", "0", "--indexed-calls", "0"])
     assert b.workspace and b.steps == 3 and b.e2e_steps == 0 and b.indexed_calls == 0
     assert b.fused in FUSED_CONFIGS
+
+
+class _FakeProc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+    def kill(self):
+        pass
+
+
+def test_clock_sampler_reads_the_timed_window_and_reasons():
+    """The clock record of the bench line: the median SM clock, the maximum
+    clock and power, and the active throttle reasons of the samples inside
+    the timed window only (fields as nvidia-smi's CSV gives them)."""
+    s = bench.ClockSampler(0)
+    s.proc = _FakeProc()
+    row = lambda mhz, pw, cap, thermal: [
+        "0", str(mhz), "2070", str(pw), "0x4", "Not Active",
+        "Active" if thermal else "Not Active", "Not Active", "Active" if cap else "Not Active"]
+    s.rows = [(0.5, row(2070, 300.0, False, True)),           # before the window
+              (1.0, row(1300, 1390.5, True, False)),
+              (1.5, row(1320, 1401.0, True, False)),
+              (2.0, row(1310, 1395.0, False, False)),
+              (3.5, row(2070, 200.0, False, True))]           # after it
+    s.mark(0.9, 2.1)
+    rec = s.stop()
+    assert rec["sm_mhz"] == 1310 and rec["sm_max_mhz"] == 2070
+    assert rec["power_w_max"] == 1401.0 and rec["samples"] == 3
+    assert rec["reasons"] == ["sw_power_cap"]
+    s2 = bench.ClockSampler(0)
+    s2.proc = _FakeProc()
+    s2.rows = [(1.0, row(1800, 900.0, False, True))]
+    s2.mark(0.5, 1.5)
+    assert s2.stop()["reasons"] == ["hw_thermal_slowdown"]

@@ -25,18 +25,12 @@ template <typename T>
 struct Elt;
 template <>
 struct Elt<__half> {
-  static __device__ __forceinline__ uint16_t cvt(float v) {
-    return __half_as_ushort(__float2half_rn(v));
-  }
   static __device__ __forceinline__ float bias(const void* p, int64_t i) {
     return __half2float(static_cast<const __half*>(p)[i]);
   }
 };
 template <>
 struct Elt<__nv_bfloat16> {
-  static __device__ __forceinline__ uint16_t cvt(float v) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  }
   static __device__ __forceinline__ float bias(const void* p, int64_t i) {
     return static_cast<const float*>(p)[i];
   }
@@ -190,7 +184,7 @@ __device__ __forceinline__ void epilogue_rows_u(const P& p, uint32_t t_base, int
           if (n + 1 < p.H) f1 += Elt<T>::bias(brow, (int64_t)e * p.H + n + 1);
         }
       }
-      w[i] = (uint32_t)Elt<T>::cvt(f0) | ((uint32_t)Elt<T>::cvt(f1) << 16);
+      w[i] = Out<T>::pack(f0, f1);   // one paired RNE conversion: f0 low, f1 high
     }
     // stage: buffer element k holds column k - delta (delta = 0 off the fast
     // path).  Word q + i of the row buffer (q = delta / 2) joins w[i-1] and

@@ -551,3 +551,31 @@ def test_exchange_ring_protocol_under_random_schedules():
     for stages in (A2AV_WARPS * 2 + 1, 11):
         assert not all(_ring_schedule(stages, 4 if stages == 11 else A2AV_WARPS, 200, rng)
                        for _ in range(100))
+
+
+@pytest.mark.parametrize("pairs_per_cluster", [1, 2])
+@pytest.mark.parametrize("group_m", [0, 4, 16])
+def test_cluster_super_tiles_cover_every_tile_once(pairs_per_cluster, group_m):
+    """fused_tc2.cu with CL pairs per cluster: super-tile st (CL m tiles of one
+    n tile, walked by tile_coord with super-rows of group_m / CL) gives pair
+    pc the m tile CL * mt' + pc.  Every output tile is computed by exactly
+    one (super-tile, pair); the only extra work is the second pair's tile
+    past the last m tile when the m-tile count is odd, which the kernel
+    loads as zeros and does not store."""
+    CL = pairs_per_cluster
+    gs = max(group_m // CL, 1) if group_m > 0 else 0
+    for m_tiles in range(1, 21):
+        for n_tiles in range(1, 9):
+            groups = 2
+            m_super = (m_tiles + CL - 1) // CL
+            seen, extra = {}, 0
+            for st in range(groups * m_super * n_tiles):
+                g, ms, nt = _tile_coord(st, m_super, n_tiles, gs)
+                for pc in range(CL):
+                    mt = ms * CL + pc
+                    if mt >= m_tiles:
+                        extra += 1
+                        continue
+                    seen[(g, mt, nt)] = seen.get((g, mt, nt), 0) + 1
+            assert len(seen) == groups * m_tiles * n_tiles and set(seen.values()) == {1}
+            assert extra == (groups * n_tiles if CL == 2 and m_tiles % 2 else 0)

@@ -563,7 +563,7 @@ def test_cluster_super_tiles_cover_every_tile_once(pairs_per_cluster, group_m):
     past the last m tile when the m-tile count is odd, which the kernel
     loads as zeros and does not store."""
     CL = pairs_per_cluster
-    gs = max(group_m // CL, 1) if group_m > 0 else 0
+    gs = group_m // CL if group_m // CL > 0 else 1   # kGroupS of the kernel
     for m_tiles in range(1, 21):
         for n_tiles in range(1, 9):
             groups = 2
